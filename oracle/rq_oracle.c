@@ -1,0 +1,345 @@
+/*
+ * rq_oracle.c -- plain, slow, single-threaded fp64 oracle for the rotation-based
+ * W4A4 hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg may load this library.  It shares no code, header, table or
+ * constant with the CUDA library, and it never reads anything the CUDA library
+ * produced.
+ *
+ * Sources (page title, then section / equation):
+ *   [ROT]  "Rotational Quantization: How Orthogonal Transforms and Hadamard
+ *          Incoherence Enable Outlier-Free Low-Bit Inference" (llms.blog)
+ *   [QR]   aicassindra.com, quantization series, "QuaRot" page
+ *   [SQ]   aicassindra.com, quantization series, "SpinQuant" page
+ *
+ * Every function states the passage it follows.  Where the pages are silent the
+ * reading taken is stated at the function ("reading: ...").
+ *
+ * Parity status: every function below is pinned by the CPU tests (closed forms,
+ * library routines, brute force, published test vectors); none is "parity
+ * unpinned".
+ *
+ * Compile with -ffp-contract=off so that no multiply-add is fused: the results
+ * are then the same on x86-64 and aarch64 hosts.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define RQO_OK 0
+#define RQO_ERR_ARG 1
+#define RQO_ERR_OVERFLOW 2
+#define RQO_ERR_NOMEM 3
+
+/* flags bit 0: rotation form.
+ *   0: y = (x H_n) diag(s)    -- R = H_d diag(s)            [ROT] §Incoherence, eq. R = H_d·diag(s)
+ *   1: y = (x diag(s)) H_n    -- sign flip then transform   (the "x·diag(±1)·H_n/√n" form)
+ * Both are orthogonal and each is the transpose of the other (H_n is symmetric). */
+#define RQO_SIGNS_FIRST 1u
+
+/* ------------------------------------------------------------------------- */
+/* Random signs.                                                              */
+/* ------------------------------------------------------------------------- */
+
+/* SplitMix64, as published by Steele, Lea and Flood ("Fast splittable
+ * pseudorandom number generators", OOPSLA 2014) and in Vigna's reference
+ * splitmix64.c: the state advances by the golden-ratio increment before each
+ * output, and each output is the state passed through two xor-shift-multiply
+ * rounds and a final xor-shift.  Returns output number i (0-based) of the
+ * stream seeded with `seed`, i.e. the mix of seed + (i+1)*increment. */
+uint64_t rqo_splitmix64(uint64_t seed, uint64_t i)
+{
+    const uint64_t golden_gamma = 0x9e3779b97f4a7c15ULL;
+    uint64_t z = seed + (i + 1u) * golden_gamma;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+    return z ^ (z >> 31);
+}
+
+/* Rademacher vector s in {-1,+1}^n: [ROT] §Incoherence ("s ... sampled uniformly
+ * from ±1").  Reading: s_i = +1 when the top bit of SplitMix64 output i is 0,
+ * else -1.  The pages fix no generator; this one is ours. */
+void rqo_signs(uint64_t seed, int64_t n, int8_t *s)
+{
+    for (int64_t i = 0; i < n; ++i)
+        s[i] = (rqo_splitmix64(seed, (uint64_t)i) >> 63) ? (int8_t)-1 : (int8_t)1;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Hadamard transform.                                                        */
+/* ------------------------------------------------------------------------- */
+
+/* x <- H_n x for the normalized Sylvester Hadamard matrix, written as the
+ * recursion of [ROT] §Incoherence: H_1 = [1] and
+ *     H_2k = (1/sqrt 2) [[H_k, H_k], [H_k, -H_k]].
+ * Applying the block form to x = [top; bottom] gives
+ *     H_2k x = (1/sqrt 2) [H_k top + H_k bottom; H_k top - H_k bottom],
+ * so the routine transforms each half recursively and then combines.
+ * H_n is symmetric, so the same routine computes the row-vector product x H_n. */
+static void hadamard_rec(double *x, int64_t n)
+{
+    if (n == 1)
+        return;
+    const int64_t h = n / 2;
+    hadamard_rec(x, h);
+    hadamard_rec(x + h, h);
+    const double r = 1.0 / sqrt(2.0);
+    for (int64_t i = 0; i < h; ++i) {
+        const double a = x[i];
+        const double b = x[i + h];
+        x[i] = (a + b) * r;
+        x[i + h] = (a - b) * r;
+    }
+}
+
+static int is_pow2(int64_t n) { return n >= 1 && (n & (n - 1)) == 0; }
+
+int rqo_hadamard(double *x, int64_t n)
+{
+    if (!is_pow2(n))
+        return RQO_ERR_ARG;
+    hadamard_rec(x, n);
+    return RQO_OK;
+}
+
+/* One rotated row y = x R for the randomized Hadamard R, in the form chosen by
+ * flags bit 0 (see RQO_SIGNS_FIRST).  [ROT] §Incoherence, eq. R = H_d·diag(s)
+ * and eq. x~ = x R. */
+int rqo_rotate_row(const double *x, int64_t n, const int8_t *s, uint32_t flags, double *y)
+{
+    if (!is_pow2(n))
+        return RQO_ERR_ARG;
+    if (flags & RQO_SIGNS_FIRST) {
+        for (int64_t i = 0; i < n; ++i)
+            y[i] = x[i] * (double)s[i];
+        hadamard_rec(y, n);
+    } else {
+        memcpy(y, x, (size_t)n * sizeof(double));
+        hadamard_rec(y, n);
+        for (int64_t i = 0; i < n; ++i)
+            y[i] = y[i] * (double)s[i];
+    }
+    return RQO_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Symmetric INT4 quantization and packing.                                   */
+/* ------------------------------------------------------------------------- */
+
+/* Per-row symmetric INT4: scale = max|y| / 7, q = clamp(round_half_even(y / scale),
+ * -8, 7).  The pages name an "INT4 quantizer" with per-channel scales ([QR]
+ * §The architecture; [SQ] §The architecture) and the asymmetric step
+ * (max-min)/(2^b-1) ([ROT] §The Activation Outlier Bottleneck); the symmetric
+ * absmax/7 form with round-half-even and the [-8,7] clamp is the reading taken.
+ * Reading for an all-zero row: scale = 0 and every code 0.
+ * nearbyint() rounds in the default mode, which is round-half-to-even.
+ * `ratio` (nullable) receives y/scale, used by the tests' tie-window count. */
+void rqo_quant_row(const double *y, int64_t n, int8_t *q, double *scale, double *ratio)
+{
+    double amax = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        const double a = fabs(y[i]);
+        if (a > amax)
+            amax = a;
+    }
+    if (amax == 0.0) {
+        *scale = 0.0;
+        for (int64_t i = 0; i < n; ++i) {
+            q[i] = 0;
+            if (ratio)
+                ratio[i] = 0.0;
+        }
+        return;
+    }
+    const double sc = amax / 7.0;
+    *scale = sc;
+    for (int64_t i = 0; i < n; ++i) {
+        const double r = y[i] / sc;
+        double c = nearbyint(r);
+        if (c < -8.0)
+            c = -8.0;
+        if (c > 7.0)
+            c = 7.0;
+        q[i] = (int8_t)c;
+        if (ratio)
+            ratio[i] = r;
+    }
+}
+
+/* Nibble packing (reading; the pages fix no layout): byte j holds element 2j in
+ * bits 3..0 and element 2j+1 in bits 7..4, each as a 4-bit two's-complement
+ * code.  n must be even. */
+void rqo_pack_row(const int8_t *q, int64_t n, uint8_t *out)
+{
+    for (int64_t j = 0; j < n / 2; ++j) {
+        const unsigned lo = (unsigned)q[2 * j] & 0xFu;
+        const unsigned hi = (unsigned)q[2 * j + 1] & 0xFu;
+        out[j] = (uint8_t)(lo | (hi << 4));
+    }
+}
+
+static int8_t nibble_to_int(unsigned v)
+{
+    v &= 0xFu;
+    return (int8_t)(v >= 8u ? (int)v - 16 : (int)v);
+}
+
+void rqo_unpack_row(const uint8_t *in, int64_t n, int8_t *q)
+{
+    for (int64_t j = 0; j < n / 2; ++j) {
+        q[2 * j] = nibble_to_int(in[j]);
+        q[2 * j + 1] = nibble_to_int((unsigned)in[j] >> 4);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Online rotation + quantization of a row-major matrix.                      */
+/* ------------------------------------------------------------------------- */
+
+/* For each row r of x (rows x n, row stride ld_x, fp64): y = x_r R, then the
+ * per-row INT4 quantizer and packing.  Outputs: q (rows x n/2 bytes, row stride
+ * n/2), scales (rows, fp32, rounded from the fp64 scale), and optionally the
+ * fp64 rotated rows y (rows x n) and the ratios y/scale (rows x n).
+ * [QR] §End-to-end flow ("an online Hadamard transform rotates the activation
+ * ... The rotated activation is quantized to INT4"); [ROT] §Weight Absorption,
+ * 2. Online Fast Walsh-Hadamard Transform. */
+int rqo_fwht_quant(const double *x, int64_t rows, int64_t n, int64_t ld_x, uint64_t seed,
+                   uint32_t flags, uint8_t *q, float *scales, double *y_out, double *ratio_out)
+{
+    if (!is_pow2(n) || n < 2 || rows < 0 || ld_x < n)
+        return RQO_ERR_ARG;
+    int8_t *s = (int8_t *)malloc((size_t)n);
+    double *y = (double *)malloc((size_t)n * sizeof(double));
+    int8_t *codes = (int8_t *)malloc((size_t)n);
+    if (!s || !y || !codes) {
+        free(s);
+        free(y);
+        free(codes);
+        return RQO_ERR_NOMEM;
+    }
+    rqo_signs(seed, n, s);
+    for (int64_t r = 0; r < rows; ++r) {
+        double sc = 0.0;
+        rqo_rotate_row(x + r * ld_x, n, s, flags, y);
+        rqo_quant_row(y, n, codes, &sc, ratio_out ? ratio_out + r * n : NULL);
+        rqo_pack_row(codes, n, q + r * (n / 2));
+        scales[r] = (float)sc;
+        if (y_out)
+            memcpy(y_out + r * n, y, (size_t)n * sizeof(double));
+    }
+    free(s);
+    free(y);
+    free(codes);
+    return RQO_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* W4A4 linear layer.                                                         */
+/* ------------------------------------------------------------------------- */
+
+/* acc[m][c] = sum_k qa[m][k] * qw[c][k] in exact integer arithmetic, and
+ * y[m][c] = acc[m][c] * sa[m] * sw[c] (scales widened from fp32 to fp64).
+ * A is M x K (packed, M x K/2 bytes), W is N x K (packed, N x K/2 bytes): both
+ * K-major, W holding one output channel per row.  The integer form of the
+ * rotated product Q(XR)·Q(R^T W) of [ROT] §Learned Orthogonal Rotations
+ * (loss L(S)) and §The Principle of Computational Invariance (Y = (XR)(R^T W));
+ * [QR] §End-to-end flow ("multiplied against the INT4 folded weights").
+ * Either output may be NULL.  Returns RQO_ERR_OVERFLOW if an accumulator
+ * leaves the int32 range. */
+int rqo_w4a4_gemm(const uint8_t *aq, const float *sa, const uint8_t *wq, const float *sw,
+                  int64_t M, int64_t N, int64_t K, int64_t *acc, double *y)
+{
+    if (M < 0 || N < 0 || K < 0 || (K & 1))
+        return RQO_ERR_ARG;
+    int8_t *a = (int8_t *)malloc((size_t)(K > 0 ? K : 1));
+    int8_t *w = (int8_t *)malloc((size_t)(K > 0 ? K : 1) * (size_t)(N > 0 ? N : 1));
+    if (!a || !w) {
+        free(a);
+        free(w);
+        return RQO_ERR_NOMEM;
+    }
+    for (int64_t c = 0; c < N; ++c)
+        rqo_unpack_row(wq + c * (K / 2), K, w + c * K);
+    int status = RQO_OK;
+    for (int64_t m = 0; m < M; ++m) {
+        rqo_unpack_row(aq + m * (K / 2), K, a);
+        for (int64_t c = 0; c < N; ++c) {
+            int64_t s = 0;
+            const int8_t *wc = w + c * K;
+            for (int64_t k = 0; k < K; ++k)
+                s += (int64_t)a[k] * (int64_t)wc[k];
+            if (s > INT32_MAX || s < INT32_MIN)
+                status = RQO_ERR_OVERFLOW;
+            if (acc)
+                acc[m * N + c] = s;
+            if (y)
+                y[m * N + c] = (double)s * (double)sa[m] * (double)sw[c];
+        }
+    }
+    free(a);
+    free(w);
+    return status;
+}
+
+/* The same products for a list of (m, c) output positions only, for checks at
+ * sizes where the full product would take too long on one core. */
+int rqo_w4a4_gemm_entries(const uint8_t *aq, const float *sa, const uint8_t *wq, const float *sw,
+                          int64_t K, int64_t count, const int64_t *ms, const int64_t *cs,
+                          int64_t *acc, double *y)
+{
+    if (K < 0 || (K & 1) || count < 0)
+        return RQO_ERR_ARG;
+    int8_t *a = (int8_t *)malloc((size_t)(K > 0 ? K : 1));
+    int8_t *w = (int8_t *)malloc((size_t)(K > 0 ? K : 1));
+    if (!a || !w) {
+        free(a);
+        free(w);
+        return RQO_ERR_NOMEM;
+    }
+    int status = RQO_OK;
+    for (int64_t e = 0; e < count; ++e) {
+        rqo_unpack_row(aq + ms[e] * (K / 2), K, a);
+        rqo_unpack_row(wq + cs[e] * (K / 2), K, w);
+        int64_t s = 0;
+        for (int64_t k = 0; k < K; ++k)
+            s += (int64_t)a[k] * (int64_t)w[k];
+        if (s > INT32_MAX || s < INT32_MIN)
+            status = RQO_ERR_OVERFLOW;
+        if (acc)
+            acc[e] = s;
+        if (y)
+            y[e] = (double)s * (double)sa[ms[e]] * (double)sw[cs[e]];
+    }
+    free(a);
+    free(w);
+    return status;
+}
+
+/* ------------------------------------------------------------------------- */
+/* KV cache write: head-wise rotation + quantization.                         */
+/* ------------------------------------------------------------------------- */
+
+/* K and V, each [tokens][heads][head_dim] (fp64 here), are rotated per (token,
+ * head) vector by the randomized Hadamard of size head_dim and quantized per
+ * (token, head): [QR] §The architecture ("The KV-cache rotation box ... keys and
+ * values stored per token are themselves rotated before being quantized") and
+ * §End-to-end flow, "The KV cache"; [ROT] §Hardware Execution, 2. End-to-End KV
+ * Cache Footprint Reduction.  Reading: one sign vector of length head_dim drawn
+ * from `seed`, shared by every head and by K and V.  Either tensor may be NULL
+ * (its outputs are then untouched). */
+int rqo_kv_rotate_quant(const double *k, const double *v, int64_t tokens, int64_t heads,
+                        int64_t head_dim, uint64_t seed, uint32_t flags, uint8_t *kq,
+                        float *ks, uint8_t *vq, float *vs)
+{
+    if (tokens < 0 || heads < 0 || !is_pow2(head_dim) || head_dim < 2)
+        return RQO_ERR_ARG;
+    const int64_t rows = tokens * heads;
+    int st = RQO_OK;
+    if (k)
+        st = rqo_fwht_quant(k, rows, head_dim, head_dim, seed, flags, kq, ks, NULL, NULL);
+    if (st == RQO_OK && v)
+        st = rqo_fwht_quant(v, rows, head_dim, head_dim, seed, flags, vq, vs, NULL, NULL);
+    return st;
+}

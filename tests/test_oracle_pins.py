@@ -1,0 +1,367 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Every oracle function is checked here against something other than itself: a
+closed form, a library routine (scipy's Sylvester Hadamard, numpy's integer
+matmul), a published test vector, brute force on tiny inputs, or an invariant the
+pages state.  Each test names the passage it pins.
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+def _matrix_of(fn, n):
+    """Columns j = fn(e_j): the matrix of a linear row-map x -> fn(x) as x M."""
+    eye = np.eye(n)
+    return np.stack([fn(eye[i]) for i in range(n)])  # row i = e_i M
+
+
+# --------------------------------------------------------------------------
+# SplitMix64 / signs
+# --------------------------------------------------------------------------
+
+def test_splitmix64_published_vector():
+    rows = _read_golden("splitmix64.txt")
+    seed = int(rows[0][1])
+    for idx, val in rows[1:]:
+        assert oracle.splitmix64(seed, int(idx)) == int(val)
+
+
+def test_signs_are_rademacher():
+    s = oracle.signs(0x5EED, 1 << 16)
+    assert set(np.unique(s).tolist()) == {-1, 1}
+    # A fair +-1 sequence: mean within 5 sigma of 0, and both halves balanced.
+    assert abs(s.mean()) < 5 / np.sqrt(s.size)
+    # The sign is the top bit of the generator output, element by element.
+    for i in (0, 1, 2, 1000, 65535):
+        top = oracle.splitmix64(0x5EED, i) >> 63
+        assert s[i] == (-1 if top else 1)
+
+
+# --------------------------------------------------------------------------
+# Hadamard transform (the H_n recursion of "Incoherence Processing via
+# Randomized Hadamard Transforms")
+# --------------------------------------------------------------------------
+
+def test_hadamard_small_matrices_from_page_recursion():
+    rows = _read_golden("hadamard_small.txt")
+    i = 0
+    while i < len(rows):
+        n = int(rows[i][1])
+        expect = np.array([[float(v) for v in rows[i + 1 + r]] for r in range(n)]) / np.sqrt(n)
+        got = _matrix_of(lambda e: oracle.hadamard(e), n)
+        np.testing.assert_allclose(got, expect, rtol=0, atol=1e-15)
+        i += 1 + n
+
+
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 32, 64])
+def test_hadamard_closed_form_and_orthogonality(n):
+    h = _matrix_of(lambda e: oracle.hadamard(e), n)
+    i, j = np.meshgrid(np.arange(n), np.arange(n), indexing="ij")
+    pop = np.vectorize(lambda v: bin(int(v)).count("1"))(i & j)
+    closed = (-1.0) ** pop / np.sqrt(n)
+    np.testing.assert_allclose(h, closed, rtol=0, atol=1e-15)
+    # Every entry is +-1/sqrt(n) and H H^T = I.
+    np.testing.assert_allclose(np.abs(h), 1 / np.sqrt(n), rtol=1e-15)
+    np.testing.assert_allclose(h @ h.T, np.eye(n), atol=1e-14)
+
+
+@pytest.mark.parametrize("n", [2, 64, 1024, 4096])
+def test_hadamard_equals_scipy_sylvester_matmul(n):
+    rng = np.random.default_rng(n)
+    x = rng.standard_normal((3, n))
+    ref = x @ (scipy.linalg.hadamard(n).astype(np.float64) / np.sqrt(n))
+    np.testing.assert_allclose(oracle.hadamard(x), ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+
+
+def test_hadamard_is_an_involution():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((4, 512))
+    np.testing.assert_allclose(oracle.hadamard(oracle.hadamard(x)), x, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# Randomized rotation R ("R = H_d diag(s)") and its invariants
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("flags", [0, oracle.SIGNS_FIRST])
+def test_rotation_matrix_closed_form(flags):
+    n, seed = 32, 99
+    s = oracle.signs(seed, n).astype(np.float64)
+    h = scipy.linalg.hadamard(n) / np.sqrt(n)
+    r = _matrix_of(lambda e: oracle.rotate(e[None], seed, flags)[0], n)
+    expect = h @ np.diag(s) if flags == 0 else np.diag(s) @ h
+    np.testing.assert_allclose(r, expect, atol=1e-15)
+    np.testing.assert_allclose(r @ r.T, np.eye(n), atol=1e-14)
+
+
+def test_rotation_forms_are_transposes():
+    n, seed = 64, 5
+    r0 = _matrix_of(lambda e: oracle.rotate(e[None], seed, 0)[0], n)
+    r1 = _matrix_of(lambda e: oracle.rotate(e[None], seed, oracle.SIGNS_FIRST)[0], n)
+    np.testing.assert_allclose(r0, r1.T, atol=1e-15)
+
+
+@pytest.mark.parametrize("flags", [0, oracle.SIGNS_FIRST])
+def test_rotation_preserves_norm_and_rms(flags):
+    # "The Principle of Computational Invariance": ||xR||_2 = ||x||_2 and
+    # therefore RMS(xR) = RMS(x), the RMSNorm denominator.
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((5, 4096)) * np.array([1, 10, 1e-3, 100, 1])[:, None]
+    y = oracle.rotate(x, 0x5EED, flags)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+    rms = lambda v: np.sqrt(np.mean(v * v, axis=1))
+    np.testing.assert_allclose(rms(y), rms(x), rtol=1e-13)
+
+
+@pytest.mark.parametrize("flags", [0, oracle.SIGNS_FIRST])
+def test_computational_invariance_xw_equals_xr_rtw(flags):
+    # "The Principle of Computational Invariance": Y = XW = (XR)(R^T W).
+    # R^T W is formed column by column as the same row rotation applied to the
+    # rows of W^T (the offline fold), so this also pins the fold's transpose and
+    # sign side.
+    rng = np.random.default_rng(3)
+    d, k, b = 256, 40, 6
+    x = rng.standard_normal((b, d))
+    w = rng.standard_normal((d, k)) * 0.02
+    xr = oracle.rotate(x, 0x5EED, flags)
+    rtw = oracle.rotate(w.T, 0x5EED, flags).T
+    np.testing.assert_allclose(xr @ rtw, x @ w, rtol=0, atol=1e-13 * np.abs(x @ w).max())
+
+
+@pytest.mark.parametrize("d,attenuation,tol", [(int(a), float(b), float(c))
+                                               for a, b, c in _read_golden("spike_attenuation.txt")])
+@pytest.mark.parametrize("flags", [0, oracle.SIGNS_FIRST])
+def test_single_spike_spreads_to_m_over_sqrt_d(d, attenuation, tol, flags):
+    # "Incoherence Processing ...": x~_j = O(M/sqrt d); for one spike it is
+    # exactly +-M/sqrt(d) in every coordinate.
+    m = 100.0
+    for pos in (0, 1, d // 3, d - 1):
+        x = np.zeros((1, d))
+        x[0, pos] = m
+        y = oracle.rotate(x, 0x5EED, flags)[0]
+        np.testing.assert_allclose(np.abs(y), m / np.sqrt(d), rtol=1e-13)
+        assert abs(m / np.abs(y).max() - attenuation) <= tol + 1e-9
+
+
+# --------------------------------------------------------------------------
+# Quantizer and packing
+# --------------------------------------------------------------------------
+
+def _brute_force_code(r):
+    """argmin_c |r - c| over the 16 INT4 codes, ties to the even code."""
+    best = None
+    for c in range(-8, 8):
+        d = abs(r - c)
+        if best is None or d < best[0] - 1e-300 or (d == best[0] and c % 2 == 0):
+            best = (d, c)
+    return best[1]
+
+
+def test_quant_matches_brute_force_and_invariants():
+    rng = np.random.default_rng(21)
+    y = rng.standard_normal((8, 256)) * rng.uniform(0.01, 100, size=(8, 1))
+    codes, scales, ratio = oracle.quant_rows(y)
+    for r in range(y.shape[0]):
+        amax = np.abs(y[r]).max()
+        assert scales[r] == pytest.approx(amax / 7, rel=1e-15)
+        for j in range(0, 256, 7):
+            assert codes[r, j] == _brute_force_code(y[r, j] / scales[r])
+        # the absmax element maps to +-7; codes stay in [-7, 7]; error <= scale/2
+        jm = np.argmax(np.abs(y[r]))
+        assert codes[r, jm] == (7 if y[r, jm] > 0 else -7)
+        assert codes[r].min() >= -7 and codes[r].max() <= 7
+        assert np.all(np.abs(codes[r] * scales[r] - y[r]) <= scales[r] / 2 * (1 + 1e-12))
+
+
+def test_quant_round_half_to_even_on_exact_ties():
+    # absmax 7 -> scale 1 exactly, so y/scale = y and the ties are exact.
+    y = np.array([[7.0, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 3.5, -6.5, 0.0]])
+    codes, scales, _ = oracle.quant_rows(y)
+    assert scales[0] == 1.0
+    assert codes[0].tolist() == [7, 0, 2, 2, 0, -2, -2, 4, -6, 0]
+
+
+def test_quant_degenerate_rows():
+    codes, scales, _ = oracle.quant_rows(np.zeros((1, 16)))
+    assert scales[0] == 0.0 and not codes.any()
+    y = np.zeros((1, 16))
+    y[0, 5] = -3e-7
+    codes, scales, _ = oracle.quant_rows(y)
+    assert codes[0, 5] == -7 and np.count_nonzero(codes) == 1
+
+
+def test_pack_worked_example():
+    rows = _read_golden("pack_example.txt")
+    codes = np.array([int(v) for v in rows[0][1:]], dtype=np.int8)
+    expect = np.array([int(v, 16) for v in rows[1][1:]], dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.pack(codes[None])[0], expect)
+    np.testing.assert_array_equal(oracle.unpack(expect[None], codes.size)[0], codes)
+
+
+def test_pack_roundtrip_all_codes():
+    codes = np.array(list(itertools.product(range(-8, 8), repeat=2)), dtype=np.int8).reshape(1, -1)
+    packed = oracle.pack(codes)
+    assert packed.shape == (1, codes.shape[1] // 2)
+    # bit layout: low nibble = even element, two's complement
+    lo = (packed[0] & 0xF).astype(np.int16)
+    lo[lo >= 8] -= 16
+    np.testing.assert_array_equal(lo, codes[0, 0::2])
+    np.testing.assert_array_equal(oracle.unpack(packed, codes.shape[1]), codes)
+
+
+def test_packed_size_is_a_quarter_of_16_bit():
+    # "Why architecture matters here" (QuaRot page): four-bit values quarter the
+    # bytes of sixteen-bit ones; the packed layout holds exactly n/2 bytes.
+    x = np.random.default_rng(0).standard_normal((3, 128))
+    out = oracle.fwht_quant(x, 1, oracle.SIGNS_FIRST)
+    assert out["q"].nbytes * 4 == x.size * 2
+
+
+# --------------------------------------------------------------------------
+# Rotation + quantization pipeline, and the weight fold
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("flags", [0, oracle.SIGNS_FIRST])
+def test_fwht_quant_is_rotate_then_quant_then_pack(flags):
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((6, 512))
+    out = oracle.fwht_quant(x, 77, flags, want_y=True, want_ratio=True)
+    # rotated rows: the explicit matrix product with scipy's Sylvester matrix
+    s = oracle.signs(77, 512).astype(np.float64)
+    h = scipy.linalg.hadamard(512) / np.sqrt(512)
+    ref = (x @ h) * s if flags == 0 else (x * s) @ h
+    np.testing.assert_allclose(out["y"], ref, atol=1e-12)
+    codes = oracle.unpack(out["q"], 512)
+    for r in range(6):
+        sc = np.abs(ref[r]).max() / 7
+        assert out["scales"][r] == np.float32(sc)
+        for j in range(0, 512, 11):
+            assert codes[r, j] == _brute_force_code(ref[r, j] / sc)
+
+
+def test_rotation_reduces_int4_error_on_outlier_rows():
+    # The pages' central claim ("a rotation turns a spiky, outlier-dominated
+    # vector into a smooth one ... nearly lossless", QuaRot page, "Why
+    # architecture matters here"): per-token INT4 error drops sharply after the
+    # rotation on rows with 0.1%-style outlier channels.
+    rng = np.random.default_rng(9)
+    n = 4096
+    x = rng.standard_normal((16, n))
+    x[:, [10, 700, 2000, 4000]] *= 100
+    def mse_after_quant(v):
+        c, s, _ = oracle.quant_rows(v)
+        return np.mean((c * s[:, None] - v) ** 2)
+    plain = mse_after_quant(x)
+    rot = oracle.rotate(x, 0x5EED, oracle.SIGNS_FIRST)
+    rotated = mse_after_quant(rot)  # same norm, so the errors compare directly
+    assert rotated < plain / 5  # measured about 8x on this seed
+
+
+def test_weight_fold_then_quant_keeps_invariance_up_to_quant_error():
+    # Offline fold W~ = R^T W ("Weight Absorption ...", 1. Offline Weight
+    # Absorption), then per-output-channel INT4: the W4A4 product dequantized
+    # approximates XW; with no quantization (fp64 rotated operands) it is exact.
+    rng = np.random.default_rng(12)
+    d, k, b = 1024, 32, 8
+    x = rng.standard_normal((b, d))
+    wt = rng.standard_normal((k, d)) * 0.02         # W^T, one output channel per row
+    xa = oracle.fwht_quant(x, 5, oracle.SIGNS_FIRST, want_y=True)
+    wf = oracle.fwht_quant(wt, 5, oracle.SIGNS_FIRST, want_y=True)
+    exact = x @ wt.T
+    np.testing.assert_allclose(xa["y"] @ wf["y"].T, exact, atol=1e-12)
+    acc, y = oracle.w4a4_gemm(xa["q"], xa["scales"], wf["q"], wf["scales"], b, k, d)
+    rel = np.linalg.norm(y - exact) / np.linalg.norm(exact)
+    assert rel < 0.25  # INT4 x INT4 on Gaussian data: roughly 15% relative error
+
+
+# --------------------------------------------------------------------------
+# W4A4 GEMM
+# --------------------------------------------------------------------------
+
+def _unpack_py(byte_row, k):
+    """Independent pure-Python nibble decoding for the brute-force check."""
+    out = []
+    for b in byte_row:
+        for v in (int(b) & 0xF, int(b) >> 4):
+            out.append(v - 16 if v >= 8 else v)
+    return out[:k]
+
+
+def test_gemm_brute_force_tiny():
+    rng = np.random.default_rng(31)
+    M, N, K = 3, 5, 64
+    aq = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    wq = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.uniform(0.1, 2, M).astype(np.float32)
+    sw = rng.uniform(0.1, 2, N).astype(np.float32)
+    acc, y = oracle.w4a4_gemm(aq, sa, wq, sw, M, N, K)
+    for m in range(M):
+        a = _unpack_py(aq[m], K)
+        for n in range(N):
+            w = _unpack_py(wq[n], K)
+            s = sum(ai * wi for ai, wi in zip(a, w))
+            assert acc[m, n] == s
+            assert y[m, n] == s * float(sa[m]) * float(sw[n])
+
+
+def test_gemm_matches_numpy_integer_matmul_and_entries():
+    rng = np.random.default_rng(32)
+    M, N, K = 17, 9, 256
+    aq = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    wq = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.uniform(0.1, 2, M).astype(np.float32)
+    sw = rng.uniform(0.1, 2, N).astype(np.float32)
+    acc, y = oracle.w4a4_gemm(aq, sa, wq, sw, M, N, K)
+    a = np.array([_unpack_py(r, K) for r in aq], dtype=np.int64)
+    w = np.array([_unpack_py(r, K) for r in wq], dtype=np.int64)
+    np.testing.assert_array_equal(acc, a @ w.T)
+    ms = np.array([0, 16, 5, 3])
+    cs = np.array([8, 0, 4, 4])
+    e_acc, e_y = oracle.w4a4_gemm_entries(aq, sa, wq, sw, K, ms, cs)
+    np.testing.assert_array_equal(e_acc, acc[ms, cs])
+    np.testing.assert_array_equal(e_y, y[ms, cs])
+
+
+def test_gemm_extreme_codes_fit_int32():
+    K = 8192
+    for byte, code in ((0x77, 7), (0x88, -8)):
+        aq = np.full((1, K // 2), byte, np.uint8)
+        acc, _ = oracle.w4a4_gemm(aq, np.ones(1, np.float32), aq, np.ones(1, np.float32), 1, 1, K)
+        assert acc[0, 0] == code * code * K
+
+
+# --------------------------------------------------------------------------
+# KV cache write
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("flags", [0, oracle.SIGNS_FIRST])
+def test_kv_is_per_head_rotation_then_quant(flags):
+    rng = np.random.default_rng(41)
+    T, H, D = 5, 3, 128
+    k = rng.standard_normal((T, H, D))
+    v = rng.standard_normal((T, H, D)) * 3
+    out = oracle.kv_rotate_quant(k, v, 123, flags)
+    s = oracle.signs(123, D).astype(np.float64)
+    h = scipy.linalg.hadamard(D) / np.sqrt(D)
+    for src, q, sc in ((k, out["kq"], out["ks"]), (v, out["vq"], out["vs"])):
+        codes = oracle.unpack(q, D)
+        for t in range(T):
+            for hh in range(H):
+                ref = (src[t, hh] @ h) * s if flags == 0 else (src[t, hh] * s) @ h
+                scale = np.abs(ref).max() / 7
+                assert sc[t, hh] == np.float32(scale)
+                assert all(codes[t, hh, j] == _brute_force_code(ref[j] / scale)
+                           for j in range(0, D, 9))
