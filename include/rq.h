@@ -1,0 +1,186 @@
+/*
+ * rq.h -- C ABI of the rotation-based W4A4 inference kernels (GB300, sm_103a).
+ *
+ * Three operations make up the online hot path of rotation-based 4-bit
+ * inference:
+ *
+ *   rq_fwht_quant       randomized fast Walsh-Hadamard transform of each row,
+ *                       fused with per-row symmetric INT4 quantization and
+ *                       nibble packing;
+ *   rq_w4a4_gemm        the W4A4 linear layer: exact integer product of packed
+ *                       INT4 activations and packed INT4 (rotation-folded)
+ *                       weights, with a per-token x per-channel scale epilogue;
+ *   rq_kv_rotate_quant  head-wise Hadamard rotation and INT4 quantization of K
+ *                       and V before they are written to the cache.
+ *
+ * Sources (page title, then section / equation):
+ *   [ROT] "Rotational Quantization: How Orthogonal Transforms and Hadamard
+ *         Incoherence Enable Outlier-Free Low-Bit Inference" (llms.blog)
+ *   [QR]  aicassindra.com quantization series, "QuaRot" page
+ *   [SQ]  aicassindra.com quantization series, "SpinQuant" page
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Every data pointer is a DEVICE pointer (memory the current CUDA
+ *   device can read/write: cudaMalloc / PyTorch CUDA tensors / managed memory).
+ *   The caller owns all buffers.  The library allocates no device memory and
+ *   keeps no state between calls except one device-resident error word used by
+ *   bounded waits (see rq_sync_status).
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Calls only enqueue work and return; results are ready once the
+ *   stream reaches that point.  Calls on different streams may run concurrently
+ *   as long as their output buffers do not overlap.
+ * Alignment.  Every pointer must be 16-byte aligned and every row stride a
+ *   multiple of 16 bytes; otherwise RQ_ERR_MISALIGNED.
+ * Errors.  Arguments are checked on the host before anything is enqueued; a
+ *   failing check returns a non-zero rq_status and enqueues nothing.  A failed
+ *   kernel launch returns RQ_ERR_CUDA.  Nothing is ever printed or aborted.
+ * Rotation.  R is the randomized Hadamard rotation of [ROT] §Incoherence
+ *   Processing via Randomized Hadamard Transforms: H_n is the normalized
+ *   Sylvester matrix of the page's recursion H_1 = [1],
+ *   H_2k = (1/sqrt2)[[H_k, H_k], [H_k, -H_k]] (natural order, entries
+ *   +-1/sqrt(n)), and s in {-1,+1}^n is a Rademacher vector drawn from `seed`:
+ *   s_i = +1 when the top bit of output i (0-based) of SplitMix64 seeded with
+ *   `seed` is 0, else -1.  flags bit 0 (RQ_SIGNS_FIRST) selects the form:
+ *     RQ_SIGNS_FIRST set:   y = (x diag(s)) H_n     ("x·diag(±1)·H_n/√n")
+ *     RQ_SIGNS_FIRST clear: y = (x H_n) diag(s)     (R = H_d·diag(s), [ROT] eq.)
+ *   The two forms are transposes of each other; use the same flags for the
+ *   activations and for the offline weight fold.
+ * Quantization.  Per row (token, or (token, head)): scale = max_j |y_j| / 7,
+ *   q_j = clamp(round_half_even(y_j / scale), -8, 7); an all-zero row gets
+ *   scale 0 and all-zero codes.  The scale is stored as fp32.  The GPU decides
+ *   the rounding in fp32: a code may differ by one from an exact (fp64)
+ *   computation only where y_j/scale lies within about 1e-6 of a half-integer.
+ * Packing.  A row of n codes is n/2 bytes; byte j holds code 2j in bits 3..0
+ *   and code 2j+1 in bits 7..4, each a 4-bit two's-complement value.
+ */
+#ifndef RQ_H
+#define RQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RQ_OK = 0,
+    RQ_ERR_INVALID_ARG = 1, /* a size is negative/zero where not allowed, a required pointer is NULL */
+    RQ_ERR_UNSUPPORTED = 2, /* a size outside what the kernels implement (e.g. n not a power of two) */
+    RQ_ERR_MISALIGNED = 3,  /* a pointer or stride breaks the 16-byte rule */
+    RQ_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+    RQ_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see rq_sync_status) */
+} rq_status;
+
+typedef enum {
+    RQ_F32 = 0,  /* float */
+    RQ_BF16 = 1, /* bfloat16 */
+    RQ_F16 = 2,  /* IEEE half */
+    RQ_I32 = 3   /* int32 (GEMM raw accumulators only) */
+} rq_dtype;
+
+enum { RQ_SIGNS_FIRST = 1u };
+
+/* Smallest / largest supported Hadamard size (row length n, head_dim). */
+#define RQ_MIN_N 32
+#define RQ_MAX_N 8192
+
+/*
+ * rq_fwht_quant -- rotate each row by R and quantize it to packed INT4.
+ *
+ *   [ROT] §Weight Absorption and Online Fast Walsh-Hadamard Transforms,
+ *   2. Online FWHT (n log2 n additions/subtractions, one global 1/sqrt(n)
+ *   scale); [ROT] §Incoherence (R = H_d·diag(s)); [QR] §End-to-end flow
+ *   ("an online Hadamard transform rotates the activation ... The rotated
+ *   activation is quantized to INT4").  The same call performs the offline
+ *   weight fold W~ = R^T W of [ROT] §Weight Absorption, 1. when given the rows
+ *   of W^T (one output channel per row): each output channel is then quantized
+ *   with its own scale.
+ *
+ *   x        [rows][ld_x] elements of x_dtype (RQ_F32, RQ_BF16 or RQ_F16);
+ *            row r is x + r*ld_x, its first n elements are used.
+ *   rows     number of rows, >= 0 (0: nothing is enqueued).
+ *   n        row length, a power of two in [RQ_MIN_N, RQ_MAX_N].
+ *   ld_x     row stride in elements, >= n, ld_x * sizeof(x_dtype) % 16 == 0.
+ *   seed     sign-vector seed.
+ *   flags    RQ_SIGNS_FIRST or 0.
+ *   q        out: [rows][n/2] bytes, packed codes (row stride n/2).
+ *   scales   out: [rows] fp32 scales, max|y|/7 of each rotated row.
+ *   y        out, may be NULL: [rows][n] fp32 rotated rows y = xR (parity
+ *            checks only; writing it adds 4n bytes of traffic per row).
+ */
+rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n, int64_t ld_x,
+                        uint64_t seed, uint32_t flags, uint8_t *q, float *scales, float *y,
+                        void *stream);
+
+/*
+ * rq_w4a4_gemm -- y = dequant(Q(XR) · Q(R^T W)).
+ *
+ *   acc[m][c] = sum_k qa[m][k] * qw[c][k]   (exact, int32)
+ *   y[m][c]   = acc[m][c] * a_scales[m] * w_scales[c]   (fp32 math)
+ *   [ROT] §The Principle of Computational Invariance (Y = (XR)(R^T W));
+ *   [ROT] §Learned Orthogonal Rotations (the product Q(XR)·Q(R^T W));
+ *   [ROT] §Hardware Execution, 1. True INT4 Tensor Core Utilization;
+ *   [QR] §End-to-end flow.
+ *
+ *   a_q       [M][K/2] packed activation codes (row stride K/2), e.g. from
+ *             rq_fwht_quant on X.
+ *   a_scales  [M] per-token fp32 scales.
+ *   w_q       [N][K/2] packed weight codes, one output channel per row, e.g.
+ *             from rq_fwht_quant on the rows of W^T (the offline fold).
+ *   w_scales  [N] per-channel fp32 scales.
+ *   M, N, K   M >= 0, N >= 0 (0: nothing is enqueued), K a positive multiple
+ *             of 128 and at most 65536.
+ *   seed      accepted for a uniform signature and ignored: the rotation is
+ *             already folded into w_q.
+ *   flags     must be 0.
+ *   y         out: [M][N] row-major, of y_dtype:
+ *             RQ_F16  the dequantized product rounded to fp16;
+ *             RQ_F32  the dequantized product in fp32;
+ *             RQ_I32  the raw int32 accumulators (scales unused, may be NULL).
+ *             N * sizeof(y_dtype) must be a multiple of 16 bytes.
+ */
+rq_status rq_w4a4_gemm(const uint8_t *a_q, const float *a_scales, const uint8_t *w_q,
+                       const float *w_scales, int64_t M, int64_t N, int64_t K, uint64_t seed,
+                       uint32_t flags, void *y, rq_dtype y_dtype, void *stream);
+
+/*
+ * rq_kv_rotate_quant -- rotate each (token, head) vector of K and V by the
+ * randomized Hadamard of size head_dim and quantize it per (token, head).
+ *
+ *   [QR] §The architecture ("The KV-cache rotation box ... keys and values
+ *   stored per token are themselves rotated before being quantized") and
+ *   §End-to-end flow, "The KV cache"; [ROT] §Hardware Execution, 2. End-to-End
+ *   KV Cache Footprint Reduction.  One sign vector of length head_dim (from
+ *   `seed`) is shared by every head and by K and V.
+ *
+ *   k, v       [tokens][heads][head_dim] contiguous, of dtype (RQ_BF16, RQ_F16
+ *              or RQ_F32).  Either may be NULL, not both; a NULL input skips
+ *              its outputs (which may then be NULL too).
+ *   tokens     >= 0 (0: nothing is enqueued); heads >= 1.
+ *   head_dim   a power of two in [RQ_MIN_N, 256].
+ *   kq, vq     out: [tokens][heads][head_dim/2] packed codes.
+ *   ks, vs     out: [tokens][heads] fp32 scales.
+ */
+rq_status rq_kv_rotate_quant(const void *k, const void *v, rq_dtype dtype, int64_t tokens,
+                             int64_t heads, int64_t head_dim, uint64_t seed, uint32_t flags,
+                             uint8_t *kq, float *ks, uint8_t *vq, float *vs, void *stream);
+
+/*
+ * rq_sync_status -- wait for `stream` to drain, then report and clear the
+ * device error word that bounded waits set when they give up (RQ_ERR_TIMEOUT),
+ * or RQ_ERR_CUDA if the stream itself reports an error.  RQ_OK otherwise.
+ */
+rq_status rq_sync_status(void *stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *rq_status_string(rq_status status);
+
+/* Library ABI version: (major << 16) | minor. */
+uint32_t rq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RQ_H */

@@ -1,0 +1,28 @@
+"""Rotation-based W4A4 inference kernels for GB300 (sm_103a).
+
+The compute lives in ``librq.so`` (CUDA kernels behind the C ABI declared in
+``include/rq.h``).  This package only marshals arguments: tensors in, device
+pointers, sizes and the current CUDA stream out.  There is no fallback: if the
+library cannot be loaded, every call raises.
+
+Entry points (same names as the C ABI):
+
+* :func:`fwht_quant` -- randomized Hadamard rotation of each row + per-row INT4
+  quantization and nibble packing (also the offline weight fold when given W^T);
+* :func:`w4a4_gemm` -- exact INT4 x INT4 product with per-token x per-channel
+  dequant;
+* :func:`kv_rotate_quant` -- head-wise rotation + INT4 quantization of K and V.
+"""
+from ._binding import (  # noqa: F401
+    RQ_SIGNS_FIRST,
+    RQError,
+    fwht_quant,
+    kv_rotate_quant,
+    library_path,
+    load_library,
+    sync_status,
+    w4a4_gemm,
+)
+
+__all__ = ["RQ_SIGNS_FIRST", "RQError", "fwht_quant", "kv_rotate_quant", "library_path",
+           "load_library", "sync_status", "w4a4_gemm"]

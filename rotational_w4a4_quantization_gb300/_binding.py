@@ -1,0 +1,172 @@
+"""ctypes binding of librq.so: argument marshalling only.
+
+Each function checks that tensors live on the current CUDA device with the
+expected dtype and contiguity, then passes raw device pointers, sizes and the
+current stream to the C entry point of the same name.  All compute runs in the
+library's kernels; a non-OK status raises :class:`RQError`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "librq.so")
+
+RQ_SIGNS_FIRST = 1
+
+_STATUS = {0: "RQ_OK", 1: "RQ_ERR_INVALID_ARG", 2: "RQ_ERR_UNSUPPORTED", 3: "RQ_ERR_MISALIGNED",
+           4: "RQ_ERR_CUDA", 5: "RQ_ERR_TIMEOUT"}
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.int32: 3}
+
+_lib = None
+
+
+class RQError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {_STATUS.get(status, status)}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load librq.so (built by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"librq.so not found at {_LIB_PATH}: build it first "
+                          "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, i64, u64, u32, i32 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint32,
+                             ctypes.c_int)
+    lib.rq_fwht_quant.restype = i32
+    lib.rq_fwht_quant.argtypes = [P, i32, i64, i64, i64, u64, u32, P, P, P, P]
+    lib.rq_w4a4_gemm.restype = i32
+    lib.rq_w4a4_gemm.argtypes = [P, P, P, P, i64, i64, i64, u64, u32, P, i32, P]
+    lib.rq_kv_rotate_quant.restype = i32
+    lib.rq_kv_rotate_quant.argtypes = [P, P, i32, i64, i64, i64, u64, u32, P, P, P, P, P]
+    lib.rq_sync_status.restype = i32
+    lib.rq_sync_status.argtypes = [P]
+    lib.rq_status_string.restype = ctypes.c_char_p
+    lib.rq_status_string.argtypes = [i32]
+    lib.rq_version.restype = u32
+    lib.rq_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, st):
+    if st != 0:
+        raise RQError(fn, st)
+
+
+def _dev(*tensors):
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("tensors must be on one device")
+    return dev
+
+
+def fwht_quant(x: torch.Tensor, seed: int, flags: int = RQ_SIGNS_FIRST, *, q=None, scales=None,
+               y=None, want_y: bool = False, stream=None):
+    """Rotate each row of ``x`` (rows x n; row stride may exceed n) by the
+    randomized Hadamard R and quantize it to packed INT4.
+
+    Returns ``(q, scales)`` or ``(q, scales, y)`` when ``want_y``: q is
+    (rows x n/2) uint8, scales (rows,) fp32, y (rows x n) fp32 = x R."""
+    lib = load_library()
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit stride in the last dimension")
+    if x.dtype not in (torch.float32, torch.bfloat16, torch.float16):
+        raise ValueError("x must be float32, bfloat16 or float16")
+    rows, n = x.shape
+    if q is None:
+        q = torch.empty(rows, n // 2, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if want_y and y is None:
+        y = torch.empty(rows, n, dtype=torch.float32, device=x.device)
+    _dev(x, q, scales, y)
+    with torch.cuda.device(x.device):
+        st = lib.rq_fwht_quant(_ptr(x), _DTYPES[x.dtype], rows, n, x.stride(0), seed, flags,
+                               _ptr(q), _ptr(scales), _ptr(y), _stream(stream))
+    _check("rq_fwht_quant", st)
+    return (q, scales, y) if y is not None else (q, scales)
+
+
+def w4a4_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_dtype=torch.float16,
+              seed: int = 0, out=None, stream=None):
+    """y = dequant(Q(XR) . Q(R^T W)): a_q (M x K/2), w_q (N x K/2) packed codes,
+    a_scales (M,), w_scales (N,).  out_dtype float16 / float32, or int32 for the
+    raw accumulators."""
+    lib = load_library()
+    M, kb = a_q.shape
+    N, kb2 = w_q.shape
+    if kb != kb2 or a_q.dtype != torch.uint8 or w_q.dtype != torch.uint8:
+        raise ValueError("a_q and w_q must be uint8 with the same K/2 columns")
+    if not (a_q.is_contiguous() and w_q.is_contiguous()):
+        raise ValueError("packed operands must be contiguous")
+    K = 2 * kb
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
+    _dev(a_q, w_q, a_scales, w_scales, out)
+    with torch.cuda.device(a_q.device):
+        st = lib.rq_w4a4_gemm(_ptr(a_q), _ptr(a_scales), _ptr(w_q), _ptr(w_scales), M, N, K, seed, 0,
+                              _ptr(out), _DTYPES[out.dtype], _stream(stream))
+    _check("rq_w4a4_gemm", st)
+    return out
+
+
+def kv_rotate_quant(k, v, seed: int, flags: int = RQ_SIGNS_FIRST, *, out=None, stream=None):
+    """K, V ([tokens][heads][head_dim], contiguous; either may be None) ->
+    dict(kq, ks, vq, vs): packed codes [T][H][D/2] uint8 and scales [T][H] fp32."""
+    lib = load_library()
+    ref = k if k is not None else v
+    if ref is None:
+        raise ValueError("k and v cannot both be None")
+    T, H, D = ref.shape
+    for t in (k, v):
+        if t is not None and (t.shape != ref.shape or t.dtype != ref.dtype or not t.is_contiguous()):
+            raise ValueError("k and v must be contiguous with the same shape and dtype")
+    if out is None:
+        out = {}
+        if k is not None:
+            out["kq"] = torch.empty(T, H, D // 2, dtype=torch.uint8, device=ref.device)
+            out["ks"] = torch.empty(T, H, dtype=torch.float32, device=ref.device)
+        if v is not None:
+            out["vq"] = torch.empty(T, H, D // 2, dtype=torch.uint8, device=ref.device)
+            out["vs"] = torch.empty(T, H, dtype=torch.float32, device=ref.device)
+    _dev(k, v, *out.values())
+    with torch.cuda.device(ref.device):
+        st = lib.rq_kv_rotate_quant(_ptr(k), _ptr(v), _DTYPES[ref.dtype], T, H, D, seed, flags,
+                                    _ptr(out.get("kq")), _ptr(out.get("ks")), _ptr(out.get("vq")),
+                                    _ptr(out.get("vs")), _stream(stream))
+    _check("rq_kv_rotate_quant", st)
+    return out
+
+
+def sync_status(stream=None) -> int:
+    """Drain the stream and return the library's status word (0 = OK)."""
+    return int(load_library().rq_sync_status(_stream(stream)))

@@ -1,0 +1,150 @@
+// api.cu -- the C ABI (include/rq.h): host-side argument checks, dispatch to the
+// kernels, status codes.  Nothing here allocates device memory.
+#include "../../include/rq.h"
+#include "rq_internal.h"
+
+#include <cstdint>
+
+namespace rq {
+
+cudaError_t launch_w4a4_gemm_small(const GemmArgs &g, cudaStream_t stream);
+cudaError_t launch_w4a4_gemm_tc(const GemmArgs &g, cudaStream_t stream);
+bool w4a4_gemm_tc_supported(const GemmArgs &g);
+
+namespace {
+__device__ int g_error_word;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2(int64_t n) { return n > 0 && (n & (n - 1)) == 0; }
+int log2i(int64_t n) {
+    int l = 0;
+    while ((int64_t(1) << l) < n) ++l;
+    return l;
+}
+int elem_size(rq_dtype t) {
+    switch (t) {
+        case RQ_F32: return 4;
+        case RQ_BF16: return 2;
+        case RQ_F16: return 2;
+        case RQ_I32: return 4;
+    }
+    return 0;
+}
+bool is_rot_input(rq_dtype t) { return t == RQ_F32 || t == RQ_BF16 || t == RQ_F16; }
+}  // namespace
+
+int *error_word_device_ptr() {
+    int *p = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_error_word) != cudaSuccess) return nullptr;
+    return p;
+}
+
+cudaError_t read_and_clear_error_word(int *value, cudaStream_t stream) {
+    int *p = error_word_device_ptr();
+    if (!p) return cudaErrorUnknown;
+    cudaError_t e = cudaMemcpyAsync(value, p, sizeof(int), cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    if (*value != 0) {
+        const int zero = 0;
+        e = cudaMemcpyAsync(p, &zero, sizeof(int), cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return e;
+        e = cudaStreamSynchronize(stream);
+    }
+    return e;
+}
+
+cudaError_t launch_w4a4_gemm(const GemmArgs &g, cudaStream_t stream) {
+    if (w4a4_gemm_tc_supported(g)) return launch_w4a4_gemm_tc(g, stream);
+    return launch_w4a4_gemm_small(g, stream);
+}
+
+}  // namespace rq
+
+extern "C" {
+
+rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n, int64_t ld_x,
+                        uint64_t seed, uint32_t flags, uint8_t *q, float *scales, float *y,
+                        void *stream) {
+    if (rows < 0 || n <= 0) return RQ_ERR_INVALID_ARG;
+    if (!rq::is_rot_input(x_dtype)) return RQ_ERR_UNSUPPORTED;
+    if (!rq::pow2(n) || n < RQ_MIN_N || n > RQ_MAX_N) return RQ_ERR_UNSUPPORTED;
+    if (ld_x < n) return RQ_ERR_INVALID_ARG;
+    if (flags & ~uint32_t(RQ_SIGNS_FIRST)) return RQ_ERR_INVALID_ARG;
+    if (rows == 0) return RQ_OK;
+    if (!x || !q || !scales) return RQ_ERR_INVALID_ARG;
+    if (!rq::aligned16(x) || !rq::aligned16(q) || !rq::aligned16(scales) || (y && !rq::aligned16(y)))
+        return RQ_ERR_MISALIGNED;
+    if ((ld_x * rq::elem_size(x_dtype)) % 16 != 0) return RQ_ERR_MISALIGNED;
+    rq::RotJob job{x, ld_x, rows, q, scales, y};
+    cudaError_t e = rq::launch_fwht_quant(&job, 1, rq::log2i(n), (int)x_dtype, seed, flags,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+}
+
+rq_status rq_w4a4_gemm(const uint8_t *a_q, const float *a_scales, const uint8_t *w_q,
+                       const float *w_scales, int64_t M, int64_t N, int64_t K, uint64_t seed,
+                       uint32_t flags, void *y, rq_dtype y_dtype, void *stream) {
+    (void)seed;  // the rotation is already folded into w_q
+    if (M < 0 || N < 0 || K <= 0) return RQ_ERR_INVALID_ARG;
+    if (flags != 0) return RQ_ERR_INVALID_ARG;
+    if (K % 128 != 0 || K > 65536) return RQ_ERR_UNSUPPORTED;
+    if (y_dtype != RQ_F16 && y_dtype != RQ_F32 && y_dtype != RQ_I32) return RQ_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return RQ_OK;
+    const bool need_scales = y_dtype != RQ_I32;
+    if (!a_q || !w_q || !y || (need_scales && (!a_scales || !w_scales))) return RQ_ERR_INVALID_ARG;
+    if (!rq::aligned16(a_q) || !rq::aligned16(w_q) || !rq::aligned16(y)) return RQ_ERR_MISALIGNED;
+    if (need_scales && (!rq::aligned16(a_scales) || !rq::aligned16(w_scales))) return RQ_ERR_MISALIGNED;
+    if ((N * rq::elem_size(y_dtype)) % 16 != 0) return RQ_ERR_MISALIGNED;
+    rq::GemmArgs g{a_q, a_scales, w_q, w_scales, M, N, K, y,
+                   y_dtype == RQ_F16 ? 0 : (y_dtype == RQ_F32 ? 1 : 2)};
+    cudaError_t e = rq::launch_w4a4_gemm(g, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+}
+
+rq_status rq_kv_rotate_quant(const void *k, const void *v, rq_dtype dtype, int64_t tokens,
+                             int64_t heads, int64_t head_dim, uint64_t seed, uint32_t flags,
+                             uint8_t *kq, float *ks, uint8_t *vq, float *vs, void *stream) {
+    if (tokens < 0 || heads <= 0 || head_dim <= 0) return RQ_ERR_INVALID_ARG;
+    if (!k && !v) return RQ_ERR_INVALID_ARG;
+    if (!rq::is_rot_input(dtype)) return RQ_ERR_UNSUPPORTED;
+    if (!rq::pow2(head_dim) || head_dim < RQ_MIN_N || head_dim > 256) return RQ_ERR_UNSUPPORTED;
+    if (flags & ~uint32_t(RQ_SIGNS_FIRST)) return RQ_ERR_INVALID_ARG;
+    if (tokens == 0) return RQ_OK;
+    if ((k && (!kq || !ks)) || (v && (!vq || !vs))) return RQ_ERR_INVALID_ARG;
+    const void *ptrs[6] = {k, v, kq, ks, vq, vs};
+    for (const void *p : ptrs)
+        if (p && !rq::aligned16(p)) return RQ_ERR_MISALIGNED;
+    const int64_t rows = tokens * heads;
+    rq::RotJob jobs[2];
+    int nj = 0;
+    if (k) jobs[nj++] = rq::RotJob{k, head_dim, rows, kq, ks, nullptr};
+    if (v) jobs[nj++] = rq::RotJob{v, head_dim, rows, vq, vs, nullptr};
+    cudaError_t e = rq::launch_fwht_quant(jobs, nj, rq::log2i(head_dim), (int)dtype, seed, flags,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+}
+
+rq_status rq_sync_status(void *stream) {
+    int word = 0;
+    cudaError_t e = rq::read_and_clear_error_word(&word, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return RQ_ERR_CUDA;
+    return word != 0 ? RQ_ERR_TIMEOUT : RQ_OK;
+}
+
+const char *rq_status_string(rq_status s) {
+    switch (s) {
+        case RQ_OK: return "RQ_OK";
+        case RQ_ERR_INVALID_ARG: return "RQ_ERR_INVALID_ARG";
+        case RQ_ERR_UNSUPPORTED: return "RQ_ERR_UNSUPPORTED";
+        case RQ_ERR_MISALIGNED: return "RQ_ERR_MISALIGNED";
+        case RQ_ERR_CUDA: return "RQ_ERR_CUDA";
+        case RQ_ERR_TIMEOUT: return "RQ_ERR_TIMEOUT";
+    }
+    return "RQ_ERR_UNKNOWN";
+}
+
+uint32_t rq_version(void) { return (1u << 16) | 0u; }
+
+}  // extern "C"

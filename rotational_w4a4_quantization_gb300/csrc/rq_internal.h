@@ -1,0 +1,47 @@
+// rq_internal.h -- declarations shared by the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rq {
+
+// Element types of rotation inputs (values match rq_dtype).
+enum InType : int { IN_F32 = 0, IN_BF16 = 1, IN_F16 = 2 };
+
+// One rotation+quantization job: `rows` rows of `n` elements, row stride `ld`
+// elements, written to packed codes q (row stride n/2 bytes), fp32 scales and
+// optionally fp32 rotated rows y.
+struct RotJob {
+    const void *x;
+    int64_t ld;
+    int64_t rows;
+    uint8_t *q;
+    float *scales;
+    float *y;
+};
+
+// Launch the rotation+quant kernel over up to two jobs of the same n and dtype
+// (the KV path passes K and V as two jobs of one launch).
+cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_type,
+                              uint64_t seed, uint32_t flags, cudaStream_t stream);
+
+// y_mode: 0 = fp16 out, 1 = fp32 out, 2 = raw int32 accumulators.
+struct GemmArgs {
+    const uint8_t *a_q;
+    const float *a_scales;
+    const uint8_t *w_q;
+    const float *w_scales;
+    int64_t M, N, K;
+    void *y;
+    int y_mode;
+};
+
+cudaError_t launch_w4a4_gemm(const GemmArgs &args, cudaStream_t stream);
+
+// Device-resident error word set by bounded waits that gave up.
+cudaError_t read_and_clear_error_word(int *value, cudaStream_t stream);
+int *error_word_device_ptr();
+
+}  // namespace rq

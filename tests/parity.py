@@ -1,0 +1,72 @@
+"""Comparison helpers shared by the GPU parity tests (test infrastructure).
+
+Tolerances (stated by the acceptance criteria of the hot path):
+* rotated rows y: per-row relative error ||y - y_ref||_inf / ||y_ref||_inf <= 1e-5;
+* scales: relative 1e-5 (the scale is max|y|/7, so it inherits the FWHT bound);
+* INT4 codes: identical, except where the oracle's y/scale lies within 1e-4 of a
+  half-integer; there the two sides may round differently (the GPU decides in
+  fp32, the oracle in fp64) and a difference of exactly one is allowed and
+  counted;
+* GEMM: int32 accumulators bit-exact; fp32 dequantized output within 1e-5
+  relative; fp16 output within one fp16 ulp of the exact value.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+Y_RTOL = 1e-5
+SCALE_RTOL = 1e-5
+TIE_WINDOW = 1e-4
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+def to_dev(a, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def compare_codes(gpu_q: np.ndarray, ref_q: np.ndarray, ref_ratio: np.ndarray, n: int) -> int:
+    """Assert code parity; return the number of tie-window differences."""
+    g = oracle.unpack(gpu_q.reshape(-1, n // 2), n).astype(np.int16)
+    r = oracle.unpack(ref_q.reshape(-1, n // 2), n).astype(np.int16)
+    diff = g != r
+    if not diff.any():
+        return 0
+    tie = oracle.tie_mask(ref_ratio.reshape(-1, n), TIE_WINDOW)
+    bad = diff & ~(tie & (np.abs(g - r) == 1))
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        detail = [(int(i), int(j), int(g[i, j]), int(r[i, j]), float(ref_ratio.reshape(-1, n)[i, j]))
+                  for i, j in idx]
+        raise AssertionError(f"{int(bad.sum())} codes differ outside the tie window: {detail}")
+    return int(diff.sum())
+
+
+def compare_scales(gpu_s: np.ndarray, ref_s: np.ndarray):
+    np.testing.assert_allclose(gpu_s.reshape(-1), ref_s.reshape(-1), rtol=SCALE_RTOL, atol=0)
+
+
+def compare_rows(gpu_y: np.ndarray, ref_y: np.ndarray):
+    g = gpu_y.astype(np.float64).reshape(ref_y.shape)
+    num = np.abs(g - ref_y).max(axis=-1)
+    den = np.abs(ref_y).max(axis=-1)
+    rel = np.where(den > 0, num / np.where(den > 0, den, 1), num)
+    assert rel.max() <= Y_RTOL, f"rotated rows: max per-row relative error {rel.max():.3e}"
+    return float(rel.max())
+
+
+def compare_f16(gpu: np.ndarray, ref: np.ndarray):
+    """Within one fp16 ulp of the exact (fp64) value."""
+    g = gpu.astype(np.float64)
+    ref16 = ref.astype(np.float16)
+    ulp = np.spacing(np.abs(ref16)).astype(np.float64)
+    ok = np.abs(g - ref) <= ulp
+    # values beyond the fp16 range must saturate to inf with the right sign
+    big = np.abs(ref) > 65504
+    ok |= big & np.isinf(g) & (np.sign(g) == np.sign(ref))
+    assert ok.all(), f"{int((~ok).sum())} fp16 outputs off by more than one ulp"

@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol that
+include/rq.h declares, and rejects bad arguments before enqueuing anything
+(these calls never touch a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import rotational_w4a4_quantization_gb300 as rq
+from rotational_w4a4_quantization_gb300 import build as rq_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rq_build.build()
+    return rq.load_library()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "rq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(rq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"rq_fwht_quant", "rq_w4a4_gemm", "rq_kv_rotate_quant"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert lib.rq_status_string(0) == b"RQ_OK"
+    assert lib.rq_status_string(3) == b"RQ_ERR_MISALIGNED"
+    assert lib.rq_status_string(99) == b"RQ_ERR_UNKNOWN"
+    assert lib.rq_version() >> 16 == 1
+
+
+# Fake device addresses: validation must fail before anything dereferences them.
+A16 = ctypes.c_void_p(0x10000)
+A1 = ctypes.c_void_p(0x10001)
+NULL = None
+
+
+def fq(lib, x=A16, dtype=1, rows=4, n=128, ld=128, flags=1, q=A16, s=A16, y=NULL):
+    return lib.rq_fwht_quant(x, dtype, rows, n, ld, 7, flags, q, s, y, NULL)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(rows=-1), 1),
+    (dict(n=0), 1),
+    (dict(n=48, ld=48), 2),          # not a power of two
+    (dict(n=16, ld=16), 2),          # below the smallest size
+    (dict(n=16384, ld=16384), 2),    # above the largest size
+    (dict(ld=64), 1),                # stride shorter than the row
+    (dict(flags=2), 1),
+    (dict(dtype=3), 2),              # int32 input
+    (dict(x=NULL), 1),
+    (dict(q=NULL), 1),
+    (dict(x=A1), 3),
+    (dict(y=A1), 3),
+    (dict(ld=132), 3),               # 264-byte bf16 stride is not a multiple of 16
+    (dict(rows=0, x=NULL), 0),       # empty: nothing to do
+])
+def test_fwht_quant_argument_checks(lib, kw, expect):
+    assert fq(lib, **kw) == expect
+
+
+def gemm(lib, M=16, N=64, K=256, a=A16, w=A16, sa=A16, sw=A16, y=A16, ydt=2, flags=0):
+    return lib.rq_w4a4_gemm(a, sa, w, sw, M, N, K, 0, flags, y, ydt, NULL)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(M=-1), 1),
+    (dict(K=0), 1),
+    (dict(K=200), 2),                 # not a multiple of 128
+    (dict(K=131072), 2),
+    (dict(flags=1), 1),
+    (dict(ydt=1), 2),                 # bf16 output not offered
+    (dict(a=NULL), 1),
+    (dict(sa=NULL), 1),
+    (dict(w=A1), 3),
+    (dict(N=4), 3),                   # 8-byte fp16 rows are not 16-byte multiples
+    (dict(M=0, a=NULL), 0),
+])
+def test_gemm_argument_checks(lib, kw, expect):
+    assert gemm(lib, **kw) == expect
+
+
+def kv(lib, k=A16, v=A16, dtype=1, T=4, H=2, D=128, kq=A16, ks=A16, vq=A16, vs=A16):
+    return lib.rq_kv_rotate_quant(k, v, dtype, T, H, D, 1, 1, kq, ks, vq, vs, NULL)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(T=-1), 1),
+    (dict(H=0), 1),
+    (dict(k=NULL, v=NULL), 1),
+    (dict(D=96), 2),
+    (dict(D=512), 2),
+    (dict(kq=NULL), 1),
+    (dict(vs=A1), 3),
+    (dict(T=0), 0),
+])
+def test_kv_argument_checks(lib, kw, expect):
+    assert kv(lib, **kw) == expect
+
+
+def test_binding_raises_without_library(monkeypatch, tmp_path):
+    from rotational_w4a4_quantization_gb300 import _binding
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        _binding.load_library()

@@ -1,0 +1,136 @@
+"""GPU parity of rq_w4a4_gemm against the oracle.
+
+The GEMM is fed the oracle's (or seeded random) codes, so the comparison is of
+the product alone: int32 accumulators bit-exact, fp32 dequant within 1e-5
+relative, fp16 within one ulp.  Shapes cover decode-sized and prefill-sized M,
+ragged M / N, every output mode, extreme codes, and the full-size workloads
+(checked on sampled entries against the oracle and, over the whole output, on
+row and column sums that hold at any size).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rotational_w4a4_quantization_gb300 as rq
+from rotational_w4a4_quantization_gb300 import synth
+
+from parity import compare_f16, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _codes(M, N, K, seed):
+    aq, sa = synth.random_codes(M, K, seed)
+    wq, sw = synth.random_codes(N, K, seed + 1)
+    return aq, sa, wq, sw
+
+
+def _all_modes(aq, sa, wq, sw):
+    d = [t.to(DEV) for t in (aq, sa, wq, sw)]
+    return {dt: to_np(rq.w4a4_gemm(*d, out_dtype=dt)) for dt in (torch.int32, torch.float32, torch.float16)}
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 64, 128), (16, 64, 256), (17, 72, 384), (64, 1024, 1024), (100, 136, 512),
+    (128, 256, 256), (130, 264, 512), (256, 512, 1024), (300, 392, 640), (512, 1024, 2048),
+])
+def test_shapes_all_modes(M, N, K):
+    aq, sa, wq, sw = _codes(M, N, K, M * 7 + N)
+    out = _all_modes(aq, sa, wq, sw)
+    acc, y = oracle.w4a4_gemm(aq.numpy(), sa.numpy(), wq.numpy(), sw.numpy(), M, N, K)
+    np.testing.assert_array_equal(out[torch.int32].astype(np.int64), acc)
+    np.testing.assert_allclose(out[torch.float32], y, rtol=1e-5, atol=0)
+    compare_f16(out[torch.float16], y)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 64, 65536), (256, 256, 65536)])
+@pytest.mark.parametrize("ba,bw", [(0x77, 0x77), (0x88, 0x88), (0x88, 0x77), (0x78, 0x87)])
+def test_extreme_codes_at_max_k(M, N, K, ba, bw):
+    aq = synth.extreme_codes(M, K, ba)
+    wq = synth.extreme_codes(N, K, bw)
+    one_m, one_n = torch.ones(M), torch.ones(N)
+    acc = to_np(rq.w4a4_gemm(aq.to(DEV), one_m.to(DEV), wq.to(DEV), one_n.to(DEV), out_dtype=torch.int32))
+    ref, _ = oracle.w4a4_gemm(aq[:1].numpy(), one_m[:1].numpy(), wq[:1].numpy(), one_n[:1].numpy(), 1, 1, K)
+    assert (acc.astype(np.int64) == ref[0, 0]).all()
+
+
+def test_large_then_small_partial_sums():
+    # Accumulation order hazard: a huge partial sum followed by +-1 products.
+    M, N, K = 128, 128, 16384
+    a = np.zeros((M, K), np.int8)
+    w = np.zeros((N, K), np.int8)
+    a[:, : K // 2] = 7
+    w[:, : K // 2] = 7
+    rng = np.random.default_rng(0)
+    a[:, K // 2:] = rng.choice([-1, 1], size=(M, K // 2))
+    w[:, K // 2:] = rng.choice([-1, 1], size=(N, K // 2))
+    aq, wq = oracle.pack(a), oracle.pack(w)
+    ones_m, ones_n = np.ones(M, np.float32), np.ones(N, np.float32)
+    acc = to_np(rq.w4a4_gemm(to_dev(aq), to_dev(ones_m), to_dev(wq), to_dev(ones_n), out_dtype=torch.int32))
+    ref, _ = oracle.w4a4_gemm(aq, ones_m, wq, ones_n, M, N, K)
+    np.testing.assert_array_equal(acc.astype(np.int64), ref)
+
+
+def test_pipeline_codes_from_oracle_fold():
+    # X rotated+quantized and W^T folded+quantized by the oracle, product on the GPU.
+    w = synth.TINY
+    x = synth.activations(w.rows, w.n, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor)
+    wt = synth.weights_t(w.gemm_n, w.n, w.weight_seed, w.w_std)
+    xa = oracle.fwht_quant(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+    wf = oracle.fwht_quant(wt.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+    out = _all_modes(torch.from_numpy(xa["q"]), torch.from_numpy(xa["scales"]),
+                     torch.from_numpy(wf["q"]), torch.from_numpy(wf["scales"]))
+    acc, y = oracle.w4a4_gemm(xa["q"], xa["scales"], wf["q"], wf["scales"], w.rows, w.gemm_n, w.n)
+    np.testing.assert_array_equal(out[torch.int32].astype(np.int64), acc)
+    np.testing.assert_allclose(out[torch.float32], y, rtol=1e-5, atol=0)
+    compare_f16(out[torch.float16], y)
+
+
+def _sample_positions(M, N, count, seed):
+    rng = np.random.default_rng(seed)
+    ms = list(rng.integers(0, M, count)) + [0, M - 1, 0, M - 1, min(127, M - 1), min(128, M - 1)]
+    cs = list(rng.integers(0, N, count)) + [0, N - 1, N - 1, 0, min(255, N - 1), min(256, N - 1)]
+    return np.array(ms, np.int64), np.array(cs, np.int64)
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "large"])
+def test_workload_full_size(name):
+    w = synth.WORKLOADS[name]
+    M, N, K = w.rows, w.gemm_n, w.n
+    aq, sa, wq, sw = _codes(M, N, K, 1000 + w.data_seed)
+    d = [t.to(DEV) for t in (aq, sa, wq, sw)]
+    acc = rq.w4a4_gemm(*d, out_dtype=torch.int32)
+    yf = to_np(rq.w4a4_gemm(*d, out_dtype=torch.float32))
+    yh = to_np(rq.w4a4_gemm(*d, out_dtype=torch.float16))
+    ms, cs = _sample_positions(M, N, 2000, w.data_seed)
+    r_acc, r_y = oracle.w4a4_gemm_entries(aq.numpy(), sa.numpy(), wq.numpy(), sw.numpy(), K, ms, cs)
+    acc_np = to_np(acc).astype(np.int64)
+    np.testing.assert_array_equal(acc_np[ms, cs], r_acc)
+    np.testing.assert_allclose(yf[ms, cs], r_y, rtol=1e-5, atol=0)
+    compare_f16(yh[ms, cs], r_y)
+    # Whole-output properties: sum_c acc[m,c] = a_m . (sum_c w_c) and
+    # sum_m acc[m,c] = (sum_m a_m) . w_c, from the oracle's code decoding.
+    a = oracle.unpack(aq.numpy(), K)
+    wc = oracle.unpack(wq.numpy(), K)
+    a_sum = a.sum(axis=0, dtype=np.int64)
+    w_sum = wc.sum(axis=0, dtype=np.int64)
+    row_ref = np.concatenate([a[i:i + 512].astype(np.int64) @ w_sum for i in range(0, M, 512)])
+    col_ref = np.concatenate([wc[i:i + 512].astype(np.int64) @ a_sum for i in range(0, N, 512)])
+    np.testing.assert_array_equal(acc_np.sum(axis=1), row_ref)
+    np.testing.assert_array_equal(acc_np.sum(axis=0), col_ref)
+
+
+def test_repeatable_bitwise():
+    aq, sa, wq, sw = _codes(512, 1024, 4096, 3)
+    d = [t.to(DEV) for t in (aq, sa, wq, sw)]
+    r1 = rq.w4a4_gemm(*d, out_dtype=torch.float16)
+    r2 = rq.w4a4_gemm(*d, out_dtype=torch.float16)
+    assert torch.equal(r1, r2)
