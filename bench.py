@@ -1,0 +1,464 @@
+"""Benchmark of the rotation-based W4A4 hot path on GB300.
+
+One step = one pass of the whole online path over one batch of synthetic input:
+  1. rq_fwht_quant      X (tokens x hidden, bf16) -> packed INT4 codes + scales
+  2. rq_w4a4_gemm       codes x folded INT4 weights -> Y (tokens x out, fp16)
+  3. rq_kv_rotate_quant K, V ([tokens][heads][head_dim] bf16) -> packed INT4 cache
+The weights are folded and quantized once, before timing (the offline step).
+
+Default workload: "prefill" -- X 2048 x 4096 bf16 (0.1% outlier channels x100),
+GEMM 2048 x 4096 -> 14336, plus the KV write of 8192 tokens x 32 heads x 128.
+
+Output: one JSON line.  `value` is the W4A4 layer's integer-op throughput over
+the whole step (2*M*N*K per step / step time, TOPS); the per-kernel figures
+(GB/s of the rotation kernels, TOPS of the GEMM, roofline fractions) are in
+`kernels`.  L2 is flushed (a 2x-L2 buffer is written) between timed steps,
+outside the timed events.
+
+`--impl reference` times the CPU oracle instead (on a bounded sample of each
+step's work, scaled to the same unit); it is the reference arm of this repo.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own batch (the path
+shards by rows with no exchange), timing is the max over ranks and `value` the
+sum of the ranks' work over that time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from rotational_w4a4_quantization_gb300 import synth  # noqa: E402
+
+METRIC = "FWHT+INT4-quant GB/s; W4A4 GEMM TOPS; % of HBM / dense-INT8 roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 4.5 / 2.25   # nominal dense ratio (fp8 / bf16) on GB300
+SLEEP_CYCLES = 400_000       # ~0.2 ms GPU-side pause between timed steps
+
+
+# --------------------------------------------------------------------------
+# work accounting (algorithmic bytes / ops)
+# --------------------------------------------------------------------------
+
+def fwht_bytes(rows, n, in_bytes=2):
+    return rows * (n * in_bytes + n // 2 + 4)
+
+
+def gemm_ops(M, N, K):
+    return 2 * M * N * K
+
+
+def gemm_bytes(M, N, K, out_bytes=2):
+    return M * K // 2 + N * K // 2 + 4 * M + 4 * N + out_bytes * M * N
+
+
+def kv_bytes(T, H, D, in_bytes=2):
+    return 2 * T * H * (D * in_bytes + D // 2 + 4)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------
+# distributed helpers (weak scaling, no data-path collective)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_units: float, local_seconds: float, group=None):
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time.  Returns (total_units, max_seconds)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_units, local_seconds
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(u.item()), float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+
+def gpu_selector(dev, local):
+    """nvidia-smi -i argument for this device (its UUID when torch exposes it)."""
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    if uuid:
+        u = str(uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    return str(local)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="rq_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------
+
+def make_inputs(work, kvw, dev):
+    x = synth.activations(work.rows, work.n, work.x_dtype, work.data_seed, work.n_outliers,
+                          work.outlier_factor)
+    wt = synth.weights_t(work.gemm_n, work.n, work.weight_seed, work.w_std)
+    k, v = synth.kv_pair(kvw.kv_tokens, kvw.kv_heads, kvw.kv_head_dim, kvw.data_seed,
+                         kvw.kv_outliers_per_head, kvw.kv_outlier_factor)
+    return x, wt, k, v
+
+
+def run_gpu(args, work, kvw):
+    import rotational_w4a4_quantization_gb300 as rq
+    import __graft_entry__
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        __graft_entry__.build()
+    barrier()
+    rq.load_library()
+
+    seed, flags = synth.SIGN_SEED, rq.RQ_SIGNS_FIRST
+    M, K, N = work.rows, work.n, work.gemm_n
+    T, H, D = kvw.kv_tokens, kvw.kv_heads, kvw.kv_head_dim
+    x_cpu, wt_cpu, k_cpu, v_cpu = make_inputs(work, kvw, dev)
+    x, k, v = x_cpu.to(dev), k_cpu.to(dev), v_cpu.to(dev)
+
+    # offline fold + weight quantization (not timed)
+    wq, ws = rq.fwht_quant(wt_cpu.to(dev), seed, flags)
+    del wt_cpu
+
+    # preallocated outputs
+    aq = torch.empty(M, K // 2, dtype=torch.uint8, device=dev)
+    as_ = torch.empty(M, dtype=torch.float32, device=dev)
+    y = torch.empty(M, N, dtype=torch.float16, device=dev)
+    kv_out = {"kq": torch.empty(T, H, D // 2, dtype=torch.uint8, device=dev),
+              "ks": torch.empty(T, H, dtype=torch.float32, device=dev),
+              "vq": torch.empty(T, H, D // 2, dtype=torch.uint8, device=dev),
+              "vs": torch.empty(T, H, dtype=torch.float32, device=dev)}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        rq.fwht_quant(x, seed, flags, q=aq, scales=as_)
+        if ev:
+            ev[1].record(stream)
+        rq.w4a4_gemm(aq, as_, wq, ws, out=y)
+        if ev:
+            ev[2].record(stream)
+        rq.kv_rotate_quant(k, v, seed, flags, out=kv_out)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    assert rq.sync_status() == 0
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_selector(dev, local)) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            # keep the GPU busy while the host enqueues the step, so the step's
+            # events measure kernels, not host launch latency (outside the events)
+            torch.cuda._sleep(SLEEP_CYCLES)
+            step(events[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier()
+    clocks = clk.summary()
+
+    per = {"fwht": [], "gemm": [], "kv": [], "step": []}
+    for ev in events:
+        per["fwht"].append(ev[0].elapsed_time(ev[1]) / 1e3)
+        per["gemm"].append(ev[1].elapsed_time(ev[2]) / 1e3)
+        per["kv"].append(ev[2].elapsed_time(ev[3]) / 1e3)
+        per["step"].append(ev[0].elapsed_time(ev[3]) / 1e3)
+    step_s = sum(per["step"])
+    ops_step = gemm_ops(M, N, K)
+    total_ops, max_s = aggregate(ops_step * args.steps, step_s)
+
+    # end to end through the public API: host inputs in, host results out
+    x_h = x_cpu.pin_memory()
+    k_h, v_h = k_cpu.pin_memory(), v_cpu.pin_memory()
+    y_h = torch.empty(M, N, dtype=torch.float16).pin_memory()
+    kvh = {key: torch.empty(t.shape, dtype=t.dtype).pin_memory() for key, t in kv_out.items()}
+    h2d = x_h.numel() * x_h.element_size() + 2 * k_h.numel() * k_h.element_size()
+    d2h = y_h.numel() * 2 + sum(t.numel() * t.element_size() for t in kvh.values())
+
+    def e2e_step():
+        x.copy_(x_h, non_blocking=True)
+        k.copy_(k_h, non_blocking=True)
+        v.copy_(v_h, non_blocking=True)
+        step()
+        y_h.copy_(y, non_blocking=True)
+        for key in kvh:
+            kvh[key].copy_(kv_out[key], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    e2e_ops, e2e_max = aggregate(ops_step * args.steps, e2e_s)
+    assert rq.sync_status() == 0
+
+    if rank != 0:
+        return None
+
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    avg = {key: sum(vals) / len(vals) for key, vals in per.items()}
+    fb = fwht_bytes(M, K)
+    gb_ops = gemm_ops(M, N, K)
+    kb = kv_bytes(T, H, D)
+    kernels = {
+        "fwht_quant": {"us": avg["fwht"] * 1e6, "GB/s": fb / avg["fwht"] / 1e9,
+                       "frac_hbm": fb / avg["fwht"] / 1e9 / peaks["hbm_gbs"], "bytes": fb},
+        "w4a4_gemm": {"us": avg["gemm"] * 1e6, "TOPS": gb_ops / avg["gemm"] / 1e12,
+                      "frac_fp8_tensor": gb_ops / avg["gemm"] / 1e12 / fp8_peak, "ops": gb_ops,
+                      "GB/s": gemm_bytes(M, N, K) / avg["gemm"] / 1e9},
+        "kv_rotate_quant": {"us": avg["kv"] * 1e6, "GB/s": kb / avg["kv"] / 1e9,
+                            "frac_hbm": kb / avg["kv"] / 1e9 / peaks["hbm_gbs"], "bytes": kb},
+    }
+    # dominant kernel by time
+    dom = max(("fwht", "gemm", "kv"), key=lambda key: avg[key])
+    if dom == "gemm":
+        ach = gb_ops / avg["gemm"] / 1e12
+        roof = {"kernel": "w4a4_gemm", "bound": "tensor", "achieved": ach, "peak": fp8_peak,
+                "unit": "TFLOP/s", "frac": ach / fp8_peak, "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (fp8 dense ratio)"}
+    else:
+        key = "fwht_quant" if dom == "fwht" else "kv_rotate_quant"
+        b = fb if dom == "fwht" else kb
+        ach = b / avg[dom] / 1e9
+        roof = {"kernel": key, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": f"{peaks['source']} hbm copy"}
+
+    line = {
+        "metric": METRIC,
+        "value": total_ops / max_s / 1e12,
+        "unit": "TOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": max_s / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int4",
+        "data": "synthetic",
+        "config": {"workload": f"{work.name}: X {M}x{K} bf16 -> fwht+int4 -> W4A4 GEMM {M}x{K}x{N} fp16; "
+                               f"kv {T}x{H}x{D} bf16 K,V",
+                   "l2": "flushed between timed steps (2x L2 write, outside timed events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "kernels": kernels,
+        "roofline": roof,
+        "e2e": {"value": e2e_ops / e2e_max / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_loop": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(work, kvw, budget_s=args.cpu_budget)
+    return line
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle as baseline / reference arm
+# --------------------------------------------------------------------------
+
+def _oracle_sample(work, kvw, gemm_rows, fwht_rows, kv_tokens):
+    """Time the oracle on a bounded sample of one step; return seconds for the
+    whole step extrapolated by rows (every part is linear in rows)."""
+    import oracle
+    oracle.build()
+    seed, flags = synth.SIGN_SEED, 1
+    M, K, N = work.rows, work.n, work.gemm_n
+    x = synth.activations(fwht_rows, K, work.x_dtype, work.data_seed, work.n_outliers,
+                          work.outlier_factor).double().numpy()
+    t0 = time.perf_counter()
+    oracle.fwht_quant(x, seed, flags)
+    t_fwht = (time.perf_counter() - t0) * (M / fwht_rows)
+    aq, sa = synth.random_codes(gemm_rows, K, 1)
+    wq, sw = synth.random_codes(N, K, 2)
+    t0 = time.perf_counter()
+    oracle.w4a4_gemm(aq.numpy(), sa.numpy(), wq.numpy(), sw.numpy(), gemm_rows, N, K)
+    t_gemm = (time.perf_counter() - t0) * (M / gemm_rows)
+    kk, vv = synth.kv_pair(kv_tokens, kvw.kv_heads, kvw.kv_head_dim, kvw.data_seed)
+    kk, vv = kk.double().numpy(), vv.double().numpy()
+    t0 = time.perf_counter()
+    oracle.kv_rotate_quant(kk, vv, seed, flags)
+    t_kv = (time.perf_counter() - t0) * (kvw.kv_tokens / kv_tokens)
+    return t_fwht + t_gemm + t_kv, {"fwht_s": t_fwht, "gemm_s": t_gemm, "kv_s": t_kv}
+
+
+def cpu_baseline(work, kvw, budget_s=15.0):
+    # sample sizes: about budget_s of single-core work in total
+    gemm_rows = max(1, int(budget_s * 0.5e9 / (work.gemm_n * work.n)))
+    step_s, parts = _oracle_sample(work, kvw, gemm_rows=gemm_rows, fwht_rows=64, kv_tokens=256)
+    ops = gemm_ops(work.rows, work.gemm_n, work.n)
+    return {"value": ops / step_s / 1e12, "unit": "TOPS", "cores": 1, "kind": "oracle",
+            "sample": f"oracle (fp64 C, 1 thread) on {gemm_rows} GEMM rows, 64 rotation rows, "
+                      f"256 KV tokens; scaled by rows to one full step",
+            "step_seconds_extrapolated": step_s, "parts_s": parts}
+
+
+def run_reference(args, work, kvw):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    gemm_rows = 2
+    for _ in range(args.warmup):
+        _oracle_sample(work, kvw, gemm_rows, 16, 64)
+    total = 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s, _parts = _oracle_sample(work, kvw, gemm_rows, 16, 64)
+        total += s
+    wall = time.perf_counter() - t0
+    ops = gemm_ops(work.rows, work.gemm_n, work.n)
+    value = ops * args.steps / total / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": wall / args.steps * 1e3,          # measured: one sampled step
+        "full_step_ms_extrapolated": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4",
+        "data": "synthetic",
+        "config": {"workload": f"{work.name}: X {work.rows}x{work.n} -> W4A4 GEMM "
+                               f"{work.rows}x{work.n}x{work.gemm_n}; kv {kvw.kv_tokens}x{kvw.kv_heads}x{kvw.kv_head_dim}"},
+        "cpu_baseline": {"value": value, "unit": "TOPS", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: {gemm_rows} GEMM rows, 16 rotation rows, 64 KV tokens, "
+                                   "scaled by rows to one full step"},
+        "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["rq", "reference"], default="rq")
+    ap.add_argument("--workload", choices=["prefill", "large", "decode", "tiny"], default="prefill")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    work = synth.WORKLOADS[args.workload]
+    kvw = synth.KV
+    line = run_reference(args, work, kvw) if args.impl == "reference" else run_gpu(args, work, kvw)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
