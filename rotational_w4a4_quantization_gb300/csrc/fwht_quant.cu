@@ -20,19 +20,27 @@
 //    (C = L-3 bits).  Each thread owns 16 chunks (128 elements) of one row in
 //    registers; P = 2^(C-4) threads share a row (1 for n <= 128, 32 for n = 4096,
 //    64 for n = 8192).
-//  * Phase 1: the thread loads its chunks with 128-bit loads (chunk bits 0,1 on
-//    lanes, so four lanes read 64 contiguous bytes), flips signs, and runs the
-//    butterflies of every bit it holds (e bits and 4 chunk bits) in registers,
-//    two at a time with the packed f32x2 add/sub; one or two further bits for
-//    n >= 4096 are exchanged with warp shuffles.
+//  * Loads never stall the butterflies: every warp copies its NEXT group of rows
+//    into a private shared-memory buffer with cp.async while it computes the
+//    current one.  The buffer is laid out lane-major per 16-byte granule, so the
+//    phase-1 reads (one 128-bit load per chunk) are bank-conflict free.
+//  * Values live as fp32 pairs in 64-bit registers for the whole transform, so
+//    every butterfly stage except the one inside a pair runs two lanes at a time
+//    with the packed add/sub.f32x2; the in-pair stage is fused with the bf16
+//    unpack (mixed-precision add/sub.f32.bf16 on the two halves of a word).
+//  * Phase 1: the thread reads its chunks (chunk bits 0,1 on lanes, so four
+//    lanes fetch 64 contiguous bytes from HBM), flips signs, and runs the
+//    butterflies of every bit it holds (e bits and 4 chunk bits) in registers;
+//    one or two further bits for n >= 4096 are exchanged with warp shuffles.
 //  * The row goes through shared memory once, as fp32 (XOR-swizzled 16-byte
 //    granules: conflict-free for n >= 1024), into the phase-2 layout, where the
 //    thread holds the remaining bits plus chunk bits 0 and 1, i.e. four runs
 //    of 32 consecutive elements.
 //  * Phase 2: remaining butterflies, row absmax (registers, shuffles, and a
 //    shared-memory exchange when a row spans two warps), codes by one fused
-//    multiply-add against a 1.5*2^23 bias (round-half-even to an integer whose
-//    low bits are the two's-complement code), packing with byte permutes, and
+//    multiply-add against a 1.5*2^23 bias, two values per f32x2 FMA
+//    (round-half-even to an integer whose low bits are the two's-complement
+//    code), packing with byte permutes, and
 //    16-byte stores of 32 codes each, coalesced across the warp.
 //  * CTAs are persistent: each computes the sign masks of its n positions once
 //    (SplitMix64, one call per element) into shared memory and then walks
@@ -54,20 +62,23 @@ constexpr int kThreads = 128;
 // --------------------------------------------------------------------------
 template <int C>
 struct Plan {
-    static constexpr int S = C <= 4 ? C : 4;
+    // slot bits per thread: the whole row for n <= 64, half a row for n = 128
+    // (two threads per row: a lighter register footprint, so more warps hide
+    // the butterflies' latencies), 16 chunks beyond that
+    static constexpr int S = C <= 3 ? C : (C == 4 ? 3 : 4);
     static constexpr int T = C - S;
     static constexpr int P = 1 << T;
     static constexpr int NSLOT = 1 << S;
     static constexpr int E = 8 * NSLOT;
     static constexpr int ROWS = kThreads / P;
-    static constexpr bool kTwoPhase = T > 0;
+    static constexpr bool kTwoPhase = C >= 5;
 
     static constexpr int a(int k) {
         return C <= 4 ? k : (C == 5 ? k + 1 : k + 2);
     }
     static constexpr int ta(int k) {
-        // C=5: {0}; C=6: {0,1}; C>=7: {0,1,6,7,...}
-        return k < 2 ? k : k + 4;
+        // C=4: {3}; C=5: {0}; C=6: {0,1}; C>=7: {0,1,6,7,...}
+        return C == 4 ? 3 : (k < 2 ? k : k + 4);
     }
     static constexpr int b(int k) {
         if (C <= 4) return k;
@@ -78,8 +89,9 @@ struct Plan {
         if (C <= 6) return 4 + k;               // {4} / {4,5}
         return 2 + k;                           // {2,...}
     }
-    static constexpr int kNumShuf = C >= 9 ? C - 8 : 0;
-    static constexpr int shuf(int j) { return 2 + j; }   // row-thread bits 2 (and 3)
+    static constexpr int kNumShuf = C >= 9 ? C - 8 : (C == 4 ? 1 : 0);
+    // row-thread bits exchanged by shuffles: bit 0 for n = 128, bits 2 (and 3) for n >= 4096
+    static constexpr int shuf(int j) { return C == 4 ? 0 : 2 + j; }
 
     static constexpr bool chunk_bit_done_in_phase1(int cb) {
         for (int k = 0; k < S; ++k)
@@ -98,59 +110,77 @@ __device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t i) {
     return z ^ (z >> 31);
 }
 
-// (a0,a1),(b0,b1) -> (a0+b0, a1+b1), (a0-b0, a1-b1) with packed fp32x2 ops.
-__device__ __forceinline__ void bfly2(float &a0, float &a1, float &b0, float &b1) {
-    asm("{\n\t.reg .b64 A, B, S, D;\n\t"
-        "mov.b64 A, {%0, %1};\n\t"
-        "mov.b64 B, {%2, %3};\n\t"
-        "add.rn.f32x2 S, A, B;\n\t"
-        "sub.rn.f32x2 D, A, B;\n\t"
-        "mov.b64 {%0, %1}, S;\n\t"
-        "mov.b64 {%2, %3}, D;\n\t}"
-        : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
+// ---- fp32 pairs in 64-bit registers (low word = even element) ----
+using pair_t = unsigned long long;
+
+__device__ __forceinline__ pair_t add2(pair_t a, pair_t b) {
+    pair_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ pair_t sub2(pair_t a, pair_t b) {
+    pair_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ pair_t fma2(pair_t a, pair_t b, pair_t c) {
+    pair_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ pair_t mk2(float lo, float hi) {
+    pair_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float lo2(pair_t p) { return __uint_as_float((uint32_t)p); }
+__device__ __forceinline__ float hi2(pair_t p) { return __uint_as_float((uint32_t)(p >> 32)); }
+// butterfly inside a pair: (x, y) -> (x + y, x - y)
+__device__ __forceinline__ pair_t bfly_in(pair_t p) {
+    pair_t r;
+    asm("{\n\t.reg .f32 x, y, s, d;\n\t"
+        "mov.b64 {x, y}, %1;\n\t"
+        "add.rn.f32 s, x, y;\n\t"
+        "sub.rn.f32 d, x, y;\n\t"
+        "mov.b64 %0, {s, d};\n\t}"
+        : "=l"(r) : "l"(p));
+    return r;
+}
+// bf16x2 word (x0 low, x1 high) -> (x0 + x1, x0 - x1) in fp32, the first
+// butterfly stage fused with the widening.
+__device__ __forceinline__ pair_t bf16w_bfly(uint32_t w) {
+    pair_t r;
+    asm("{\n\t.reg .b16 l, h;\n\t.reg .f32 x1, s, d;\n\t"
+        "mov.b32 {l, h}, %1;\n\t"
+        "and.b32 x1, %1, 0xffff0000;\n\t"
+        "add.rn.f32.bf16 s, l, x1;\n\t"
+        "sub.rn.f32.bf16 d, l, x1;\n\t"
+        "mov.b64 %0, {s, d};\n\t}"
+        : "=l"(r) : "r"(w));
+    return r;
 }
 
-// (v0,v1) <- (v0,v1)*(m,m) + (p0,p1)
-__device__ __forceinline__ void fma2_scalar(float &v0, float &v1, float m, float p0, float p1) {
-    asm("{\n\t.reg .b64 V, M, Q;\n\t"
-        "mov.b64 V, {%0, %1};\n\t"
-        "mov.b64 M, {%2, %2};\n\t"
-        "mov.b64 Q, {%3, %4};\n\t"
-        "fma.rn.f32x2 V, V, M, Q;\n\t"
-        "mov.b64 {%0, %1}, V;\n\t}"
-        : "+f"(v0), "+f"(v1)
-        : "f"(m), "f"(p0), "f"(p1));
-}
-
-// Butterflies over register-index bit `rb` of v[E] (E elements, 8 per chunk slot).
-template <int E>
-__device__ __forceinline__ void butterfly_reg_bit(float (&v)[E], int rb) {
-    if (rb == 0) {
+// Butterflies over register-element bit rb >= 1 of v (pairs pi and pi ^ 2^(rb-1)).
+template <int NP>
+__device__ __forceinline__ void butterfly_pairs(pair_t (&v)[NP], int rb) {
+    const int st = 1 << (rb - 1);
 #pragma unroll
-        for (int r = 0; r < E; r += 2) {
-            const float a = v[r], b = v[r + 1];
-            v[r] = a + b;
-            v[r + 1] = a - b;
-        }
-    } else {
-        const int st = 1 << rb;
-#pragma unroll
-        for (int r = 0; r < E; r += 2) {
-            if (!(r & st)) bfly2(v[r], v[r + 1], v[r + st], v[r + st + 1]);
+    for (int i = 0; i < NP; ++i) {
+        if (!(i & st)) {
+            const pair_t a = v[i], b = v[i + st];
+            v[i] = add2(a, b);
+            v[i + st] = sub2(a, b);
         }
     }
 }
 
-// Unpack one 16-byte chunk (8 elements) of bf16/f16 with sign masks m (bit 15 /
-// bit 31 of each word flip element 2k / 2k+1), or 2x16 bytes of fp32.
+// One chunk (8 elements, 4 pairs) from its raw granule(s): signs (bit 15 / bit 31
+// of mask word k flip element 2k / 2k+1), widening, and the in-pair butterfly.
 template <int IN>
-__device__ __forceinline__ void load_chunk(const void *row, int c, uint4 m, bool use_sign,
-                                           float *out) {
+__device__ __forceinline__ void convert_chunk(const uint4 *g, uint4 m, bool use_sign, pair_t *out) {
+    const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
     if constexpr (IN == IN_F32) {
-        const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const float *>(row) + 8 * c);
-        uint4 lo = __ldg(p), hi = __ldg(p + 1);
-        uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
+        const uint32_t w[8] = {g[0].x, g[0].y, g[0].z, g[0].w, g[1].x, g[1].y, g[1].z, g[1].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             uint32_t e0 = w[2 * k], e1 = w[2 * k + 1];
@@ -158,25 +188,19 @@ __device__ __forceinline__ void load_chunk(const void *row, int c, uint4 m, bool
                 e0 ^= mm[k] << 16;
                 e1 ^= mm[k] & 0x80000000u;
             }
-            out[2 * k] = __uint_as_float(e0);
-            out[2 * k + 1] = __uint_as_float(e1);
+            out[k] = bfly_in(mk2(__uint_as_float(e0), __uint_as_float(e1)));
         }
     } else {
-        const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(row) + 8 * c);
-        uint4 raw = __ldg(p);
-        uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
+        const uint32_t w[4] = {g[0].x, g[0].y, g[0].z, g[0].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const uint32_t x = use_sign ? (w[k] ^ mm[k]) : w[k];
             if constexpr (IN == IN_BF16) {
-                out[2 * k] = __uint_as_float(x << 16);
-                out[2 * k + 1] = __uint_as_float(x & 0xffff0000u);
+                out[k] = bf16w_bfly(x);
             } else {
-                __half2 h = *reinterpret_cast<const __half2 *>(&x);
-                float2 f = __half22float2(h);
-                out[2 * k] = f.x;
-                out[2 * k + 1] = f.y;
+                const __half2 h = *reinterpret_cast<const __half2 *>(&x);
+                const float2 f = __half22float2(h);
+                out[k] = bfly_in(mk2(f.x, f.y));
             }
         }
     }
@@ -200,32 +224,114 @@ struct KParams {
     int64_t groups_per_job;
     uint64_t seed;
     uint32_t flags;
+    int *err;          // library error word: set when a bounded wait gives up
 };
 
-// Shared-memory granule position of 16-byte half h of chunk c in a row buffer.
-__device__ __forceinline__ int granule(int c, int h, int row_in_cta) {
-    const int sw = (((c >> 2) ^ (c >> 6)) & 1) | (((c >> 3) & 1) << 1) | (((c >> 4) & 1) << 2);
-    return ((2 * c + h) ^ sw ^ (row_in_cta & 7));
+constexpr long long kWaitLimitCycles = 4000000000ll;    // ~2 s at 2 GHz
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for a bulk copy; on expiry raise the error word and report failure.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *b, uint32_t parity, int *err) {
+    if (mbar_try_wait(b, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(b, parity)) {
+        if (clock64() - t0 > kWaitLimitCycles) {
+            atomicExch(err, 1);
+            return false;
+        }
+    }
+    return true;
+}
+// Bulk global -> shared copy (TMA engine), completing on an mbarrier.
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Shared-memory granule position of 16-byte half h of chunk c in a row buffer:
+// (2c + h) ^ swz(c) ^ (row & 7).  swz is a XOR of chunk bits, so for c = cs | ct
+// (slot bits cs known at compile time, thread bits ct at run time, disjoint)
+// the position splits into granule_k(cs, h) ^ granule_t(ct, row).
+__host__ __device__ constexpr int swz(int c) {
+    return (((c >> 2) ^ (c >> 6)) & 1) | (((c >> 3) & 1) << 1) | (((c >> 4) & 1) << 2);
+}
+__host__ __device__ constexpr int granule_k(int cs, int h) { return (2 * cs + h) ^ swz(cs); }
+__device__ __forceinline__ int granule_t(int ct, int row_in_cta) { return (2 * ct) ^ swz(ct) ^ (row_in_cta & 7); }
+
+// chunk index = slot part | thread part
+template <int C>
+__host__ __device__ constexpr int chunk_s(int s, bool phase2) {
+    int c = 0;
+    for (int k = 0; k < Plan<C>::S; ++k) c |= ((s >> k) & 1) << (phase2 ? Plan<C>::b(k) : Plan<C>::a(k));
+    return c;
+}
+template <int C>
+__device__ __forceinline__ int chunk_t(int t, bool phase2) {
+    using PL = Plan<C>;
+    int c = 0;
+#pragma unroll
+    for (int k = 0; k < PL::T; ++k) c |= ((t >> k) & 1) << (phase2 ? PL::tb(k) : PL::ta(k));
+    return c;
+}
+template <int C>
+__device__ __forceinline__ int chunk_of(int t, int s, bool phase2) {
+    return chunk_s<C>(s, phase2) | chunk_t<C>(t, phase2);
 }
 
 template <int LOGN, int IN>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, LOGN == 7 ? 4 : 1)
 fwht_quant_kernel(const __grid_constant__ KParams prm) {
     constexpr int C = LOGN - 3;
     using PL = Plan<C>;
     constexpr int n = 1 << LOGN;
-    constexpr int E = PL::E;
     constexpr int NSLOT = PL::NSLOT;
+    constexpr int NP = PL::E / 2;                        // fp32 pairs per thread
     constexpr int P = PL::P;
     constexpr int ROWS = PL::ROWS;
+    constexpr int G = IN == IN_F32 ? 2 : 1;              // 16-byte granules per chunk
+    constexpr int Q = NSLOT * G;                         // granules per thread per group
+    constexpr int ES = IN == IN_F32 ? 4 : 2;             // input element bytes
 
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    uint32_t *sgn = reinterpret_cast<uint32_t *>(smem_raw);          // n/2 words
-    float *red = reinterpret_cast<float *>(smem_raw + n * 2);        // ROWS*2 floats
-    float4 *rowbuf = reinterpret_cast<float4 *>(smem_raw + n * 2 + 16 * ((ROWS * 2 * 4 + 15) / 16));
+    constexpr int DEPTH = PL::kTwoPhase ? 1 : 2;          // input groups in flight per warp
+    constexpr int NW = kThreads / 32;
+    constexpr int WREG = 32 * Q * 16;                     // bytes of one warp's input region
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw);                       // NW*DEPTH
+    uint32_t *sgn = reinterpret_cast<uint32_t *>(smem_raw + 128);                  // n/2 words
+    float *red = reinterpret_cast<float *>(smem_raw + 128 + n * 2);               // ROWS*2 floats
+    unsigned char *inbuf = smem_raw + 128 + n * 2 + 128 * ((ROWS * 2 * 4 + 127) / 128);
+    ulonglong2 *rowbuf = reinterpret_cast<ulonglong2 *>(inbuf + NW * DEPTH * WREG);
+    // one row per thread: packed codes of a warp's 32 rows (contiguous in q) are
+    // staged here and written by one bulk store; two buffers per warp
+    constexpr int OSTG = PL::kTwoPhase ? 0 : (32 / P) * (n / 2);
+    unsigned char *ostage = inbuf + NW * DEPTH * WREG + (PL::kTwoPhase ? (size_t)ROWS * n * 4 : 0);
 
     const bool signs_first = (prm.flags & 1u) != 0;
 
+    if (threadIdx.x < NW * DEPTH) mbar_init(&bars[threadIdx.x], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // Sign masks: word j covers elements 2j (bit 15) and 2j+1 (bit 31).
     for (int j = threadIdx.x; j < n / 2; j += kThreads) {
         const uint32_t s0 = (uint32_t)(splitmix64_at(prm.seed, 2ull * j) >> 63);
@@ -236,68 +342,130 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
 
     const int row_in_cta = threadIdx.x / P;
     const int t = threadIdx.x % P;
+    const int lane = threadIdx.x & 31;
+    const int gt1 = granule_t(chunk_t<C>(t, false), row_in_cta);   // per-thread swizzle parts
+    const int gt2 = granule_t(chunk_t<C>(t, true), row_in_cta);
     const float inv_sqrt_n = (LOGN & 1) ? (0.70710678118654752440f / (float)(1 << (LOGN / 2)))
                                         : (1.0f / (float)(1 << (LOGN / 2)));
-    const float shuf_sign0 = ((t >> (PL::kNumShuf > 0 ? PL::shuf(0) : 0)) & 1) ? -1.f : 1.f;
-    const float shuf_sign1 = ((t >> (PL::kNumShuf > 1 ? PL::shuf(1) : 0)) & 1) ? -1.f : 1.f;
     const unsigned full = 0xffffffffu;
-
+    const int warp = threadIdx.x >> 5;
     const int64_t total_groups = prm.groups_per_job * prm.njobs;
+
+    // Single-phase plans: the threads of warp row r read their chunks in slot
+    // order s ^ r, so a shared-memory wavefront spreads over the bank groups of
+    // the linear input copy.  Running the Sylvester network on input permuted by
+    // XOR with a leaves output j in place but multiplied by (-1)^popcount(j & a);
+    // all threads of a row share a, so the factor passes through the shuffle
+    // stage and is folded into the quantization multiplier below.  Two-phase
+    // plans exchange values between rows' threads with different layouts, so
+    // they read in natural order (a = 0).
+    const int xr = PL::kTwoPhase ? 0 : ((lane / P) & (NSLOT - 1));
+    const int cb1 = chunk_t<C>(t, false) | chunk_s<C>(xr, false);   // chunk(s) = cb1 ^ chunk_s(s)
+    // byte offset of this thread's chunk base inside the warp's input region
+    constexpr int RB = n * ES;                                        // bytes per input row
+    constexpr int RPW = P <= 32 ? 32 / P : 1;                         // rows per warp region
+    constexpr int REG_BYTES = P <= 32 ? RPW * RB : RB / 2;
+    static_assert(REG_BYTES == WREG, "warp input region size");
+    const int rw = P <= 32 ? lane / P : 0;                            // row within the warp region
+    const uint32_t xin = (uint32_t)(rw * RB) + (uint32_t)((16 * G * cb1) & (P <= 32 ? RB - 1 : RB / 2 - 1));
+    // transpose swizzle base including the XOR permutation
+    const int gt1x = gt1 ^ granule_k(chunk_s<C>(xr, false), 0);
+
+    // Issue the bulk copies of group g's rows for this warp (lane 0 only).
+    auto issue = [&](int64_t g, int slot) {
+        const int jb = (int)(g / prm.groups_per_job);
+        const RotJob &job = prm.job[jb];
+        const int64_t row0 = (g - (int64_t)jb * prm.groups_per_job) * ROWS + (P <= 32 ? warp * RPW : warp / 2);
+        const char *x = static_cast<const char *>(job.x);
+        unsigned char *dst = inbuf + (warp * DEPTH + slot) * WREG;
+        uint64_t *bar = &bars[warp * DEPTH + slot];
+        if constexpr (P <= 32) {
+            int64_t valid = job.rows - row0;
+            valid = valid < 0 ? 0 : (valid > RPW ? RPW : valid);
+            mbar_expect_tx(bar, (uint32_t)(valid * RB));
+            if (job.ld * ES == RB) {
+                if (valid > 0) bulk_copy(dst, x + row0 * RB, (uint32_t)(valid * RB), bar);
+            } else {
+                for (int r = 0; r < valid; ++r) bulk_copy(dst + r * RB, x + (row0 + r) * job.ld * ES, RB, bar);
+            }
+        } else {
+            const bool valid = row0 < job.rows;
+            mbar_expect_tx(bar, valid ? (uint32_t)(RB / 2) : 0u);
+            if (valid) bulk_copy(dst, x + row0 * job.ld * ES + (warp & 1) * (RB / 2), RB / 2, bar);
+        }
+    };
+
+    if (lane == 0) {
+#pragma unroll
+        for (int d = 0; d < DEPTH; ++d) {
+            const int64_t g = (int64_t)blockIdx.x + (int64_t)d * gridDim.x;
+            if (g < total_groups) issue(g, d);
+        }
+    }
+    int slot = 0;
+    uint32_t phase = 0;
+    bool aborted = false;
+    int obuf = 0;
     for (int64_t grp = blockIdx.x; grp < total_groups; grp += gridDim.x) {
         const int jb = (int)(grp / prm.groups_per_job);
         const RotJob &job = prm.job[jb];
         const int64_t row = (grp - (int64_t)jb * prm.groups_per_job) * ROWS + row_in_cta;
-        const bool active = row < job.rows;
-        const int64_t rrow = active ? row : 0;
+        const unsigned char *wbuf = inbuf + (warp * DEPTH + slot) * WREG;
 
-        float v[E];
-        // ---------------- phase 1: load, signs, butterflies ----------------
-        {
-            const void *xrow = (IN == IN_F32)
-                ? (const void *)(static_cast<const float *>(job.x) + rrow * job.ld)
-                : (const void *)(static_cast<const uint16_t *>(job.x) + rrow * job.ld);
+        pair_t v[NP];
+        // ---------------- phase 1: input from the bulk copy, signs, butterflies ----------------
+        // A copy that never lands raises the error word; the iteration then runs
+        // on stale data with its stores disabled, so barriers stay matched.
+        if (!mbar_wait_bounded(&bars[warp * DEPTH + slot], phase, prm.err)) aborted = true;
+        const bool active = row < job.rows && !aborted;
 #pragma unroll
-            for (int s = 0; s < NSLOT; ++s) {
-                int c = 0;
+        for (int s = 0; s < NSLOT; ++s) {
+            const int c = cb1 ^ chunk_s<C>(s, false);
+            const uint4 m = reinterpret_cast<const uint4 *>(sgn)[c];
+            uint4 g[G];
 #pragma unroll
-                for (int k = 0; k < PL::S; ++k) c |= ((s >> k) & 1) << PL::a(k);
-#pragma unroll
-                for (int k = 0; k < PL::T; ++k) c |= ((t >> k) & 1) << PL::ta(k);
-                const uint4 m = reinterpret_cast<const uint4 *>(sgn)[c];
-                if (active) {
-                    load_chunk<IN>(xrow, c, m, signs_first, &v[8 * s]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[8 * s + e] = 0.f;
-                }
+            for (int h = 0; h < G; ++h) {
+                const uint32_t off = (xin ^ (uint32_t)(16 * G * chunk_s<C>(s, false))) + 16 * h;
+                g[h] = *reinterpret_cast<const uint4 *>(wbuf + off);
             }
+            convert_chunk<IN>(g, m, signs_first, &v[4 * s]);   // includes the in-pair stage
+        }
+        // Hand the buffer back to the copy engine: order these generic reads
+        // before the next bulk write (async proxy) into it.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0 && !aborted) {
+            const int64_t g = grp + (int64_t)DEPTH * gridDim.x;
+            if (g < total_groups) issue(g, slot);
+        }
+        if (++slot == DEPTH) {
+            slot = 0;
+            phase ^= 1u;
+        }
+
 #pragma unroll
-            for (int rb = 0; rb < 3 + PL::S; ++rb) butterfly_reg_bit<E>(v, rb);
+        for (int rb = 1; rb < 3 + PL::S; ++rb) butterfly_pairs<NP>(v, rb);
 #pragma unroll
-            for (int j = 0; j < PL::kNumShuf; ++j) {
-                const int lm = 1 << PL::shuf(j);
-                const float sg = j == 0 ? shuf_sign0 : shuf_sign1;
+        for (int j = 0; j < PL::kNumShuf; ++j) {
+            const int lm = 1 << PL::shuf(j);
+            const float sg = ((t >> PL::shuf(j)) & 1) ? -1.f : 1.f;
+            const pair_t sg2 = mk2(sg, sg);
 #pragma unroll
-                for (int r = 0; r < E; r += 2) {
-                    const float p0 = __shfl_xor_sync(full, v[r], lm);
-                    const float p1 = __shfl_xor_sync(full, v[r + 1], lm);
-                    fma2_scalar(v[r], v[r + 1], sg, p0, p1);
-                }
+            for (int i = 0; i < NP; ++i) {
+                const float p0 = __shfl_xor_sync(full, lo2(v[i]), lm);
+                const float p1 = __shfl_xor_sync(full, hi2(v[i]), lm);
+                v[i] = fma2(v[i], sg2, mk2(p0, p1));
             }
         }
 
         // ---------------- transpose through shared memory ----------------
         if constexpr (PL::kTwoPhase) {
-            float4 *buf = rowbuf + (size_t)row_in_cta * (n / 4);
+            ulonglong2 *buf = rowbuf + (size_t)row_in_cta * (n / 4);
 #pragma unroll
             for (int s = 0; s < NSLOT; ++s) {
-                int c = 0;
-#pragma unroll
-                for (int k = 0; k < PL::S; ++k) c |= ((s >> k) & 1) << PL::a(k);
-#pragma unroll
-                for (int k = 0; k < PL::T; ++k) c |= ((t >> k) & 1) << PL::ta(k);
-                buf[granule(c, 0, row_in_cta)] = make_float4(v[8 * s], v[8 * s + 1], v[8 * s + 2], v[8 * s + 3]);
-                buf[granule(c, 1, row_in_cta)] = make_float4(v[8 * s + 4], v[8 * s + 5], v[8 * s + 6], v[8 * s + 7]);
+                const int cs = chunk_s<C>(s, false);
+                buf[granule_k(cs, 0) ^ gt1x] = make_ulonglong2(v[4 * s], v[4 * s + 1]);
+                buf[granule_k(cs, 1) ^ gt1x] = make_ulonglong2(v[4 * s + 2], v[4 * s + 3]);
             }
             if constexpr (P > 32) {
                 asm volatile("bar.sync %0, %1;" ::"r"(1 + row_in_cta), "r"(P) : "memory");
@@ -306,27 +474,22 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
             }
 #pragma unroll
             for (int s = 0; s < NSLOT; ++s) {
-                int c = 0;
-#pragma unroll
-                for (int k = 0; k < PL::S; ++k) c |= ((s >> k) & 1) << PL::b(k);
-#pragma unroll
-                for (int k = 0; k < PL::T; ++k) c |= ((t >> k) & 1) << PL::tb(k);
-                const float4 lo = buf[granule(c, 0, row_in_cta)];
-                const float4 hi = buf[granule(c, 1, row_in_cta)];
-                v[8 * s] = lo.x; v[8 * s + 1] = lo.y; v[8 * s + 2] = lo.z; v[8 * s + 3] = lo.w;
-                v[8 * s + 4] = hi.x; v[8 * s + 5] = hi.y; v[8 * s + 6] = hi.z; v[8 * s + 7] = hi.w;
+                const int cs = chunk_s<C>(s, true);
+                const ulonglong2 lo = buf[granule_k(cs, 0) ^ gt2];
+                const ulonglong2 hi = buf[granule_k(cs, 1) ^ gt2];
+                v[4 * s] = lo.x; v[4 * s + 1] = lo.y; v[4 * s + 2] = hi.x; v[4 * s + 3] = hi.y;
             }
             // phase-2 butterflies over the slot bits not done in phase 1
 #pragma unroll
             for (int k = 0; k < PL::S; ++k) {
-                if (!PL::chunk_bit_done_in_phase1(PL::b(k))) butterfly_reg_bit<E>(v, 3 + k);
+                if (!PL::chunk_bit_done_in_phase1(PL::b(k))) butterfly_pairs<NP>(v, 3 + k);
             }
         }
 
         // ---------------- row absmax ----------------
         float amax = 0.f;
 #pragma unroll
-        for (int r = 0; r < E; ++r) amax = fmaxf(amax, fabsf(v[r]));
+        for (int i = 0; i < NP; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo2(v[i])), fabsf(hi2(v[i]))));
         if constexpr (P > 1) {
 #pragma unroll
             for (int k = 0; k < (PL::T < 5 ? PL::T : 5); ++k)
@@ -342,9 +505,16 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
 
         // ---------------- quantize, pack, store ----------------
         const float inv = amax > 0.f ? 7.0f / amax : 0.f;
+        const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
+        uint8_t *stg = ostage + (warp * 2 + obuf) * OSTG;
+        if constexpr (!PL::kTwoPhase) {
+            // the bulk store that last read this staging buffer must be done
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            __syncwarp();
+        }
         if (active) {
             if (t == 0) job.scales[row] = (amax / 7.0f) * inv_sqrt_n;
-            uint8_t *qrow = job.q + row * (int64_t)(n / 2);
+            uint8_t *qrow = PL::kTwoPhase ? job.q + row * (int64_t)(n / 2) : stg + (lane / P) * (n / 2);
             float *yrow = job.y ? job.y + row * (int64_t)n : nullptr;
 #pragma unroll
             for (int s4 = 0; s4 < NSLOT; s4 += 4) {
@@ -353,44 +523,79 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int s = s4 + cc;
-                    int c = 0;
-#pragma unroll
-                    for (int k = 0; k < PL::S; ++k) c |= ((s >> k) & 1) << (PL::kTwoPhase ? PL::b(k) : k);
-#pragma unroll
-                    for (int k = 0; k < PL::T; ++k) c |= ((t >> k) & 1) << PL::tb(k);
+                    // output chunk of slot s: phase-2 map, or natural order for one row per thread
+                    const int c = PL::kTwoPhase ? chunk_of<C>(t, s, true) : (chunk_t<C>(t, false) | s);
                     if (cc == 0) c0 = c;
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = v[8 * s + e];
+                    // (-1)^popcount(s & xr): the sign left by the permuted read order
+                    const bool neg = !PL::kTwoPhase && (__popc(s & xr) & 1);
+                    const float sinv = neg ? -inv : inv;
+                    const pair_t inv2 = mk2(sinv, sinv);
+                    pair_t f[4] = {v[4 * s], v[4 * s + 1], v[4 * s + 2], v[4 * s + 3]};
                     if (!signs_first) {
                         const uint4 m = reinterpret_cast<const uint4 *>(sgn)[c];
                         const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            f[2 * k] = __uint_as_float(__float_as_uint(f[2 * k]) ^ (mm[k] << 16));
-                            f[2 * k + 1] = __uint_as_float(__float_as_uint(f[2 * k + 1]) ^ (mm[k] & 0x80000000u));
-                        }
+                        for (int k = 0; k < 4; ++k)
+                            f[k] = f[k] ^ (((pair_t)(mm[k] & 0x80000000u) << 32) | (pair_t)(mm[k] << 16));
                     }
                     if (yrow) {
-                        float4 *yp = reinterpret_cast<float4 *>(yrow + 8 * c);
-                        yp[0] = make_float4(f[0] * inv_sqrt_n, f[1] * inv_sqrt_n, f[2] * inv_sqrt_n, f[3] * inv_sqrt_n);
-                        yp[1] = make_float4(f[4] * inv_sqrt_n, f[5] * inv_sqrt_n, f[6] * inv_sqrt_n, f[7] * inv_sqrt_n);
+                        const float ys = neg ? -inv_sqrt_n : inv_sqrt_n;
+                        const pair_t sc2 = mk2(ys, ys), z2 = 0ull;
+                        ulonglong2 *yp = reinterpret_cast<ulonglong2 *>(yrow + 8 * c);
+                        yp[0] = make_ulonglong2(fma2(f[0], sc2, z2), fma2(f[1], sc2, z2));
+                        yp[1] = make_ulonglong2(fma2(f[2], sc2, z2), fma2(f[3], sc2, z2));
                     }
                     uint32_t code[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) code[e] = __float_as_uint(__fmaf_rn(f[e], inv, 12582912.0f));
+                    for (int k = 0; k < 4; ++k) {
+                        const pair_t qq = fma2(f[k], inv2, bias2);
+                        code[2 * k] = (uint32_t)qq;
+                        code[2 * k + 1] = (uint32_t)(qq >> 32);
+                    }
                     words[cc] = pack8(code);
                 }
                 // chunks c0..c0+3 are consecutive (slot bits 0,1 = chunk bits 0,1)
                 *reinterpret_cast<uint4 *>(qrow + 4 * c0) = make_uint4(words[0], words[1], words[2], words[3]);
             }
         }
-        if constexpr (PL::kTwoPhase) {
-            if constexpr (P > 32) {
-                asm volatile("bar.sync %0, %1;" ::"r"(1 + row_in_cta), "r"(P) : "memory");
-            } else {
-                __syncwarp();
+        if constexpr (!PL::kTwoPhase) {
+            // one bulk store of this warp's valid rows
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                const int64_t wrow0 = row;                      // lane 0 holds the warp's first row
+                int64_t valid = job.rows - wrow0;
+                valid = valid < 0 ? 0 : (valid > 32 / P ? 32 / P : valid);
+                if (valid > 0 && !aborted) {
+                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                                     job.q + wrow0 * (int64_t)(n / 2)),
+                                 "r"(smem_addr(stg)), "r"((uint32_t)(valid * (n / 2)))
+                                 : "memory");
+                }
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
+            obuf ^= 1;
+        }
+        if constexpr (P > 32) {
+            // the two warps of a row leave together: share the abort decision
+            if (aborted && (t & 31) == 0) red[row_in_cta * 2] = __int_as_float(-1);
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + row_in_cta), "r"(P) : "memory");
+            const bool any = __float_as_int(red[row_in_cta * 2]) == -1;
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + row_in_cta), "r"(P) : "memory");
+            if (any) { aborted = true; break; }
+        } else {
+            if constexpr (PL::kTwoPhase) __syncwarp();
+            if (__any_sync(full, aborted)) { aborted = true; break; }
+        }
+    }
+    if constexpr (!PL::kTwoPhase) {
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    }
+    if (aborted) {
+        // wait (bounded) for this warp's copies still in flight before leaving
+        for (int d = 0; d < DEPTH; ++d) {
+            const uint32_t par = d >= slot ? phase : (phase ^ 1u);
+            mbar_wait_bounded(&bars[warp * DEPTH + d], par, prm.err);
         }
     }
 }
@@ -399,8 +604,12 @@ template <int LOGN, int IN>
 size_t smem_bytes() {
     using PL = Plan<LOGN - 3>;
     constexpr int n = 1 << LOGN;
-    size_t b = (size_t)n * 2 + 16 * ((PL::ROWS * 2 * 4 + 15) / 16);
+    constexpr int G = IN == IN_F32 ? 2 : 1;
+    constexpr int DEPTH = PL::kTwoPhase ? 1 : 2;
+    size_t b = 128 + (size_t)n * 2 + 128 * ((PL::ROWS * 2 * 4 + 127) / 128);
+    b += (size_t)(kThreads / 32) * DEPTH * 32 * PL::NSLOT * G * 16;   // bulk-copy input rings
     if (PL::kTwoPhase) b += (size_t)PL::ROWS * n * 4;
+    else b += (size_t)(kThreads / 32) * 2 * (32 / PL::P) * (n / 2);  // output staging
     return b;
 }
 
@@ -448,7 +657,11 @@ cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_t
     }
     p.seed = seed;
     p.flags = flags;
-    const int rows_per_group = kThreads >> (log_n - 3 > 4 ? log_n - 7 : 0);
+    p.err = error_word_device_ptr();
+    if (!p.err) return cudaErrorUnknown;
+    const int C = log_n - 3;
+    const int S = C <= 3 ? C : (C == 4 ? 3 : 4);      // as in Plan<C>
+    const int rows_per_group = kThreads >> (C - S);
     p.groups_per_job = (max_rows + rows_per_group - 1) / rows_per_group;
     if (p.groups_per_job == 0) return cudaSuccess;
     switch (log_n) {
