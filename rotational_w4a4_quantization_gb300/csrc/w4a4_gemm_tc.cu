@@ -17,15 +17,20 @@
 //    warps add up each row's u while widening, and the epilogue removes the
 //    offset, then applies the per-token x per-channel scales.
 //
-// Pipeline (one 128 x 256 output tile per CTA, K in blocks of 128 codes):
+// Pipeline (persistent: one CTA per SM walks 128 x 256 output tiles; K in
+// blocks of 128 codes; two TMEM accumulators so tile i's epilogue overlaps
+// tile i+1's MMAs):
 //   warp 0    TMA producer: packed A (128 x 64 B) and W (256 x 64 B) tiles into a
 //             3-stage ring (mbarrier transaction counts);
-//   warp 1    allocates 256 TMEM columns; one lane issues 4 MMAs (M128 N256 K32)
-//             per K block and commits them to the operand ring's "empty" barriers;
+//   warp 1    allocates 512 TMEM columns; one lane issues 4 MMAs (M128 N256 K32)
+//             per K block into the tile's accumulator and commits them to the
+//             operand ring's "empty" barriers and, per tile, to "acc full";
 //   warps 2-9 widen nibbles to E4M3 into a 3-stage operand ring laid out in the
 //             128-byte-swizzled K-major form the MMA descriptors expect, keep
-//             per-row code sums, and run the epilogue (tcgen05.ld of the fp32
-//             accumulator, offset removal, scales, 16-byte stores).
+//             per-row code sums, and hand each tile's offset terms and weight
+//             scales to the epilogue through shared memory;
+//   warps 10-17 epilogue: tcgen05.ld of the fp32 accumulator, offset removal,
+//             scales (broadcast from shared memory), 16-byte stores.
 // The order of k inside each 8-code group is permuted the same way for A and W
 // (even codes, then odd codes), which leaves every dot product unchanged.
 // Every mbarrier wait is bounded: on expiry the CTA raises the library's error
@@ -47,10 +52,12 @@ constexpr int BM = 128, BN = 256, BK = 128;      // tile (K in codes)
 constexpr int PK_STAGES = 3, OP_STAGES = RQ_TC_OP_STAGES;
 constexpr int kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps;
-constexpr int kThreadsTC = 32 * (2 + kConvWarps);
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreadsTC = 32 * (2 + kConvWarps + kEpiWarps);
 constexpr int PK_A = BM * BK / 2, PK_W = BN * BK / 2;   // packed bytes per stage
 constexpr int OP_A = BM * BK, OP_W = BN * BK;           // e4m3 bytes per stage
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;                 // two 128x256 fp32 accumulators
 constexpr long long kWaitLimitCycles = 4000000000ll;    // ~2 s at 2 GHz
 
 struct Smem {
@@ -58,13 +65,15 @@ struct Smem {
     alignas(1024) uint8_t opW[OP_STAGES][OP_W];
     alignas(128) uint8_t pkA[PK_STAGES][PK_A];
     alignas(128) uint8_t pkW[PK_STAGES][PK_W];
-    int sumA[BM];
-    int sumW[BN];
+    int rowterm[2][BM];      // -8 * sum_k u_a, per tile parity
+    int colterm[2][BN];      // 64 K - 8 * sum_k u_w
+    float wscale[2][BN];     // weight scales of the tile's columns
     alignas(8) uint64_t pk_full[PK_STAGES];
     uint64_t pk_empty[PK_STAGES];
     uint64_t op_full[OP_STAGES];
     uint64_t op_empty[OP_STAGES];
-    uint64_t acc_full;
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t sum_full[2], sum_empty[2];
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -189,8 +198,9 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
     const int kblocks = (int)(prm.K / BK);
+    const int64_t n_tiles_n = (prm.N + BN - 1) / BN;
+    const int64_t n_tiles = n_tiles_n * ((prm.M + BM - 1) / BM);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < PK_STAGES; ++i) {
@@ -201,7 +211,12 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             mbar_init(&s.op_full[i], kConvThreads);
             mbar_init(&s.op_empty[i], 1);
         }
-        mbar_init(&s.acc_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.acc_full[i], 1);
+            mbar_init(&s.acc_empty[i], kEpiThreads);
+            mbar_init(&s.sum_full[i], kConvThreads);
+            mbar_init(&s.sum_empty[i], kEpiThreads);
+        }
         s.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -219,144 +234,180 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int st = kb % PK_STAGES;
-                if (!mbar_wait(s, &s.pk_empty[st], ((kb / PK_STAGES) & 1) ^ 1, prm.err)) break;
-                mbar_expect_tx(&s.pk_full[st], PK_A + PK_W);
-                tma_load_2d(s.pkA[st], &tmA, &s.pk_full[st], kb * (BK / 2), (int)m0);
-                tma_load_2d(s.pkW[st], &tmW, &s.pk_full[st], kb * (BK / 2), (int)n0);
+            int64_t g = 0;                                   // global K-block counter
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+                const int m0 = (int)(tile / n_tiles_n) * BM, n0 = (int)(tile % n_tiles_n) * BN;
+                for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                    const int st = (int)(g % PK_STAGES);
+                    if (!mbar_wait(s, &s.pk_empty[st], (uint32_t)((g / PK_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
+                    mbar_expect_tx(&s.pk_full[st], PK_A + PK_W);
+                    tma_load_2d(s.pkA[st], &tmA, &s.pk_full[st], kb * (BK / 2), m0);
+                    tma_load_2d(s.pkW[st], &tmW, &s.pk_full[st], kb * (BK / 2), n0);
+                }
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
+            int64_t g = 0;
+            int it = 0;
             bool ok = true;
-            for (int kb = 0; kb < kblocks && ok; ++kb) {
-                const int st = kb % OP_STAGES;
-                ok = mbar_wait(s, &s.op_full[st], (kb / OP_STAGES) & 1, prm.err);
-                if (!ok) break;
+            for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++it) {
+                const int buf = it & 1;
+                // the epilogue must have drained this accumulator (two tiles ago)
+                if (!mbar_wait(s, &s.acc_empty[buf], (uint32_t)((it >> 1) & 1) ^ 1, prm.err)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t a0 = smem_u32(s.opA[st]), w0 = smem_u32(s.opW[st]);
+                const uint32_t d = tmem + (uint32_t)(buf * BN);
+                for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                    const int st = (int)(g % OP_STAGES);
+                    if (!mbar_wait(s, &s.op_full[st], (uint32_t)((g / OP_STAGES) & 1), prm.err)) { ok = false; break; }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t a0 = smem_u32(s.opA[st]), w0 = smem_u32(s.opW[st]);
 #pragma unroll
-                for (int k = 0; k < BK / 32; ++k)
-                    mma_f8(tmem, sw128_desc(a0 + 32 * k), sw128_desc(w0 + 32 * k), (kb | k) != 0);
-                mma_commit(&s.op_empty[st]);
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_f8(d, sw128_desc(a0 + 32 * k), sw128_desc(w0 + 32 * k), (kb | k) != 0);
+                    mma_commit(&s.op_empty[st]);
+                }
+                if (ok) mma_commit(&s.acc_full[buf]);
             }
-            if (ok) mma_commit(&s.acc_full);
         }
-    } else {
-        // ---------------- converters, then epilogue ----------------
+    } else if (warp < 2 + kConvWarps) {
+        // ---------------- converters ----------------
         const int t = threadIdx.x - 64;          // 0..255
         const int ch = t & 3;                    // 16-byte chunk of the 64-byte packed row
         const int rq = t >> 2;                   // 0..63
-        uint32_t sumA[2] = {0, 0}, sumW[4] = {0, 0, 0, 0};
+        int64_t g = 0;
+        int it = 0;
         bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const int ps = kb % PK_STAGES;
-            if (!mbar_wait(s, &s.pk_full[ps], (kb / PK_STAGES) & 1, prm.err)) { ok = false; break; }
-            uint4 a[2], w[4];
+        for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++it) {
+            const int n0 = (int)(tile % n_tiles_n) * BN;
+            uint32_t sumA[2] = {0, 0}, sumW[4] = {0, 0, 0, 0};
+            for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                const int ps = (int)(g % PK_STAGES);
+                if (!mbar_wait(s, &s.pk_full[ps], (uint32_t)((g / PK_STAGES) & 1), prm.err)) { ok = false; break; }
+                uint4 a[2], w[4];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) a[j] = reinterpret_cast<const uint4 *>(s.pkA[ps])[t + 256 * j];
+                for (int j = 0; j < 2; ++j) a[j] = reinterpret_cast<const uint4 *>(s.pkA[ps])[t + 256 * j];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) w[j] = reinterpret_cast<const uint4 *>(s.pkW[ps])[t + 256 * j];
-            // The next TMA refill of this stage writes through the async proxy:
-            // order this thread's generic reads of the stage before it, or the
-            // refill can overtake them.
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(&s.pk_empty[ps]);
+                for (int j = 0; j < 4; ++j) w[j] = reinterpret_cast<const uint4 *>(s.pkW[ps])[t + 256 * j];
+                // The next TMA refill of this stage writes through the async proxy:
+                // order this thread's generic reads of the stage before it, or the
+                // refill can overtake them.
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(&s.pk_empty[ps]);
 
-            const int os = kb % OP_STAGES;
-            if (!mbar_wait(s, &s.op_empty[os], ((kb / OP_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
-            // row r, chunk ch -> 32 e4m3 bytes = granules 2ch, 2ch+1 of the 128-byte row
-            auto emit = [&](uint8_t *base, int r, const uint4 &v, uint32_t &sum) {
-                uint32_t lo[4], hi[4], acc = 0;
-                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                const int os = (int)(g % OP_STAGES);
+                if (!mbar_wait(s, &s.op_empty[os], (uint32_t)((g / OP_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
+                // row r, chunk ch -> 32 e4m3 bytes = granules 2ch, 2ch+1 of the 128-byte row
+                auto emit = [&](uint8_t *base, int r, const uint4 &v, uint32_t &sum) {
+                    uint32_t lo[4], hi[4], acc = 0;
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc += widen(wv[i], lo[i], hi[i]);
-                sum = __dp4a(acc, 0x01010101u, sum);
-                uint8_t *row = base + r * 128;
-                const int g0 = (2 * ch) ^ (r & 7), g1 = (2 * ch + 1) ^ (r & 7);
-                *reinterpret_cast<uint4 *>(row + 16 * g0) = make_uint4(lo[0], hi[0], lo[1], hi[1]);
-                *reinterpret_cast<uint4 *>(row + 16 * g1) = make_uint4(lo[2], hi[2], lo[3], hi[3]);
-            };
+                    for (int i = 0; i < 4; ++i) acc += widen(wv[i], lo[i], hi[i]);
+                    sum = __dp4a(acc, 0x01010101u, sum);
+                    uint8_t *row = base + r * 128;
+                    const int g0 = (2 * ch) ^ (r & 7), g1 = (2 * ch + 1) ^ (r & 7);
+                    *reinterpret_cast<uint4 *>(row + 16 * g0) = make_uint4(lo[0], hi[0], lo[1], hi[1]);
+                    *reinterpret_cast<uint4 *>(row + 16 * g1) = make_uint4(lo[2], hi[2], lo[3], hi[3]);
+                };
 #pragma unroll
-            for (int j = 0; j < 2; ++j) emit(s.opA[os], rq + 64 * j, a[j], sumA[j]);
+                for (int j = 0; j < 2; ++j) emit(s.opA[os], rq + 64 * j, a[j], sumA[j]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) emit(s.opW[os], rq + 64 * j, w[j], sumW[j]);
-            // every writer makes its own stores visible to the tensor core's
-            // (async-proxy) reads, then arrives itself
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(&s.op_full[os]);
+                for (int j = 0; j < 4; ++j) emit(s.opW[os], rq + 64 * j, w[j], sumW[j]);
+                // every writer makes its own stores visible to the tensor core's
+                // (async-proxy) reads, then arrives itself
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(&s.op_full[os]);
+            }
+            if (!ok) break;
+            // row sums: the four lanes sharing a row hold its four chunks
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                sumA[j] += __shfl_xor_sync(0xffffffffu, sumA[j], 1);
+                sumA[j] += __shfl_xor_sync(0xffffffffu, sumA[j], 2);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sumW[j] += __shfl_xor_sync(0xffffffffu, sumW[j], 1);
+                sumW[j] += __shfl_xor_sync(0xffffffffu, sumW[j], 2);
+            }
+            // hand this tile's offset terms and weight scales to the epilogue
+            const int buf = it & 1;
+            if (!mbar_wait(s, &s.sum_empty[buf], (uint32_t)((it >> 1) & 1) ^ 1, prm.err)) { ok = false; break; }
+            if (ch == 0) {
+                for (int j = 0; j < 2; ++j) s.rowterm[buf][rq + 64 * j] = -8 * (int)sumA[j];
+                for (int j = 0; j < 4; ++j) s.colterm[buf][rq + 64 * j] = 64 * (int)prm.K - 8 * (int)sumW[j];
+            }
+            if (YMODE != 2) s.wscale[buf][t] = (n0 + t < prm.N) ? prm.sw[n0 + t] : 0.f;
+            mbar_arrive(&s.sum_full[buf]);
         }
-        // row sums: the four lanes sharing a row hold its four chunks
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            sumA[j] += __shfl_xor_sync(0xffffffffu, sumA[j], 1);
-            sumA[j] += __shfl_xor_sync(0xffffffffu, sumA[j], 2);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            sumW[j] += __shfl_xor_sync(0xffffffffu, sumW[j], 1);
-            sumW[j] += __shfl_xor_sync(0xffffffffu, sumW[j], 2);
-        }
-        if (ch == 0) {
-            for (int j = 0; j < 2; ++j) s.sumA[rq + 64 * j] = (int)sumA[j];
-            for (int j = 0; j < 4; ++j) s.sumW[rq + 64 * j] = (int)sumW[j];
-        }
-        asm volatile("bar.sync 1, %0;" ::"r"(32 * kConvWarps) : "memory");
-
-        if (ok) ok = mbar_wait(s, &s.acc_full, 0, prm.err);
-        if (ok) {
+    } else {
+        // ---------------- epilogue: TMEM -> offset removal -> scales -> global ----------------
+        const int e = threadIdx.x - 64 - kConvThreads;   // 0..255
+        const int q = warp & 3;                          // TMEM lane quarter this warp may read
+        const int colhalf = e >> 7;                      // columns 0-127 or 128-255
+        int it = 0;
+        for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+            const int buf = it & 1;
+            const uint32_t par = (uint32_t)((it >> 1) & 1);
+            if (!mbar_wait(s, &s.acc_full[buf], par, prm.err)) break;
+            if (!mbar_wait(s, &s.sum_full[buf], par, prm.err)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const int q = warp & 3;                      // TMEM lane quarter this warp may read
-            const int colhalf = (warp - 2) >> 2;         // columns 0-127 or 128-255
+            const int64_t m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
             const int mr = 32 * q + lane;
             const int64_t m = m0 + mr;
-            const int bias_a = 64 * (int)prm.K - 8 * s.sumA[mr];
+            const int rowt = s.rowterm[buf][mr];
             const float sa = (YMODE != 2 && m < prm.M) ? prm.sa[m] : 0.f;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 const int col0 = colhalf * 128 + 32 * c;
                 uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col0, r);
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + col0), r);
                 if (m < prm.M) {
-                int acc[32];
+                    int acc[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int u = __float2int_rn(__uint_as_float(r[j]) * 262144.0f);   // exact: x 2^18
-                    acc[j] = u + bias_a - 8 * s.sumW[col0 + j];
-                }
-                const int64_t nb = n0 + col0;
-                if (YMODE == 2) {
-                    int *yr = static_cast<int *>(prm.y) + m * prm.N + nb;
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        if (nb + j + 3 < prm.N) *reinterpret_cast<int4 *>(yr + j) = make_int4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                } else if (YMODE == 1) {
-                    float *yr = static_cast<float *>(prm.y) + m * prm.N + nb;
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        if (nb + j + 3 >= prm.N) continue;
-                        float4 o;
-                        o.x = ((float)acc[j] * sa) * prm.sw[nb + j];
-                        o.y = ((float)acc[j + 1] * sa) * prm.sw[nb + j + 1];
-                        o.z = ((float)acc[j + 2] * sa) * prm.sw[nb + j + 2];
-                        o.w = ((float)acc[j + 3] * sa) * prm.sw[nb + j + 3];
-                        *reinterpret_cast<float4 *>(yr + j) = o;
+                    for (int j = 0; j < 32; ++j) {
+                        const int u = __float2int_rn(__uint_as_float(r[j]) * 262144.0f);   // exact: x 2^18
+                        acc[j] = u + rowt + s.colterm[buf][col0 + j];
                     }
-                } else {
-                    __half *yr = static_cast<__half *>(prm.y) + m * prm.N + nb;
+                    const int64_t nb = n0 + col0;
+                    if (YMODE == 2) {
+                        int *yr = static_cast<int *>(prm.y) + m * prm.N + nb;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        if (nb + j + 7 >= prm.N) continue;
-                        __align__(16) __half h[8];
+                        for (int j = 0; j < 32; j += 4)
+                            if (nb + j + 3 < prm.N)
+                                *reinterpret_cast<int4 *>(yr + j) = make_int4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                    } else if (YMODE == 1) {
+                        float *yr = static_cast<float *>(prm.y) + m * prm.N + nb;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) h[e] = __float2half_rn(((float)acc[j + e] * sa) * prm.sw[nb + j + e]);
-                        *reinterpret_cast<uint4 *>(yr + j) = *reinterpret_cast<const uint4 *>(h);
+                        for (int j = 0; j < 32; j += 4) {
+                            if (nb + j + 3 >= prm.N) continue;
+                            float4 o;
+                            o.x = ((float)acc[j] * sa) * s.wscale[buf][col0 + j];
+                            o.y = ((float)acc[j + 1] * sa) * s.wscale[buf][col0 + j + 1];
+                            o.z = ((float)acc[j + 2] * sa) * s.wscale[buf][col0 + j + 2];
+                            o.w = ((float)acc[j + 3] * sa) * s.wscale[buf][col0 + j + 3];
+                            *reinterpret_cast<float4 *>(yr + j) = o;
+                        }
+                    } else {
+                        __half *yr = static_cast<__half *>(prm.y) + m * prm.N + nb;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8) {
+                            if (nb + j + 7 >= prm.N) continue;
+                            __align__(16) __half h[8];
+#pragma unroll
+                            for (int e2 = 0; e2 < 8; ++e2)
+                                h[e2] = __float2half_rn(((float)acc[j + e2] * sa) * s.wscale[buf][col0 + j + e2]);
+                            *reinterpret_cast<uint4 *>(yr + j) = *reinterpret_cast<const uint4 *>(h);
+                        }
                     }
-                }
                 }
             }
+            // this accumulator and these offset terms may be reused
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            mbar_arrive(&s.acc_empty[buf]);
+            mbar_arrive(&s.sum_empty[buf]);
         }
     }
 
@@ -411,7 +462,15 @@ cudaError_t launch_mode(const CUtensorMap &ta, const CUtensorMap &tw, const TcPa
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const dim3 grid((unsigned)((p.N + BN - 1) / BN), (unsigned)((p.M + BM - 1) / BM));
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t tiles = ((p.N + BN - 1) / BN) * ((p.M + BM - 1) / BM);
+    const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);   // persistent: one CTA per SM
     kern<<<grid, kThreadsTC, smem, stream>>>(ta, tw, p);
     return cudaGetLastError();
 }
