@@ -48,6 +48,14 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 4.5 / 2.25   # nominal dense ratio (fp8 / bf16) on GB300
 SLEEP_CYCLES = 400_000       # ~0.2 ms GPU-side pause between timed steps
 
+# DRAM bytes (read + write) per launch from one ncu capture of the current kernel
+# on the prefill shapes (see the summaries in profiles/); None once a kernel changes.
+NCU_TRAFFIC = {
+    "w4a4_gemm": 33_703_936 + 6_240_768,
+    "fwht_quant": None,
+    "kv_rotate_quant": None,
+}
+
 
 # --------------------------------------------------------------------------
 # work accounting (algorithmic bytes / ops)
@@ -331,14 +339,14 @@ def run_gpu(args, work, kvw):
     if dom == "gemm":
         ach = gb_ops / avg["gemm"] / 1e12
         roof = {"kernel": "w4a4_gemm", "bound": "tensor", "achieved": ach, "peak": fp8_peak,
-                "unit": "TFLOP/s", "frac": ach / fp8_peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": ach / fp8_peak, "traffic": NCU_TRAFFIC["w4a4_gemm"],
                 "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (fp8 dense ratio)"}
     else:
         key = "fwht_quant" if dom == "fwht" else "kv_rotate_quant"
         b = fb if dom == "fwht" else kb
         ach = b / avg[dom] / 1e9
         roof = {"kernel": key, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC[key],
                 "peak_source": f"{peaks['source']} hbm copy"}
 
     line = {

@@ -1,0 +1,100 @@
+"""Stand-alone timing of one kernel of the library (also the target of ncu captures).
+
+    python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel gemm --workload prefill
+    python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel fwht --workload large
+    python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel kv
+
+Runs `--warmup` untimed launches, then `--reps` launches each timed with CUDA events on the
+current stream (L2 flushed before each launch unless `--no-flush`; a GPU-side pause lets
+the host enqueue ahead so the events time the kernel, not the launch), and prints the
+median time with the algorithmic GB/s or TOPS.  GEMM operands are seeded random codes of
+the workload's shape; rotation inputs follow the workload's outlier recipe.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import torch
+
+_ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
+
+from rotational_w4a4_quantization_gb300 import build as rq_build  # noqa: E402
+from rotational_w4a4_quantization_gb300 import synth  # noqa: E402
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--kernel", choices=["fwht", "kv", "gemm"], required=True)
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="prefill")
+    ap.add_argument("--reps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--no-flush", action="store_true")
+    args = ap.parse_args(argv)
+
+    rq_build.build()
+    import rotational_w4a4_quantization_gb300 as rq
+    rq.load_library()
+    dev = torch.device("cuda")
+    w = synth.WORKLOADS[args.workload]
+    seed, flags = synth.SIGN_SEED, rq.RQ_SIGNS_FIRST
+
+    if args.kernel == "fwht":
+        if not w.rows:
+            raise SystemExit(f"workload {w.name} has no activation")
+        x = synth.activations(w.rows, w.n, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor).to(dev)
+        q = torch.empty(w.rows, w.n // 2, dtype=torch.uint8, device=dev)
+        s = torch.empty(w.rows, dtype=torch.float32, device=dev)
+        fn = lambda: rq.fwht_quant(x, seed, flags, q=q, scales=s)
+        work, unit = w.rows * (w.n * x.element_size() + w.n // 2 + 4), "GB/s"
+        what = f"fwht_quant {w.rows}x{w.n} {str(x.dtype).split('.')[-1]}"
+    elif args.kernel == "kv":
+        kw = synth.KV
+        k, v = synth.kv_pair(kw.kv_tokens, kw.kv_heads, kw.kv_head_dim, kw.data_seed,
+                             kw.kv_outliers_per_head, kw.kv_outlier_factor)
+        k, v = k.to(dev), v.to(dev)
+        out = rq.kv_rotate_quant(k, v, seed, flags)
+        fn = lambda: rq.kv_rotate_quant(k, v, seed, flags, out=out)
+        T, H, D = k.shape
+        work, unit = 2 * T * H * (D * 2 + D // 2 + 4), "GB/s"
+        what = f"kv_rotate_quant {T}x{H}x{D} bf16"
+    else:
+        if not w.gemm_n:
+            raise SystemExit(f"workload {w.name} has no GEMM")
+        M, K, N = w.rows, w.n, w.gemm_n
+        aq, sa = synth.random_codes(M, K, 1000 + w.data_seed)
+        wq, sw = synth.random_codes(N, K, 1001 + w.data_seed)
+        d = [t.to(dev) for t in (aq, sa, wq, sw)]
+        y = torch.empty(M, N, dtype=torch.float16, device=dev)
+        fn = lambda: rq.w4a4_gemm(*d, out=y)
+        work, unit = 2 * M * N * K, "TOPS"
+        what = f"w4a4_gemm {M}x{K}x{N} fp16"
+
+    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size, dtype=torch.uint8,
+                        device=dev)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = []
+    for i in range(args.reps):
+        if not args.no_flush:
+            flush.fill_(i & 0xFF)
+        torch.cuda._sleep(400_000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    assert rq.sync_status() == 0
+    times = sorted(a.elapsed_time(b) * 1e-3 for a, b in ev)
+    med = times[len(times) // 2]
+    rate = work / med / (1e9 if unit == "GB/s" else 1e12)
+    print(f"{what}: median {med * 1e6:.1f} us  min {times[0] * 1e6:.1f} us  {rate:.1f} {unit}")
+
+
+if __name__ == "__main__":
+    main()
