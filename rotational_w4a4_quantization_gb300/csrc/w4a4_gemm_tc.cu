@@ -17,15 +17,29 @@
 //    warps add up each row's u while widening, and the epilogue removes the
 //    offset, then applies the per-token x per-channel scales.
 //
-// Pipeline (persistent: one CTA per SM walks 128 x 256 output tiles; K in
-// blocks of 128 codes; two TMEM accumulators so tile i's epilogue overlaps
-// tile i+1's MMAs):
-//   warp 0    TMA producer: packed A (128 x 64 B) and W (256 x 64 B) tiles into a
-//             3-stage ring (mbarrier transaction counts);
-//   warp 1    allocates 512 TMEM columns; one lane issues 4 MMAs (M128 N256 K32)
+// Pipeline (persistent; K in blocks of 128 codes; two TMEM accumulators so tile
+// i's epilogue overlaps tile i+1's MMAs).  Two variants share the code:
+//  * CTA pairs (M > 128): a cluster of two CTAs on two SMs computes 256 x 256
+//    tiles with tcgen05.mma.cta_group::2 (M256 N256 K32).  Each CTA loads and
+//    widens its own 128 rows of A and its own half (128 rows) of the W tile, so
+//    every SM converts and serves half of B: a third less shared-memory traffic
+//    per MAC than one CTA doing 128 x 256 alone.  The leader CTA issues the MMAs;
+//    commits multicast to both CTAs' barriers.  The peer's converter warps arrive
+//    on the leader's operand barriers through distributed shared memory with a
+//    CTA-scope release: their operands stay in the peer's own shared memory and
+//    are read by the peer SM's tensor core, and a cluster-scope release there
+//    (it waits for the SM's memory traffic to drain) took longer than the K
+//    block's MMAs.  Once per tile the epilogues exchange the halves of the
+//    per-column offset terms (cluster-scope release, as the peer's threads read
+//    them) and release the accumulator to the leader;
+//  * single CTAs (64 < M <= 128): 128 x 256 tiles with cta_group::1.
+// Roles in each CTA:
+//   warp 0    TMA producer: packed A (128 x 64 B) and W (128 or 256 x 64 B) tiles
+//             into a ring (mbarrier transaction counts);
+//   warp 1    allocates 512 TMEM columns; one lane (of the leader) issues 4 MMAs
 //             per K block into the tile's accumulator and commits them to the
 //             operand ring's "empty" barriers and, per tile, to "acc full";
-//   warps 2-9 widen nibbles to E4M3 into a 3-stage operand ring laid out in the
+//   warps 2-9 widen nibbles to E4M3 into an operand ring laid out in the
 //             128-byte-swizzled K-major form the MMA descriptors expect, keep
 //             per-row code sums, and hand each tile's offset terms and weight
 //             scales to the epilogue through shared memory;
@@ -45,35 +59,42 @@
 namespace rq {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128;      // tile (K in codes)
-#ifndef RQ_TC_OP_STAGES
-#define RQ_TC_OP_STAGES 3
-#endif
-constexpr int PK_STAGES = 3, OP_STAGES = RQ_TC_OP_STAGES;
+constexpr int BM = 128, BN = 256, BK = 128;      // per-CTA A rows, tile columns, K block (codes)
 constexpr int kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kEpiWarps = 8;
-constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreadsTC = 32 * (2 + kConvWarps + kEpiWarps);
-constexpr int PK_A = BM * BK / 2, PK_W = BN * BK / 2;   // packed bytes per stage
-constexpr int OP_A = BM * BK, OP_W = BN * BK;           // e4m3 bytes per stage
-constexpr uint32_t kTmemCols = 512;                 // two 128x256 fp32 accumulators
+constexpr uint32_t kTmemCols = 512;                 // two 128 x 256 fp32 accumulators
 constexpr long long kWaitLimitCycles = 4000000000ll;    // ~2 s at 2 GHz
 
+template <bool PAIR>
+struct Cfg {
+    static constexpr int NCTA = PAIR ? 2 : 1;
+    static constexpr int WROWS = BN / NCTA;         // W rows (output channels) per CTA
+    static constexpr int TILE_M = BM * NCTA;        // output rows per tile
+    static constexpr int PK_STAGES = PAIR ? 4 : 3, OP_STAGES = PAIR ? 4 : 3;
+    static constexpr int PK_A = BM * BK / 2, PK_W = WROWS * BK / 2;   // packed bytes per stage
+    static constexpr int OP_A = BM * BK, OP_W = WROWS * BK;           // e4m3 bytes per stage
+    static constexpr int NWCH = WROWS * (BK / 32) / kConvThreads;    // W chunks per converter thread
+};
+
+template <bool PAIR>
 struct Smem {
-    alignas(1024) uint8_t opA[OP_STAGES][OP_A];
-    alignas(1024) uint8_t opW[OP_STAGES][OP_W];
-    alignas(128) uint8_t pkA[PK_STAGES][PK_A];
-    alignas(128) uint8_t pkW[PK_STAGES][PK_W];
+    using C = Cfg<PAIR>;
+    alignas(1024) uint8_t opA[C::OP_STAGES][C::OP_A];
+    alignas(1024) uint8_t opW[C::OP_STAGES][C::OP_W];
+    alignas(128) uint8_t pkA[C::PK_STAGES][C::PK_A];
+    alignas(128) uint8_t pkW[C::PK_STAGES][C::PK_W];
     int rowterm[2][BM];      // -8 * sum_k u_a, per tile parity
-    int colterm[2][BN];      // 64 K - 8 * sum_k u_w
+    int colterm[2][BN];      // 64 K - 8 * sum_k u_w, all columns of the tile
     float wscale[2][BN];     // weight scales of the tile's columns
-    alignas(8) uint64_t pk_full[PK_STAGES];
-    uint64_t pk_empty[PK_STAGES];
-    uint64_t op_full[OP_STAGES];
-    uint64_t op_empty[OP_STAGES];
-    uint64_t acc_full[2], acc_empty[2];
-    uint64_t sum_full[2], sum_empty[2];
+    alignas(8) uint64_t pk_full[C::PK_STAGES];
+    uint64_t pk_empty[C::PK_STAGES];
+    uint64_t op_full[C::OP_STAGES];      // (leader) both CTAs' converter warps
+    uint64_t op_empty[C::OP_STAGES];     // MMA commit (multicast to both CTAs)
+    uint64_t acc_full[2], acc_empty[2];  // acc_empty (leader): both CTAs' epilogues
+    uint64_t sum_full[2], sum_empty[2];  // own converters -> own epilogue and back
+    uint64_t col_full[2];                // (pair) the peer's half of colterm has arrived
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -89,8 +110,33 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+
+// Arrive on the barrier at the same offset in CTA `rank` of the cluster (the own
+// CTA included), with release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cta(const uint64_t *b, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(b)), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// Arrival on another CTA's barrier with release at CTA scope only: for operands
+// that the arriving CTA wrote into its own shared memory for its own SM's tensor
+// core (made visible to that async proxy by fence.proxy.async beforehand).  A
+// cluster-scope release would wait for the SM's memory traffic to drain, which
+// costs more than a K block's MMAs.
+__device__ __forceinline__ void mbar_arrive_remote_cta_scope(const uint64_t *b, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(b)), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
@@ -102,25 +148,39 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
                  : "memory");
 }
 
+// CLUSTER: acquire at cluster scope, for barriers that other CTAs (or the pair's
+// multicast MMA commits) arrive on; CTA scope otherwise.
+template <bool CLUSTER>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *b, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
-        : "memory");
+    if constexpr (CLUSTER) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(b)), "r"(parity)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(b)), "r"(parity)
+            : "memory");
+    }
     return ok != 0;
 }
 
 // Bounded wait: returns false (and raises the abort flag and the error word) if
 // the phase does not complete in time or another role has aborted.
-__device__ __forceinline__ bool mbar_wait(Smem &s, uint64_t *b, uint32_t parity, int *err) {
-    if (mbar_try_wait(b, parity)) return true;
+template <bool CLUSTER = false, bool PAIR>
+__device__ __forceinline__ bool mbar_wait(Smem<PAIR> &s, uint64_t *b, uint32_t parity, int *err) {
+    if (mbar_try_wait<CLUSTER>(b, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(b, parity)) return true;
+        if (mbar_try_wait<CLUSTER>(b, parity)) return true;
         if (s.abort_flag) return false;
         if (clock64() - t0 > kWaitLimitCycles) {
             s.abort_flag = 1;
@@ -150,22 +210,45 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor: kind::f8f6f4, A = B = E4M3, D = F32, both K-major.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-        : "memory");
+// Instruction descriptor: kind::f8f6f4, A = B = E4M3, D = F32, both K-major, N = 256.
+template <bool PAIR>
+constexpr uint32_t idesc() {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
+           ((uint32_t)(Cfg<PAIR>::TILE_M >> 4) << 24);
 }
 
+template <bool PAIR>
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    if constexpr (PAIR) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc<PAIR>()), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc<PAIR>()), "r"(accumulate)
+            : "memory");
+    }
+}
+
+// Signal `bar` when the MMAs issued so far complete: in every CTA of the pair.
+template <bool PAIR>
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
+    if constexpr (PAIR) {
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                smem_u32(bar)),
+            "h"((uint16_t)3)
+            : "memory");
+    } else {
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                     : "memory");
+    }
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -190,44 +273,69 @@ __device__ __forceinline__ uint32_t widen(uint32_t w, uint32_t &lo, uint32_t &hi
     return lo + hi;   // four bytes, each <= 30
 }
 
-template <int YMODE>
+template <bool PAIR>
+__device__ __forceinline__ void cluster_sync() {
+    if constexpr (PAIR) {
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    } else {
+        __syncthreads();
+    }
+}
+
+template <int YMODE, bool PAIR>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                const __grid_constant__ TcParams prm) {
+    using C = Cfg<PAIR>;
+    using S = Smem<PAIR>;
     extern __shared__ uint8_t smem_raw[];
-    Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // align by offsetting the shared array itself, so the compiler keeps the
+    // shared address space (plain LDS/STS instead of generic accesses)
+    S &s = *reinterpret_cast<S *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_rank() : 0;
     const int kblocks = (int)(prm.K / BK);
     const int64_t n_tiles_n = (prm.N + BN - 1) / BN;
-    const int64_t n_tiles = n_tiles_n * ((prm.M + BM - 1) / BM);
+    const int64_t n_tiles = n_tiles_n * ((prm.M + C::TILE_M - 1) / C::TILE_M);
+    const int64_t first_tile = blockIdx.x / C::NCTA, tile_step = gridDim.x / C::NCTA;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < PK_STAGES; ++i) {
+        for (int i = 0; i < C::PK_STAGES; ++i) {
             mbar_init(&s.pk_full[i], 1);
-            mbar_init(&s.pk_empty[i], kConvThreads);
+            mbar_init(&s.pk_empty[i], kConvWarps);
         }
-        for (int i = 0; i < OP_STAGES; ++i) {
-            mbar_init(&s.op_full[i], kConvThreads);
+        for (int i = 0; i < C::OP_STAGES; ++i) {
+            mbar_init(&s.op_full[i], kConvWarps * C::NCTA);
             mbar_init(&s.op_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.acc_full[i], 1);
-            mbar_init(&s.acc_empty[i], kEpiThreads);
-            mbar_init(&s.sum_full[i], kConvThreads);
-            mbar_init(&s.sum_empty[i], kEpiThreads);
+            mbar_init(&s.acc_empty[i], kEpiWarps * C::NCTA);
+            mbar_init(&s.sum_full[i], kConvWarps);
+            mbar_init(&s.sum_empty[i], kEpiWarps);
+            mbar_init(&s.col_full[i], kEpiWarps);
         }
         s.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s.tmem_base)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if constexpr (PAIR) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(&s.tmem_base)),
+                         "r"(kTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(&s.tmem_base)),
+                         "r"(kTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
+    cluster_sync<PAIR>();    // barriers initialized and TMEM allocated in both CTAs
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = s.tmem_base;
 
@@ -236,40 +344,41 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0) {
             int64_t g = 0;                                   // global K-block counter
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const int m0 = (int)(tile / n_tiles_n) * BM, n0 = (int)(tile % n_tiles_n) * BN;
+            for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step) {
+                const int m0 = (int)(tile / n_tiles_n) * C::TILE_M + (int)rank * BM;
+                const int n0 = (int)(tile % n_tiles_n) * BN + (int)rank * C::WROWS;
                 for (int kb = 0; kb < kblocks; ++kb, ++g) {
-                    const int st = (int)(g % PK_STAGES);
-                    if (!mbar_wait(s, &s.pk_empty[st], (uint32_t)((g / PK_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
-                    mbar_expect_tx(&s.pk_full[st], PK_A + PK_W);
+                    const int st = (int)(g % C::PK_STAGES);
+                    if (!mbar_wait(s, &s.pk_empty[st], (uint32_t)((g / C::PK_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
+                    mbar_expect_tx(&s.pk_full[st], C::PK_A + C::PK_W);
                     tma_load_2d(s.pkA[st], &tmA, &s.pk_full[st], kb * (BK / 2), m0);
                     tma_load_2d(s.pkW[st], &tmW, &s.pk_full[st], kb * (BK / 2), n0);
                 }
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+        // ---------------- MMA issuer (the leader CTA of a pair) ----------------
+        if (lane == 0 && rank == 0) {
             int64_t g = 0;
             int it = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++it) {
+            for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step, ++it) {
                 const int buf = it & 1;
-                // the epilogue must have drained this accumulator (two tiles ago)
-                if (!mbar_wait(s, &s.acc_empty[buf], (uint32_t)((it >> 1) & 1) ^ 1, prm.err)) break;
+                // the epilogues must have drained this accumulator (two tiles ago)
+                if (!mbar_wait<PAIR>(s, &s.acc_empty[buf], (uint32_t)((it >> 1) & 1) ^ 1, prm.err)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t d = tmem + (uint32_t)(buf * BN);
                 for (int kb = 0; kb < kblocks; ++kb, ++g) {
-                    const int st = (int)(g % OP_STAGES);
-                    if (!mbar_wait(s, &s.op_full[st], (uint32_t)((g / OP_STAGES) & 1), prm.err)) { ok = false; break; }
+                    const int st = (int)(g % C::OP_STAGES);
+                    if (!mbar_wait<PAIR>(s, &s.op_full[st], (uint32_t)((g / C::OP_STAGES) & 1), prm.err)) { ok = false; break; }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     const uint32_t a0 = smem_u32(s.opA[st]), w0 = smem_u32(s.opW[st]);
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
-                        mma_f8(d, sw128_desc(a0 + 32 * k), sw128_desc(w0 + 32 * k), (kb | k) != 0);
-                    mma_commit(&s.op_empty[st]);
+                        mma_f8<PAIR>(d, sw128_desc(a0 + 32 * k), sw128_desc(w0 + 32 * k), (kb | k) != 0);
+                    mma_commit<PAIR>(&s.op_empty[st]);
                 }
-                if (ok) mma_commit(&s.acc_full[buf]);
+                if (ok) mma_commit<PAIR>(&s.acc_full[buf]);
             }
         }
     } else if (warp < 2 + kConvWarps) {
@@ -280,25 +389,30 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int64_t g = 0;
         int it = 0;
         bool ok = true;
-        for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++it) {
+        for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step, ++it) {
             const int n0 = (int)(tile % n_tiles_n) * BN;
-            uint32_t sumA[2] = {0, 0}, sumW[4] = {0, 0, 0, 0};
+            uint32_t sumA[2] = {0, 0}, sumW[C::NWCH];
+#pragma unroll
+            for (int j = 0; j < C::NWCH; ++j) sumW[j] = 0;
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
-                const int ps = (int)(g % PK_STAGES);
-                if (!mbar_wait(s, &s.pk_full[ps], (uint32_t)((g / PK_STAGES) & 1), prm.err)) { ok = false; break; }
-                uint4 a[2], w[4];
+                const int ps = (int)(g % C::PK_STAGES);
+                if (!mbar_wait(s, &s.pk_full[ps], (uint32_t)((g / C::PK_STAGES) & 1), prm.err)) { ok = false; break; }
+                uint4 a[2], w[C::NWCH];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) a[j] = reinterpret_cast<const uint4 *>(s.pkA[ps])[t + 256 * j];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) w[j] = reinterpret_cast<const uint4 *>(s.pkW[ps])[t + 256 * j];
-                // The next TMA refill of this stage writes through the async proxy:
-                // order this thread's generic reads of the stage before it, or the
-                // refill can overtake them.
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(&s.pk_empty[ps]);
-
-                const int os = (int)(g % OP_STAGES);
-                if (!mbar_wait(s, &s.op_empty[os], (uint32_t)((g / OP_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
+                for (int j = 0; j < C::NWCH; ++j) w[j] = reinterpret_cast<const uint4 *>(s.pkW[ps])[t + 256 * j];
+                const int os = (int)(g % C::OP_STAGES);
+                if constexpr (PAIR) {
+                    // one cluster-scope acquire per warp (the release is the leader's
+                    // multicast commit); __syncwarp orders the other lanes after it
+                    int got = 1;
+                    if (lane == 0) got = mbar_wait<true>(s, &s.op_empty[os], (uint32_t)((g / C::OP_STAGES) & 1) ^ 1, prm.err);
+                    __syncwarp();
+                    if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+                } else {
+                    if (!mbar_wait(s, &s.op_empty[os], (uint32_t)((g / C::OP_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
+                }
                 // row r, chunk ch -> 32 e4m3 bytes = granules 2ch, 2ch+1 of the 128-byte row
                 auto emit = [&](uint8_t *base, int r, const uint4 &v, uint32_t &sum) {
                     uint32_t lo[4], hi[4], acc = 0;
@@ -314,11 +428,19 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                 for (int j = 0; j < 2; ++j) emit(s.opA[os], rq + 64 * j, a[j], sumA[j]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) emit(s.opW[os], rq + 64 * j, w[j], sumW[j]);
-                // every writer makes its own stores visible to the tensor core's
-                // (async-proxy) reads, then arrives itself
+                for (int j = 0; j < C::NWCH; ++j) emit(s.opW[os], rq + 64 * j, w[j], sumW[j]);
+                // One proxy fence per thread orders both its generic reads of the
+                // packed stage before the next TMA refill of it (or the refill can
+                // overtake them) and its operand stores before the tensor core's
+                // reads; then one lane per warp releases both stages (the operand
+                // stage through the leader for a pair).
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(&s.op_full[os]);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&s.pk_empty[ps]);
+                    if (rank == 0) mbar_arrive(&s.op_full[os]);
+                    else mbar_arrive_remote_cta_scope(&s.op_full[os], 0);
+                }
             }
             if (!ok) break;
             // row sums: the four lanes sharing a row hold its four chunks
@@ -328,19 +450,23 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 sumA[j] += __shfl_xor_sync(0xffffffffu, sumA[j], 2);
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < C::NWCH; ++j) {
                 sumW[j] += __shfl_xor_sync(0xffffffffu, sumW[j], 1);
                 sumW[j] += __shfl_xor_sync(0xffffffffu, sumW[j], 2);
             }
-            // hand this tile's offset terms and weight scales to the epilogue
+            // hand this tile's offset terms and weight scales to the own epilogue
+            // (for a pair, its epilogue passes this CTA's half of the column terms
+            // on to the peer)
             const int buf = it & 1;
             if (!mbar_wait(s, &s.sum_empty[buf], (uint32_t)((it >> 1) & 1) ^ 1, prm.err)) { ok = false; break; }
             if (ch == 0) {
                 for (int j = 0; j < 2; ++j) s.rowterm[buf][rq + 64 * j] = -8 * (int)sumA[j];
-                for (int j = 0; j < 4; ++j) s.colterm[buf][rq + 64 * j] = 64 * (int)prm.K - 8 * (int)sumW[j];
+                for (int j = 0; j < C::NWCH; ++j)
+                    s.colterm[buf][(int)rank * C::WROWS + rq + 64 * j] = 64 * (int)prm.K - 8 * (int)sumW[j];
             }
             if (YMODE != 2) s.wscale[buf][t] = (n0 + t < prm.N) ? prm.sw[n0 + t] : 0.f;
-            mbar_arrive(&s.sum_full[buf]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.sum_full[buf]);
         }
     } else {
         // ---------------- epilogue: TMEM -> offset removal -> scales -> global ----------------
@@ -348,13 +474,31 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int q = warp & 3;                          // TMEM lane quarter this warp may read
         const int colhalf = e >> 7;                      // columns 0-127 or 128-255
         int it = 0;
-        for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+        for (int64_t tile = first_tile; tile < n_tiles; tile += tile_step, ++it) {
             const int buf = it & 1;
             const uint32_t par = (uint32_t)((it >> 1) & 1);
-            if (!mbar_wait(s, &s.acc_full[buf], par, prm.err)) break;
+            if (!mbar_wait<PAIR>(s, &s.acc_full[buf], par, prm.err)) break;
             if (!mbar_wait(s, &s.sum_full[buf], par, prm.err)) break;
+            if constexpr (PAIR) {
+                // Exchange the halves of the column terms: write this CTA's half into
+                // the peer, release at cluster scope (generic data read by the peer's
+                // threads), and wait for the peer's half.  Both epilogues are past
+                // this tile's acc_full, so both have finished the tile that last used
+                // this buffer.
+                if (e < C::WROWS) {
+                    const int col = (int)rank * C::WROWS + e;
+                    uint32_t remote;
+                    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                                 : "=r"(remote)
+                                 : "r"(smem_u32(&s.colterm[buf][col])), "r"(rank ^ 1u));
+                    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(s.colterm[buf][col]) : "memory");
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cta(&s.col_full[buf], rank ^ 1u);
+                if (!mbar_wait<true>(s, &s.col_full[buf], par, prm.err)) break;
+            }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const int64_t m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
+            const int64_t m0 = (tile / n_tiles_n) * C::TILE_M + (int64_t)rank * BM, n0 = (tile % n_tiles_n) * BN;
             const int mr = 32 * q + lane;
             const int64_t m = m0 + mr;
             const int rowt = s.rowterm[buf][mr];
@@ -406,16 +550,24 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             // this accumulator and these offset terms may be reused
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            mbar_arrive(&s.acc_empty[buf]);
-            mbar_arrive(&s.sum_empty[buf]);
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (PAIR) mbar_arrive_cta(&s.acc_empty[buf], 0);
+                else mbar_arrive(&s.acc_empty[buf]);
+                mbar_arrive(&s.sum_empty[buf]);
+            }
         }
     }
 
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
+    cluster_sync<PAIR>();    // all MMAs done and all TMEM reads finished in both CTAs
     if (warp == 1) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+        if constexpr (PAIR) {
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+        } else {
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+        }
     }
 }
 
@@ -452,27 +604,48 @@ bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row_byte
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int YMODE>
-cudaError_t launch_mode(const CUtensorMap &ta, const CUtensorMap &tw, const TcParams &p, cudaStream_t stream) {
-    auto kern = w4a4_tc_kernel<YMODE>;
-    const size_t smem = sizeof(Smem) + 1024;
+int sm_count() {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 0;
+    }
+    return sms;
+}
+
+template <int YMODE, bool PAIR>
+cudaError_t launch_mode(const GemmArgs &g, const TcParams &p, cudaStream_t stream) {
+    using C = Cfg<PAIR>;
+    CUtensorMap ta, tw;
+    if (!make_map(&ta, g.a_q, g.M, g.K / 2, BM) || !make_map(&tw, g.w_q, g.N, g.K / 2, C::WROWS))
+        return cudaErrorInvalidValue;
+    auto kern = w4a4_tc_kernel<YMODE, PAIR>;
+    const size_t smem = sizeof(Smem<PAIR>) + 1024;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
-    const int64_t tiles = ((p.N + BN - 1) / BN) * ((p.M + BM - 1) / BM);
-    const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);   // persistent: one CTA per SM
-    kern<<<grid, kThreadsTC, smem, stream>>>(ta, tw, p);
-    return cudaGetLastError();
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorUnknown;
+    const int64_t tiles = ((p.N + BN - 1) / BN) * ((p.M + C::TILE_M - 1) / C::TILE_M);
+    // persistent: one CTA per SM (one pair per two SMs)
+    const int64_t units = tiles < sms / C::NCTA ? tiles : sms / C::NCTA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units * C::NCTA));
+    cfg.blockDim = dim3(kThreadsTC);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C::NCTA;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tw, p);
 }
 
 }  // namespace
@@ -480,15 +653,16 @@ cudaError_t launch_mode(const CUtensorMap &ta, const CUtensorMap &tw, const TcPa
 bool w4a4_gemm_tc_supported(const GemmArgs &g) { return g.M > 64 && g.K % BK == 0 && g.K <= 65536; }
 
 cudaError_t launch_w4a4_gemm_tc(const GemmArgs &g, cudaStream_t stream) {
-    CUtensorMap ta, tw;
-    if (!make_map(&ta, g.a_q, g.M, g.K / 2, BM) || !make_map(&tw, g.w_q, g.N, g.K / 2, BN))
-        return cudaErrorInvalidValue;
     TcParams p{g.a_scales, g.w_scales, g.y, g.M, g.N, g.K, error_word_device_ptr()};
     if (!p.err) return cudaErrorUnknown;
-    switch (g.y_mode) {
-        case 0: return launch_mode<0>(ta, tw, p, stream);
-        case 1: return launch_mode<1>(ta, tw, p, stream);
-        default: return launch_mode<2>(ta, tw, p, stream);
+    const bool pair = g.M > BM;   // tiles of 256 rows on SM pairs; one SM for M <= 128
+    switch (g.y_mode * 2 + (pair ? 1 : 0)) {
+        case 0: return launch_mode<0, false>(g, p, stream);
+        case 1: return launch_mode<0, true>(g, p, stream);
+        case 2: return launch_mode<1, false>(g, p, stream);
+        case 3: return launch_mode<1, true>(g, p, stream);
+        case 4: return launch_mode<2, false>(g, p, stream);
+        default: return launch_mode<2, true>(g, p, stream);
     }
 }
 
