@@ -86,8 +86,8 @@ struct Smem {
     alignas(128) uint8_t pkA[C::PK_STAGES][C::PK_A];
     alignas(128) uint8_t pkW[C::PK_STAGES][C::PK_W];
     int rowterm[2][BM];      // -8 * sum_k u_a, per tile parity
-    int colterm[2][BN];      // 64 K - 8 * sum_k u_w, all columns of the tile
-    float wscale[2][BN];     // weight scales of the tile's columns
+    alignas(16) int colterm[2][BN];      // 64 K - 8 * sum_k u_w, all columns of the tile
+    alignas(16) float wscale[2][BN];     // weight scales of the tile's columns
     alignas(8) uint64_t pk_full[C::PK_STAGES];
     uint64_t pk_empty[C::PK_STAGES];
     uint64_t op_full[C::OP_STAGES];      // (leader) both CTAs' converter warps
@@ -391,6 +391,9 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         bool ok = true;
         for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step, ++it) {
             const int n0 = (int)(tile % n_tiles_n) * BN;
+            // the tile's weight scale for column t, loaded now so that its latency
+            // is not on the converters' path at the end of the tile
+            const float wsc = (YMODE != 2 && n0 + t < prm.N) ? prm.sw[n0 + t] : 0.f;
             uint32_t sumA[2] = {0, 0}, sumW[C::NWCH];
 #pragma unroll
             for (int j = 0; j < C::NWCH; ++j) sumW[j] = 0;
@@ -464,7 +467,7 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int j = 0; j < C::NWCH; ++j)
                     s.colterm[buf][(int)rank * C::WROWS + rq + 64 * j] = 64 * (int)prm.K - 8 * (int)sumW[j];
             }
-            if (YMODE != 2) s.wscale[buf][t] = (n0 + t < prm.N) ? prm.sw[n0 + t] : 0.f;
+            if (YMODE != 2) s.wscale[buf][t] = wsc;
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.sum_full[buf]);
         }
@@ -510,11 +513,18 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + col0), r);
                 if (m < prm.M) {
                     int acc[32];
+                    const int4 *ct = reinterpret_cast<const int4 *>(&s.colterm[buf][col0]);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int u = __float2int_rn(__uint_as_float(r[j]) * 262144.0f);   // exact: x 2^18
-                        acc[j] = u + rowt + s.colterm[buf][col0 + j];
+                    for (int j = 0; j < 32; j += 4) {
+                        const int4 c4 = ct[j / 4];
+                        const int cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int u = __float2int_rn(__uint_as_float(r[j + i]) * 262144.0f);   // exact: x 2^18
+                            acc[j + i] = u + rowt + cv[i];
+                        }
                     }
+                    const float4 *ws4 = reinterpret_cast<const float4 *>(&s.wscale[buf][col0]);
                     const int64_t nb = n0 + col0;
                     if (YMODE == 2) {
                         int *yr = static_cast<int *>(prm.y) + m * prm.N + nb;
@@ -527,11 +537,12 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                         for (int j = 0; j < 32; j += 4) {
                             if (nb + j + 3 >= prm.N) continue;
+                            const float4 w4 = ws4[j / 4];
                             float4 o;
-                            o.x = ((float)acc[j] * sa) * s.wscale[buf][col0 + j];
-                            o.y = ((float)acc[j + 1] * sa) * s.wscale[buf][col0 + j + 1];
-                            o.z = ((float)acc[j + 2] * sa) * s.wscale[buf][col0 + j + 2];
-                            o.w = ((float)acc[j + 3] * sa) * s.wscale[buf][col0 + j + 3];
+                            o.x = ((float)acc[j] * sa) * w4.x;
+                            o.y = ((float)acc[j + 1] * sa) * w4.y;
+                            o.z = ((float)acc[j + 2] * sa) * w4.z;
+                            o.w = ((float)acc[j + 3] * sa) * w4.w;
                             *reinterpret_cast<float4 *>(yr + j) = o;
                         }
                     } else {
@@ -540,9 +551,11 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         for (int j = 0; j < 32; j += 8) {
                             if (nb + j + 7 >= prm.N) continue;
                             __align__(16) __half h[8];
+                            const float4 wa = ws4[j / 4], wb = ws4[j / 4 + 1];
+                            const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
                             for (int e2 = 0; e2 < 8; ++e2)
-                                h[e2] = __float2half_rn(((float)acc[j + e2] * sa) * s.wscale[buf][col0 + j + e2]);
+                                h[e2] = __float2half_rn(((float)acc[j + e2] * sa) * wv[e2]);
                             *reinterpret_cast<uint4 *>(yr + j) = *reinterpret_cast<const uint4 *>(h);
                         }
                     }
@@ -559,6 +572,7 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
     }
 
+    __syncwarp();            // lanes that skipped a single-lane role wait for it here
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     cluster_sync<PAIR>();    // all MMAs done and all TMEM reads finished in both CTAs
     if (warp == 1) {
