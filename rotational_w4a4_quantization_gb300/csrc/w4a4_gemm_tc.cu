@@ -17,34 +17,44 @@
 //    warps add up each row's u while widening, and the epilogue removes the
 //    offset, then applies the per-token x per-channel scales.
 //
-// Pipeline (persistent; K in blocks of 128 codes; two TMEM accumulators so tile
-// i's epilogue overlaps tile i+1's MMAs).  Two variants share the code:
+// Data path per K block of 128 codes (persistent kernel; two 128 x 256 fp32
+// accumulators in TMEM, all 512 columns, so tile i's epilogue overlaps tile
+// i+1's MMAs): TMA brings the packed tiles into a shared-memory ring, converter
+// warps widen them into an operand ring in the 128-byte-swizzled K-major layout
+// of the MMA descriptors, one thread issues the MMAs.
+//
+// Two variants share the code:
 //  * CTA pairs (M > 128): a cluster of two CTAs on two SMs computes 256 x 256
 //    tiles with tcgen05.mma.cta_group::2 (M256 N256 K32).  Each CTA loads and
 //    widens its own 128 rows of A and its own half (128 rows) of the W tile, so
 //    every SM converts and serves half of B: a third less shared-memory traffic
-//    per MAC than one CTA doing 128 x 256 alone.  The leader CTA issues the MMAs;
-//    commits multicast to both CTAs' barriers.  The peer's converter warps arrive
-//    on the leader's operand barriers through distributed shared memory with a
-//    CTA-scope release: their operands stay in the peer's own shared memory and
-//    are read by the peer SM's tensor core, and a cluster-scope release there
-//    (it waits for the SM's memory traffic to drain) took longer than the K
-//    block's MMAs.  Once per tile the epilogues exchange the halves of the
-//    per-column offset terms (cluster-scope release, as the peer's threads read
-//    them) and release the accumulator to the leader;
+//    per MAC than one CTA doing 128 x 256 alone.  The
+//    leader CTA issues the MMAs; commits multicast to both CTAs' barriers.  The
+//    peer's converter warps arrive on the leader's operand barriers through
+//    distributed shared memory with a CTA-scope release: their operands stay in
+//    the peer's own shared memory and are read by the peer SM's tensor
+//    core, and a cluster-scope release there (it waits for the SM's memory
+//    traffic to drain) took longer than the K block's MMAs.  Once per tile the
+//    epilogues exchange the halves of the per-column offset terms (cluster-scope
+//    release, as the peer's threads read them) and release the accumulator to
+//    the leader;
 //  * single CTAs (64 < M <= 128): 128 x 256 tiles with cta_group::1.
 // Roles in each CTA:
-//   warp 0    TMA producer: packed A (128 x 64 B) and W (128 or 256 x 64 B) tiles
-//             into a ring (mbarrier transaction counts);
+//   warp 0    TMA producer: packed A (128 x 64 B) and W (128 or 256 x 64 B)
+//             tiles into a ring (mbarrier transaction counts);
 //   warp 1    allocates 512 TMEM columns; one lane (of the leader) issues 4 MMAs
 //             per K block into the tile's accumulator and commits them to the
-//             operand ring's "empty" barriers and, per tile, to "acc full";
-//   warps 2-9 widen nibbles to E4M3 into an operand ring laid out in the
-//             128-byte-swizzled K-major form the MMA descriptors expect, keep
-//             per-row code sums, and hand each tile's offset terms and weight
-//             scales to the epilogue through shared memory;
-//   warps 10-17 epilogue: tcgen05.ld of the fp32 accumulator, offset removal,
-//             scales (broadcast from shared memory), 16-byte stores.
+//             operand rings' "empty" barriers and, per tile, to "acc full";
+//   warps 2-13 converters, three teams of four (team t takes the K blocks g with
+//             g % 3 == t, so each warp has three MMA periods for its block: the
+//             widening of one block is a chain of shared-memory loads, ALU work
+//             and stores that takes several MMA periods).  A team widens all of
+//             its block's A and W chunks.  Each team keeps partial per-row code
+//             sums and hands them, and the weight scales, to the epilogue through
+//             shared memory;
+//   warps 14-17 epilogue (one per TMEM lane quarter): tcgen05.ld of the fp32
+//             accumulator, offset removal, scales (broadcast from shared memory),
+//             16-byte stores.
 // The order of k inside each 8-code group is permuted the same way for A and W
 // (even codes, then odd codes), which leaves every dot product unchanged.
 // Every mbarrier wait is bounded: on expiry the CTA raises the library's error
@@ -60,11 +70,13 @@ namespace rq {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;      // per-CTA A rows, tile columns, K block (codes)
-constexpr int kConvWarps = 8;
-constexpr int kConvThreads = 32 * kConvWarps;
-constexpr int kEpiWarps = 8;
+constexpr int kTeamWarps = 4;                     // one per TMEM lane quarter
+constexpr int kTeams = 3;                         // team t converts the K blocks g with g % 3 == t
+constexpr int kConvWarps = kTeams * kTeamWarps;
+constexpr int kTeamThreads = 32 * kTeamWarps;
+constexpr int kEpiWarps = 4;                      // one per TMEM lane quarter
 constexpr int kThreadsTC = 32 * (2 + kConvWarps + kEpiWarps);
-constexpr uint32_t kTmemCols = 512;                 // two 128 x 256 fp32 accumulators
+constexpr uint32_t kTmemCols = 2 * BN;            // two 128 x 256 fp32 accumulators
 constexpr long long kWaitLimitCycles = 4000000000ll;    // ~2 s at 2 GHz
 
 template <bool PAIR>
@@ -72,10 +84,20 @@ struct Cfg {
     static constexpr int NCTA = PAIR ? 2 : 1;
     static constexpr int WROWS = BN / NCTA;         // W rows (output channels) per CTA
     static constexpr int TILE_M = BM * NCTA;        // output rows per tile
-    static constexpr int PK_STAGES = PAIR ? 4 : 3, OP_STAGES = PAIR ? 4 : 3;
+    // Stage counts and the team rotation must keep every mbarrier parity wait at
+    // most one phase ahead of its barrier: a packed stage is owned by one team
+    // (PK_STAGES a multiple of kTeams, so the phase before the one a team waits
+    // for is its own finished block), and MMA commits complete in order, so an
+    // operand-ring wait is safe with OP_STAGES >= kTeams.
+    // The packed ring is the deeper one: it covers the TMA latency from L2/HBM
+    // (6 + 3 stages ran the prefill GEMM ~7% faster than 3 + 5).
+    static constexpr int PK_STAGES = PAIR ? 2 * kTeams : kTeams, OP_STAGES = 3;
     static constexpr int PK_A = BM * BK / 2, PK_W = WROWS * BK / 2;   // packed bytes per stage
     static constexpr int OP_A = BM * BK, OP_W = WROWS * BK;           // e4m3 bytes per stage
-    static constexpr int NWCH = WROWS * (BK / 32) / kConvThreads;    // W chunks per converter thread
+    static constexpr int NACH = BM * (BK / 32) / kTeamThreads;       // A chunks per thread and K block
+    static constexpr int NWCH = WROWS * (BK / 32) / kTeamThreads;    // W chunks per thread and K block
+    static_assert(WROWS * (BK / 32) % kTeamThreads == 0, "W chunks split evenly");
+    static_assert(PK_STAGES % kTeams == 0 && OP_STAGES >= kTeams, "parity waits stay one phase ahead at most");
 };
 
 template <bool PAIR>
@@ -85,7 +107,8 @@ struct Smem {
     alignas(1024) uint8_t opW[C::OP_STAGES][C::OP_W];
     alignas(128) uint8_t pkA[C::PK_STAGES][C::PK_A];
     alignas(128) uint8_t pkW[C::PK_STAGES][C::PK_W];
-    int rowterm[2][BM];      // -8 * sum_k u_a, per tile parity
+    alignas(16) int rowsum[2][BM];       // per tile parity: sum_k u_a (the teams add in; the epilogue clears)
+    alignas(16) int colsum[2][BN];       // the same for sum_k u_w, this CTA's W rows
     alignas(16) int colterm[2][BN];      // 64 K - 8 * sum_k u_w, all columns of the tile
     alignas(16) float wscale[2][BN];     // weight scales of the tile's columns
     alignas(8) uint64_t pk_full[C::PK_STAGES];
@@ -94,7 +117,7 @@ struct Smem {
     uint64_t op_empty[C::OP_STAGES];     // MMA commit (multicast to both CTAs)
     uint64_t acc_full[2], acc_empty[2];  // acc_empty (leader): both CTAs' epilogues
     uint64_t sum_full[2], sum_empty[2];  // own converters -> own epilogue and back
-    uint64_t col_full[2];                // (pair) the peer's half of colterm has arrived
+    uint64_t col_full[2];                // colterm complete: own and (pair) the peer's epilogue warps
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -129,10 +152,10 @@ __device__ __forceinline__ void mbar_arrive_cta(const uint64_t *b, uint32_t rank
 }
 
 // Arrival on another CTA's barrier with release at CTA scope only: for operands
-// that the arriving CTA wrote into its own shared memory for its own SM's tensor
-// core (made visible to that async proxy by fence.proxy.async beforehand).  A
-// cluster-scope release would wait for the SM's memory traffic to drain, which
-// costs more than a K block's MMAs.
+// that the arriving CTA wrote into its own shared or tensor memory for its own
+// SM's tensor core (made visible to it by fence.proxy.async / tcgen05.wait::st
+// beforehand).  A cluster-scope release would wait for the SM's memory traffic
+// to drain, which costs more than a K block's MMAs.
 __device__ __forceinline__ void mbar_arrive_remote_cta_scope(const uint64_t *b, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(b)), "r"(rank));
@@ -174,12 +197,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *b, uint32_t parity) {
 }
 
 // Bounded wait: returns false (and raises the abort flag and the error word) if
-// the phase does not complete in time or another role has aborted.
-template <bool CLUSTER = false, bool PAIR>
+// the phase does not complete in time or another role has aborted.  SLEEP backs
+// off with __nanosleep between polls: for the roles with slack (the producer,
+// the epilogue), whose polling would otherwise take issue and shared-memory pipe
+// slots from the converter warps of the same SM sub-partition.
+template <bool CLUSTER = false, bool SLEEP = false, bool PAIR>
 __device__ __forceinline__ bool mbar_wait(Smem<PAIR> &s, uint64_t *b, uint32_t parity, int *err) {
     if (mbar_try_wait<CLUSTER>(b, parity)) return true;
     const long long t0 = clock64();
     while (true) {
+        if constexpr (SLEEP) __nanosleep(128);
         if (mbar_try_wait<CLUSTER>(b, parity)) return true;
         if (s.abort_flag) return false;
         if (clock64() - t0 > kWaitLimitCycles) {
@@ -187,6 +214,20 @@ __device__ __forceinline__ bool mbar_wait(Smem<PAIR> &s, uint64_t *b, uint32_t p
             atomicExch(err, 1);
             return false;
         }
+    }
+}
+
+// Warp-wide wait on a barrier that the pair's multicast MMA commit releases: one
+// cluster-scope acquire per warp, and __syncwarp orders the other lanes after it.
+template <bool PAIR>
+__device__ __forceinline__ bool warp_wait_commit(Smem<PAIR> &s, uint64_t *b, uint32_t parity, int lane, int *err) {
+    if constexpr (PAIR) {
+        int got = 1;
+        if (lane == 0) got = mbar_wait<true>(s, b, parity, err);
+        __syncwarp();
+        return __shfl_sync(0xffffffffu, got, 0) != 0;
+    } else {
+        return mbar_wait(s, b, parity, err);
     }
 }
 
@@ -217,6 +258,7 @@ constexpr uint32_t idesc() {
            ((uint32_t)(Cfg<PAIR>::TILE_M >> 4) << 24);
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, K = 32.
 template <bool PAIR>
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
     if constexpr (PAIR) {
@@ -303,10 +345,10 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::PK_STAGES; ++i) {
             mbar_init(&s.pk_full[i], 1);
-            mbar_init(&s.pk_empty[i], kConvWarps);
+            mbar_init(&s.pk_empty[i], kTeamWarps);
         }
         for (int i = 0; i < C::OP_STAGES; ++i) {
-            mbar_init(&s.op_full[i], kConvWarps * C::NCTA);
+            mbar_init(&s.op_full[i], kTeamWarps * C::NCTA);
             mbar_init(&s.op_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -314,11 +356,13 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             mbar_init(&s.acc_empty[i], kEpiWarps * C::NCTA);
             mbar_init(&s.sum_full[i], kConvWarps);
             mbar_init(&s.sum_empty[i], kEpiWarps);
-            mbar_init(&s.col_full[i], kEpiWarps);
+            mbar_init(&s.col_full[i], kEpiWarps * C::NCTA);
         }
         s.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    for (int i = threadIdx.x; i < 2 * BM; i += blockDim.x) (&s.rowsum[0][0])[i] = 0;
+    for (int i = threadIdx.x; i < 2 * BN; i += blockDim.x) (&s.colsum[0][0])[i] = 0;
     if (warp == 1) {
         if constexpr (PAIR) {
             asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -349,7 +393,7 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int n0 = (int)(tile % n_tiles_n) * BN + (int)rank * C::WROWS;
                 for (int kb = 0; kb < kblocks; ++kb, ++g) {
                     const int st = (int)(g % C::PK_STAGES);
-                    if (!mbar_wait(s, &s.pk_empty[st], (uint32_t)((g / C::PK_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
+                    if (!mbar_wait<false, true>(s, &s.pk_empty[st], (uint32_t)((g / C::PK_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
                     mbar_expect_tx(&s.pk_full[st], C::PK_A + C::PK_W);
                     tma_load_2d(s.pkA[st], &tmA, &s.pk_full[st], kb * (BK / 2), m0);
                     tma_load_2d(s.pkW[st], &tmW, &s.pk_full[st], kb * (BK / 2), n0);
@@ -383,60 +427,56 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
     } else if (warp < 2 + kConvWarps) {
         // ---------------- converters ----------------
-        const int t = threadIdx.x - 64;          // 0..255
-        const int ch = t & 3;                    // 16-byte chunk of the 64-byte packed row
-        const int rq = t >> 2;                   // 0..63
+        const int tc = threadIdx.x - 64;                  // 0..383
+        const int team = (warp - 2) / kTeamWarps;         // K blocks with g % kTeams == team
+        // chunk tt + 128 j of a stage = row (tt >> 2) + 32 j, 16-byte chunk tt & 3
+        const int tt = tc - kTeamThreads * team;
+        const int ch = tt & 3, rq = tt >> 2;
         int64_t g = 0;
         int it = 0;
         bool ok = true;
         for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step, ++it) {
             const int n0 = (int)(tile % n_tiles_n) * BN;
-            // the tile's weight scale for column t, loaded now so that its latency
+            // the tile's weight scale for column tc, loaded now so that its latency
             // is not on the converters' path at the end of the tile
-            const float wsc = (YMODE != 2 && n0 + t < prm.N) ? prm.sw[n0 + t] : 0.f;
-            uint32_t sumA[2] = {0, 0}, sumW[C::NWCH];
+            const float wsc = (YMODE != 2 && tc < BN && n0 + tc < prm.N) ? prm.sw[n0 + tc] : 0.f;
+            uint32_t sumA[C::NACH], sumW[C::NWCH];
+#pragma unroll
+            for (int j = 0; j < C::NACH; ++j) sumA[j] = 0;
 #pragma unroll
             for (int j = 0; j < C::NWCH; ++j) sumW[j] = 0;
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                if ((int)(g % kTeams) != team) continue;
                 const int ps = (int)(g % C::PK_STAGES);
-                if (!mbar_wait(s, &s.pk_full[ps], (uint32_t)((g / C::PK_STAGES) & 1), prm.err)) { ok = false; break; }
-                uint4 a[2], w[C::NWCH];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) a[j] = reinterpret_cast<const uint4 *>(s.pkA[ps])[t + 256 * j];
-#pragma unroll
-                for (int j = 0; j < C::NWCH; ++j) w[j] = reinterpret_cast<const uint4 *>(s.pkW[ps])[t + 256 * j];
                 const int os = (int)(g % C::OP_STAGES);
-                if constexpr (PAIR) {
-                    // one cluster-scope acquire per warp (the release is the leader's
-                    // multicast commit); __syncwarp orders the other lanes after it
-                    int got = 1;
-                    if (lane == 0) got = mbar_wait<true>(s, &s.op_empty[os], (uint32_t)((g / C::OP_STAGES) & 1) ^ 1, prm.err);
-                    __syncwarp();
-                    if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
-                } else {
-                    if (!mbar_wait(s, &s.op_empty[os], (uint32_t)((g / C::OP_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
-                }
-                // row r, chunk ch -> 32 e4m3 bytes = granules 2ch, 2ch+1 of the 128-byte row
-                auto emit = [&](uint8_t *base, int r, const uint4 &v, uint32_t &sum) {
+                if (!mbar_wait(s, &s.pk_full[ps], (uint32_t)((g / C::PK_STAGES) & 1), prm.err)) { ok = false; break; }
+                uint4 a[C::NACH], w[C::NWCH];
+#pragma unroll
+                for (int j = 0; j < C::NACH; ++j) a[j] = reinterpret_cast<const uint4 *>(s.pkA[ps])[tt + kTeamThreads * j];
+#pragma unroll
+                for (int j = 0; j < C::NWCH; ++j) w[j] = reinterpret_cast<const uint4 *>(s.pkW[ps])[tt + kTeamThreads * j];
+                if (!warp_wait_commit(s, &s.op_empty[os], (uint32_t)((g / C::OP_STAGES) & 1) ^ 1, lane, prm.err)) { ok = false; break; }
+                // row, chunk ch -> 32 e4m3 bytes = granules 2ch, 2ch+1 of the 128-byte row
+                auto emit = [&](uint8_t *base, int row, const uint4 &v, uint32_t &sum) {
                     uint32_t lo[4], hi[4], acc = 0;
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc += widen(wv[i], lo[i], hi[i]);
                     sum = __dp4a(acc, 0x01010101u, sum);
-                    uint8_t *row = base + r * 128;
-                    const int g0 = (2 * ch) ^ (r & 7), g1 = (2 * ch + 1) ^ (r & 7);
-                    *reinterpret_cast<uint4 *>(row + 16 * g0) = make_uint4(lo[0], hi[0], lo[1], hi[1]);
-                    *reinterpret_cast<uint4 *>(row + 16 * g1) = make_uint4(lo[2], hi[2], lo[3], hi[3]);
+                    uint8_t *rowp = base + row * 128;
+                    const int g0 = (2 * ch) ^ (row & 7), g1 = (2 * ch + 1) ^ (row & 7);
+                    *reinterpret_cast<uint4 *>(rowp + 16 * g0) = make_uint4(lo[0], hi[0], lo[1], hi[1]);
+                    *reinterpret_cast<uint4 *>(rowp + 16 * g1) = make_uint4(lo[2], hi[2], lo[3], hi[3]);
                 };
 #pragma unroll
-                for (int j = 0; j < 2; ++j) emit(s.opA[os], rq + 64 * j, a[j], sumA[j]);
+                for (int j = 0; j < C::NACH; ++j) emit(s.opA[os], rq + 32 * j, a[j], sumA[j]);
 #pragma unroll
-                for (int j = 0; j < C::NWCH; ++j) emit(s.opW[os], rq + 64 * j, w[j], sumW[j]);
-                // One proxy fence per thread orders both its generic reads of the
-                // packed stage before the next TMA refill of it (or the refill can
-                // overtake them) and its operand stores before the tensor core's
-                // reads; then one lane per warp releases both stages (the operand
-                // stage through the leader for a pair).
+                for (int j = 0; j < C::NWCH; ++j) emit(s.opW[os], rq + 32 * j, w[j], sumW[j]);
+                // One proxy fence per thread orders its generic reads of the packed
+                // stage before the next TMA refill of it (or the refill can overtake
+                // them) and its operand stores before the tensor core's reads; then
+                // one lane per warp releases both stages (the operand stage at the
+                // leader for a pair).
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) {
@@ -448,7 +488,7 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!ok) break;
             // row sums: the four lanes sharing a row hold its four chunks
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
+            for (int j = 0; j < C::NACH; ++j) {
                 sumA[j] += __shfl_xor_sync(0xffffffffu, sumA[j], 1);
                 sumA[j] += __shfl_xor_sync(0xffffffffu, sumA[j], 2);
             }
@@ -457,58 +497,66 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 sumW[j] += __shfl_xor_sync(0xffffffffu, sumW[j], 1);
                 sumW[j] += __shfl_xor_sync(0xffffffffu, sumW[j], 2);
             }
-            // hand this tile's offset terms and weight scales to the own epilogue
-            // (for a pair, its epilogue passes this CTA's half of the column terms
-            // on to the peer)
+            // add this team's partial sums for the own epilogue, and hand it the
+            // weight scales (for a pair, the epilogue passes this CTA's half of
+            // the column terms on to the peer)
             const int buf = it & 1;
             if (!mbar_wait(s, &s.sum_empty[buf], (uint32_t)((it >> 1) & 1) ^ 1, prm.err)) { ok = false; break; }
             if (ch == 0) {
-                for (int j = 0; j < 2; ++j) s.rowterm[buf][rq + 64 * j] = -8 * (int)sumA[j];
-                for (int j = 0; j < C::NWCH; ++j)
-                    s.colterm[buf][(int)rank * C::WROWS + rq + 64 * j] = 64 * (int)prm.K - 8 * (int)sumW[j];
+#pragma unroll
+                for (int j = 0; j < C::NACH; ++j) atomicAdd(&s.rowsum[buf][rq + 32 * j], (int)sumA[j]);
+#pragma unroll
+                for (int j = 0; j < C::NWCH; ++j) atomicAdd(&s.colsum[buf][rq + 32 * j], (int)sumW[j]);
             }
-            if (YMODE != 2) s.wscale[buf][t] = wsc;
+            if (YMODE != 2 && tc < BN) s.wscale[buf][tc] = wsc;
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.sum_full[buf]);
         }
     } else {
         // ---------------- epilogue: TMEM -> offset removal -> scales -> global ----------------
-        const int e = threadIdx.x - 64 - kConvThreads;   // 0..255
-        const int q = warp & 3;                          // TMEM lane quarter this warp may read
-        const int colhalf = e >> 7;                      // columns 0-127 or 128-255
+        const int e = threadIdx.x - 64 - 32 * kConvWarps;   // 0..127
+        const int q = warp & 3;                              // TMEM lane quarter this warp may read
         int it = 0;
         for (int64_t tile = first_tile; tile < n_tiles; tile += tile_step, ++it) {
             const int buf = it & 1;
             const uint32_t par = (uint32_t)((it >> 1) & 1);
-            if (!mbar_wait<PAIR>(s, &s.acc_full[buf], par, prm.err)) break;
-            if (!mbar_wait(s, &s.sum_full[buf], par, prm.err)) break;
-            if constexpr (PAIR) {
-                // Exchange the halves of the column terms: write this CTA's half into
-                // the peer, release at cluster scope (generic data read by the peer's
-                // threads), and wait for the peer's half.  Both epilogues are past
-                // this tile's acc_full, so both have finished the tile that last used
-                // this buffer.
-                if (e < C::WROWS) {
-                    const int col = (int)rank * C::WROWS + e;
+            if (!mbar_wait<PAIR, true>(s, &s.acc_full[buf], par, prm.err)) break;
+            if (!mbar_wait<false, true>(s, &s.sum_full[buf], par, prm.err)) break;
+            // this CTA's column terms (the sums are cleared for the tile after next)
+            for (int cl = e; cl < C::WROWS; cl += 32 * kEpiWarps) {
+                const int v = 64 * (int)prm.K - 8 * s.colsum[buf][cl];
+                s.colsum[buf][cl] = 0;
+                const int col = (int)rank * C::WROWS + cl;
+                s.colterm[buf][col] = v;
+                if constexpr (PAIR) {
+                    // the peer's epilogue needs this half of the columns too
                     uint32_t remote;
                     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                                  : "=r"(remote)
                                  : "r"(smem_u32(&s.colterm[buf][col])), "r"(rank ^ 1u));
-                    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(s.colterm[buf][col]) : "memory");
+                    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cta(&s.col_full[buf], rank ^ 1u);
-                if (!mbar_wait<true>(s, &s.col_full[buf], par, prm.err)) break;
             }
+            // Every epilogue warp of both CTAs arrives once the column terms it wrote
+            // are in place (at the peer with a cluster-scope release: generic data
+            // read by the peer's threads).  Both epilogues are past this tile's
+            // acc_full, so both have finished the tile that last used this buffer.
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&s.col_full[buf]);
+                if constexpr (PAIR) mbar_arrive_cta(&s.col_full[buf], rank ^ 1u);
+            }
+            if (!mbar_wait<PAIR, true>(s, &s.col_full[buf], par, prm.err)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const int64_t m0 = (tile / n_tiles_n) * C::TILE_M + (int64_t)rank * BM, n0 = (tile % n_tiles_n) * BN;
             const int mr = 32 * q + lane;
             const int64_t m = m0 + mr;
-            const int rowt = s.rowterm[buf][mr];
+            const int rowt = -8 * s.rowsum[buf][mr];
+            s.rowsum[buf][mr] = 0;
             const float sa = (YMODE != 2 && m < prm.M) ? prm.sa[m] : 0.f;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                const int col0 = colhalf * 128 + 32 * c;
+            for (int c = 0; c < BN / 32; ++c) {
+                const int col0 = 32 * c;
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + col0), r);
                 if (m < prm.M) {
@@ -606,7 +654,8 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row_bytes, int box_rows) {
+bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row_bytes, int box_rows,
+              CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
@@ -614,7 +663,7 @@ bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row_byte
     const cuuint32_t box[2] = {BK / 2, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -632,7 +681,8 @@ template <int YMODE, bool PAIR>
 cudaError_t launch_mode(const GemmArgs &g, const TcParams &p, cudaStream_t stream) {
     using C = Cfg<PAIR>;
     CUtensorMap ta, tw;
-    if (!make_map(&ta, g.a_q, g.M, g.K / 2, BM) || !make_map(&tw, g.w_q, g.N, g.K / 2, C::WROWS))
+    if (!make_map(&ta, g.a_q, g.M, g.K / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tw, g.w_q, g.N, g.K / 2, C::WROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     auto kern = w4a4_tc_kernel<YMODE, PAIR>;
     const size_t smem = sizeof(Smem<PAIR>) + 1024;
