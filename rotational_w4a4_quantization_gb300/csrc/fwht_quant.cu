@@ -43,8 +43,10 @@
 //    code), packing with byte permutes, and
 //    16-byte stores of 32 codes each, coalesced across the warp.
 //  * CTAs are persistent: each computes the sign masks of its n positions once
-//    (SplitMix64, one call per element) into shared memory and then walks
-//    groups of rows.
+//    (SplitMix64, one call per element) into shared memory, while its first
+//    input copies are in flight, and then walks groups of rows.
+//  * n = 4096 (the activation size of the serving path) has its own variant
+//    with 64 values per thread and three butterfly phases (see below).
 #include "rq_internal.h"
 
 #include <cuda_bf16.h>
@@ -53,7 +55,6 @@
 namespace rq {
 namespace {
 
-constexpr int kThreads = 128;
 
 // --------------------------------------------------------------------------
 // Bit plans.  a(k)/ta(k): chunk bit held by phase-1 slot bit k / row-thread
@@ -70,7 +71,6 @@ struct Plan {
     static constexpr int P = 1 << T;
     static constexpr int NSLOT = 1 << S;
     static constexpr int E = 8 * NSLOT;
-    static constexpr int ROWS = kThreads / P;
     static constexpr bool kTwoPhase = C >= 5;
 
     static constexpr int a(int k) {
@@ -300,8 +300,16 @@ __device__ __forceinline__ int chunk_of(int t, int s, bool phase2) {
     return chunk_s<C>(s, phase2) | chunk_t<C>(t, phase2);
 }
 
+// Threads per CTA: 8 warps for the two-phase plans with 16-bit input, so that
+// one CTA per SM shares the sign-mask setup (n SplitMix64 calls) among 8 rows;
+// 4 warps otherwise (with fp32 input, 8 warps' input rings and row buffers would
+// not fit in shared memory).
+__host__ __device__ constexpr int threads_for(int log_n, int in_type) {
+    return (log_n - 3 >= 5 && in_type != IN_F32) ? 256 : 128;
+}
+
 template <int LOGN, int IN>
-__global__ void __launch_bounds__(kThreads, LOGN == 7 ? 4 : 1)
+__global__ void __launch_bounds__(threads_for(LOGN, IN), LOGN == 7 ? 4 : 1)
 fwht_quant_kernel(const __grid_constant__ KParams prm) {
     constexpr int C = LOGN - 3;
     using PL = Plan<C>;
@@ -309,13 +317,14 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
     constexpr int NSLOT = PL::NSLOT;
     constexpr int NP = PL::E / 2;                        // fp32 pairs per thread
     constexpr int P = PL::P;
-    constexpr int ROWS = PL::ROWS;
+    constexpr int THREADS = threads_for(LOGN, IN);
+    constexpr int ROWS = THREADS / P;
     constexpr int G = IN == IN_F32 ? 2 : 1;              // 16-byte granules per chunk
     constexpr int Q = NSLOT * G;                         // granules per thread per group
     constexpr int ES = IN == IN_F32 ? 4 : 2;             // input element bytes
 
     constexpr int DEPTH = PL::kTwoPhase ? 1 : 2;          // input groups in flight per warp
-    constexpr int NW = kThreads / 32;
+    constexpr int NW = THREADS / 32;
     constexpr int WREG = 32 * Q * 16;                     // bytes of one warp's input region
     extern __shared__ __align__(128) unsigned char smem_raw[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw);                       // NW*DEPTH
@@ -332,13 +341,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
 
     if (threadIdx.x < NW * DEPTH) mbar_init(&bars[threadIdx.x], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    // Sign masks: word j covers elements 2j (bit 15) and 2j+1 (bit 31).
-    for (int j = threadIdx.x; j < n / 2; j += kThreads) {
-        const uint32_t s0 = (uint32_t)(splitmix64_at(prm.seed, 2ull * j) >> 63);
-        const uint32_t s1 = (uint32_t)(splitmix64_at(prm.seed, 2ull * j + 1) >> 63);
-        sgn[j] = (s0 << 15) | (s1 << 31);
-    }
-    __syncthreads();
+    __syncthreads();    // barriers initialized before the warps issue their first copies
 
     const int row_in_cta = threadIdx.x / P;
     const int t = threadIdx.x % P;
@@ -402,6 +405,15 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
             if (g < total_groups) issue(g, d);
         }
     }
+    // Sign masks (computed while the first copies are in flight): word j covers elements 2j (bit 15) and 2j+1 (bit 31).
+    for (int j = threadIdx.x; j < n / 2; j += THREADS) {
+        const uint32_t s0 = (uint32_t)(splitmix64_at(prm.seed, 2ull * j) >> 63);
+        const uint32_t s1 = (uint32_t)(splitmix64_at(prm.seed, 2ull * j + 1) >> 63);
+        sgn[j] = (s0 << 15) | (s1 << 31);
+    }
+    __syncthreads();
+
+
     int slot = 0;
     uint32_t phase = 0;
     bool aborted = false;
@@ -600,16 +612,261 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
     }
 }
 
+// --------------------------------------------------------------------------
+// n = 4096: three butterfly phases with two transposes, 64 values per thread.
+//
+// The general plan above keeps 128 values per thread, which needs the whole
+// register file (8 warps per SM) and leaves the kernel latency-bound.  For the
+// activation size of the serving path this variant halves the per-thread state
+// (two warps per row, 16 warps per SM) and replaces the shuffle stage by a
+// second shared-memory transpose.  Chunk c = 8 elements, 9 chunk bits; a thread
+// t (0..63; bit 5 = which warp of the row) holds 8 chunks (slot s = 3 bits):
+//   phase 1: slots = chunk bits 3,4,5; t0,t1,t2 -> bits 0,1,2; t3,t4 -> 6,7; t5 -> 8
+//            (8 lanes read 128 contiguous input bytes; element bits and slot
+//            bits: 6 butterfly stages in registers)
+//   phase 2: slots = chunk bits 6,7,8; t0..t5 -> bits 0..5 (3 stages)
+//   phase 3: slots = chunk bits 0,1,2; t0..t5 -> bits 3..8 (3 stages): a thread
+//            ends with 64 consecutive elements, i.e. 32 bytes of codes.
+// Row buffer: fp32, 16-byte granule g = 2c + h (h = half chunk) XOR a swizzle of
+// chunk bits that makes every quarter-warp access touch 8 different bank groups
+// on both sides of each transpose:
+//   transpose 1: granule bit 0 ^= c2
+//   transpose 2: granule bits 0,1,2 ^= (c2 ^ c5, c3, c4)
+// --------------------------------------------------------------------------
+constexpr int K4_LOGN = 12, K4_N = 4096;
+
+__host__ __device__ constexpr int k4_threads(int in_type) { return in_type == IN_F32 ? 256 : 512; }
+
+__device__ __forceinline__ int k4_chunk1(int t, int s) {
+    return (t & 7) | (s << 3) | (((t >> 3) & 3) << 6) | ((t >> 5) << 8);
+}
+__device__ __forceinline__ int k4_chunk2(int t, int s) { return (t & 63) | (s << 6); }
+__device__ __forceinline__ int k4_chunk3(int t, int s) { return (t << 3) | s; }
+__device__ __forceinline__ int k4_pos1(int c, int h) { return (2 * c + h) ^ ((c >> 2) & 1); }
+__device__ __forceinline__ int k4_pos2(int c, int h) {
+    return (2 * c + h) ^ ((((c >> 2) ^ (c >> 5)) & 1) | (((c >> 3) & 1) << 1) | (((c >> 4) & 1) << 2));
+}
+
+template <int IN>
+size_t k4_smem_bytes() {
+    constexpr int THREADS = k4_threads(IN);
+    constexpr int NW = THREADS / 32, ROWS = THREADS / 64;
+    constexpr int ES = IN == IN_F32 ? 4 : 2;
+    // barriers | sign words | absmax exchange | per-warp input halves | fp32 row buffers
+    return 128 + (size_t)K4_N * 2 + 128 + (size_t)NW * (K4_N * ES / 2) + (size_t)ROWS * K4_N * 4;
+}
+
+template <int IN>
+__global__ void __launch_bounds__(k4_threads(IN), 1)
+fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
+    constexpr int n = K4_N;
+    constexpr int THREADS = k4_threads(IN);
+    constexpr int NW = THREADS / 32, ROWS = THREADS / 64;
+    constexpr int G = IN == IN_F32 ? 2 : 1;              // 16-byte granules per input chunk
+    constexpr int ES = IN == IN_F32 ? 4 : 2;
+    constexpr int HB = n * ES / 2;                        // input bytes of half a row (one warp)
+    constexpr int NP = 32;                                // fp32 pairs per thread
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw);                  // NW
+    uint32_t *sgn = reinterpret_cast<uint32_t *>(smem_raw + 128);             // n/2 words
+    float *red = reinterpret_cast<float *>(smem_raw + 128 + n * 2);          // ROWS*2
+    unsigned char *inbuf = smem_raw + 128 + n * 2 + 128;                      // NW halves
+    ulonglong2 *rowbuf = reinterpret_cast<ulonglong2 *>(inbuf + NW * HB);    // ROWS rows
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row_in_cta = warp >> 1;
+    const int t = threadIdx.x & 63;
+    const int half = t >> 5;
+    const bool signs_first = (prm.flags & 1u) != 0;
+    const unsigned full = 0xffffffffu;
+    const int64_t total_groups = prm.groups_per_job * prm.njobs;
+    unsigned char *wbuf = inbuf + warp * HB;
+    ulonglong2 *buf = rowbuf + (size_t)row_in_cta * (n / 4);
+    const uint32_t rbar = 1 + row_in_cta;                  // named barrier of the row's two warps
+
+    if (threadIdx.x < NW) mbar_init(&bars[threadIdx.x], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();    // barriers initialized before the warps issue their first copies
+
+    // This warp's half of row (group g, row_in_cta): chunks with bit 8 = half.
+    auto issue = [&](int64_t g) {
+        const int jb = (int)(g / prm.groups_per_job);
+        const RotJob &job = prm.job[jb];
+        const int64_t row = (g - (int64_t)jb * prm.groups_per_job) * ROWS + row_in_cta;
+        const bool valid = row < job.rows;
+        mbar_expect_tx(&bars[warp], valid ? (uint32_t)HB : 0u);
+        if (valid)
+            bulk_copy(wbuf, static_cast<const char *>(job.x) + (row * job.ld) * ES + half * HB, HB, &bars[warp]);
+    };
+    if (lane == 0 && (int64_t)blockIdx.x < total_groups) issue(blockIdx.x);
+    // Sign masks (computed while the first copies are in flight): word j covers
+    // elements 2j (bit 15) and 2j+1 (bit 31).
+    for (int j = threadIdx.x; j < n / 2; j += THREADS) {
+        const uint32_t s0 = (uint32_t)(splitmix64_at(prm.seed, 2ull * j) >> 63);
+        const uint32_t s1 = (uint32_t)(splitmix64_at(prm.seed, 2ull * j + 1) >> 63);
+        sgn[j] = (s0 << 15) | (s1 << 31);
+    }
+    __syncthreads();
+
+    const float inv_sqrt_n = 1.0f / 64.0f;
+    uint32_t phase = 0;
+    bool aborted = false;
+    for (int64_t grp = blockIdx.x; grp < total_groups; grp += gridDim.x) {
+        const int jb = (int)(grp / prm.groups_per_job);
+        const RotJob &job = prm.job[jb];
+        const int64_t row = (grp - (int64_t)jb * prm.groups_per_job) * ROWS + row_in_cta;
+
+        pair_t v[NP];
+        // ---------------- phase 1: input, signs, 6 stages ----------------
+        // A copy that never lands raises the error word; the iteration then runs
+        // on stale data with its stores disabled, so barriers stay matched.
+        if (!mbar_wait_bounded(&bars[warp], phase, prm.err)) aborted = true;
+        phase ^= 1u;
+        const bool active = row < job.rows && !aborted;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int c = k4_chunk1(t, s);
+            const uint4 m = reinterpret_cast<const uint4 *>(sgn)[c];
+            uint4 g[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                g[h] = *reinterpret_cast<const uint4 *>(wbuf + 16 * G * (c & 255) + 16 * h);
+            convert_chunk<IN>(g, m, signs_first, &v[4 * s]);   // includes the in-pair stage
+        }
+        // hand the input half back to the copy engine (generic reads before the
+        // next bulk write) and fetch this warp's half of its next row
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0 && !aborted && grp + gridDim.x < total_groups) issue(grp + gridDim.x);
+#pragma unroll
+        for (int rb = 1; rb <= 5; ++rb) butterfly_pairs<NP>(v, rb);
+
+        // ---------------- transpose 1, phase 2 ----------------
+        // the row's other warp may still be reading the previous row's phase 3
+        asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int c = k4_chunk1(t, s);
+            buf[k4_pos1(c, 0)] = make_ulonglong2(v[4 * s], v[4 * s + 1]);
+            buf[k4_pos1(c, 1)] = make_ulonglong2(v[4 * s + 2], v[4 * s + 3]);
+        }
+        asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int c = k4_chunk2(t, s);
+            const ulonglong2 lo = buf[k4_pos1(c, 0)], hi = buf[k4_pos1(c, 1)];
+            v[4 * s] = lo.x; v[4 * s + 1] = lo.y; v[4 * s + 2] = hi.x; v[4 * s + 3] = hi.y;
+        }
+#pragma unroll
+        for (int rb = 3; rb <= 5; ++rb) butterfly_pairs<NP>(v, rb);
+
+        // ---------------- transpose 2, phase 3 ----------------
+        asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int c = k4_chunk2(t, s);
+            buf[k4_pos2(c, 0)] = make_ulonglong2(v[4 * s], v[4 * s + 1]);
+            buf[k4_pos2(c, 1)] = make_ulonglong2(v[4 * s + 2], v[4 * s + 3]);
+        }
+        asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int c = k4_chunk3(t, s);
+            const ulonglong2 lo = buf[k4_pos2(c, 0)], hi = buf[k4_pos2(c, 1)];
+            v[4 * s] = lo.x; v[4 * s + 1] = lo.y; v[4 * s + 2] = hi.x; v[4 * s + 3] = hi.y;
+        }
+#pragma unroll
+        for (int rb = 3; rb <= 5; ++rb) butterfly_pairs<NP>(v, rb);
+
+        // ---------------- row absmax (two warps) ----------------
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < NP; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo2(v[i])), fabsf(hi2(v[i]))));
+#pragma unroll
+        for (int k = 0; k < 5; ++k) amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1 << k));
+        if (lane == 0) red[row_in_cta * 2 + half] = aborted ? __int_as_float(-1) : amax;
+        asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
+        const float r0 = red[row_in_cta * 2], r1 = red[row_in_cta * 2 + 1];
+        // the two warps of a row leave together: share the abort decision
+        const bool any_abort = __float_as_int(r0) == -1 || __float_as_int(r1) == -1;
+        amax = fmaxf(r0, r1);
+        if (any_abort) { aborted = true; break; }
+
+        // ---------------- quantize, pack, store: 64 consecutive elements ----------------
+        if (active) {
+            const float inv = amax > 0.f ? 7.0f / amax : 0.f;
+            const pair_t inv2 = mk2(inv, inv);
+            const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
+            if (t == 0) job.scales[row] = (amax / 7.0f) * inv_sqrt_n;
+            float *yrow = job.y ? job.y + row * (int64_t)n : nullptr;
+            uint32_t words[8];
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int c = k4_chunk3(t, s);
+                pair_t f[4] = {v[4 * s], v[4 * s + 1], v[4 * s + 2], v[4 * s + 3]};
+                if (!signs_first) {
+                    const uint4 m = reinterpret_cast<const uint4 *>(sgn)[c];
+                    const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        f[k] = f[k] ^ (((pair_t)(mm[k] & 0x80000000u) << 32) | (pair_t)(mm[k] << 16));
+                }
+                if (yrow) {
+                    const pair_t sc2 = mk2(inv_sqrt_n, inv_sqrt_n), z2 = 0ull;
+                    ulonglong2 *yp = reinterpret_cast<ulonglong2 *>(yrow + 8 * c);
+                    yp[0] = make_ulonglong2(fma2(f[0], sc2, z2), fma2(f[1], sc2, z2));
+                    yp[1] = make_ulonglong2(fma2(f[2], sc2, z2), fma2(f[3], sc2, z2));
+                }
+                uint32_t code[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const pair_t qq = fma2(f[k], inv2, bias2);
+                    code[2 * k] = (uint32_t)qq;
+                    code[2 * k + 1] = (uint32_t)(qq >> 32);
+                }
+                words[s] = pack8(code);
+            }
+            uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)(n / 2) + 32 * t);
+            qp[0] = make_uint4(words[0], words[1], words[2], words[3]);
+            qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
+        }
+    }
+    if (aborted) {
+        // wait (bounded) for this warp's copy still in flight before leaving
+        mbar_wait_bounded(&bars[warp], phase, prm.err);
+    }
+}
+
+template <int IN>
+cudaError_t launch_k4(const KParams &p, cudaStream_t stream) {
+    auto kern = fwht_quant_k4_kernel<IN>;
+    const size_t smem = k4_smem_bytes<IN>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t total = p.groups_per_job * p.njobs;
+    int64_t grid = sms;                                   // one CTA per SM
+    if (grid > total) grid = total;
+    kern<<<(unsigned)grid, k4_threads(IN), smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <int LOGN, int IN>
 size_t smem_bytes() {
     using PL = Plan<LOGN - 3>;
     constexpr int n = 1 << LOGN;
     constexpr int G = IN == IN_F32 ? 2 : 1;
     constexpr int DEPTH = PL::kTwoPhase ? 1 : 2;
-    size_t b = 128 + (size_t)n * 2 + 128 * ((PL::ROWS * 2 * 4 + 127) / 128);
-    b += (size_t)(kThreads / 32) * DEPTH * 32 * PL::NSLOT * G * 16;   // bulk-copy input rings
-    if (PL::kTwoPhase) b += (size_t)PL::ROWS * n * 4;
-    else b += (size_t)(kThreads / 32) * 2 * (32 / PL::P) * (n / 2);  // output staging
+    constexpr int THREADS = threads_for(LOGN, IN);
+    constexpr int ROWS = THREADS / PL::P;
+    size_t b = 128 + (size_t)n * 2 + 128 * ((ROWS * 2 * 4 + 127) / 128);
+    b += (size_t)(THREADS / 32) * DEPTH * 32 * PL::NSLOT * G * 16;   // bulk-copy input rings
+    if (PL::kTwoPhase) b += (size_t)ROWS * n * 4;
+    else b += (size_t)(THREADS / 32) * 2 * (32 / PL::P) * (n / 2);  // output staging
     return b;
 }
 
@@ -624,13 +881,13 @@ cudaError_t launch_t(const KParams &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads_for(LOGN, IN), smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const int64_t total = p.groups_per_job * p.njobs;
     int64_t grid = (int64_t)sms * per_sm;
     if (grid > total) grid = total;
-    kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
+    kern<<<(unsigned)grid, threads_for(LOGN, IN), smem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -661,7 +918,8 @@ cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_t
     if (!p.err) return cudaErrorUnknown;
     const int C = log_n - 3;
     const int S = C <= 3 ? C : (C == 4 ? 3 : 4);      // as in Plan<C>
-    const int rows_per_group = kThreads >> (C - S);
+    const int rows_per_group =
+        log_n == K4_LOGN ? k4_threads(in_type) / 64 : threads_for(log_n, in_type) >> (C - S);
     p.groups_per_job = (max_rows + rows_per_group - 1) / rows_per_group;
     if (p.groups_per_job == 0) return cudaSuccess;
     switch (log_n) {
@@ -672,7 +930,13 @@ cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_t
         case 9: return launch_n<9>(p, in_type, stream);
         case 10: return launch_n<10>(p, in_type, stream);
         case 11: return launch_n<11>(p, in_type, stream);
-        case 12: return launch_n<12>(p, in_type, stream);
+        case 12:
+            switch (in_type) {
+                case IN_F32: return launch_k4<IN_F32>(p, stream);
+                case IN_BF16: return launch_k4<IN_BF16>(p, stream);
+                case IN_F16: return launch_k4<IN_F16>(p, stream);
+                default: return cudaErrorInvalidValue;
+            }
         case 13: return launch_n<13>(p, in_type, stream);
         default: return cudaErrorInvalidValue;
     }
