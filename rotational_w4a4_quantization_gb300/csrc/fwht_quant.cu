@@ -160,6 +160,23 @@ __device__ __forceinline__ pair_t bf16w_bfly(uint32_t w) {
     return r;
 }
 
+// max |y| over the values of v: eight independent running maxima and a tree at the
+// end (a single running maximum is a serial chain as long as v).
+template <int NP>
+__device__ __forceinline__ float pairs_absmax(const pair_t (&v)[NP]) {
+    constexpr int A = NP < 8 ? NP : 8;
+    float m[A];
+#pragma unroll
+    for (int j = 0; j < A; ++j) m[j] = fmaxf(fabsf(lo2(v[j])), fabsf(hi2(v[j])));
+#pragma unroll
+    for (int i = A; i < NP; ++i) m[i % A] = fmaxf(m[i % A], fmaxf(fabsf(lo2(v[i])), fabsf(hi2(v[i]))));
+#pragma unroll
+    for (int w = A / 2; w >= 1; w /= 2)
+#pragma unroll
+        for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+    return m[0];
+}
+
 // Butterflies over register-element bit rb >= 1 of v (pairs pi and pi ^ 2^(rb-1)).
 template <int NP>
 __device__ __forceinline__ void butterfly_pairs(pair_t (&v)[NP], int rb) {
@@ -499,9 +516,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
         }
 
         // ---------------- row absmax ----------------
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < NP; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo2(v[i])), fabsf(hi2(v[i]))));
+        float amax = pairs_absmax<NP>(v);
         if constexpr (P > 1) {
 #pragma unroll
             for (int k = 0; k < (PL::T < 5 ? PL::T : 5); ++k)
@@ -779,9 +794,7 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
         for (int rb = 3; rb <= 5; ++rb) butterfly_pairs<NP>(v, rb);
 
         // ---------------- row absmax (two warps) ----------------
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < NP; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo2(v[i])), fabsf(hi2(v[i]))));
+        float amax = pairs_absmax<NP>(v);
 #pragma unroll
         for (int k = 0; k < 5; ++k) amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1 << k));
         if (lane == 0) red[row_in_cta * 2 + half] = aborted ? __int_as_float(-1) : amax;
