@@ -62,6 +62,25 @@ def test_extreme_codes_at_max_k(M, N, K, ba, bw):
     assert (acc.astype(np.int64) == ref[0, 0]).all()
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (128, 81920, 128),    # one CTA per tile row: 320 tiles, 1 K block each
+    (96, 51200, 640),     # single CTAs, 200 tiles, 5 K blocks (not a multiple of 3)
+    (256, 40960, 384),    # CTA pairs: 160 tiles on 76 pairs, 3 K blocks
+    (384, 20480, 640),    # CTA pairs, 160 tiles, 5 K blocks, ragged last M tile
+])
+def test_many_tiles_per_cta(M, N, K):
+    """Persistent CTAs walk several tiles; the converter teams take K blocks
+    round-robin across tile boundaries and the per-tile sums and accumulators
+    alternate between two buffers."""
+    aq, sa, wq, sw = _codes(M, N, K, 11 + M + K)
+    d = [t.to(DEV) for t in (aq, sa, wq, sw)]
+    acc_gpu = to_np(rq.w4a4_gemm(*d, out_dtype=torch.int32)).astype(np.int64)
+    y_gpu = to_np(rq.w4a4_gemm(*d, out_dtype=torch.float32))
+    acc, y = oracle.w4a4_gemm(aq.numpy(), sa.numpy(), wq.numpy(), sw.numpy(), M, N, K)
+    np.testing.assert_array_equal(acc_gpu, acc)
+    np.testing.assert_allclose(y_gpu, y, rtol=1e-5, atol=0)
+
+
 def test_large_then_small_partial_sums():
     # Accumulation order hazard: a huge partial sum followed by +-1 products.
     M, N, K = 128, 128, 16384
