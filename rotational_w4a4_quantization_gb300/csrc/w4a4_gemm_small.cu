@@ -8,14 +8,20 @@
 // With a handful of tokens the layer is bound by reading the packed weights
 // from HBM (K*N/2 bytes), so this kernel is built around streaming W once:
 //  * a CTA owns 16 output channels and one block of up to 64 tokens; its four
-//    warps split K four ways and meet in shared memory at the end (no global
+//    eight warps split K and meet in shared memory at the end (no global
 //    workspace);
 //  * each thread issues 16-byte loads: for one channel row, four lanes read 64
-//    contiguous bytes (128 codes) per step;
-//  * nibbles widen to int8 with one shift and one mask per 4 codes: the byte
-//    (w << 4) & 0xF0 holds 16*q of the even code and w & 0xF0 holds 16*q of
-//    the odd one, so the int8 MMA (mma.sync m16n8k32 s8, exact int32
-//    accumulation) produces 256*acc, undone by an exact arithmetic shift;
+//    contiguous bytes (128 codes) per step.  A warp issues the loads of W and of
+//    the activations for a group of steps (all of its steps for K = 4096 and up
+//    to 16 tokens) before any MMA, so that the whole weight slice of the CTA is
+//    in flight at once: the kernel is bound by reading W, and what limits that
+//    is the number of bytes in flight, not the arithmetic;
+//  * the MMA is the FP8 one (mma.sync m16n8k32 e4m3, fp32 accumulation): on
+//    this part the legacy int8 MMA runs at ~158 TOPS against ~2200 for e4m3.
+//    A code q becomes the E4M3 byte u = q + 8 (the nibble with its top bit
+//    flipped; bytes 0x00..0x0F are exactly u * 2^-9), so the accumulator holds
+//    sum u_a u_w * 2^-18 exactly, and sum q_a q_w = sum u_a u_w - 8 sum u_a -
+//    8 sum u_w + 64 K with the u sums kept per row and per column alongside;
 //  * the order of k inside each 128-code step is the same permutation for A
 //    and W (a dot product does not depend on the order of its terms).
 #include "rq_internal.h"
@@ -25,22 +31,27 @@
 namespace rq {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kThreadsS = 32 * kWarps;
 constexpr int kChan = 16;     // output channels per CTA (two n8 MMA tiles)
 constexpr int kMBlk = 64;     // tokens per CTA (four m16 MMA tiles)
-constexpr int kUnroll = 4;    // 128-code steps in flight per warp
+// 128-code steps whose loads a warp issues together (registers: 8 per step for W
+// plus 8 per m16 tile for the activations)
+__host__ __device__ constexpr int unroll_for(int mt) { return mt == 1 ? 4 : (mt == 2 ? 2 : 1); }
 
-__device__ __forceinline__ void mma_s8(int (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
     asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 "
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-__device__ __forceinline__ uint32_t lo16(uint32_t w) { return (w << 4) & 0xf0f0f0f0u; }
-__device__ __forceinline__ uint32_t hi16(uint32_t w) { return w & 0xf0f0f0f0u; }
+// E4M3 bytes u = q + 8 of the even (ulo) and odd (uhi) codes of a packed word
+__device__ __forceinline__ uint32_t ulo(uint32_t w) { return (w ^ 0x88888888u) & 0x0f0f0f0fu; }
+__device__ __forceinline__ uint32_t uhi(uint32_t w) { return ((w >> 4) ^ 0x08080808u) & 0x0f0f0f0fu; }
+// sum of the u of both halves of a word (bytes <= 30, no carries)
+__device__ __forceinline__ int usum(uint32_t lo, uint32_t hi, int acc) { return __dp4a((int)(lo + hi), 0x01010101, acc); }
 
 template <int MT>  // number of m16 tiles handled (1..4)
 __global__ void __launch_bounds__(kThreadsS)
@@ -48,6 +59,7 @@ w4a4_small_kernel(const uint8_t *__restrict__ aq, const float *__restrict__ sa,
                   const uint8_t *__restrict__ wq, const float *__restrict__ sw,
                   int64_t M, int64_t N, int64_t K, void *__restrict__ y, int y_mode) {
     __shared__ int part[kWarps][kMBlk][kChan + 1];
+    __shared__ int rsum[kWarps][kMBlk], csum[kWarps][kChan];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;
@@ -57,13 +69,18 @@ w4a4_small_kernel(const uint8_t *__restrict__ aq, const float *__restrict__ sa,
     const int64_t steps = K / 128;                  // 128-code steps (64 bytes per row)
     const int64_t s_begin = steps * warp / kWarps, s_end = steps * (warp + 1) / kWarps;
 
-    int acc[MT][2][4];
+    // acc holds sum u_a u_w * 2^-18 exactly (every partial sum is a multiple of
+    // 2^-18 below 2^6); sa_ / sw_ are this thread's sums of u over its k
+    float acc[MT][2][4];
+    int sa_[MT][2], sw_[2] = {0, 0};
 #pragma unroll
     for (int i = 0; i < MT; ++i)
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < 2; ++j) {
+            sa_[i][j] = 0;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) acc[i][j][r] = 0;
+            for (int r = 0; r < 4; ++r) acc[i][j][r] = 0.f;
+        }
 
     // row pointers (clamped: rows past M / N read row 0 and are never stored)
     const uint8_t *wrow[2];
@@ -81,62 +98,91 @@ w4a4_small_kernel(const uint8_t *__restrict__ aq, const float *__restrict__ sa,
             arow[i][h] = aq + (m < M ? m : 0) * kb + tq * 16;
         }
 
-    for (int64_t s = s_begin; s < s_end; s += kUnroll) {
-        uint4 wv[kUnroll][2];
+    constexpr int U = unroll_for(MT);
+    for (int64_t s = s_begin; s < s_end; s += U) {
+        uint4 wv[U][2], avu[U][MT][2];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
+        for (int u = 0; u < U; ++u) {
+            const bool valid = s + u < s_end;
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-                wv[u][j] = (s + u < s_end) ? __ldg(reinterpret_cast<const uint4 *>(wrow[j] + (s + u) * 64))
-                                           : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            if (s + u >= s_end) break;
-            uint4 av[MT][2];
+                wv[u][j] = valid ? __ldg(reinterpret_cast<const uint4 *>(wrow[j] + (s + u) * 64)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int i = 0; i < MT; ++i)
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    av[i][h] = __ldg(reinterpret_cast<const uint4 *>(arow[i][h] + (s + u) * 64));
+                    avu[u][i][h] = valid ? __ldg(reinterpret_cast<const uint4 *>(arow[i][h] + (s + u) * 64))
+                                         : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (s + u >= s_end) break;
+            const uint4 (&av)[MT][2] = avu[u];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {   // four k32 MMA steps per 128 codes
                 uint32_t b[2][2];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const uint32_t w = (&wv[u][j].x)[q];
-                    b[j][0] = lo16(w);
-                    b[j][1] = hi16(w);
+                    b[j][0] = ulo(w);
+                    b[j][1] = uhi(w);
+                    sw_[j] = usum(b[j][0], b[j][1], sw_[j]);
                 }
 #pragma unroll
                 for (int i = 0; i < MT; ++i) {
                     const uint32_t x0 = (&av[i][0].x)[q], x1 = (&av[i][1].x)[q];
-                    const uint32_t a[4] = {lo16(x0), lo16(x1), hi16(x0), hi16(x1)};
+                    const uint32_t a[4] = {ulo(x0), ulo(x1), uhi(x0), uhi(x1)};
+                    sa_[i][0] = usum(a[0], a[2], sa_[i][0]);
+                    sa_[i][1] = usum(a[1], a[3], sa_[i][1]);
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) mma_s8(acc[i][j], a, b[j]);
+                    for (int j = 0; j < 2; ++j) mma_e4m3(acc[i][j], a, b[j]);
                 }
             }
         }
     }
 
-    // split-K reduction across the warps through shared memory
+    // split-K reduction across the warps through shared memory: the partial
+    // sums of u_a u_w as exact integers (x 2^18), and each row's / column's sum
+    // of u (the four lanes sharing a row or column hold its four 16-byte chunks)
+    auto to_int = [](float v) { return __float2int_rn(v * 262144.0f); };
 #pragma unroll
     for (int i = 0; i < MT; ++i)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            part[warp][i * 16 + g][j * 8 + tq * 2] = acc[i][j][0];
-            part[warp][i * 16 + g][j * 8 + tq * 2 + 1] = acc[i][j][1];
-            part[warp][i * 16 + g + 8][j * 8 + tq * 2] = acc[i][j][2];
-            part[warp][i * 16 + g + 8][j * 8 + tq * 2 + 1] = acc[i][j][3];
+            part[warp][i * 16 + g][j * 8 + tq * 2] = to_int(acc[i][j][0]);
+            part[warp][i * 16 + g][j * 8 + tq * 2 + 1] = to_int(acc[i][j][1]);
+            part[warp][i * 16 + g + 8][j * 8 + tq * 2] = to_int(acc[i][j][2]);
+            part[warp][i * 16 + g + 8][j * 8 + tq * 2 + 1] = to_int(acc[i][j][3]);
         }
+#pragma unroll
+    for (int i = 0; i < MT; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            int v = sa_[i][h];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            if (tq == 0) rsum[warp][i * 16 + h * 8 + g] = v;
+        }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        int v = sw_[j];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (tq == 0) csum[warp][j * 8 + g] = v;
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < MT * 16 * kChan; e += kThreadsS) {
         const int mm = e / kChan, cc = e % kChan;
         const int64_t m = m0 + mm, c = c0 + cc;
         if (m >= M || c >= N) continue;
-        int s = 0;
+        // sum q_a q_w = sum u_a u_w - 8 sum u_a - 8 sum u_w + 64 K
+        int s = 0, su = 0;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += part[w][mm][cc];
-        const int a = s >> 8;   // exact: every product carried a factor 16*16
+        for (int w = 0; w < kWarps; ++w) {
+            s += part[w][mm][cc];
+            su += rsum[w][mm] + csum[w][cc];
+        }
+        const int a = s - 8 * su + 64 * (int)K;
         if (y_mode == 2) {
             static_cast<int *>(y)[m * N + c] = a;
         } else {
