@@ -650,7 +650,15 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
 // --------------------------------------------------------------------------
 constexpr int K4_LOGN = 12, K4_N = 4096;
 
-__host__ __device__ constexpr int k4_threads(int in_type) { return in_type == IN_F32 ? 256 : 512; }
+// Threads per CTA (two warps per row): at most 8 rows (4 for fp32 input, whose
+// buffers are twice as large); small batches use 2-row CTAs so that they spread
+// over more SMs (16 decode rows: 8 CTAs instead of 2).
+__host__ __device__ constexpr int k4_max_threads(int in_type) { return in_type == IN_F32 ? 256 : 512; }
+inline int k4_pick_threads(int64_t rows, int in_type, int sms) {
+    for (int t = k4_max_threads(in_type); t > 128; t /= 2)
+        if ((rows + t / 64 - 1) / (t / 64) >= sms) return t;
+    return 128;
+}
 
 __device__ __forceinline__ int k4_chunk1(int t, int s) {
     return (t & 7) | (s << 3) | (((t >> 3) & 3) << 6) | ((t >> 5) << 8);
@@ -662,20 +670,18 @@ __device__ __forceinline__ int k4_pos2(int c, int h) {
     return (2 * c + h) ^ ((((c >> 2) ^ (c >> 5)) & 1) | (((c >> 3) & 1) << 1) | (((c >> 4) & 1) << 2));
 }
 
-template <int IN>
+template <int IN, int THREADS>
 size_t k4_smem_bytes() {
-    constexpr int THREADS = k4_threads(IN);
     constexpr int NW = THREADS / 32, ROWS = THREADS / 64;
     constexpr int ES = IN == IN_F32 ? 4 : 2;
     // barriers | sign words | absmax exchange | per-warp input halves | fp32 row buffers
     return 128 + (size_t)K4_N * 2 + 128 + (size_t)NW * (K4_N * ES / 2) + (size_t)ROWS * K4_N * 4;
 }
 
-template <int IN>
-__global__ void __launch_bounds__(k4_threads(IN), 1)
+template <int IN, int THREADS>
+__global__ void __launch_bounds__(THREADS, 1)
 fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
     constexpr int n = K4_N;
-    constexpr int THREADS = k4_threads(IN);
     constexpr int NW = THREADS / 32, ROWS = THREADS / 64;
     constexpr int G = IN == IN_F32 ? 2 : 1;              // 16-byte granules per input chunk
     constexpr int ES = IN == IN_F32 ? 4 : 2;
@@ -850,10 +856,10 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
     }
 }
 
-template <int IN>
-cudaError_t launch_k4(const KParams &p, cudaStream_t stream) {
-    auto kern = fwht_quant_k4_kernel<IN>;
-    const size_t smem = k4_smem_bytes<IN>();
+template <int IN, int THREADS>
+cudaError_t launch_k4_t(const KParams &p, cudaStream_t stream) {
+    auto kern = fwht_quant_k4_kernel<IN, THREADS>;
+    const size_t smem = k4_smem_bytes<IN, THREADS>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -864,8 +870,19 @@ cudaError_t launch_k4(const KParams &p, cudaStream_t stream) {
     const int64_t total = p.groups_per_job * p.njobs;
     int64_t grid = sms;                                   // one CTA per SM
     if (grid > total) grid = total;
-    kern<<<(unsigned)grid, k4_threads(IN), smem, stream>>>(p);
+    kern<<<(unsigned)grid, THREADS, smem, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <int IN>
+cudaError_t launch_k4(const KParams &p, int threads, cudaStream_t stream) {
+    switch (threads) {
+        case 128: return launch_k4_t<IN, 128>(p, stream);
+        case 256: return launch_k4_t<IN, 256>(p, stream);
+        default:
+            if constexpr (k4_max_threads(IN) >= 512) return launch_k4_t<IN, 512>(p, stream);
+            return cudaErrorInvalidValue;
+    }
 }
 
 template <int LOGN, int IN>
@@ -931,8 +948,15 @@ cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_t
     if (!p.err) return cudaErrorUnknown;
     const int C = log_n - 3;
     const int S = C <= 3 ? C : (C == 4 ? 3 : 4);      // as in Plan<C>
-    const int rows_per_group =
-        log_n == K4_LOGN ? k4_threads(in_type) / 64 : threads_for(log_n, in_type) >> (C - S);
+    int k4_threads = 0;
+    if (log_n == K4_LOGN) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaErrorUnknown;
+        k4_threads = k4_pick_threads(max_rows, in_type, sms);
+    }
+    const int rows_per_group = log_n == K4_LOGN ? k4_threads / 64 : threads_for(log_n, in_type) >> (C - S);
     p.groups_per_job = (max_rows + rows_per_group - 1) / rows_per_group;
     if (p.groups_per_job == 0) return cudaSuccess;
     switch (log_n) {
@@ -945,9 +969,9 @@ cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_t
         case 11: return launch_n<11>(p, in_type, stream);
         case 12:
             switch (in_type) {
-                case IN_F32: return launch_k4<IN_F32>(p, stream);
-                case IN_BF16: return launch_k4<IN_BF16>(p, stream);
-                case IN_F16: return launch_k4<IN_F16>(p, stream);
+                case IN_F32: return launch_k4<IN_F32>(p, k4_threads, stream);
+                case IN_BF16: return launch_k4<IN_BF16>(p, k4_threads, stream);
+                case IN_F16: return launch_k4<IN_F16>(p, k4_threads, stream);
                 default: return cudaErrorInvalidValue;
             }
         case 13: return launch_n<13>(p, in_type, stream);
