@@ -12,6 +12,9 @@
  *                       weights, with a per-token x per-channel scale epilogue;
  *   rq_kv_rotate_quant  head-wise Hadamard rotation and INT4 quantization of K
  *                       and V before they are written to the cache.
+ *   rq_fwht_quant_gemm  decode-sized fusion of rq_fwht_quant and rq_w4a4_gemm:
+ *                       rotation, quantization and the W4A4 product in one
+ *                       launch, the rotated activations never reaching HBM.
  *
  * Sources (page title, then section / equation):
  *   [ROT] "Rotational Quantization: How Orthogonal Transforms and Hadamard
@@ -165,6 +168,37 @@ rq_status rq_w4a4_gemm(const uint8_t *a_q, const float *a_scales, const uint8_t 
 rq_status rq_kv_rotate_quant(const void *k, const void *v, rq_dtype dtype, int64_t tokens,
                              int64_t heads, int64_t head_dim, uint64_t seed, uint32_t flags,
                              uint8_t *kq, float *ks, uint8_t *vq, float *vs, void *stream);
+
+/*
+ * rq_fwht_quant_gemm -- y = dequant(Q(x R) . w_q) for a few tokens, in one launch.
+ *
+ *   The rotation and quantization of rq_fwht_quant ([ROT] §Incoherence
+ *   Processing via Randomized Hadamard Transforms; §Weight Absorption and
+ *   Online Fast Walsh-Hadamard Transforms, 2.) fused with the product of
+ *   rq_w4a4_gemm ([ROT] §Hardware Execution and Serving Economics, 1.): the
+ *   codes of x R are formed in on-chip memory and consumed there.  The result
+ *   equals rq_fwht_quant followed by rq_w4a4_gemm on the same inputs (the same
+ *   codes and scales, bit for bit).
+ *
+ *   x         [M][ld_x] activation rows, bf16 or fp16 (x_dtype), ld_x >= K.
+ *   M         1 <= M <= 16 (decode batches).
+ *   K         the row length; 4096 only (RQ_ERR_UNSUPPORTED otherwise).
+ *   seed, flags   as for rq_fwht_quant; must match the fold of w_q.
+ *   w_q, w_scales, N   as for rq_w4a4_gemm; N a multiple of 128.
+ *   y, y_dtype as for rq_w4a4_gemm (RQ_F16, RQ_F32, or RQ_I32 raw accumulators).
+ *   a_q, a_scales  optional (NULL to skip): receive the activation codes
+ *              [M][K/2] and scales [M], as rq_fwht_quant would write them.
+ *   Errors: as for rq_fwht_quant and rq_w4a4_gemm (RQ_ERR_INVALID_ARG,
+ *   RQ_ERR_UNSUPPORTED for a shape or dtype outside the above,
+ *   RQ_ERR_MISALIGNED for pointers or a row stride off their 16-byte rules);
+ *   M == 0 or N == 0 returns RQ_OK without a launch.  The launch has N/32
+ *   CTAs in thread-block clusters of 4, ~186 KB of shared memory each; a
+ *   bounded wait that gives up sets the error word that rq_sync_status reads.
+ */
+rq_status rq_fwht_quant_gemm(const void *x, rq_dtype x_dtype, int64_t M, int64_t K, int64_t ld_x,
+                             uint64_t seed, uint32_t flags, const uint8_t *w_q, const float *w_scales,
+                             int64_t N, void *y, rq_dtype y_dtype, uint8_t *a_q, float *a_scales,
+                             void *stream);
 
 /*
  * rq_sync_status -- wait for `stream` to drain, then report and clear the

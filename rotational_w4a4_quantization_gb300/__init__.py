@@ -11,12 +11,15 @@ Entry points (same names as the C ABI):
   quantization and nibble packing (also the offline weight fold when given W^T);
 * :func:`w4a4_gemm` -- exact INT4 x INT4 product with per-token x per-channel
   dequant;
-* :func:`kv_rotate_quant` -- head-wise rotation + INT4 quantization of K and V.
+* :func:`kv_rotate_quant` -- head-wise rotation + INT4 quantization of K and V;
+* :func:`fwht_quant_gemm` -- decode-sized fusion of the rotation, quantization
+  and W4A4 product in one launch.
 """
 from ._binding import (  # noqa: F401
     RQ_SIGNS_FIRST,
     RQError,
     fwht_quant,
+    fwht_quant_gemm,
     kv_rotate_quant,
     library_path,
     load_library,
@@ -24,5 +27,5 @@ from ._binding import (  # noqa: F401
     w4a4_gemm,
 )
 
-__all__ = ["RQ_SIGNS_FIRST", "RQError", "fwht_quant", "kv_rotate_quant", "library_path",
+__all__ = ["RQ_SIGNS_FIRST", "RQError", "fwht_quant", "fwht_quant_gemm", "kv_rotate_quant", "library_path",
            "load_library", "sync_status", "w4a4_gemm"]

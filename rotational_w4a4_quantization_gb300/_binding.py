@@ -51,6 +51,8 @@ def load_library() -> ctypes.CDLL:
     lib.rq_w4a4_gemm.argtypes = [P, P, P, P, i64, i64, i64, u64, u32, P, i32, P]
     lib.rq_kv_rotate_quant.restype = i32
     lib.rq_kv_rotate_quant.argtypes = [P, P, i32, i64, i64, i64, u64, u32, P, P, P, P, P]
+    lib.rq_fwht_quant_gemm.restype = i32
+    lib.rq_fwht_quant_gemm.argtypes = [P, i32, i64, i64, i64, u64, u32, P, P, i64, P, i32, P, P, P]
     lib.rq_sync_status.restype = i32
     lib.rq_sync_status.argtypes = [P]
     lib.rq_status_string.restype = ctypes.c_char_p
@@ -164,6 +166,32 @@ def kv_rotate_quant(k, v, seed: int, flags: int = RQ_SIGNS_FIRST, *, out=None, s
                                     _ptr(out.get("kq")), _ptr(out.get("ks")), _ptr(out.get("vq")),
                                     _ptr(out.get("vs")), _stream(stream))
     _check("rq_kv_rotate_quant", st)
+    return out
+
+
+def fwht_quant_gemm(x: torch.Tensor, seed: int, flags: int, w_q: torch.Tensor, w_scales, *,
+                    out_dtype=torch.float16, out=None, a_q=None, a_scales=None, stream=None):
+    """Decode-sized fusion of :func:`fwht_quant` and :func:`w4a4_gemm`: x (M x K,
+    bf16/fp16, unit stride in the last dimension; M <= 16, K = 4096) is rotated,
+    quantized and multiplied by w_q (N x K/2 packed codes, N a multiple of 128)
+    in one launch.  Returns y (M x N, out_dtype float16 / float32 / int32 raw
+    accumulators); a_q (M x K/2) and a_scales (M,), when given, receive the
+    activation codes and scales."""
+    lib = load_library()
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit stride in the last dimension")
+    M, K = x.shape
+    N, kb = w_q.shape
+    if kb * 2 != K or w_q.dtype != torch.uint8 or not w_q.is_contiguous():
+        raise ValueError("w_q must be contiguous uint8 with K/2 columns")
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=x.device)
+    _dev(x, w_q, w_scales, out, a_q, a_scales)
+    with torch.cuda.device(x.device):
+        st = lib.rq_fwht_quant_gemm(_ptr(x), _DTYPES[x.dtype], M, K, x.stride(0), seed, flags, _ptr(w_q),
+                                    _ptr(w_scales), N, _ptr(out), _DTYPES[out.dtype], _ptr(a_q), _ptr(a_scales),
+                                    _stream(stream))
+    _check("rq_fwht_quant_gemm", st)
     return out
 
 

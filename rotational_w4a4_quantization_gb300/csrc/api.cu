@@ -126,6 +126,30 @@ rq_status rq_kv_rotate_quant(const void *k, const void *v, rq_dtype dtype, int64
     return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }
 
+rq_status rq_fwht_quant_gemm(const void *x, rq_dtype x_dtype, int64_t M, int64_t K, int64_t ld_x,
+                             uint64_t seed, uint32_t flags, const uint8_t *w_q, const float *w_scales,
+                             int64_t N, void *y, rq_dtype y_dtype, uint8_t *a_q, float *a_scales,
+                             void *stream) {
+    if (M < 0 || N < 0 || K <= 0) return RQ_ERR_INVALID_ARG;
+    if (flags & ~uint32_t(RQ_SIGNS_FIRST)) return RQ_ERR_INVALID_ARG;
+    if (x_dtype != RQ_BF16 && x_dtype != RQ_F16) return RQ_ERR_UNSUPPORTED;
+    if (y_dtype != RQ_F16 && y_dtype != RQ_F32 && y_dtype != RQ_I32) return RQ_ERR_UNSUPPORTED;
+    if (ld_x < K) return RQ_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return RQ_OK;
+    if (!rq::fused_decode_supported(M, K, N)) return RQ_ERR_UNSUPPORTED;
+    const bool need_scales = y_dtype != RQ_I32;
+    if (!x || !w_q || !y || (need_scales && !w_scales)) return RQ_ERR_INVALID_ARG;
+    const void *ptrs[6] = {x, w_q, y, w_scales, a_q, a_scales};
+    for (const void *p : ptrs)
+        if (p && !rq::aligned16(p)) return RQ_ERR_MISALIGNED;
+    if ((ld_x * rq::elem_size(x_dtype)) % 16 != 0) return RQ_ERR_MISALIGNED;
+    if ((N * rq::elem_size(y_dtype)) % 16 != 0) return RQ_ERR_MISALIGNED;
+    const int y_mode = y_dtype == RQ_F16 ? 0 : (y_dtype == RQ_F32 ? 1 : 2);
+    cudaError_t e = rq::launch_fused_decode(x, (int)x_dtype, M, ld_x, seed, flags, w_q, w_scales, N, y, y_mode,
+                                            a_q, a_scales, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+}
+
 rq_status rq_sync_status(void *stream) {
     int word = 0;
     cudaError_t e = rq::read_and_clear_error_word(&word, static_cast<cudaStream_t>(stream));

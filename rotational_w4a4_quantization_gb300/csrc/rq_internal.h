@@ -40,6 +40,12 @@ struct GemmArgs {
 
 cudaError_t launch_w4a4_gemm(const GemmArgs &args, cudaStream_t stream);
 
+// Fused decode path (rotation + quantization + W4A4 product in one launch).
+bool fused_decode_supported(int64_t M, int64_t K, int64_t N);
+cudaError_t launch_fused_decode(const void *x, int in_type, int64_t M, int64_t ldx, uint64_t seed, uint32_t flags,
+                                const uint8_t *wq, const float *sw, int64_t N, void *y, int y_mode, uint8_t *aq,
+                                float *as, cudaStream_t stream);
+
 // Device-resident error word set by bounded waits that gave up.
 cudaError_t read_and_clear_error_word(int *value, cudaStream_t stream);
 int *error_word_device_ptr();

@@ -3,12 +3,17 @@
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel gemm --workload prefill
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel fwht --workload large
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel kv
+    python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel fused --workload decode
+    python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel unfused --workload decode
 
 Runs `--warmup` untimed launches, then `--reps` launches each timed with CUDA events on the
 current stream (L2 flushed before each launch unless `--no-flush`; a GPU-side pause lets
 the host enqueue ahead so the events time the kernel, not the launch), and prints the
 median time with the algorithmic GB/s or TOPS.  GEMM operands are seeded random codes of
-the workload's shape; rotation inputs follow the workload's outlier recipe.
+the workload's shape; rotation inputs follow the workload's outlier recipe.  `fused` times
+the one-launch rotation + quantization + product of a decode batch, `unfused` the same
+result from the rotation kernel followed by the GEMM kernel (two launches, one timed
+region); both count the bytes of x, the packed weights and scales, and y.
 """
 from __future__ import annotations
 
@@ -28,7 +33,7 @@ from rotational_w4a4_quantization_gb300 import synth  # noqa: E402
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["fwht", "kv", "gemm"], required=True)
+    ap.add_argument("--kernel", choices=["fwht", "kv", "gemm", "fused", "unfused"], required=True)
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="prefill")
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
@@ -61,6 +66,25 @@ def main(argv=None):
         T, H, D = k.shape
         work, unit = 2 * T * H * (D * 2 + D // 2 + 4), "GB/s"
         what = f"kv_rotate_quant {T}x{H}x{D} bf16"
+    elif args.kernel in ("fused", "unfused"):
+        if not w.gemm_n or not w.rows:
+            raise SystemExit(f"workload {w.name} has no activation GEMM")
+        M, K, N = w.rows, w.n, w.gemm_n
+        x = synth.activations(M, K, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor).to(dev)
+        wq, sw = synth.random_codes(N, K, 1001 + w.data_seed)
+        wq, sw = wq.to(dev), sw.to(dev)
+        y = torch.empty(M, N, dtype=torch.float16, device=dev)
+        if args.kernel == "fused":
+            fn = lambda: rq.fwht_quant_gemm(x, seed, flags, wq, sw, out=y)
+        else:
+            q = torch.empty(M, K // 2, dtype=torch.uint8, device=dev)
+            s = torch.empty(M, dtype=torch.float32, device=dev)
+
+            def fn():
+                rq.fwht_quant(x, seed, flags, q=q, scales=s)
+                rq.w4a4_gemm(q, s, wq, sw, out=y)
+        work, unit = M * K * x.element_size() + N * K // 2 + 4 * N + 2 * M * N, "GB/s"
+        what = f"{args.kernel} rotate+quant+gemm {M}x{K}x{N} {str(x.dtype).split('.')[-1]} -> fp16"
     else:
         if not w.gemm_n:
             raise SystemExit(f"workload {w.name} has no GEMM")
@@ -93,7 +117,9 @@ def main(argv=None):
     times = sorted(a.elapsed_time(b) * 1e-3 for a, b in ev)
     med = times[len(times) // 2]
     rate = work / med / (1e9 if unit == "GB/s" else 1e12)
-    print(f"{what}: median {med * 1e6:.1f} us  min {times[0] * 1e6:.1f} us  {rate:.1f} {unit}")
+    mean = sum(times) / len(times)   # events tick in ~2 us steps here: the mean of many reps resolves finer
+    print(f"{what}: median {med * 1e6:.1f} us  mean {mean * 1e6:.2f} us  min {times[0] * 1e6:.1f} us  "
+          f"{rate:.1f} {unit} (median)")
 
 
 if __name__ == "__main__":

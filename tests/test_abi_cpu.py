@@ -114,3 +114,29 @@ def test_binding_raises_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_binding, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         _binding.load_library()
+
+
+def fused(lib, x=A16, dt=1, M=16, K=4096, ld=4096, flags=1, w=A16, ws=A16, N=4096, y=A16, ydt=2,
+          aq=NULL, asc=NULL):
+    return lib.rq_fwht_quant_gemm(x, dt, M, K, ld, 7, flags, w, ws, N, y, ydt, aq, asc, NULL)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(M=-1), 1),
+    (dict(K=0), 1),
+    (dict(flags=2), 1),
+    (dict(ld=4000), 1),               # stride shorter than the row
+    (dict(dt=0), 2),                  # fp32 activations not offered by the fused path
+    (dict(ydt=1), 2),                 # bf16 output not offered
+    (dict(M=17), 2),                  # more than one m16 tile of tokens
+    (dict(K=2048, ld=2048), 2),       # the fused rotation is 4096 long
+    (dict(N=4000), 2),                # N not a multiple of 128
+    (dict(x=NULL), 1),
+    (dict(ws=NULL), 1),
+    (dict(y=A1), 3),
+    (dict(aq=A1), 3),
+    (dict(ld=4100), 3),               # 8200-byte stride is not a multiple of 16
+    (dict(M=0, x=NULL), 0),           # empty: nothing to do
+])
+def test_fused_argument_checks(lib, kw, expect):
+    assert fused(lib, **kw) == expect

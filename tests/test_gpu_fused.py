@@ -1,0 +1,110 @@
+"""GPU parity of rq_fwht_quant_gemm, the decode-sized fusion of the rotation,
+INT4 quantization and W4A4 product, against the oracle and against the unfused
+entry points.
+
+The fused kernel forms the activation codes on chip and multiplies them in the
+same launch.  It must produce what rq_fwht_quant followed by rq_w4a4_gemm
+produce, bit for bit (the same arithmetic in the same order), and that must
+match the oracle: codes within the tie window, scales within 1e-5, the int32
+accumulators exact for the GPU's own codes, fp32 within 1e-5, fp16 within one
+ulp.  Shapes cover M = 1..16 (rows missing from some cluster ranks), several N
+(cluster counts), both input dtypes, both sign forms and every output mode.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rotational_w4a4_quantization_gb300 as rq
+from rotational_w4a4_quantization_gb300 import synth
+
+from parity import compare_codes, compare_f16, compare_scales, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+K = 4096
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _inputs(M, N, dt, seed):
+    x = synth.activations(M, K, dt, seed, 4, 100.0)
+    wq, sw = synth.random_codes(N, K, seed + 50)
+    return x, wq, sw
+
+
+def _fused(x, flags, wq, sw, out_dtype):
+    M = x.shape[0]
+    aq = torch.empty(M, K // 2, dtype=torch.uint8, device=DEV)
+    asc = torch.empty(M, dtype=torch.float32, device=DEV)
+    y = rq.fwht_quant_gemm(x.to(DEV), synth.SIGN_SEED, flags, wq.to(DEV), sw.to(DEV),
+                           out_dtype=out_dtype, a_q=aq, a_scales=asc)
+    return y, aq, asc
+
+
+@pytest.mark.parametrize("M", [1, 5, 8, 9, 16])
+@pytest.mark.parametrize("N", [128, 640, 4096])
+@pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
+def test_matches_unfused_and_oracle(M, N, flags):
+    x, wq, sw = _inputs(M, N, torch.bfloat16, 3 * M + N)
+    xd, wd, sd = x.to(DEV), wq.to(DEV), sw.to(DEV)
+    # unfused reference on the GPU
+    q_u, s_u = rq.fwht_quant(xd, synth.SIGN_SEED, flags)
+    for out_dtype in (torch.int32, torch.float32, torch.float16):
+        y, aq, asc = _fused(x, flags, wq, sw, out_dtype)
+        y_u = rq.w4a4_gemm(q_u, s_u, wd, sd, out_dtype=out_dtype)
+        assert torch.equal(aq, q_u), "codes differ from rq_fwht_quant"
+        assert torch.equal(asc, s_u), "scales differ from rq_fwht_quant"
+        assert torch.equal(y, y_u), f"{out_dtype} output differs from rq_w4a4_gemm"
+    # oracle: codes and scales of the rotation, then the product on the GPU's codes
+    ref = oracle.fwht_quant(x.double().numpy(), synth.SIGN_SEED, flags, want_ratio=True)
+    compare_scales(to_np(asc), ref["scales"])
+    compare_codes(to_np(aq), ref["q"], ref["ratio"], K)
+    acc, yref = oracle.w4a4_gemm(to_np(aq), to_np(asc), wq.numpy(), sw.numpy(), M, N, K)
+    y32 = _fused(x, flags, wq, sw, torch.int32)[0]
+    np.testing.assert_array_equal(to_np(y32).astype(np.int64), acc)
+    yf = _fused(x, flags, wq, sw, torch.float32)[0]
+    np.testing.assert_allclose(to_np(yf), yref, rtol=1e-5, atol=0)
+    compare_f16(to_np(_fused(x, flags, wq, sw, torch.float16)[0]), yref)
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+def test_dtypes_and_strided_rows(dt):
+    M, N = 12, 1024
+    x, wq, sw = _inputs(M, N, dt, 77)
+    big = torch.zeros(M, K + 64, dtype=dt)
+    big[:, :K] = x
+    xd = big.to(DEV)[:, :K]                       # row stride K + 64 elements
+    y = rq.fwht_quant_gemm(xd, synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, wq.to(DEV), sw.to(DEV), out_dtype=torch.int32)
+    q_u, s_u = rq.fwht_quant(x.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+    y_u = rq.w4a4_gemm(q_u, s_u, wq.to(DEV), sw.to(DEV), out_dtype=torch.int32)
+    assert torch.equal(y, y_u)
+
+
+def test_zero_row_and_no_code_outputs():
+    M, N = 3, 256
+    x, wq, sw = _inputs(M, N, torch.bfloat16, 5)
+    x[1] = 0
+    y = rq.fwht_quant_gemm(x.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, wq.to(DEV), sw.to(DEV),
+                           out_dtype=torch.float32)
+    assert torch.all(y[1] == 0)
+    q_u, s_u = rq.fwht_quant(x.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+    assert torch.equal(y, rq.w4a4_gemm(q_u, s_u, wq.to(DEV), sw.to(DEV), out_dtype=torch.float32))
+
+
+def test_decode_workload_full_size():
+    """16 tokens x 4096 -> 4096 with the folded weights of the oracle's fold."""
+    w = synth.WORKLOADS["decode"]
+    x = synth.activations(w.rows, w.n, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor)
+    wt = synth.weights_t(w.gemm_n, w.n, w.weight_seed, w.w_std)             # W^T, N x K fp32
+    fold = oracle.fwht_quant(wt.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+    wq, sw = torch.from_numpy(fold["q"]), torch.from_numpy(fold["scales"])
+    y, aq, asc = _fused(x, rq.RQ_SIGNS_FIRST, wq, sw, torch.float32)
+    ref = oracle.fwht_quant(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, want_ratio=True)
+    compare_codes(to_np(aq), ref["q"], ref["ratio"], K)
+    _, yref = oracle.w4a4_gemm(to_np(aq), to_np(asc), fold["q"], fold["scales"], w.rows, w.gemm_n, K)
+    np.testing.assert_allclose(to_np(y), yref, rtol=1e-5, atol=0)
