@@ -192,11 +192,12 @@ fused_decode_kernel(const __grid_constant__ FParams prm) {
     const int64_t row = (int64_t)rank + kFCluster * slot;
     const int t = threadIdx.x & 63, half = t >> 5;
     const bool active = row < prm.M;
+    const K4Addr ad = k4_addr(t);                      // thread bases of every access below
     uint4 xg[8];
     {
-        const char *xrow = static_cast<const char *>(prm.x) + (active ? row : 0) * prm.ldx * ES;
+        const char *xrow = static_cast<const char *>(prm.x) + (active ? row : 0) * prm.ldx * ES + 16 * ad.c1;
 #pragma unroll
-        for (int sl = 0; sl < 8; ++sl) xg[sl] = __ldg(reinterpret_cast<const uint4 *>(xrow + 16 * k4_chunk1(t, sl)));
+        for (int sl = 0; sl < 8; ++sl) xg[sl] = __ldg(reinterpret_cast<const uint4 *>(xrow + 128 * sl));
     }
     // the weight scale of this thread's output channel (the epilogue's channel
     // c0 + lane for both of its outputs), fetched now, off the epilogue's path
@@ -213,6 +214,7 @@ fused_decode_kernel(const __grid_constant__ FParams prm) {
     {
         const uint32_t rbar = 1 + slot;
         const bool signs_first = (prm.flags & 1u) != 0;
+        const uint32_t msel = signs_first ? 0xffffffffu : 0u;
         const unsigned full = 0xffffffffu;
         ulonglong2 *buf = s.rowbuf[slot];
         constexpr int NP = 32;
@@ -220,8 +222,8 @@ fused_decode_kernel(const __grid_constant__ FParams prm) {
         // phase 1: the chunks loaded above, signs, 6 stages
 #pragma unroll
         for (int sl = 0; sl < 8; ++sl) {
-            const uint4 m = reinterpret_cast<const uint4 *>(s.sgn)[k4_chunk1(t, sl)];
-            convert_chunk<IN>(&xg[sl], m, signs_first, &v[4 * sl]);
+            const uint4 m = reinterpret_cast<const uint4 *>(s.sgn)[ad.c1 + 8 * sl];
+            convert_chunk<IN>(&xg[sl], m, msel, &v[4 * sl]);
         }
         // the activations are in: now the CTA's 32 weight rows (contiguous, 64 KB)
         // in one bulk copy, which would have delayed them in the memory system
@@ -241,15 +243,13 @@ fused_decode_kernel(const __grid_constant__ FParams prm) {
         // transpose 1, phase 2
 #pragma unroll
         for (int sl = 0; sl < 8; ++sl) {
-            const int c = k4_chunk1(t, sl);
-            buf[k4_pos1(c, 0)] = make_ulonglong2(v[4 * sl], v[4 * sl + 1]);
-            buf[k4_pos1(c, 1)] = make_ulonglong2(v[4 * sl + 2], v[4 * sl + 3]);
+            buf[ad.w1 + 16 * sl] = make_ulonglong2(v[4 * sl], v[4 * sl + 1]);
+            buf[(ad.w1 ^ 1) + 16 * sl] = make_ulonglong2(v[4 * sl + 2], v[4 * sl + 3]);
         }
         asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
 #pragma unroll
         for (int sl = 0; sl < 8; ++sl) {
-            const int c = k4_chunk2(t, sl);
-            const ulonglong2 lo = buf[k4_pos1(c, 0)], hi = buf[k4_pos1(c, 1)];
+            const ulonglong2 lo = buf[ad.r1 + 128 * sl], hi = buf[(ad.r1 ^ 1) + 128 * sl];
             v[4 * sl] = lo.x; v[4 * sl + 1] = lo.y; v[4 * sl + 2] = hi.x; v[4 * sl + 3] = hi.y;
         }
 #pragma unroll
@@ -258,15 +258,13 @@ fused_decode_kernel(const __grid_constant__ FParams prm) {
         asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
 #pragma unroll
         for (int sl = 0; sl < 8; ++sl) {
-            const int c = k4_chunk2(t, sl);
-            buf[k4_pos2(c, 0)] = make_ulonglong2(v[4 * sl], v[4 * sl + 1]);
-            buf[k4_pos2(c, 1)] = make_ulonglong2(v[4 * sl + 2], v[4 * sl + 3]);
+            buf[ad.w2 + 128 * sl] = make_ulonglong2(v[4 * sl], v[4 * sl + 1]);
+            buf[(ad.w2 ^ 1) + 128 * sl] = make_ulonglong2(v[4 * sl + 2], v[4 * sl + 3]);
         }
         asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
 #pragma unroll
         for (int sl = 0; sl < 8; ++sl) {
-            const int c = k4_chunk3(t, sl);
-            const ulonglong2 lo = buf[k4_pos2(c, 0)], hi = buf[k4_pos2(c, 1)];
+            const ulonglong2 lo = buf[16 * t + (k4_k3(sl, 0) ^ ad.m3)], hi = buf[16 * t + (k4_k3(sl, 1) ^ ad.m3)];
             v[4 * sl] = lo.x; v[4 * sl + 1] = lo.y; v[4 * sl + 2] = hi.x; v[4 * sl + 3] = hi.y;
         }
 #pragma unroll
@@ -282,23 +280,24 @@ fused_decode_kernel(const __grid_constant__ FParams prm) {
         const float inv = amax > 0.f ? 7.0f / amax : 0.f;
         const pair_t inv2 = mk2(inv, inv);
         const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
+        if (!signs_first) {                           // signs after the transform: one branch
+#pragma unroll
+            for (int sl = 0; sl < 8; ++sl) {
+                const uint4 m = reinterpret_cast<const uint4 *>(s.sgn)[8 * t + sl];
+                const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    v[4 * sl + k] ^= ((pair_t)(mm[k] & 0x80000000u) << 32) | (pair_t)(mm[k] << 16);
+            }
+        }
         uint32_t words[8];
         int usum = 0;
 #pragma unroll
         for (int sl = 0; sl < 8; ++sl) {
-            const int c = k4_chunk3(t, sl);
-            pair_t f[4] = {v[4 * sl], v[4 * sl + 1], v[4 * sl + 2], v[4 * sl + 3]};
-            if (!signs_first) {
-                const uint4 m = reinterpret_cast<const uint4 *>(s.sgn)[c];
-                const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    f[k] = f[k] ^ (((pair_t)(mm[k] & 0x80000000u) << 32) | (pair_t)(mm[k] << 16));
-            }
             uint32_t code[8];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const pair_t qq = fma2(f[k], inv2, bias2);
+                const pair_t qq = fma2(v[4 * sl + k], inv2, bias2);
                 code[2 * k] = (uint32_t)qq;
                 code[2 * k + 1] = (uint32_t)(qq >> 32);
             }

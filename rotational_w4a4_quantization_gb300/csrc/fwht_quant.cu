@@ -114,6 +114,10 @@ struct KParams {
 
 constexpr long long kWaitLimitCycles = 4000000000ll;    // ~2 s at 2 GHz
 
+// Job of row group g (jobs hold groups_per_job groups each; at most two jobs, so
+// a comparison replaces the 64-bit division).
+__device__ __forceinline__ int job_of(int64_t g, int64_t groups_per_job) { return g >= groups_per_job ? 1 : 0; }
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -223,6 +227,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
     unsigned char *ostage = inbuf + NW * DEPTH * WREG + (PL::kTwoPhase ? (size_t)ROWS * n * 4 : 0);
 
     const bool signs_first = (prm.flags & 1u) != 0;
+    const uint32_t msel = signs_first ? 0xffffffffu : 0u;
 
     if (threadIdx.x < NW * DEPTH) mbar_init(&bars[threadIdx.x], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -261,7 +266,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
 
     // Issue the bulk copies of group g's rows for this warp (lane 0 only).
     auto issue = [&](int64_t g, int slot) {
-        const int jb = (int)(g / prm.groups_per_job);
+        const int jb = job_of(g, prm.groups_per_job);
         const RotJob &job = prm.job[jb];
         const int64_t row0 = (g - (int64_t)jb * prm.groups_per_job) * ROWS + (P <= 32 ? warp * RPW : warp / 2);
         const char *x = static_cast<const char *>(job.x);
@@ -304,7 +309,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
     bool aborted = false;
     int obuf = 0;
     for (int64_t grp = blockIdx.x; grp < total_groups; grp += gridDim.x) {
-        const int jb = (int)(grp / prm.groups_per_job);
+        const int jb = job_of(grp, prm.groups_per_job);
         const RotJob &job = prm.job[jb];
         const int64_t row = (grp - (int64_t)jb * prm.groups_per_job) * ROWS + row_in_cta;
         const unsigned char *wbuf = inbuf + (warp * DEPTH + slot) * WREG;
@@ -325,7 +330,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
                 const uint32_t off = (xin ^ (uint32_t)(16 * G * chunk_s<C>(s, false))) + 16 * h;
                 g[h] = *reinterpret_cast<const uint4 *>(wbuf + off);
             }
-            convert_chunk<IN>(g, m, signs_first, &v[4 * s]);   // includes the in-pair stage
+            convert_chunk<IN>(g, m, msel, &v[4 * s]);   // includes the in-pair stage
         }
         // Hand the buffer back to the copy engine: order these generic reads
         // before the next bulk write (async proxy) into it.
@@ -410,40 +415,45 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
         if (active) {
             if (t == 0) job.scales[row] = (amax / 7.0f) * inv_sqrt_n;
             uint8_t *qrow = PL::kTwoPhase ? job.q + row * (int64_t)(n / 2) : stg + (lane / P) * (n / 2);
-            float *yrow = job.y ? job.y + row * (int64_t)n : nullptr;
+            // output chunk of slot s: phase-2 map, or natural order for one row per thread
+            auto out_chunk = [&](int s) { return PL::kTwoPhase ? chunk_of<C>(t, s, true) : (chunk_t<C>(t, false) | s); };
+            // (-1)^popcount(s & xr): the sign left by the permuted read order
+            auto out_neg = [&](int s) { return !PL::kTwoPhase && (__popc(s & xr) & 1); };
+            // one branch per row for each option (signs after the transform, fp32 output)
+            if (!signs_first) {
+#pragma unroll
+                for (int s = 0; s < NSLOT; ++s) {
+                    const uint4 m = reinterpret_cast<const uint4 *>(sgn)[out_chunk(s)];
+                    const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        v[4 * s + k] ^= ((pair_t)(mm[k] & 0x80000000u) << 32) | (pair_t)(mm[k] << 16);
+                }
+            }
+            if (job.y) {
+                float *yrow = job.y + row * (int64_t)n;
+#pragma unroll
+                for (int s = 0; s < NSLOT; ++s) {
+                    const float ys = out_neg(s) ? -inv_sqrt_n : inv_sqrt_n;
+                    const pair_t sc2 = mk2(ys, ys), z2 = 0ull;
+                    ulonglong2 *yp = reinterpret_cast<ulonglong2 *>(yrow + 8 * out_chunk(s));
+                    yp[0] = make_ulonglong2(fma2(v[4 * s], sc2, z2), fma2(v[4 * s + 1], sc2, z2));
+                    yp[1] = make_ulonglong2(fma2(v[4 * s + 2], sc2, z2), fma2(v[4 * s + 3], sc2, z2));
+                }
+            }
 #pragma unroll
             for (int s4 = 0; s4 < NSLOT; s4 += 4) {
                 uint32_t words[4];
-                int c0 = 0;
+                const int c0 = out_chunk(s4);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int s = s4 + cc;
-                    // output chunk of slot s: phase-2 map, or natural order for one row per thread
-                    const int c = PL::kTwoPhase ? chunk_of<C>(t, s, true) : (chunk_t<C>(t, false) | s);
-                    if (cc == 0) c0 = c;
-                    // (-1)^popcount(s & xr): the sign left by the permuted read order
-                    const bool neg = !PL::kTwoPhase && (__popc(s & xr) & 1);
-                    const float sinv = neg ? -inv : inv;
+                    const float sinv = out_neg(s) ? -inv : inv;
                     const pair_t inv2 = mk2(sinv, sinv);
-                    pair_t f[4] = {v[4 * s], v[4 * s + 1], v[4 * s + 2], v[4 * s + 3]};
-                    if (!signs_first) {
-                        const uint4 m = reinterpret_cast<const uint4 *>(sgn)[c];
-                        const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            f[k] = f[k] ^ (((pair_t)(mm[k] & 0x80000000u) << 32) | (pair_t)(mm[k] << 16));
-                    }
-                    if (yrow) {
-                        const float ys = neg ? -inv_sqrt_n : inv_sqrt_n;
-                        const pair_t sc2 = mk2(ys, ys), z2 = 0ull;
-                        ulonglong2 *yp = reinterpret_cast<ulonglong2 *>(yrow + 8 * c);
-                        yp[0] = make_ulonglong2(fma2(f[0], sc2, z2), fma2(f[1], sc2, z2));
-                        yp[1] = make_ulonglong2(fma2(f[2], sc2, z2), fma2(f[3], sc2, z2));
-                    }
                     uint32_t code[8];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const pair_t qq = fma2(f[k], inv2, bias2);
+                        const pair_t qq = fma2(v[4 * s + k], inv2, bias2);
                         code[2 * k] = (uint32_t)qq;
                         code[2 * k + 1] = (uint32_t)(qq >> 32);
                     }
@@ -557,11 +567,21 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
     const int t = threadIdx.x & 63;
     const int half = t >> 5;
     const bool signs_first = (prm.flags & 1u) != 0;
+    const uint32_t msel = signs_first ? 0xffffffffu : 0u;
     const unsigned full = 0xffffffffu;
     const int64_t total_groups = prm.groups_per_job * prm.njobs;
     unsigned char *wbuf = inbuf + warp * HB;
     ulonglong2 *buf = rowbuf + (size_t)row_in_cta * (n / 4);
     const uint32_t rbar = 1 + row_in_cta;                  // named barrier of the row's two warps
+    // thread bases of every access (slot s adds a compile-time offset)
+    const K4Addr ad = k4_addr(t);
+    const uint4 *sg1 = reinterpret_cast<const uint4 *>(sgn) + ad.c1;         // mask of chunk1(t, s): sg1[8 s]
+    const uint4 *sg3 = reinterpret_cast<const uint4 *>(sgn) + 8 * t;         // mask of chunk3(t, s): sg3[s]
+    const unsigned char *xb = wbuf + 16 * G * (ad.c1 & 255);                 // input of chunk1(t, s): + 128 G s
+    ulonglong2 *const bw1[2] = {buf + ad.w1, buf + (ad.w1 ^ 1)};             // transpose 1 write: [16 s]
+    const ulonglong2 *const br1[2] = {buf + ad.r1, buf + (ad.r1 ^ 1)};       // transpose 1 read: [128 s]
+    ulonglong2 *const bw2[2] = {buf + ad.w2, buf + (ad.w2 ^ 1)};             // transpose 2 write: [128 s]
+    const ulonglong2 *const br2 = buf + 16 * t;                              // transpose 2 read: [k3 ^ m3]
 
     if (threadIdx.x < NW) mbar_init(&bars[threadIdx.x], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -569,7 +589,7 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
 
     // This warp's half of row (group g, row_in_cta): chunks with bit 8 = half.
     auto issue = [&](int64_t g) {
-        const int jb = (int)(g / prm.groups_per_job);
+        const int jb = job_of(g, prm.groups_per_job);
         const RotJob &job = prm.job[jb];
         const int64_t row = (g - (int64_t)jb * prm.groups_per_job) * ROWS + row_in_cta;
         const bool valid = row < job.rows;
@@ -591,7 +611,7 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
     uint32_t phase = 0;
     bool aborted = false;
     for (int64_t grp = blockIdx.x; grp < total_groups; grp += gridDim.x) {
-        const int jb = (int)(grp / prm.groups_per_job);
+        const int jb = job_of(grp, prm.groups_per_job);
         const RotJob &job = prm.job[jb];
         const int64_t row = (grp - (int64_t)jb * prm.groups_per_job) * ROWS + row_in_cta;
 
@@ -604,13 +624,11 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
         const bool active = row < job.rows && !aborted;
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-            const int c = k4_chunk1(t, s);
-            const uint4 m = reinterpret_cast<const uint4 *>(sgn)[c];
+            const uint4 m = sg1[8 * s];
             uint4 g[G];
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-                g[h] = *reinterpret_cast<const uint4 *>(wbuf + 16 * G * (c & 255) + 16 * h);
-            convert_chunk<IN>(g, m, signs_first, &v[4 * s]);   // includes the in-pair stage
+            for (int h = 0; h < G; ++h) g[h] = *reinterpret_cast<const uint4 *>(xb + 128 * G * s + 16 * h);
+            convert_chunk<IN>(g, m, msel, &v[4 * s]);   // includes the in-pair stage
         }
         // hand the input half back to the copy engine (generic reads before the
         // next bulk write) and fetch this warp's half of its next row
@@ -625,15 +643,13 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
         asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-            const int c = k4_chunk1(t, s);
-            buf[k4_pos1(c, 0)] = make_ulonglong2(v[4 * s], v[4 * s + 1]);
-            buf[k4_pos1(c, 1)] = make_ulonglong2(v[4 * s + 2], v[4 * s + 3]);
+            bw1[0][16 * s] = make_ulonglong2(v[4 * s], v[4 * s + 1]);
+            bw1[1][16 * s] = make_ulonglong2(v[4 * s + 2], v[4 * s + 3]);
         }
         asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-            const int c = k4_chunk2(t, s);
-            const ulonglong2 lo = buf[k4_pos1(c, 0)], hi = buf[k4_pos1(c, 1)];
+            const ulonglong2 lo = br1[0][128 * s], hi = br1[1][128 * s];
             v[4 * s] = lo.x; v[4 * s + 1] = lo.y; v[4 * s + 2] = hi.x; v[4 * s + 3] = hi.y;
         }
 #pragma unroll
@@ -643,15 +659,13 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
         asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-            const int c = k4_chunk2(t, s);
-            buf[k4_pos2(c, 0)] = make_ulonglong2(v[4 * s], v[4 * s + 1]);
-            buf[k4_pos2(c, 1)] = make_ulonglong2(v[4 * s + 2], v[4 * s + 3]);
+            bw2[0][128 * s] = make_ulonglong2(v[4 * s], v[4 * s + 1]);
+            bw2[1][128 * s] = make_ulonglong2(v[4 * s + 2], v[4 * s + 3]);
         }
         asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-            const int c = k4_chunk3(t, s);
-            const ulonglong2 lo = buf[k4_pos2(c, 0)], hi = buf[k4_pos2(c, 1)];
+            const ulonglong2 lo = br2[k4_k3(s, 0) ^ ad.m3], hi = br2[k4_k3(s, 1) ^ ad.m3];
             v[4 * s] = lo.x; v[4 * s + 1] = lo.y; v[4 * s + 2] = hi.x; v[4 * s + 3] = hi.y;
         }
 #pragma unroll
@@ -675,29 +689,34 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
             const pair_t inv2 = mk2(inv, inv);
             const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
             if (t == 0) job.scales[row] = (amax / 7.0f) * inv_sqrt_n;
-            float *yrow = job.y ? job.y + row * (int64_t)n : nullptr;
-            uint32_t words[8];
+            // the thread's 64 consecutive elements are chunks 8t + s; one branch per
+            // row for each option (signs after the transform, fp32 output)
+            if (!signs_first) {
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const int c = k4_chunk3(t, s);
-                pair_t f[4] = {v[4 * s], v[4 * s + 1], v[4 * s + 2], v[4 * s + 3]};
-                if (!signs_first) {
-                    const uint4 m = reinterpret_cast<const uint4 *>(sgn)[c];
+                for (int s = 0; s < 8; ++s) {
+                    const uint4 m = sg3[s];
                     const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        f[k] = f[k] ^ (((pair_t)(mm[k] & 0x80000000u) << 32) | (pair_t)(mm[k] << 16));
+                        v[4 * s + k] ^= ((pair_t)(mm[k] & 0x80000000u) << 32) | (pair_t)(mm[k] << 16);
                 }
-                if (yrow) {
-                    const pair_t sc2 = mk2(inv_sqrt_n, inv_sqrt_n), z2 = 0ull;
-                    ulonglong2 *yp = reinterpret_cast<ulonglong2 *>(yrow + 8 * c);
-                    yp[0] = make_ulonglong2(fma2(f[0], sc2, z2), fma2(f[1], sc2, z2));
-                    yp[1] = make_ulonglong2(fma2(f[2], sc2, z2), fma2(f[3], sc2, z2));
+            }
+            if (job.y) {
+                const pair_t sc2 = mk2(inv_sqrt_n, inv_sqrt_n), z2 = 0ull;
+                ulonglong2 *yp = reinterpret_cast<ulonglong2 *>(job.y + row * (int64_t)n + 64 * t);
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    yp[2 * s] = make_ulonglong2(fma2(v[4 * s], sc2, z2), fma2(v[4 * s + 1], sc2, z2));
+                    yp[2 * s + 1] = make_ulonglong2(fma2(v[4 * s + 2], sc2, z2), fma2(v[4 * s + 3], sc2, z2));
                 }
+            }
+            uint32_t words[8];
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
                 uint32_t code[8];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const pair_t qq = fma2(f[k], inv2, bias2);
+                    const pair_t qq = fma2(v[4 * s + k], inv2, bias2);
                     code[2 * k] = (uint32_t)qq;
                     code[2 * k + 1] = (uint32_t)(qq >> 32);
                 }
@@ -793,6 +812,7 @@ cudaError_t launch_n(const KParams &p, int in_type, cudaStream_t stream) {
 
 cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_type, uint64_t seed,
                               uint32_t flags, cudaStream_t stream) {
+    if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;   // job_of() assumes one or two jobs
     KParams p{};
     p.njobs = njobs;
     int64_t max_rows = 0;

@@ -104,26 +104,24 @@ __device__ __forceinline__ void butterfly_pairs(pair_t (&v)[NP], int rb) {
 }
 
 // One chunk (8 elements, 4 pairs) from its raw granule(s): signs (bit 15 / bit 31
-// of mask word k flip element 2k / 2k+1), widening, and the in-pair butterfly.
+// of mask word k flip element 2k / 2k+1; msel = ~0 applies them, 0 skips them,
+// one three-input logic op either way), widening, and the in-pair butterfly.
 template <int IN>
-__device__ __forceinline__ void convert_chunk(const uint4 *g, uint4 m, bool use_sign, pair_t *out) {
-    const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
+__device__ __forceinline__ void convert_chunk(const uint4 *g, uint4 m, uint32_t msel, pair_t *out) {
+    const uint32_t mm[4] = {m.x & msel, m.y & msel, m.z & msel, m.w & msel};
     if constexpr (IN == IN_F32) {
         const uint32_t w[8] = {g[0].x, g[0].y, g[0].z, g[0].w, g[1].x, g[1].y, g[1].z, g[1].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            uint32_t e0 = w[2 * k], e1 = w[2 * k + 1];
-            if (use_sign) {
-                e0 ^= mm[k] << 16;
-                e1 ^= mm[k] & 0x80000000u;
-            }
+            const uint32_t e0 = w[2 * k] ^ (mm[k] << 16);
+            const uint32_t e1 = w[2 * k + 1] ^ (mm[k] & 0x80000000u);
             out[k] = bfly_in(mk2(__uint_as_float(e0), __uint_as_float(e1)));
         }
     } else {
         const uint32_t w[4] = {g[0].x, g[0].y, g[0].z, g[0].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const uint32_t x = use_sign ? (w[k] ^ mm[k]) : w[k];
+            const uint32_t x = w[k] ^ mm[k];
             if constexpr (IN == IN_BF16) {
                 out[k] = bf16w_bfly(x);
             } else {
@@ -156,6 +154,31 @@ __device__ __forceinline__ int k4_pos1(int c, int h) { return (2 * c + h) ^ ((c 
 __device__ __forceinline__ int k4_pos2(int c, int h) {
     return (2 * c + h) ^ ((((c >> 2) ^ (c >> 5)) & 1) | (((c >> 3) & 1) << 1) | (((c >> 4) & 1) << 2));
 }
+
+// Per-thread parts of the maps above (t = 0..63).  The swizzle XORs of the first
+// transpose and of the second one's write side take thread bits only, so those
+// granule positions are a thread base plus 16 s or 128 s; the second transpose's
+// read side XORs slot bit 2 as well, leaving one XOR with a thread constant per
+// access:
+//   k4_chunk1(t, s)           == c1 + 8 s
+//   k4_pos1(k4_chunk1(t,s),h) == (w1 ^ h) + 16 s
+//   k4_pos1(k4_chunk2(t,s),h) == (r1 ^ h) + 128 s
+//   k4_pos2(k4_chunk2(t,s),h) == (w2 ^ h) + 128 s
+//   k4_pos2(k4_chunk3(t,s),h) == 16 t + (k4_k3(s, h) ^ m3)
+struct K4Addr {
+    int c1, w1, r1, w2, m3;
+};
+__device__ __forceinline__ K4Addr k4_addr(int t) {
+    const int x2 = (t >> 2) & 1;
+    K4Addr a;
+    a.c1 = k4_chunk1(t, 0);
+    a.w1 = 2 * a.c1 + x2;
+    a.r1 = 2 * t + x2;
+    a.w2 = (2 * t) ^ ((((t >> 2) ^ (t >> 5)) & 1) | (((t >> 3) & 1) << 1) | (((t >> 4) & 1) << 2));
+    a.m3 = x2 | ((t & 1) << 1) | (((t >> 1) & 1) << 2);
+    return a;
+}
+__host__ __device__ constexpr int k4_k3(int s, int h) { return (2 * s + h) ^ ((s >> 2) & 1); }
 
 }  // namespace
 }  // namespace rq
