@@ -73,6 +73,8 @@ def _load():
     lib.rqo_w4a4_gemm_entries.argtypes = [P, P, P, P, i64, i64, P, P, P, P]
     lib.rqo_kv_rotate_quant.restype = ctypes.c_int
     lib.rqo_kv_rotate_quant.argtypes = [P, P, i64, i64, i64, u64, u32, P, P, P, P]
+    lib.rqo_attn_decode.restype = ctypes.c_int
+    lib.rqo_attn_decode.argtypes = [P, i64, i64, i64, P, P, P, P, i64, u64, u32, ctypes.c_double, ctypes.c_int, P]
     _lib = lib
     return lib
 
@@ -244,6 +246,26 @@ def kv_rotate_quant(k, v, seed: int, flags: int):
                                      _ptr(vq), _ptr(vs))
     _check(st, "kv_rotate_quant")
     return {"kq": kq, "ks": ks, "vq": vq, "vs": vs}
+
+
+def attn_decode(q, kq, ks, vq, vs, seed: int, flags: int, softmax_scale: float, rotated_out: bool = False):
+    """Attention of query rows q [M][heads][head_dim] over the rotated INT4 cache
+    (kq, vq [T][heads][head_dim/2] uint8; ks, vs [T][heads] fp32), in fp64.
+
+    Returns out [M][heads][head_dim] fp64: o~ R^T, or o~ with rotated_out."""
+    qq = _f64(q)
+    M, H, D = qq.shape
+    T = kq.shape[0]
+    kq = np.ascontiguousarray(kq, dtype=np.uint8)
+    vq = np.ascontiguousarray(vq, dtype=np.uint8)
+    ks = np.ascontiguousarray(ks, dtype=np.float32)
+    vs = np.ascontiguousarray(vs, dtype=np.float32)
+    assert kq.shape == (T, H, D // 2) and vq.shape == (T, H, D // 2) and ks.shape == (T, H) and vs.shape == (T, H)
+    out = np.empty((M, H, D), dtype=np.float64)
+    st = _load().rqo_attn_decode(_ptr(qq), M, H, D, _ptr(kq), _ptr(ks), _ptr(vq), _ptr(vs), T, seed, flags,
+                                 float(softmax_scale), 1 if rotated_out else 0, _ptr(out))
+    _check(st, "attn_decode")
+    return out
 
 
 def tie_mask(ratio, window: float = 1e-4) -> np.ndarray:

@@ -343,3 +343,89 @@ int rqo_kv_rotate_quant(const double *k, const double *v, int64_t tokens, int64_
         st = rqo_fwht_quant(v, rows, head_dim, head_dim, seed, flags, vq, vs, NULL, NULL);
     return st;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Attention read of the rotated INT4 cache.                                  */
+/* ------------------------------------------------------------------------- */
+
+/* Decode-time attention over a cache written by rqo_kv_rotate_quant.  [QR]
+ * §End-to-end flow, "The KV cache": on a later token attention reads the
+ * four-bit rotated cache, and rotation invariance keeps the scores those of the
+ * full-precision computation; [QR] §The architecture (the invariance box: a
+ * rotation is cancelled by its transpose downstream, or by a Hadamard of its
+ * own).
+ *
+ * For every query row m and head h (q is [M][heads][head_dim], fp64):
+ *   q~   = q[m][h] R                       (the cache's rotation, same seed/flags)
+ *   k^_t = unpack(kq[t][h]) * ks[t][h]     (dequantized rotated key, fp64)
+ *   e_t  = softmax_scale * (q~ . k^_t),   p_t = exp(e_t - max e) / sum exp(e - max e)
+ *   o~   = sum_t p_t * v^_t                (v^ as k^)
+ *   out  = o~ R^T, or o~ itself when `rotated_out` is set.
+ * Since R is orthogonal, q~ . k^_t = q . (k^_t R^T): the scores are those of
+ * plain attention on the cache taken back to the original basis.  R^T is the
+ * rotation with the other sign side (H is symmetric), i.e. rqo_rotate_row with
+ * flags bit 0 flipped.
+ * Readings: every query row sees every cached token (no mask); one sign vector
+ * for all heads, as the cache write.  out is [M][heads][head_dim], fp64. */
+int rqo_attn_decode(const double *q, int64_t M, int64_t heads, int64_t head_dim, const uint8_t *kq,
+                    const float *ks, const uint8_t *vq, const float *vs, int64_t tokens, uint64_t seed,
+                    uint32_t flags, double softmax_scale, int rotated_out, double *out)
+{
+    if (M < 0 || heads < 0 || tokens < 1 || !is_pow2(head_dim) || head_dim < 2)
+        return RQO_ERR_ARG;
+    const int64_t D = head_dim;
+    int8_t *s = (int8_t *)malloc((size_t)D);
+    double *qr = (double *)malloc((size_t)D * sizeof(double));
+    double *o = (double *)malloc((size_t)D * sizeof(double));
+    double *e = (double *)malloc((size_t)tokens * sizeof(double));
+    int8_t *c = (int8_t *)malloc((size_t)D);
+    if (!s || !qr || !o || !e || !c) {
+        free(s);
+        free(qr);
+        free(o);
+        free(e);
+        free(c);
+        return RQO_ERR_NOMEM;
+    }
+    rqo_signs(seed, D, s);
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t h = 0; h < heads; ++h) {
+            rqo_rotate_row(q + (m * heads + h) * D, D, s, flags, qr);
+            double emax = -INFINITY;
+            for (int64_t t = 0; t < tokens; ++t) {
+                rqo_unpack_row(kq + (t * heads + h) * (D / 2), D, c);
+                const double sk = (double)ks[t * heads + h];
+                double dot = 0.0;
+                for (int64_t j = 0; j < D; ++j)
+                    dot += qr[j] * ((double)c[j] * sk);
+                e[t] = softmax_scale * dot;
+                if (e[t] > emax)
+                    emax = e[t];
+            }
+            double z = 0.0;
+            for (int64_t t = 0; t < tokens; ++t) {
+                e[t] = exp(e[t] - emax);
+                z += e[t];
+            }
+            for (int64_t j = 0; j < D; ++j)
+                o[j] = 0.0;
+            for (int64_t t = 0; t < tokens; ++t) {
+                rqo_unpack_row(vq + (t * heads + h) * (D / 2), D, c);
+                const double pv = (e[t] / z) * (double)vs[t * heads + h];
+                for (int64_t j = 0; j < D; ++j)
+                    o[j] += pv * (double)c[j];
+            }
+            double *dst = out + (m * heads + h) * D;
+            if (rotated_out)
+                memcpy(dst, o, (size_t)D * sizeof(double));
+            else
+                rqo_rotate_row(o, D, s, flags ^ RQO_SIGNS_FIRST, dst);
+        }
+    }
+    free(s);
+    free(qr);
+    free(o);
+    free(e);
+    free(c);
+    return RQO_OK;
+}

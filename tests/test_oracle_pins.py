@@ -365,3 +365,112 @@ def test_kv_is_per_head_rotation_then_quant(flags):
                 assert sc[t, hh] == np.float32(scale)
                 assert all(codes[t, hh, j] == _brute_force_code(ref[j] / scale)
                            for j in range(0, D, 9))
+
+
+# --------------------------------------------------------------------------
+# Attention read of the rotated INT4 cache ([QR] §End-to-end flow, "The KV
+# cache"; §The architecture, the invariance box)
+# --------------------------------------------------------------------------
+
+def _rot_matrix(D, seed, flags):
+    """R as an explicit matrix from scipy's Sylvester Hadamard: diag(s) H / sqrt(D)
+    (signs first) or H diag(s) / sqrt(D)."""
+    H = scipy.linalg.hadamard(D).astype(np.float64) / np.sqrt(D)
+    S = np.diag(oracle.signs(seed, D).astype(np.float64))
+    return S @ H if flags & 1 else H @ S
+
+
+def _dequant_np(packed, scales, D):
+    """Codes from the packed bytes by plain bit arithmetic (byte j: code 2j in the
+    low nibble, 2j+1 in the high one, 4-bit two's complement), times the scale."""
+    b = packed.astype(np.int64)
+    nib = np.stack([b & 15, b >> 4], axis=-1).reshape(*packed.shape[:-1], D)
+    codes = np.where(nib >= 8, nib - 16, nib).astype(np.float64)
+    return codes * scales.astype(np.float64)[..., None]
+
+
+def _attn_cache(T, H, D, seed_data, flags):
+    rng = np.random.default_rng(seed_data)
+    k = rng.standard_normal((T, H, D))
+    v = rng.standard_normal((T, H, D))
+    k[:, :, 3] *= 30.0
+    return oracle.kv_rotate_quant(k, v, 321, flags)
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_attn_matches_explicit_matrices(flags):
+    """Brute force with an explicit R: q~ = q R, scores on the dequantized rotated
+    keys, numpy softmax, weighted rotated values, then o~ R^T."""
+    T, H, D, M = 9, 3, 16, 2
+    c = _attn_cache(T, H, D, 11, flags)
+    q = np.random.default_rng(12).standard_normal((M, H, D))
+    scale = 1.0 / np.sqrt(D)
+    R = _rot_matrix(D, 321, flags)
+    kh = _dequant_np(c["kq"], c["ks"], D)          # [T][H][D]
+    vh = _dequant_np(c["vq"], c["vs"], D)
+    ref_rot = np.empty((M, H, D))
+    for m in range(M):
+        for h in range(H):
+            e = scale * (kh[:, h, :] @ (q[m, h] @ R))
+            p = np.exp(e - e.max())
+            p /= p.sum()
+            ref_rot[m, h] = p @ vh[:, h, :]
+    got_rot = oracle.attn_decode(q, c["kq"], c["ks"], c["vq"], c["vs"], 321, flags, scale, rotated_out=True)
+    got = oracle.attn_decode(q, c["kq"], c["ks"], c["vq"], c["vs"], 321, flags, scale)
+    np.testing.assert_allclose(got_rot, ref_rot, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(got, ref_rot @ R.T, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_attn_rotation_invariance(flags):
+    """Scores through the rotated cache equal plain attention in the original
+    basis on the cache taken back by R^T (R orthogonal): q~ . k^ = q . (k^ R^T)."""
+    T, H, D = 17, 2, 32
+    c = _attn_cache(T, H, D, 21, flags)
+    q = np.random.default_rng(22).standard_normal((1, H, D)) * 2.0
+    R = _rot_matrix(D, 321, flags)
+    kb = _dequant_np(c["kq"], c["ks"], D) @ R.T     # original-basis keys
+    vb = _dequant_np(c["vq"], c["vs"], D) @ R.T
+    scale = 0.3
+    got = oracle.attn_decode(q, c["kq"], c["ks"], c["vq"], c["vs"], 321, flags, scale)
+    for h in range(H):
+        e = scale * (kb[:, h, :] @ q[0, h])
+        p = np.exp(e - e.max())
+        p /= p.sum()
+        np.testing.assert_allclose(got[0, h], p @ vb[:, h, :], rtol=0, atol=1e-12)
+
+
+def test_attn_special_cases():
+    """One cached token: the output is that token's value.  Identical keys, or a
+    zero softmax scale: uniform weights, the mean of the values."""
+    D, H = 8, 2
+    c = _attn_cache(5, H, D, 31, 1)
+    q = np.random.default_rng(32).standard_normal((1, H, D))
+    vh = _dequant_np(c["vq"], c["vs"], D)
+    one = oracle.attn_decode(q, c["kq"][:1], c["ks"][:1], c["vq"][:1], c["vs"][:1], 321, 1, 0.5, rotated_out=True)
+    np.testing.assert_allclose(one[0], vh[0], rtol=0, atol=1e-15)
+    zero = oracle.attn_decode(q, c["kq"], c["ks"], c["vq"], c["vs"], 321, 1, 0.0, rotated_out=True)
+    np.testing.assert_allclose(zero[0], vh.mean(axis=0), rtol=0, atol=1e-14)
+    kq_same = np.broadcast_to(c["kq"][:1], c["kq"].shape).copy()
+    ks_same = np.broadcast_to(c["ks"][:1], c["ks"].shape).copy()
+    same = oracle.attn_decode(q, kq_same, ks_same, c["vq"], c["vs"], 321, 1, 1.0, rotated_out=True)
+    np.testing.assert_allclose(same[0], vh.mean(axis=0), rtol=0, atol=1e-14)
+
+
+def test_attn_dominant_key_selects_its_value():
+    """A key aligned with the rotated query at a large softmax scale takes all the
+    weight (the others are below e^-50 relative)."""
+    D, H, T, flags = 16, 1, 6, 1
+    rng = np.random.default_rng(41)
+    k = rng.standard_normal((T, H, D))
+    v = rng.standard_normal((T, H, D))
+    q = k[2:3].copy()                                  # query = key 2
+    c = oracle.kv_rotate_quant(k, v, 321, flags)
+    kh = _dequant_np(c["kq"], c["ks"], D)
+    qr = q[0, 0] @ _rot_matrix(D, 321, flags)
+    e = kh[:, 0, :] @ qr
+    assert np.argmax(e) == 2
+    scale = 60.0 / (e[2] - np.partition(e, -2)[-2])    # margin of 60 to the runner-up
+    got = oracle.attn_decode(q, c["kq"], c["ks"], c["vq"], c["vs"], 321, flags, scale, rotated_out=True)
+    vh = _dequant_np(c["vq"], c["vs"], D)
+    np.testing.assert_allclose(got[0, 0], vh[2, 0], rtol=0, atol=1e-12)
