@@ -15,6 +15,8 @@
  *   rq_fwht_quant_gemm  decode-sized fusion of rq_fwht_quant and rq_w4a4_gemm:
  *                       rotation, quantization and the W4A4 product in one
  *                       launch, the rotated activations never reaching HBM.
+ *   rq_attn_decode      attention of decode queries over the rotated INT4 KV
+ *                       cache that rq_kv_rotate_quant writes.
  *
  * Sources (page title, then section / equation):
  *   [ROT] "Rotational Quantization: How Orthogonal Transforms and Hadamard
@@ -83,6 +85,8 @@ typedef enum {
 } rq_dtype;
 
 enum { RQ_SIGNS_FIRST = 1u };
+/* rq_attn_decode: leave the output in the rotated basis (o~ instead of o~ R^T). */
+enum { RQ_ATTN_ROTATED_OUT = 2u };
 
 /* Smallest / largest supported Hadamard size (row length n, head_dim). */
 #define RQ_MIN_N 32
@@ -199,6 +203,42 @@ rq_status rq_fwht_quant_gemm(const void *x, rq_dtype x_dtype, int64_t M, int64_t
                              uint64_t seed, uint32_t flags, const uint8_t *w_q, const float *w_scales,
                              int64_t N, void *y, rq_dtype y_dtype, uint8_t *a_q, float *a_scales,
                              void *stream);
+
+/*
+ * rq_attn_decode -- attention of decode queries over the rotated INT4 KV cache.
+ *
+ *   [QR] §End-to-end flow, "The KV cache": a later token's attention reads the
+ *   four-bit rotated cache, and rotation invariance keeps the scores those of
+ *   the full-precision computation; [QR] §The architecture (the invariance box:
+ *   a rotation is cancelled by its transpose, folded into the next weight or
+ *   applied as its own Hadamard).  For query row m and head h:
+ *     q~   = q[m][h] R                        (R as the cache write: seed, flags)
+ *     e_t  = softmax_scale * (q~ . k^_t)      k^_t = codes(kq[t][h]) * ks[t][h]
+ *     p    = softmax over t of e
+ *     out  = (sum_t p_t v^_t) R^T             v^_t = codes(vq[t][h]) * vs[t][h]
+ *   or the sum itself with RQ_ATTN_ROTATED_OUT (for an output weight with R
+ *   folded in).  Every query row attends to every cached token (no mask).
+ *
+ *   q          [M][heads][head_dim] activations, fp32, bf16 or fp16 (q_dtype),
+ *              contiguous.
+ *   kq, vq     [tokens][heads][head_dim/2] packed codes; ks, vs [tokens][heads]
+ *              fp32 scales: the layout rq_kv_rotate_quant writes.
+ *   tokens     >= 1 cached tokens.
+ *   head_dim   32, 64, 128 or 256 (RQ_ERR_UNSUPPORTED otherwise).
+ *   seed       the cache's sign seed.
+ *   flags      RQ_SIGNS_FIRST (as the cache was written) | RQ_ATTN_ROTATED_OUT.
+ *   softmax_scale  multiplies the scores (usually 1/sqrt(head_dim)).
+ *   out        [M][heads][head_dim] fp32.
+ *   Errors: RQ_ERR_INVALID_ARG (negative sizes, tokens < 1 with work to do,
+ *   unknown flags, NULL pointers), RQ_ERR_UNSUPPORTED (dtype, head_dim),
+ *   RQ_ERR_MISALIGNED (q, kq, vq, out not 16-byte aligned; ks, vs not 4-byte
+ *   aligned).  M == 0 or heads == 0 returns RQ_OK without a launch.  One
+ *   cluster of 8 CTAs per (row, head), each reading an eighth of the tokens;
+ *   no global scratch.
+ */
+rq_status rq_attn_decode(const void *q, rq_dtype q_dtype, int64_t M, int64_t heads, int64_t head_dim,
+                         const uint8_t *kq, const float *ks, const uint8_t *vq, const float *vs, int64_t tokens,
+                         uint64_t seed, uint32_t flags, float softmax_scale, float *out, void *stream);
 
 /*
  * rq_sync_status -- wait for `stream` to drain, then report and clear the

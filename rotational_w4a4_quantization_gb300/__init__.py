@@ -13,11 +13,15 @@ Entry points (same names as the C ABI):
   dequant;
 * :func:`kv_rotate_quant` -- head-wise rotation + INT4 quantization of K and V;
 * :func:`fwht_quant_gemm` -- decode-sized fusion of the rotation, quantization
-  and W4A4 product in one launch.
+  and W4A4 product in one launch;
+* :func:`attn_decode` -- attention of decode queries over the rotated INT4 KV
+  cache.
 """
 from ._binding import (  # noqa: F401
+    RQ_ATTN_ROTATED_OUT,
     RQ_SIGNS_FIRST,
     RQError,
+    attn_decode,
     fwht_quant,
     fwht_quant_gemm,
     kv_rotate_quant,
@@ -27,5 +31,5 @@ from ._binding import (  # noqa: F401
     w4a4_gemm,
 )
 
-__all__ = ["RQ_SIGNS_FIRST", "RQError", "fwht_quant", "fwht_quant_gemm", "kv_rotate_quant", "library_path",
-           "load_library", "sync_status", "w4a4_gemm"]
+__all__ = ["RQ_ATTN_ROTATED_OUT", "RQ_SIGNS_FIRST", "RQError", "attn_decode", "fwht_quant", "fwht_quant_gemm",
+           "kv_rotate_quant", "library_path", "load_library", "sync_status", "w4a4_gemm"]

@@ -16,6 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "librq.so")
 
 RQ_SIGNS_FIRST = 1
+RQ_ATTN_ROTATED_OUT = 2
 
 _STATUS = {0: "RQ_OK", 1: "RQ_ERR_INVALID_ARG", 2: "RQ_ERR_UNSUPPORTED", 3: "RQ_ERR_MISALIGNED",
            4: "RQ_ERR_CUDA", 5: "RQ_ERR_TIMEOUT"}
@@ -53,6 +54,8 @@ def load_library() -> ctypes.CDLL:
     lib.rq_kv_rotate_quant.argtypes = [P, P, i32, i64, i64, i64, u64, u32, P, P, P, P, P]
     lib.rq_fwht_quant_gemm.restype = i32
     lib.rq_fwht_quant_gemm.argtypes = [P, i32, i64, i64, i64, u64, u32, P, P, i64, P, i32, P, P, P]
+    lib.rq_attn_decode.restype = i32
+    lib.rq_attn_decode.argtypes = [P, i32, i64, i64, i64, P, P, P, P, i64, u64, u32, ctypes.c_float, P, P]
     lib.rq_sync_status.restype = i32
     lib.rq_sync_status.argtypes = [P]
     lib.rq_status_string.restype = ctypes.c_char_p
@@ -192,6 +195,35 @@ def fwht_quant_gemm(x: torch.Tensor, seed: int, flags: int, w_q: torch.Tensor, w
                                     _ptr(w_scales), N, _ptr(out), _DTYPES[out.dtype], _ptr(a_q), _ptr(a_scales),
                                     _stream(stream))
     _check("rq_fwht_quant_gemm", st)
+    return out
+
+
+def attn_decode(q: torch.Tensor, cache: dict, seed: int, flags: int = RQ_SIGNS_FIRST, softmax_scale=None, *,
+                out=None, stream=None):
+    """Attention of query rows q ([M][heads][head_dim], contiguous fp32/bf16/fp16)
+    over the rotated INT4 cache that :func:`kv_rotate_quant` wrote (a dict with kq,
+    ks, vq, vs).  Returns out [M][heads][head_dim] fp32: (sum_t p_t v^_t) R^T, or the
+    rotated sum with RQ_ATTN_ROTATED_OUT in flags.  softmax_scale defaults to
+    1/sqrt(head_dim)."""
+    lib = load_library()
+    if q.dim() != 3 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous [M][heads][head_dim] tensor")
+    M, H, D = q.shape
+    kq, ks, vq, vs = cache["kq"], cache["ks"], cache["vq"], cache["vs"]
+    T = kq.shape[0]
+    for t, shape, dt in ((kq, (T, H, D // 2), torch.uint8), (vq, (T, H, D // 2), torch.uint8),
+                         (ks, (T, H), torch.float32), (vs, (T, H), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dt or not t.is_contiguous():
+            raise ValueError("cache tensors must be contiguous with the kv_rotate_quant layout")
+    if softmax_scale is None:
+        softmax_scale = D ** -0.5
+    if out is None:
+        out = torch.empty(M, H, D, dtype=torch.float32, device=q.device)
+    _dev(q, kq, ks, vq, vs, out)
+    with torch.cuda.device(q.device):
+        st = lib.rq_attn_decode(_ptr(q), _DTYPES[q.dtype], M, H, D, _ptr(kq), _ptr(ks), _ptr(vq), _ptr(vs), T,
+                                seed, flags, float(softmax_scale), _ptr(out), _stream(stream))
+    _check("rq_attn_decode", st)
     return out
 
 

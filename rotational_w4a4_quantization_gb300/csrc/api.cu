@@ -150,6 +150,25 @@ rq_status rq_fwht_quant_gemm(const void *x, rq_dtype x_dtype, int64_t M, int64_t
     return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }
 
+rq_status rq_attn_decode(const void *q, rq_dtype q_dtype, int64_t M, int64_t heads, int64_t head_dim,
+                         const uint8_t *kq, const float *ks, const uint8_t *vq, const float *vs, int64_t tokens,
+                         uint64_t seed, uint32_t flags, float softmax_scale, float *out, void *stream) {
+    if (M < 0 || heads < 0 || head_dim <= 0 || tokens < 0) return RQ_ERR_INVALID_ARG;
+    if (flags & ~uint32_t(RQ_SIGNS_FIRST | RQ_ATTN_ROTATED_OUT)) return RQ_ERR_INVALID_ARG;
+    if (!rq::is_rot_input(q_dtype)) return RQ_ERR_UNSUPPORTED;
+    if (!rq::attn_decode_supported(head_dim)) return RQ_ERR_UNSUPPORTED;
+    if (M == 0 || heads == 0) return RQ_OK;
+    if (tokens < 1) return RQ_ERR_INVALID_ARG;   // a softmax over no tokens is undefined
+    if (!q || !kq || !ks || !vq || !vs || !out) return RQ_ERR_INVALID_ARG;
+    if (!rq::aligned16(q) || !rq::aligned16(kq) || !rq::aligned16(vq) || !rq::aligned16(out))
+        return RQ_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(ks) & 3u) || (reinterpret_cast<uintptr_t>(vs) & 3u)) return RQ_ERR_MISALIGNED;
+    if (heads > 65535 / 8 || M > 65535) return RQ_ERR_UNSUPPORTED;   // grid limits: 8 CTAs per head, M rows
+    cudaError_t e = rq::launch_attn_decode(q, (int)q_dtype, M, heads, head_dim, kq, ks, vq, vs, tokens, seed, flags,
+                                           softmax_scale, out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+}
+
 rq_status rq_sync_status(void *stream) {
     int word = 0;
     cudaError_t e = rq::read_and_clear_error_word(&word, static_cast<cudaStream_t>(stream));

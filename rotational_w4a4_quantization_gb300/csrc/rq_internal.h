@@ -46,6 +46,13 @@ cudaError_t launch_fused_decode(const void *x, int in_type, int64_t M, int64_t l
                                 const uint8_t *wq, const float *sw, int64_t N, void *y, int y_mode, uint8_t *aq,
                                 float *as, cudaStream_t stream);
 
+// Attention of decode queries over the rotated INT4 KV cache.
+bool attn_decode_supported(int64_t head_dim);
+cudaError_t launch_attn_decode(const void *q, int in_type, int64_t M, int64_t heads, int64_t head_dim,
+                               const uint8_t *kq, const float *ks, const uint8_t *vq, const float *vs,
+                               int64_t tokens, uint64_t seed, uint32_t flags, float softmax_scale, float *out,
+                               cudaStream_t stream);
+
 // Device-resident error word set by bounded waits that gave up.
 cudaError_t read_and_clear_error_word(int *value, cudaStream_t stream);
 int *error_word_device_ptr();

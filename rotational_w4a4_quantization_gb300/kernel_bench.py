@@ -5,6 +5,7 @@
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel kv
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel fused --workload decode
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel unfused --workload decode
+    python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel attn
 
 Runs `--warmup` untimed launches, then `--reps` launches each timed with CUDA events on the
 current stream (L2 flushed before each launch unless `--no-flush`; a GPU-side pause lets
@@ -13,7 +14,9 @@ median time with the algorithmic GB/s or TOPS.  GEMM operands are seeded random 
 the workload's shape; rotation inputs follow the workload's outlier recipe.  `fused` times
 the one-launch rotation + quantization + product of a decode batch, `unfused` the same
 result from the rotation kernel followed by the GEMM kernel (two launches, one timed
-region); both count the bytes of x, the packed weights and scales, and y.
+region); both count the bytes of x, the packed weights and scales, and y.  `attn`
+times one decode query per head over the KV workload's cache (written by the KV
+kernel, 8192 tokens x 32 heads x 128) and counts the cache, the query and the output.
 """
 from __future__ import annotations
 
@@ -33,7 +36,7 @@ from rotational_w4a4_quantization_gb300 import synth  # noqa: E402
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["fwht", "kv", "gemm", "fused", "unfused"], required=True)
+    ap.add_argument("--kernel", choices=["fwht", "kv", "gemm", "fused", "unfused", "attn"], required=True)
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="prefill")
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
@@ -66,6 +69,17 @@ def main(argv=None):
         T, H, D = k.shape
         work, unit = 2 * T * H * (D * 2 + D // 2 + 4), "GB/s"
         what = f"kv_rotate_quant {T}x{H}x{D} bf16"
+    elif args.kernel == "attn":
+        kw = synth.KV
+        k, v = synth.kv_pair(kw.kv_tokens, kw.kv_heads, kw.kv_head_dim, kw.data_seed,
+                             kw.kv_outliers_per_head, kw.kv_outlier_factor)
+        cache = rq.kv_rotate_quant(k.to(dev), v.to(dev), seed, flags)
+        T, H, D = k.shape
+        qd = synth.kv_pair(1, H, D, kw.data_seed + 500, kw.kv_outliers_per_head, kw.kv_outlier_factor)[0].to(dev)
+        o = torch.empty(1, H, D, dtype=torch.float32, device=dev)
+        fn = lambda: rq.attn_decode(qd, cache, seed, flags, out=o)
+        work, unit = 2 * T * H * (D // 2 + 4) + H * D * 2 + H * D * 4, "GB/s"
+        what = f"attn_decode 1 query x {H} heads x {D} over {T} cached tokens"
     elif args.kernel in ("fused", "unfused"):
         if not w.gemm_n or not w.rows:
             raise SystemExit(f"workload {w.name} has no activation GEMM")

@@ -140,3 +140,27 @@ def fused(lib, x=A16, dt=1, M=16, K=4096, ld=4096, flags=1, w=A16, ws=A16, N=409
 ])
 def test_fused_argument_checks(lib, kw, expect):
     assert fused(lib, **kw) == expect
+
+
+def attn(lib, q=A16, dt=1, M=1, H=32, D=128, kq=A16, ks=A16, vq=A16, vs=A16, T=8192, flags=1, out=A16):
+    return lib.rq_attn_decode(q, dt, M, H, D, kq, ks, vq, vs, T, 7, flags, 0.088, out, NULL)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(M=-1), 1),
+    (dict(T=-1), 1),
+    (dict(flags=4), 1),               # unknown flag bit
+    (dict(dt=3), 2),                  # int32 queries
+    (dict(D=96), 2),
+    (dict(D=512), 2),
+    (dict(T=0), 1),                   # a softmax over no tokens
+    (dict(kq=NULL), 1),
+    (dict(out=NULL), 1),
+    (dict(q=A1), 3),
+    (dict(vq=A1), 3),
+    (dict(ks=A1), 3),                 # scales need 4-byte alignment
+    (dict(M=0, q=NULL), 0),           # empty: nothing to do
+    (dict(H=0), 0),
+])
+def test_attn_argument_checks(lib, kw, expect):
+    assert attn(lib, **kw) == expect
