@@ -18,14 +18,19 @@
 //  * warp 0 rotates the query (shuffle FWHT) and folds softmax_scale * log2(e)
 //    into it, so the scores come out in base 2 for exp2;
 //  * a token is read by head_dim/32 lanes, each holding 32 dimensions (16 bytes
-//    of codes of K and of V): codes become fp32 through a byte permute into
-//    0x4B0000nn (2^23 + n, n = q + 8) and one f32x2 add of -(2^23 + 8); the dot
-//    product and the value accumulation are f32x2 FMAs;
-//  * online softmax per token slot (running max, running sum, rescale when the
-//    max grows), then the slots of a warp, the warps of a CTA and the CTAs of a
-//    cluster are merged with the same rule; the 7 other CTAs bulk-copy their
-//    partial (max, sum, accumulator) into rank 0's shared memory, completing on
-//    its mbarrier; a relaxed cluster barrier keeps the sources alive until then;
+//    of codes of K and of V), streamed through a per-lane cp.async ring four
+//    tokens deep (the first requests go out before the query is rotated);
+//  * key codes enter the dot product as the denormals n 2^-149 (n = q + 8, one
+//    byte permute each, exact), against the lane's query values pre-scaled by a
+//    power of two; the lane's partial is scaled back and 8 sum(q~) removed.  Value
+//    codes become fp32 through a byte permute into 0x4B0000nn (2^23 + n) and one
+//    f32x2 add of -(2^23 + 8).  Products are f32x2 FMAs;
+//  * online softmax per token slot with a lazy reference maximum (moved only
+//    when a score passes it by 8 in log2 units), then the slots of a warp, the
+//    warps of a CTA and the CTAs of a cluster are merged with the same rule;
+//    the 7 other CTAs bulk-copy their partial (reference, sum, accumulator) into
+//    rank 0's shared memory, completing on its mbarrier; a relaxed cluster
+//    barrier keeps the sources alive until then;
 //  * rank 0 normalizes, takes the result back by R^T (warp FWHT) unless the
 //    caller keeps the rotated basis, and writes fp32.
 #include "rq.h"
@@ -102,11 +107,14 @@ __device__ __forceinline__ float load_elem(const void *base, int64_t i) {
 // lane * E + e): signs (before or after), Sylvester butterflies over the e bits in
 // registers and over the lane bits by shuffles, then a scale.
 template <int E>
-__device__ __forceinline__ void warp_rotate(float (&v)[E], int lane, uint64_t seed, bool signs_before, float scale) {
-    float sg[E];
+__device__ __forceinline__ void lane_signs(float (&sg)[E], int lane, uint64_t seed) {
 #pragma unroll
     for (int e = 0; e < E; ++e)
         sg[e] = (splitmix64_at(seed, (uint64_t)(lane * E + e)) >> 63) ? -1.f : 1.f;
+}
+template <int E>
+__device__ __forceinline__ void warp_rotate(float (&v)[E], const float (&sg)[E], int lane, bool signs_before,
+                                            float scale) {
     if (signs_before) {
 #pragma unroll
         for (int e = 0; e < E; ++e) v[e] *= sg[e];
@@ -162,6 +170,19 @@ __device__ __forceinline__ void cp4(void *dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(a_smem_u32(dst)), "l"(src) : "memory");
 }
 
+// 8 codes of a packed word -> four pairs of fp32 whose bits are n = q + 8 (the
+// denormals n * 2^-149, exact): one byte permute per value, no arithmetic.
+__device__ __forceinline__ void nibbles_to_denormal_pairs(uint32_t w, pair_t (&c)[4]) {
+    const uint32_t x = w ^ 0x88888888u;
+    const uint32_t lo = x & 0x0f0f0f0fu, hi = (x >> 4) & 0x0f0f0f0fu;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t e0 = __byte_perm(lo, 0u, 0x4440u + k);
+        const uint32_t e1 = __byte_perm(hi, 0u, 0x4440u + k);
+        c[k] = ((pair_t)e1 << 32) | (pair_t)e0;
+    }
+}
+
 // Merge partial softmax state (mb, lb) into (m, l); returns the factors for the
 // accumulators (an empty state has m = -inf and contributes nothing).
 __device__ __forceinline__ void merge_factors(float &m, float &l, float mb, float lb, float &fa, float &fb) {
@@ -215,28 +236,68 @@ attn_decode_kernel(const __grid_constant__ AParams p) {
     }
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
-    // ---- the rotated query, scaled for base-2 scores ----
-    if (warp == 0) {
-        const void *qrow = static_cast<const char *>(p.q) + ((m * p.H + h) * D) * (IN == IN_F32 ? 4 : 2);
-        float v[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[e] = load_elem<IN>(qrow, lane * E + e);
-        warp_rotate<E>(v, lane, p.seed, signs_first, p.qscale);
-#pragma unroll
-        for (int e = 0; e < E; ++e) s.qr[lane * E + e] = v[e];
-    }
-    __syncthreads();
-
     // ---- this lane: dimensions 32 j .. 32 j + 31 of token slot tq ----
     const int j = lane % LPT, tq = lane / LPT;
     // the token slot's lanes: they run the token loop in lockstep (lanes of other
     // slots may leave it one iteration earlier), so shuffles inside it name only them
     const unsigned gmask = (LPT == 32 ? 0xffffffffu : ((1u << LPT) - 1u)) << (tq * LPT);
-    pair_t q2[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) q2[i] = mk2(s.qr[32 * j + 2 * i], s.qr[32 * j + 2 * i + 1]);
     const int64_t t_begin = p.T * rank / kACluster, t_end = p.T * (rank + 1) / kACluster;
     constexpr int STRIDE = kAWarps * TPW;
+
+    // The lane's tokens t_i = t0 + i STRIDE stream through a kARing-deep ring of
+    // cp.async groups: token i + kARing is requested as soon as token i is read.
+    // Groups are committed for every index, empty past the slice end, so that
+    // "wait until at most kARing - 1 groups are pending" always means "token i
+    // has landed".  The first requests go out before the query is rotated.
+    const int64_t t0 = t_begin + warp * TPW + tq;
+    const int nt = t0 < t_end ? (int)((t_end - t0 + STRIDE - 1) / STRIDE) : 0;
+    auto request = [&](int i) {
+        if (i < nt) {
+            const int64_t r = (t0 + (int64_t)i * STRIDE) * p.H + h;
+            ALane &sl = s.ring[i % kARing][threadIdx.x];
+            cp16(&sl.k, p.kq + r * RB + 16 * j);
+            cp16(&sl.v, p.vq + r * RB + 16 * j);
+            cp4(&sl.ks, p.ks + r);
+            cp4(&sl.vs, p.vs + r);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+#pragma unroll
+    for (int i = 0; i < kARing; ++i) request(i);
+
+    // ---- the rotated query, scaled for base-2 scores (warp 0 keeps its signs) ----
+    float sg[E];
+    if (warp == 0) {
+        const void *qrow = static_cast<const char *>(p.q) + ((m * p.H + h) * D) * (IN == IN_F32 ? 4 : 2);
+        float v[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = load_elem<IN>(qrow, lane * E + e);
+        lane_signs<E>(sg, lane, p.seed);
+        warp_rotate<E>(v, sg, lane, signs_first, p.qscale);
+#pragma unroll
+        for (int e = 0; e < E; ++e) s.qr[lane * E + e] = v[e];
+    }
+    __syncthreads();
+
+    // The keys' codes enter as the denormals n 2^-149 (n = q + 8), so the lane's
+    // query values are pre-scaled by 2^kq (its largest below 2^125); a lane's
+    // partial score is then dot * 2^(149 - kq) - 8 sum(q~) over its 32 values.
+    float qmax = 0.f, qsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        qmax = fmaxf(qmax, fabsf(s.qr[32 * j + i]));
+        qsum += s.qr[32 * j + i];
+    }
+    int qex = 0;
+    frexpf(qmax, &qex);                                   // qmax < 2^qex
+    const int kq = qmax > 0.f ? 125 - qex : 0;
+    const int bk = 149 - kq;                              // back-scale exponent, split in two steps
+    const float back1 = qmax > 0.f ? ldexpf(1.f, bk / 2) : 0.f, back2 = ldexpf(1.f, bk - bk / 2);
+    const float qcorr = 8.f * qsum;
+    pair_t q2[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        q2[i] = mk2(ldexpf(s.qr[32 * j + 2 * i], kq), ldexpf(s.qr[32 * j + 2 * i + 1], kq));
     float mrun = -INFINITY, lrun = 0.f;
     pair_t acc[16];
 #pragma unroll
@@ -249,20 +310,22 @@ attn_decode_kernel(const __grid_constant__ AParams p) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             pair_t c[4];
-            codes_to_pairs(kw[i], c);
+            nibbles_to_denormal_pairs(kw[i], c);
             d0 = fma2(c[0], q2[4 * i], d0);
             d1 = fma2(c[1], q2[4 * i + 1], d1);
             d0 = fma2(c[2], q2[4 * i + 2], d0);
             d1 = fma2(c[3], q2[4 * i + 3], d1);
         }
         const pair_t dd = add2(d0, d1);
-        float sc = lo2(dd) + hi2(dd);
+        float sc = ((lo2(dd) + hi2(dd)) * back1) * back2 - qcorr;
 #pragma unroll
         for (int o = 1; o < LPT; o <<= 1) sc += __shfl_xor_sync(gmask, sc, o);
         sc *= ksc;
-        // online softmax
-        if (sc > mrun) {
-            const float f = ex2(mrun - sc);     // 0 for the first token (mrun = -inf)
+        // online softmax with a lazy maximum: the running reference moves only when
+        // a score passes it by more than 8 (weights stay below 2^8), so the rescale
+        // is rare; the first token always sets it (mrun = -inf)
+        if (sc > mrun + 8.f) {
+            const float f = ex2(mrun - sc);     // 0 for the first token
             lrun *= f;
             const pair_t f2 = mk2(f, f), z2 = 0ull;
 #pragma unroll
@@ -283,26 +346,6 @@ attn_decode_kernel(const __grid_constant__ AParams p) {
         }
     };
 
-    // The lane's tokens t_i = t0 + i STRIDE stream through a kARing-deep ring of
-    // cp.async groups: token i + kARing is requested as soon as token i is read.
-    // Groups are committed for every index, empty past the slice end, so that
-    // "wait until at most kARing - 1 groups are pending" always means "token i
-    // has landed".
-    const int64_t t0 = t_begin + warp * TPW + tq;
-    const int nt = t0 < t_end ? (int)((t_end - t0 + STRIDE - 1) / STRIDE) : 0;
-    auto request = [&](int i) {
-        if (i < nt) {
-            const int64_t r = (t0 + (int64_t)i * STRIDE) * p.H + h;
-            ALane &sl = s.ring[i % kARing][threadIdx.x];
-            cp16(&sl.k, p.kq + r * RB + 16 * j);
-            cp16(&sl.v, p.vq + r * RB + 16 * j);
-            cp4(&sl.ks, p.ks + r);
-            cp4(&sl.vs, p.vs + r);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-#pragma unroll
-    for (int i = 0; i < kARing; ++i) request(i);
     for (int i = 0; i < nt; ++i) {
         asm volatile("cp.async.wait_group %0;" ::"n"(kARing - 1) : "memory");
         const ALane &sl = s.ring[i % kARing][threadIdx.x];
@@ -343,16 +386,19 @@ attn_decode_kernel(const __grid_constant__ AParams p) {
 
     // ---- merge the warps into this CTA's record (slot `rank`) ----
     APart<D> &mine = s.part[rank];
-    for (int d = threadIdx.x; d < D; d += kAThreads) {
-        float mm = -INFINITY, ll = 0.f, a = 0.f;
+    if (threadIdx.x < D) {
+        float mm = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kAWarps; ++w) mm = fmaxf(mm, s.wm[w]);
+        float ll = 0.f, a = 0.f;
 #pragma unroll
         for (int w = 0; w < kAWarps; ++w) {
-            float fa, fb;
-            merge_factors(mm, ll, s.wm[w], s.wl[w], fa, fb);
-            a = a * fa + s.wacc[w][d] * fb;
+            const float f = s.wm[w] == -INFINITY ? 0.f : ex2(s.wm[w] - mm);
+            ll += s.wl[w] * f;
+            a += s.wacc[w][threadIdx.x] * f;
         }
-        mine.acc[d] = a;
-        if (d == 0) {
+        mine.acc[threadIdx.x] = a;
+        if (threadIdx.x == 0) {
             mine.m = mm;
             mine.l = ll;
         }
@@ -378,21 +424,26 @@ attn_decode_kernel(const __grid_constant__ AParams p) {
     a_mbar_wait(&s.pbar, 0, p.err);
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     if (warp == 0) {
+        float mm = -INFINITY, f[kACluster], ll = 0.f;
+#pragma unroll
+        for (int r = 0; r < kACluster; ++r) mm = fmaxf(mm, s.part[r].m);
+#pragma unroll
+        for (int r = 0; r < kACluster; ++r) {
+            f[r] = s.part[r].m == -INFINITY ? 0.f : ex2(s.part[r].m - mm);
+            ll += s.part[r].l * f[r];
+        }
+        const float il = 1.f / ll;
         float v[E];
 #pragma unroll
         for (int e = 0; e < E; ++e) {
             const int d = lane * E + e;
-            float mm = -INFINITY, ll = 0.f, a = 0.f;
+            float a = 0.f;
 #pragma unroll
-            for (int r = 0; r < kACluster; ++r) {
-                float fa, fb;
-                merge_factors(mm, ll, s.part[r].m, s.part[r].l, fa, fb);
-                a = a * fa + s.part[r].acc[d] * fb;
-            }
-            v[e] = a / ll;
+            for (int r = 0; r < kACluster; ++r) a += s.part[r].acc[d] * f[r];
+            v[e] = a * il;
         }
         if (!(p.flags & RQ_ATTN_ROTATED_OUT))
-            warp_rotate<E>(v, lane, p.seed, !signs_first, p.inv_sqrt_d);
+            warp_rotate<E>(v, sg, lane, !signs_first, p.inv_sqrt_d);
         float *orow = p.out + (m * p.H + h) * D;
 #pragma unroll
         for (int e = 0; e < E; ++e) orow[lane * E + e] = v[e];
