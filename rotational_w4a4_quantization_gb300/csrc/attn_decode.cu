@@ -15,8 +15,8 @@
 // Design (bound by reading the cache: 2 (head_dim/2 + 4) bytes per token and head):
 //  * one cluster of 8 CTAs per (query row, head); CTA r takes the r-th eighth of
 //    the tokens, so a 8192-token, 32-head cache runs as 256 CTAs, two per SM;
-//  * warp 0 rotates the query (shuffle FWHT) and folds softmax_scale * log2(e)
-//    into it, so the scores come out in base 2 for exp2;
+//  * every warp rotates the query (shuffle FWHT, its own copy: no CTA barrier)
+//    and folds softmax_scale * log2(e) into it, so the scores come out in base 2;
 //  * a token is read by head_dim/32 lanes, each holding 32 dimensions (16 bytes
 //    of codes of K and of V), streamed through a per-lane cp.async ring four
 //    tokens deep (the first requests go out before the query is rotated);
@@ -49,12 +49,7 @@ constexpr int kACluster = 8;
 constexpr int kARing = 4;                         // tokens in flight per lane (cp.async ring)
 constexpr long long kAWaitLimit = 4000000000ll;   // ~2 s at 2 GHz
 
-// One lane's share of one cached token, as its asynchronous copies land: 16 bytes
-// of K codes, 16 of V codes, and the token's two scales.
-struct ALane {
-    uint4 k, v;
-    float ks, vs, pad[2];
-};
+
 
 struct AParams {
     const void *q;
@@ -78,8 +73,11 @@ struct APart {
 
 template <int D>
 struct ASmem {
-    ALane ring[kARing][kAThreads];      // per-lane copy ring (each lane reads back only its own slots)
-    float qr[D];                        // rotated, scaled query
+    // per-lane copy ring, one array per field so that consecutive lanes touch
+    // consecutive words (each lane reads back only its own slots)
+    uint4 rk[kARing][kAThreads], rv[kARing][kAThreads];
+    float rks[kARing][kAThreads], rvs[kARing][kAThreads];
+    float qr[kAWarps][D];               // rotated, scaled query (one copy per warp)
     float wm[kAWarps], wl[kAWarps];     // per-warp partial states
     float wacc[kAWarps][D];
     alignas(16) APart<D> part[kACluster];   // slot r: CTA r's partial (rank 0 holds all)
@@ -254,20 +252,22 @@ attn_decode_kernel(const __grid_constant__ AParams p) {
     auto request = [&](int i) {
         if (i < nt) {
             const int64_t r = (t0 + (int64_t)i * STRIDE) * p.H + h;
-            ALane &sl = s.ring[i % kARing][threadIdx.x];
-            cp16(&sl.k, p.kq + r * RB + 16 * j);
-            cp16(&sl.v, p.vq + r * RB + 16 * j);
-            cp4(&sl.ks, p.ks + r);
-            cp4(&sl.vs, p.vs + r);
+            const int sl = i % kARing;
+            cp16(&s.rk[sl][threadIdx.x], p.kq + r * RB + 16 * j);
+            cp16(&s.rv[sl][threadIdx.x], p.vq + r * RB + 16 * j);
+            cp4(&s.rks[sl][threadIdx.x], p.ks + r);
+            cp4(&s.rvs[sl][threadIdx.x], p.vs + r);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
 #pragma unroll
     for (int i = 0; i < kARing; ++i) request(i);
 
-    // ---- the rotated query, scaled for base-2 scores (warp 0 keeps its signs) ----
+    // ---- the rotated query, scaled for base-2 scores: every warp rotates its own
+    // copy (no CTA barrier; the signs stay in registers for the final R^T) ----
     float sg[E];
-    if (warp == 0) {
+    float *qw = s.qr[warp];
+    {
         const void *qrow = static_cast<const char *>(p.q) + ((m * p.H + h) * D) * (IN == IN_F32 ? 4 : 2);
         float v[E];
 #pragma unroll
@@ -275,9 +275,9 @@ attn_decode_kernel(const __grid_constant__ AParams p) {
         lane_signs<E>(sg, lane, p.seed);
         warp_rotate<E>(v, sg, lane, signs_first, p.qscale);
 #pragma unroll
-        for (int e = 0; e < E; ++e) s.qr[lane * E + e] = v[e];
+        for (int e = 0; e < E; ++e) qw[lane * E + e] = v[e];
     }
-    __syncthreads();
+    __syncwarp();
 
     // The keys' codes enter as the denormals n 2^-149 (n = q + 8), so the lane's
     // query values are pre-scaled by 2^kq (its largest below 2^125); a lane's
@@ -285,8 +285,8 @@ attn_decode_kernel(const __grid_constant__ AParams p) {
     float qmax = 0.f, qsum = 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        qmax = fmaxf(qmax, fabsf(s.qr[32 * j + i]));
-        qsum += s.qr[32 * j + i];
+        qmax = fmaxf(qmax, fabsf(qw[32 * j + i]));
+        qsum += qw[32 * j + i];
     }
     int qex = 0;
     frexpf(qmax, &qex);                                   // qmax < 2^qex
@@ -297,7 +297,7 @@ attn_decode_kernel(const __grid_constant__ AParams p) {
     pair_t q2[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-        q2[i] = mk2(ldexpf(s.qr[32 * j + 2 * i], kq), ldexpf(s.qr[32 * j + 2 * i + 1], kq));
+        q2[i] = mk2(ldexpf(qw[32 * j + 2 * i], kq), ldexpf(qw[32 * j + 2 * i + 1], kq));
     float mrun = -INFINITY, lrun = 0.f;
     pair_t acc[16];
 #pragma unroll
@@ -348,9 +348,9 @@ attn_decode_kernel(const __grid_constant__ AParams p) {
 
     for (int i = 0; i < nt; ++i) {
         asm volatile("cp.async.wait_group %0;" ::"n"(kARing - 1) : "memory");
-        const ALane &sl = s.ring[i % kARing][threadIdx.x];
-        const uint4 kc = sl.k, vc = sl.v;
-        const float ksc = sl.ks, vsc = sl.vs;
+        const int sl = i % kARing;
+        const uint4 kc = s.rk[sl][threadIdx.x], vc = s.rv[sl][threadIdx.x];
+        const float ksc = s.rks[sl][threadIdx.x], vsc = s.rvs[sl][threadIdx.x];
         step(kc, ksc, vc, vsc);
         request(i + kARing);
     }
