@@ -71,7 +71,7 @@ extern "C" {
 typedef enum {
     RQ_OK = 0,
     RQ_ERR_INVALID_ARG = 1, /* a size is negative/zero where not allowed, a required pointer is NULL */
-    RQ_ERR_UNSUPPORTED = 2, /* a size outside what the kernels implement (e.g. n not a power of two) */
+    RQ_ERR_UNSUPPORTED = 2, /* a size outside what the kernels implement (e.g. n = 24) */
     RQ_ERR_MISALIGNED = 3,  /* a pointer or stride breaks the 16-byte rule */
     RQ_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
     RQ_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see rq_sync_status) */
@@ -107,7 +107,18 @@ enum { RQ_ATTN_ROTATED_OUT = 2u };
  *   x        [rows][ld_x] elements of x_dtype (RQ_F32, RQ_BF16 or RQ_F16);
  *            row r is x + r*ld_x, its first n elements are used.
  *   rows     number of rows, >= 0 (0: nothing is enqueued).
- *   n        row length, a power of two in [RQ_MIN_N, RQ_MAX_N].
+ *   n        row length: a power of two in [RQ_MIN_N, RQ_MAX_N], or m 2^k with
+ *            m in {12, 20, 28} and 2^k in [32, 1024] (e.g. 3072, 5120, 14336,
+ *            28672).  For the latter, H_n is H_m (x) H_{2^k} with H_m a Paley
+ *            Hadamard matrix ([ROT] §The Computational Cost of Arbitrary
+ *            Rotations and §SpinQuant: sizes that are not powers of two, via
+ *            products of Sylvester-compatible sizes):
+ *              chi = quadratic character mod q, Q[i][j] = chi(j - i);
+ *              m = 12, 20 (q = 11, 19): H = I + [[0, 1^T], [-1, Q]];
+ *              m = 28 (q = 13): S = [[0, 1^T], [1, Q]],
+ *                H = S (x) [[1, 1], [1, -1]] + I (x) [[1, -1], [-1, -1]];
+ *            element a 2^k + j of a row is segment a, offset j, and
+ *            y = x diag(s) (H_m (x) H_{2^k}) / sqrt(n) (or diag(s) after).
  *   ld_x     row stride in elements, >= n, ld_x * sizeof(x_dtype) % 16 == 0.
  *   seed     sign-vector seed.
  *   flags    RQ_SIGNS_FIRST or 0.

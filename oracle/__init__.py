@@ -73,6 +73,8 @@ def _load():
     lib.rqo_w4a4_gemm_entries.argtypes = [P, P, P, P, i64, i64, P, P, P, P]
     lib.rqo_kv_rotate_quant.restype = ctypes.c_int
     lib.rqo_kv_rotate_quant.argtypes = [P, P, i64, i64, i64, u64, u32, P, P, P, P]
+    lib.rqo_paley.restype = ctypes.c_int
+    lib.rqo_paley.argtypes = [ctypes.c_int, P]
     lib.rqo_attn_decode.restype = ctypes.c_int
     lib.rqo_attn_decode.argtypes = [P, i64, i64, i64, P, P, P, P, i64, u64, u32, ctypes.c_double, ctypes.c_int, P]
     _lib = lib
@@ -115,6 +117,13 @@ def hadamard(x) -> np.ndarray:
         _check(lib.rqo_hadamard(_ptr(row), n), "hadamard")
         flat[r] = row
     return flat.reshape(y.shape)
+
+
+def paley(m: int) -> np.ndarray:
+    """The Hadamard block H_m (m in {12, 20, 28}) of rotations of size n = m 2^k."""
+    H = np.empty((m, m), dtype=np.int8)
+    _check(_load().rqo_paley(m, _ptr(H)), "paley")
+    return H
 
 
 def rotate(x, seed: int, flags: int) -> np.ndarray:

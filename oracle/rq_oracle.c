@@ -96,6 +96,94 @@ static void hadamard_rec(double *x, int64_t n)
 
 static int is_pow2(int64_t n) { return n >= 1 && (n & (n - 1)) == 0; }
 
+/* ------------------------------------------------------------------------- */
+/* Sizes that are not powers of two: n = m 2^k with a Hadamard block H_m.      */
+/* ------------------------------------------------------------------------- */
+
+/* Quadratic character of x modulo the prime q: 0 for x = 0, +1 for a nonzero
+ * square, -1 otherwise (found by listing the squares). */
+static int qchar(int64_t x, int q)
+{
+    x %= q;
+    if (x < 0)
+        x += q;
+    if (x == 0)
+        return 0;
+    for (int64_t y = 1; y < q; ++y)
+        if ((y * y) % q == x)
+            return 1;
+    return -1;
+}
+
+/* Hadamard matrix of order m in {12, 20, 28} (row-major int8, entries +-1).
+ * [ROT] §The Computational Cost of Arbitrary Rotations / §SpinQuant mention sizes
+ * that are not powers of two (padding, or products of Sylvester-compatible
+ * sizes); reading: n = m 2^k with R = (H_m (x) H_{2^k}) / sqrt(n) and H_m from
+ * Paley's constructions over the prime field GF(q):
+ *   Jacobsthal matrix Q[i][j] = qchar(j - i), i, j < q;
+ *   m = 12, 20 (Paley I, q = 11, 19, q = 3 mod 4): S = [[0, 1^T], [-1, Q]],
+ *     H = I + S;
+ *   m = 28 (Paley II, q = 13, q = 1 mod 4): S = [[0, 1^T], [1, Q]],
+ *     H = S (x) [[1, 1], [1, -1]] + I (x) [[1, -1], [-1, -1]].
+ * Returns RQO_ERR_ARG for any other m. */
+int rqo_paley(int m, int8_t *H)
+{
+    int q, two;
+    if (m == 12) {
+        q = 11;
+        two = 0;
+    } else if (m == 20) {
+        q = 19;
+        two = 0;
+    } else if (m == 28) {
+        q = 13;
+        two = 1;
+    } else {
+        return RQO_ERR_ARG;
+    }
+    const int o = q + 1;
+    int S[32][32];
+    for (int i = 0; i < o; ++i)
+        for (int j = 0; j < o; ++j) {
+            if (i == 0 && j == 0)
+                S[i][j] = 0;
+            else if (i == 0)
+                S[i][j] = 1;
+            else if (j == 0)
+                S[i][j] = two ? 1 : -1;
+            else
+                S[i][j] = qchar((int64_t)(j - 1) - (int64_t)(i - 1), q);
+        }
+    if (!two) {
+        for (int i = 0; i < o; ++i)
+            for (int j = 0; j < o; ++j)
+                H[i * m + j] = (int8_t)(S[i][j] + (i == j ? 1 : 0));
+    } else {
+        const int A[2][2] = {{1, 1}, {1, -1}};
+        const int B[2][2] = {{1, -1}, {-1, -1}};
+        for (int i = 0; i < o; ++i)
+            for (int j = 0; j < o; ++j)
+                for (int u = 0; u < 2; ++u)
+                    for (int v = 0; v < 2; ++v)
+                        H[(2 * i + u) * m + (2 * j + v)] =
+                            (int8_t)(S[i][j] * A[u][v] + (i == j ? B[u][v] : 0));
+    }
+    return RQO_OK;
+}
+
+/* n = m 2^k with m in {1, 12, 20, 28} (m = 1: a power of two).  Returns m, or 0
+ * when n has no such form. */
+static int rot_block(int64_t n)
+{
+    if (is_pow2(n))
+        return 1;
+    const int ms[3] = {12, 20, 28};
+    for (int i = 0; i < 3; ++i)
+        if (n % ms[i] == 0 && is_pow2(n / ms[i]))
+            return ms[i];
+    return 0;
+}
+
 int rqo_hadamard(double *x, int64_t n)
 {
     if (!is_pow2(n))
@@ -104,20 +192,50 @@ int rqo_hadamard(double *x, int64_t n)
     return RQO_OK;
 }
 
+/* y = x (H_m (x) H_b) / sqrt(m) for n = m b, b a power of two: the normalized
+ * Sylvester transform of every length-b segment a (elements a b .. a b + b - 1),
+ * then, for every offset j, the row-vector product of the m values x[a b + j]
+ * with H_m / sqrt(m): out[a' b + j] = sum_a x[a b + j] H_m[a][a'] / sqrt(m). */
+static int kron_rotate(double *y, int64_t n, int m)
+{
+    const int64_t b = n / m;
+    for (int a = 0; a < m; ++a)
+        hadamard_rec(y + a * b, b);
+    if (m == 1)
+        return RQO_OK;
+    int8_t H[28 * 28];
+    double col[28];
+    rqo_paley(m, H);
+    const double r = 1.0 / sqrt((double)m);
+    for (int64_t j = 0; j < b; ++j) {
+        for (int a = 0; a < m; ++a)
+            col[a] = y[a * b + j];
+        for (int a2 = 0; a2 < m; ++a2) {
+            double acc = 0.0;
+            for (int a = 0; a < m; ++a)
+                acc += col[a] * (double)H[a * m + a2];
+            y[a2 * b + j] = acc * r;
+        }
+    }
+    return RQO_OK;
+}
+
 /* One rotated row y = x R for the randomized Hadamard R, in the form chosen by
  * flags bit 0 (see RQO_SIGNS_FIRST).  [ROT] §Incoherence, eq. R = H_d·diag(s)
- * and eq. x~ = x R. */
+ * and eq. x~ = x R.  For n = m 2^k (m in {12, 20, 28}) H_d is H_m (x) H_{2^k}
+ * (see rqo_paley). */
 int rqo_rotate_row(const double *x, int64_t n, const int8_t *s, uint32_t flags, double *y)
 {
-    if (!is_pow2(n))
+    const int m = rot_block(n);
+    if (m == 0)
         return RQO_ERR_ARG;
     if (flags & RQO_SIGNS_FIRST) {
         for (int64_t i = 0; i < n; ++i)
             y[i] = x[i] * (double)s[i];
-        hadamard_rec(y, n);
+        kron_rotate(y, n, m);
     } else {
         memcpy(y, x, (size_t)n * sizeof(double));
-        hadamard_rec(y, n);
+        kron_rotate(y, n, m);
         for (int64_t i = 0; i < n; ++i)
             y[i] = y[i] * (double)s[i];
     }
@@ -208,7 +326,7 @@ void rqo_unpack_row(const uint8_t *in, int64_t n, int8_t *q)
 int rqo_fwht_quant(const double *x, int64_t rows, int64_t n, int64_t ld_x, uint64_t seed,
                    uint32_t flags, uint8_t *q, float *scales, double *y_out, double *ratio_out)
 {
-    if (!is_pow2(n) || n < 2 || rows < 0 || ld_x < n)
+    if (rot_block(n) == 0 || n < 2 || (n & 1) || rows < 0 || ld_x < n)
         return RQO_ERR_ARG;
     int8_t *s = (int8_t *)malloc((size_t)n);
     double *y = (double *)malloc((size_t)n * sizeof(double));

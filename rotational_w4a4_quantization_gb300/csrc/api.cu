@@ -69,7 +69,9 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
                         void *stream) {
     if (rows < 0 || n <= 0) return RQ_ERR_INVALID_ARG;
     if (!rq::is_rot_input(x_dtype)) return RQ_ERR_UNSUPPORTED;
-    if (!rq::pow2(n) || n < RQ_MIN_N || n > RQ_MAX_N) return RQ_ERR_UNSUPPORTED;
+    int km = 0, klb = 0;   // n = km 2^klb with a Hadamard block of order km (not a power of two)
+    const bool kron = !rq::pow2(n) && rq::kron_block_of(n, &km, &klb);
+    if (!kron && (!rq::pow2(n) || n < RQ_MIN_N || n > RQ_MAX_N)) return RQ_ERR_UNSUPPORTED;
     if (ld_x < n) return RQ_ERR_INVALID_ARG;
     if (flags & ~uint32_t(RQ_SIGNS_FIRST)) return RQ_ERR_INVALID_ARG;
     if (rows == 0) return RQ_OK;
@@ -78,8 +80,10 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
         return RQ_ERR_MISALIGNED;
     if ((ld_x * rq::elem_size(x_dtype)) % 16 != 0) return RQ_ERR_MISALIGNED;
     rq::RotJob job{x, ld_x, rows, q, scales, y};
-    cudaError_t e = rq::launch_fwht_quant(&job, 1, rq::log2i(n), (int)x_dtype, seed, flags,
-                                          static_cast<cudaStream_t>(stream));
+    cudaError_t e = kron ? rq::launch_fwht_kron(job, km, klb, (int)x_dtype, seed, flags,
+                                                static_cast<cudaStream_t>(stream))
+                         : rq::launch_fwht_quant(&job, 1, rq::log2i(n), (int)x_dtype, seed, flags,
+                                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }
 

@@ -27,6 +27,12 @@ struct RotJob {
 cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_type,
                               uint64_t seed, uint32_t flags, cudaStream_t stream);
 
+// Row lengths n = m 2^k (m in {12, 20, 28}, 2^k in [32, 1024]): R = diag(s) (H_m (x)
+// H_{2^k}) / sqrt(n) with Paley blocks H_m.  kron_block_of reports m and k.
+bool kron_block_of(int64_t n, int *m, int *logb);
+cudaError_t launch_fwht_kron(const RotJob &job, int m, int logb, int in_type, uint64_t seed, uint32_t flags,
+                             cudaStream_t stream);
+
 // y_mode: 0 = fp16 out, 1 = fp32 out, 2 = raw int32 accumulators.
 struct GemmArgs {
     const uint8_t *a_q;

@@ -2,6 +2,7 @@
 
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel gemm --workload prefill
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel fwht --workload large
+    python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel fwht --n 14336   # 28 x 512
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel kv
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel fused --workload decode
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel unfused --workload decode
@@ -41,6 +42,8 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--n", type=int, default=0,
+                    help="fwht: row length instead of the workload's (e.g. 14336 = 28 x 512), same rows and recipe")
     args = ap.parse_args(argv)
 
     rq_build.build()
@@ -53,12 +56,14 @@ def main(argv=None):
     if args.kernel == "fwht":
         if not w.rows:
             raise SystemExit(f"workload {w.name} has no activation")
-        x = synth.activations(w.rows, w.n, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor).to(dev)
-        q = torch.empty(w.rows, w.n // 2, dtype=torch.uint8, device=dev)
+        n = args.n or w.n
+        n_out = synth._n_outliers(n) if args.n else w.n_outliers
+        x = synth.activations(w.rows, n, w.x_dtype, w.data_seed, n_out, w.outlier_factor).to(dev)
+        q = torch.empty(w.rows, n // 2, dtype=torch.uint8, device=dev)
         s = torch.empty(w.rows, dtype=torch.float32, device=dev)
         fn = lambda: rq.fwht_quant(x, seed, flags, q=q, scales=s)
-        work, unit = w.rows * (w.n * x.element_size() + w.n // 2 + 4), "GB/s"
-        what = f"fwht_quant {w.rows}x{w.n} {str(x.dtype).split('.')[-1]}"
+        work, unit = w.rows * (n * x.element_size() + n // 2 + 4), "GB/s"
+        what = f"fwht_quant {w.rows}x{n} {str(x.dtype).split('.')[-1]}"
     elif args.kernel == "kv":
         kw = synth.KV
         k, v = synth.kv_pair(kw.kv_tokens, kw.kv_heads, kw.kv_head_dim, kw.data_seed,

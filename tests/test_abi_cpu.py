@@ -55,6 +55,12 @@ def fq(lib, x=A16, dtype=1, rows=4, n=128, ld=128, flags=1, q=A16, s=A16, y=NULL
     (dict(n=48, ld=48), 2),          # not a power of two
     (dict(n=16, ld=16), 2),          # below the smallest size
     (dict(n=16384, ld=16384), 2),    # above the largest size
+    (dict(n=12 * 16, ld=12 * 16), 2),        # 12 x 16: the power-of-two factor is below 32
+    (dict(n=36 * 64, ld=36 * 64), 2),        # 36 is not one of the Hadamard blocks 12, 20, 28
+    (dict(n=28 * 2048, ld=28 * 2048), 2),    # 28 x 2048: the power-of-two factor is above 1024
+    (dict(n=28 * 512, ld=28 * 512, rows=0), 0),   # 14336 = 28 x 512: accepted
+    (dict(n=12 * 256, ld=12 * 256, rows=0), 0),   # 3072 = 12 x 256: accepted
+    (dict(n=20 * 1024, ld=20 * 1024 - 1, rows=0), 1),   # stride shorter than the row
     (dict(ld=64), 1),                # stride shorter than the row
     (dict(flags=2), 1),
     (dict(dtype=3), 2),              # int32 input

@@ -474,3 +474,58 @@ def test_attn_dominant_key_selects_its_value():
     got = oracle.attn_decode(q, c["kq"], c["ks"], c["vq"], c["vs"], 321, flags, scale, rotated_out=True)
     vh = _dequant_np(c["vq"], c["vs"], D)
     np.testing.assert_allclose(got[0, 0], vh[2, 0], rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Sizes that are not powers of two: n = m 2^k, R = diag(s)(H_m (x) H_{2^k})/sqrt(n)
+# ([ROT] §The Computational Cost of Arbitrary Rotations, §SpinQuant: padding or
+# products of Sylvester-compatible sizes)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("m", [12, 20, 28])
+def test_paley_blocks_are_hadamard(m):
+    """Entries +-1 and H H^T = m I exactly: the defining property of a Hadamard
+    matrix, so H_m / sqrt(m) is orthogonal."""
+    H = oracle.paley(m).astype(np.int64)
+    assert set(np.unique(H)) == {-1, 1}
+    np.testing.assert_array_equal(H @ H.T, m * np.eye(m, dtype=np.int64))
+    if m in (12, 20):                      # Paley I: normalized first row, antisymmetric core
+        assert np.all(H[0] == 1)
+        core = H - np.eye(m, dtype=np.int64)
+        np.testing.assert_array_equal(core, -core.T)
+
+
+@pytest.mark.parametrize("m,b", [(12, 2), (12, 32), (20, 4), (20, 64), (28, 8), (28, 16)])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_kron_rotation_matches_explicit_matrix(m, b, flags):
+    """y = x R with R built by numpy's Kronecker product of H_m and scipy's
+    Sylvester H_b (element a b + j of a row: segment a, offset j)."""
+    n = m * b
+    s = oracle.signs(77, n).astype(np.float64)
+    K = np.kron(oracle.paley(m).astype(np.float64), scipy.linalg.hadamard(b).astype(np.float64)) / np.sqrt(n)
+    R = np.diag(s) @ K if flags & 1 else K @ np.diag(s)
+    x = np.random.default_rng(m + b).standard_normal((3, n))
+    np.testing.assert_allclose(oracle.rotate(x, 77, flags), x @ R, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("n", [12 * 64, 20 * 128, 28 * 512])
+def test_kron_rotation_norm_and_spike(n):
+    """Orthogonal: norms kept.  Every entry of H_m (x) H_b is +-1, so a single spike
+    of magnitude M lands as +-M/sqrt(n) on every coordinate."""
+    x = np.random.default_rng(n).standard_normal((2, n))
+    y = oracle.rotate(x, 5, 1)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-12)
+    spike = np.zeros((1, n))
+    spike[0, n // 3] = 250.0
+    np.testing.assert_allclose(np.abs(oracle.rotate(spike, 5, 0)), 250.0 / np.sqrt(n), rtol=1e-12)
+
+
+def test_kron_fwht_quant_is_rotate_then_quant_then_pack():
+    n = 28 * 32
+    x = np.random.default_rng(3).standard_normal((4, n)) * 3.0
+    out = oracle.fwht_quant(x, 9, 1, want_y=True)
+    y = oracle.rotate(x, 9, 1)
+    np.testing.assert_allclose(out["y"], y, rtol=0, atol=0)
+    codes, scales, _ = oracle.quant_rows(y)
+    np.testing.assert_array_equal(out["q"], oracle.pack(codes))
+    np.testing.assert_allclose(out["scales"], scales.astype(np.float32), rtol=0, atol=0)
