@@ -73,6 +73,14 @@ def _load():
     lib.rqo_w4a4_gemm_entries.argtypes = [P, P, P, P, i64, i64, P, P, P, P]
     lib.rqo_kv_rotate_quant.restype = ctypes.c_int
     lib.rqo_kv_rotate_quant.argtypes = [P, P, i64, i64, i64, u64, u32, P, P, P, P]
+    lib.rqo_quant_row8.restype = None
+    lib.rqo_quant_row8.argtypes = [P, i64, P, P, P]
+    lib.rqo_fwht_quant8.restype = ctypes.c_int
+    lib.rqo_fwht_quant8.argtypes = [P, i64, i64, i64, u64, u32, P, P, P]
+    lib.rqo_fwht_quant_groups.restype = ctypes.c_int
+    lib.rqo_fwht_quant_groups.argtypes = [P, i64, i64, i64, u64, u32, i64, P, P, P]
+    lib.rqo_w4a8_gemm.restype = ctypes.c_int
+    lib.rqo_w4a8_gemm.argtypes = [P, P, P, P, i64, i64, i64, i64, P, P]
     lib.rqo_paley.restype = ctypes.c_int
     lib.rqo_paley.argtypes = [ctypes.c_int, P]
     lib.rqo_attn_decode.restype = ctypes.c_int
@@ -275,6 +283,70 @@ def attn_decode(q, kq, ks, vq, vs, seed: int, flags: int, softmax_scale: float, 
                                  float(softmax_scale), 1 if rotated_out else 0, _ptr(out))
     _check(st, "attn_decode")
     return out
+
+
+def quant_rows8(y):
+    """Per-row symmetric INT8: returns (codes int8, scales fp64, ratios y/scale)."""
+    ys = _f64(y)
+    n = ys.shape[-1]
+    flat = ys.reshape(-1, n)
+    codes = np.empty(flat.shape, dtype=np.int8)
+    ratio = np.empty(flat.shape, dtype=np.float64)
+    scales = np.empty(flat.shape[0], dtype=np.float64)
+    sc = ctypes.c_double()
+    lib = _load()
+    for r in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[r])
+        c = np.empty(n, dtype=np.int8)
+        rt = np.empty(n, dtype=np.float64)
+        lib.rqo_quant_row8(_ptr(row), n, _ptr(c), ctypes.byref(sc), _ptr(rt))
+        codes[r], ratio[r], scales[r] = c, rt, sc.value
+    return codes.reshape(ys.shape), scales.reshape(ys.shape[:-1]), ratio.reshape(ys.shape)
+
+
+def fwht_quant8(x, seed: int, flags: int, want_ratio: bool = False):
+    """Rotation then per-row INT8: dict(q [rows][n] int8, scales fp32[, ratio])."""
+    xs = _f64(x)
+    rows, n = xs.shape
+    q = np.empty((rows, n), dtype=np.int8)
+    scales = np.empty(rows, dtype=np.float32)
+    ratio = np.empty((rows, n), dtype=np.float64) if want_ratio else None
+    _check(_load().rqo_fwht_quant8(_ptr(xs), rows, n, n, seed, flags, _ptr(q), _ptr(scales), _ptr(ratio)),
+           "fwht_quant8")
+    out = {"q": q, "scales": scales}
+    if want_ratio:
+        out["ratio"] = ratio
+    return out
+
+
+def fwht_quant_groups(x, seed: int, flags: int, group: int, want_ratio: bool = False):
+    """Rotation then INT4 per group of `group` elements: dict(q [rows][n/2], scales
+    [rows][n/group] fp32[, ratio])."""
+    xs = _f64(x)
+    rows, n = xs.shape
+    q = np.empty((rows, n // 2), dtype=np.uint8)
+    scales = np.empty((rows, n // group), dtype=np.float32)
+    ratio = np.empty((rows, n), dtype=np.float64) if want_ratio else None
+    _check(_load().rqo_fwht_quant_groups(_ptr(xs), rows, n, n, seed, flags, group, _ptr(q), _ptr(scales),
+                                         _ptr(ratio)), "fwht_quant_groups")
+    out = {"q": q, "scales": scales}
+    if want_ratio:
+        out["ratio"] = ratio
+    return out
+
+
+def w4a8_gemm(aq, sa, wq, sw, M: int, N: int, K: int, group: int):
+    """INT8 activations x packed INT4 weights with per-group scales sw [N][K/group].
+    Returns (acc int64 [M][N] (group == K only, else None), y fp64 [M][N])."""
+    aq = np.ascontiguousarray(aq, dtype=np.int8)
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    sa = np.ascontiguousarray(sa, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    acc = np.empty((M, N), dtype=np.int64) if group == K else None
+    y = np.empty((M, N), dtype=np.float64)
+    _check(_load().rqo_w4a8_gemm(_ptr(aq), _ptr(sa), _ptr(wq), _ptr(sw), M, N, K, group, _ptr(acc), _ptr(y)),
+           "w4a8_gemm")
+    return acc, y
 
 
 def tie_mask(ratio, window: float = 1e-4) -> np.ndarray:

@@ -547,3 +547,135 @@ int rqo_attn_decode(const double *q, int64_t M, int64_t heads, int64_t head_dim,
     free(c);
     return RQO_OK;
 }
+
+/* ------------------------------------------------------------------------- */
+/* W4A8 and per-group weight scales.                                          */
+/* ------------------------------------------------------------------------- */
+
+/* Per-row symmetric INT8 for activations: [SQ] §The architecture ("maps them to
+ * INT4 (weights) and INT8 (activations) with ordinary per-channel or per-group
+ * scales"), §End-to-end flow ("quantizes the rotated activation to INT8").
+ * Reading: scale = max|y| / 127, q = clamp(round_half_even(y / scale), -128, 127)
+ * (-128 never occurs with this scale); an all-zero row gets scale 0, codes 0.
+ * `ratio` (nullable) receives y / scale. */
+void rqo_quant_row8(const double *y, int64_t n, int8_t *q, double *scale, double *ratio)
+{
+    double amax = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        if (fabs(y[i]) > amax)
+            amax = fabs(y[i]);
+    *scale = amax / 127.0;
+    for (int64_t i = 0; i < n; ++i) {
+        const double r = amax > 0.0 ? y[i] / *scale : 0.0;
+        double c = nearbyint(r);
+        if (c < -128.0)
+            c = -128.0;
+        if (c > 127.0)
+            c = 127.0;
+        q[i] = (int8_t)c;
+        if (ratio)
+            ratio[i] = r;
+    }
+}
+
+/* For each row of x: y = x R, then per-row INT8 codes (rows x n bytes) and fp32
+ * scales.  Optional fp64 ratios y / scale (rows x n). */
+int rqo_fwht_quant8(const double *x, int64_t rows, int64_t n, int64_t ld_x, uint64_t seed, uint32_t flags,
+                    int8_t *q, float *scales, double *ratio_out)
+{
+    if (rot_block(n) == 0 || rows < 0 || ld_x < n)
+        return RQO_ERR_ARG;
+    int8_t *s = (int8_t *)malloc((size_t)n);
+    double *y = (double *)malloc((size_t)n * sizeof(double));
+    if (!s || !y) {
+        free(s);
+        free(y);
+        return RQO_ERR_NOMEM;
+    }
+    rqo_signs(seed, n, s);
+    for (int64_t r = 0; r < rows; ++r) {
+        double sc = 0.0;
+        rqo_rotate_row(x + r * ld_x, n, s, flags, y);
+        rqo_quant_row8(y, n, q + r * n, &sc, ratio_out ? ratio_out + r * n : NULL);
+        scales[r] = (float)sc;
+    }
+    free(s);
+    free(y);
+    return RQO_OK;
+}
+
+/* Per-group INT4 weights ([SQ] §The architecture, "per-group scales"): each row
+ * of W^T is rotated (the fold), then every group of `group` consecutive elements
+ * is quantized on its own with the INT4 rule of rqo_quant_row (scale =
+ * max|y_g| / 7).  q: rows x n/2 packed; scales: rows x n/group fp32; ratio
+ * (nullable): rows x n. */
+int rqo_fwht_quant_groups(const double *x, int64_t rows, int64_t n, int64_t ld_x, uint64_t seed, uint32_t flags,
+                          int64_t group, uint8_t *q, float *scales, double *ratio_out)
+{
+    if (rot_block(n) == 0 || rows < 0 || ld_x < n || group < 2 || (group & 1) || n % group)
+        return RQO_ERR_ARG;
+    int8_t *s = (int8_t *)malloc((size_t)n);
+    double *y = (double *)malloc((size_t)n * sizeof(double));
+    int8_t *codes = (int8_t *)malloc((size_t)n);
+    if (!s || !y || !codes) {
+        free(s);
+        free(y);
+        free(codes);
+        return RQO_ERR_NOMEM;
+    }
+    rqo_signs(seed, n, s);
+    const int64_t ng = n / group;
+    for (int64_t r = 0; r < rows; ++r) {
+        rqo_rotate_row(x + r * ld_x, n, s, flags, y);
+        for (int64_t g = 0; g < ng; ++g) {
+            double sc = 0.0;
+            rqo_quant_row(y + g * group, group, codes + g * group, &sc,
+                          ratio_out ? ratio_out + r * n + g * group : NULL);
+            scales[r * ng + g] = (float)sc;
+        }
+        rqo_pack_row(codes, n, q + r * (n / 2));
+    }
+    free(s);
+    free(y);
+    free(codes);
+    return RQO_OK;
+}
+
+/* W4A8 linear layer: INT8 activations (M x K bytes, per-row scales sa) times
+ * packed INT4 weights (N x K/2, one output channel per row) with per-group
+ * scales sw (N x K/group; group == K is per-channel):
+ *   acc_g[m][c] = sum_{k in group g} qa[m][k] qw[c][k]   (exact integers)
+ *   y[m][c]     = sa[m] * sum_g sw[c][g] * acc_g[m][c]    (fp64)
+ * [SQ] §End-to-end flow ("quantizes the rotated activation to INT8, and
+ * multiplies it against the INT4 rotated weights"), §The architecture.
+ * acc (nullable, per-channel only): the whole-K integer sums. */
+int rqo_w4a8_gemm(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M, int64_t N,
+                  int64_t K, int64_t group, int64_t *acc, double *y)
+{
+    if (M < 0 || N < 0 || K <= 0 || (K & 1) || group <= 0 || K % group || (acc && group != K))
+        return RQO_ERR_ARG;
+    int8_t *wrow = (int8_t *)malloc((size_t)K);
+    if (!wrow)
+        return RQO_ERR_NOMEM;
+    const int64_t ng = K / group;
+    for (int64_t c = 0; c < N; ++c) {
+        rqo_unpack_row(wq + c * (K / 2), K, wrow);
+        for (int64_t m = 0; m < M; ++m) {
+            double yy = 0.0;
+            int64_t total = 0;
+            for (int64_t g = 0; g < ng; ++g) {
+                int64_t a = 0;
+                for (int64_t k = g * group; k < (g + 1) * group; ++k)
+                    a += (int64_t)aq[m * K + k] * (int64_t)wrow[k];
+                total += a;
+                yy += (double)sw[c * ng + g] * (double)a;
+            }
+            if (acc)
+                acc[m * N + c] = total;
+            if (y)
+                y[m * N + c] = (double)sa[m] * yy;
+        }
+    }
+    free(wrow);
+    return RQO_OK;
+}

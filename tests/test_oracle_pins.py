@@ -529,3 +529,75 @@ def test_kron_fwht_quant_is_rotate_then_quant_then_pack():
     codes, scales, _ = oracle.quant_rows(y)
     np.testing.assert_array_equal(out["q"], oracle.pack(codes))
     np.testing.assert_allclose(out["scales"], scales.astype(np.float32), rtol=0, atol=0)
+
+
+# --------------------------------------------------------------------------
+# W4A8 and per-group weight scales ([SQ] §The architecture: INT4 weights, INT8
+# activations, per-channel or per-group scales; §End-to-end flow)
+# --------------------------------------------------------------------------
+
+def test_int8_quant_round_half_even_and_range():
+    """scale = max|y|/127: the largest element maps to +-127; exact ties at .5
+    round to even; every dequantized value lies within scale/2."""
+    y = np.array([[127.0, 0.5, 1.5, 2.5, -0.5, -1.5, -126.5, 3.0]])
+    codes, scales, _ = oracle.quant_rows8(y)
+    assert scales[0] == 1.0
+    np.testing.assert_array_equal(codes[0], [127, 0, 2, 2, 0, -2, -126, 3])
+    rng = np.random.default_rng(8)
+    y = rng.standard_normal((5, 300)) * np.array([[1.0], [1e-3], [50.0], [7.0], [0.2]])
+    codes, scales, _ = oracle.quant_rows8(y)
+    assert np.all(np.abs(codes).max(axis=1) == 127)
+    err = np.abs(codes * scales[:, None] - y)
+    assert np.all(err <= scales[:, None] / 2 * (1 + 1e-12))
+    zc, zs, _ = oracle.quant_rows8(np.zeros((1, 16)))
+    assert zs[0] == 0.0 and not zc.any()
+
+
+def test_fwht_quant8_is_rotate_then_int8():
+    x = np.random.default_rng(9).standard_normal((4, 512)) * 4.0
+    out = oracle.fwht_quant8(x, 3, 1)
+    codes, scales, _ = oracle.quant_rows8(oracle.rotate(x, 3, 1))
+    np.testing.assert_array_equal(out["q"], codes)
+    np.testing.assert_array_equal(out["scales"], scales.astype(np.float32))
+
+
+def test_group_quant_reduces_to_per_row_and_group_scales():
+    """With one group per row the per-group fold is the per-row fold; with groups
+    of 128 each group's scale is max|y_g|/7 of the rotated row."""
+    x = np.random.default_rng(10).standard_normal((3, 1024))
+    whole = oracle.fwht_quant_groups(x, 4, 1, 1024)
+    row = oracle.fwht_quant(x, 4, 1)
+    np.testing.assert_array_equal(whole["q"], row["q"])
+    np.testing.assert_array_equal(whole["scales"][:, 0], row["scales"])
+    g = oracle.fwht_quant_groups(x, 4, 1, 128)
+    y = oracle.rotate(x, 4, 1).reshape(3, 8, 128)
+    np.testing.assert_allclose(g["scales"], (np.abs(y).max(axis=2) / 7.0).astype(np.float32), rtol=0, atol=0)
+
+
+def _unpack_np(packed, K):
+    b = packed.astype(np.int64)
+    nib = np.stack([b & 15, b >> 4], axis=-1).reshape(packed.shape[0], K)
+    return np.where(nib >= 8, nib - 16, nib)
+
+
+@pytest.mark.parametrize("group", [32, 128, 256])
+def test_w4a8_gemm_brute_force(group):
+    """Per group: numpy integer matmul of the INT8 codes with the INT4 codes
+    (decoded here by plain bit arithmetic); y = sa * sum_g sw_g * acc_g."""
+    M, N, K = 5, 7, 512
+    rng = np.random.default_rng(group)
+    qa = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+    qw = rng.integers(0, 256, size=(N, K // 2)).astype(np.uint8)
+    sa = rng.random(M).astype(np.float32) + 0.1
+    sw = rng.random((N, K // group)).astype(np.float32) + 0.1
+    w = _unpack_np(qw, K)
+    a = qa.astype(np.int64)
+    ng = K // group
+    accg = np.stack([a[:, g * group:(g + 1) * group] @ w[:, g * group:(g + 1) * group].T for g in range(ng)])
+    ref = sa.astype(np.float64)[:, None] * np.einsum("gmn,ng->mn", accg.astype(np.float64), sw.astype(np.float64))
+    acc, y = oracle.w4a8_gemm(qa, sa, qw, sw, M, N, K, group)
+    assert acc is None
+    np.testing.assert_allclose(y, ref, rtol=1e-13, atol=0)
+    swc = rng.random((N, 1)).astype(np.float32)
+    acc, y = oracle.w4a8_gemm(qa, sa, qw, swc, M, N, K, K)
+    np.testing.assert_array_equal(acc, a @ w.T)
