@@ -16,7 +16,9 @@
  *                       rotation, quantization and the W4A4 product in one
  *                       launch, the rotated activations never reaching HBM.
  *   rq_attn_decode      attention of decode queries over the rotated INT4 KV
- *                       cache that rq_kv_rotate_quant writes.
+ *                       cache that rq_kv_rotate_quant writes;
+ *   rq_w4a8_gemm        the W4A8 variant of the linear layer (INT8 activations),
+ *                       with per-channel or per-group weight scales.
  *
  * Sources (page title, then section / equation):
  *   [ROT] "Rotational Quantization: How Orthogonal Transforms and Hadamard
@@ -87,6 +89,10 @@ typedef enum {
 enum { RQ_SIGNS_FIRST = 1u };
 /* rq_attn_decode: leave the output in the rotated basis (o~ instead of o~ R^T). */
 enum { RQ_ATTN_ROTATED_OUT = 2u };
+/* rq_fwht_quant (n = 4096): INT8 codes per row (activations of the W4A8 layer),
+ * or INT4 codes with one scale per group of 128 elements (weights of the W4A8
+ * layer with per-group scales). */
+enum { RQ_INT8_CODES = 4u, RQ_GROUP_SCALES = 8u };
 
 /* Smallest / largest supported Hadamard size (row length n, head_dim). */
 #define RQ_MIN_N 32
@@ -121,7 +127,15 @@ enum { RQ_ATTN_ROTATED_OUT = 2u };
  *            y = x diag(s) (H_m (x) H_{2^k}) / sqrt(n) (or diag(s) after).
  *   ld_x     row stride in elements, >= n, ld_x * sizeof(x_dtype) % 16 == 0.
  *   seed     sign-vector seed.
- *   flags    RQ_SIGNS_FIRST or 0.
+ *   flags    RQ_SIGNS_FIRST or 0, plus at most one of (n = 4096 only):
+ *            RQ_INT8_CODES: per-row INT8 codes for the W4A8 layer's
+ *              activations ([SQ] §End-to-end flow): q is [rows][n] int8,
+ *              scale = max|y| / 127, q = clamp(round_half_even(y / scale),
+ *              -128, 127), scales [rows] fp32 as above;
+ *            RQ_GROUP_SCALES: INT4 codes with one scale per group of 128
+ *              consecutive elements ([SQ] §The architecture, per-group scales;
+ *              the weight fold of the W4A8 layer): q as above, scales
+ *              [rows][n/128] fp32.
  *   q        out: [rows][n/2] bytes, packed codes (row stride n/2).
  *   scales   out: [rows] fp32 scales, max|y|/7 of each rotated row.
  *   y        out, may be NULL: [rows][n] fp32 rotated rows y = xR (parity
@@ -250,6 +264,33 @@ rq_status rq_fwht_quant_gemm(const void *x, rq_dtype x_dtype, int64_t M, int64_t
 rq_status rq_attn_decode(const void *q, rq_dtype q_dtype, int64_t M, int64_t heads, int64_t head_dim,
                          const uint8_t *kq, const float *ks, const uint8_t *vq, const float *vs, int64_t tokens,
                          uint64_t seed, uint32_t flags, float softmax_scale, float *out, void *stream);
+
+/*
+ * rq_w4a8_gemm -- the W4A8 linear layer with per-channel or per-group weight scales.
+ *
+ *   [SQ] §The architecture (INT4 weights, INT8 activations, per-channel or
+ *   per-group scales), §End-to-end flow (the rotated activation quantized to
+ *   INT8 and multiplied against the INT4 rotated weights):
+ *     acc_g[m][c] = sum_{k in group g} a_q[m][k] * w_q[c][k]   (exact integers)
+ *     y[m][c]     = a_scales[m] * sum_g w_scales[c][g] * acc_g[m][c]
+ *
+ *   a_q       [M][K] int8 codes (rq_fwht_quant with RQ_INT8_CODES).
+ *   a_scales  [M] fp32.
+ *   w_q       [N][K/2] packed INT4 codes, one output channel per row.
+ *   w_scales  [N] fp32 (group == K) or [N][K/128] fp32 (group == 128,
+ *             rq_fwht_quant with RQ_GROUP_SCALES on the rows of W^T).
+ *   K         a multiple of 128.  group: 128 or K.
+ *   y, y_dtype  [M][N]: RQ_F16, RQ_F32, or RQ_I32 (raw exact sums, group == K
+ *             only).
+ *   Decode-oriented: every M goes through one kernel of legacy tensor-core MMAs
+ *   (int8 x int8 -> int32), CTAs of 16 channels x 32 tokens.
+ *   Errors: RQ_ERR_INVALID_ARG (negative sizes, NULL pointers),
+ *   RQ_ERR_UNSUPPORTED (K, group, y_dtype), RQ_ERR_MISALIGNED (a_q, w_q, y not
+ *   16-byte aligned; scales not 4-byte aligned).  M == 0 or N == 0 returns
+ *   RQ_OK without a launch.
+ */
+rq_status rq_w4a8_gemm(const int8_t *a_q, const float *a_scales, const uint8_t *w_q, const float *w_scales,
+                       int64_t M, int64_t N, int64_t K, int64_t group, void *y, rq_dtype y_dtype, void *stream);
 
 /*
  * rq_sync_status -- wait for `stream` to drain, then report and clear the

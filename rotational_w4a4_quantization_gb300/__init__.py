@@ -15,10 +15,15 @@ Entry points (same names as the C ABI):
 * :func:`fwht_quant_gemm` -- decode-sized fusion of the rotation, quantization
   and W4A4 product in one launch;
 * :func:`attn_decode` -- attention of decode queries over the rotated INT4 KV
-  cache.
+  cache;
+* :func:`w4a8_gemm` -- the W4A8 linear layer (INT8 activations from
+  :func:`fwht_quant` with ``RQ_INT8_CODES``), per-channel or per-group weight
+  scales.
 """
 from ._binding import (  # noqa: F401
     RQ_ATTN_ROTATED_OUT,
+    RQ_GROUP_SCALES,
+    RQ_INT8_CODES,
     RQ_SIGNS_FIRST,
     RQError,
     attn_decode,
@@ -29,7 +34,9 @@ from ._binding import (  # noqa: F401
     load_library,
     sync_status,
     w4a4_gemm,
+    w4a8_gemm,
 )
 
-__all__ = ["RQ_ATTN_ROTATED_OUT", "RQ_SIGNS_FIRST", "RQError", "attn_decode", "fwht_quant", "fwht_quant_gemm",
-           "kv_rotate_quant", "library_path", "load_library", "sync_status", "w4a4_gemm"]
+__all__ = ["RQ_ATTN_ROTATED_OUT", "RQ_GROUP_SCALES", "RQ_INT8_CODES", "RQ_SIGNS_FIRST", "RQError", "attn_decode",
+           "fwht_quant", "fwht_quant_gemm", "kv_rotate_quant", "library_path", "load_library", "sync_status",
+           "w4a4_gemm", "w4a8_gemm"]

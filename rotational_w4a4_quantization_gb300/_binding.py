@@ -17,6 +17,8 @@ _LIB_PATH = os.path.join(_HERE, "librq.so")
 
 RQ_SIGNS_FIRST = 1
 RQ_ATTN_ROTATED_OUT = 2
+RQ_INT8_CODES = 4
+RQ_GROUP_SCALES = 8
 
 _STATUS = {0: "RQ_OK", 1: "RQ_ERR_INVALID_ARG", 2: "RQ_ERR_UNSUPPORTED", 3: "RQ_ERR_MISALIGNED",
            4: "RQ_ERR_CUDA", 5: "RQ_ERR_TIMEOUT"}
@@ -54,6 +56,8 @@ def load_library() -> ctypes.CDLL:
     lib.rq_kv_rotate_quant.argtypes = [P, P, i32, i64, i64, i64, u64, u32, P, P, P, P, P]
     lib.rq_fwht_quant_gemm.restype = i32
     lib.rq_fwht_quant_gemm.argtypes = [P, i32, i64, i64, i64, u64, u32, P, P, i64, P, i32, P, P, P]
+    lib.rq_w4a8_gemm.restype = i32
+    lib.rq_w4a8_gemm.argtypes = [P, P, P, P, i64, i64, i64, i64, P, i32, P]
     lib.rq_attn_decode.restype = i32
     lib.rq_attn_decode.argtypes = [P, i32, i64, i64, i64, P, P, P, P, i64, u64, u32, ctypes.c_float, P, P]
     lib.rq_sync_status.restype = i32
@@ -100,7 +104,9 @@ def fwht_quant(x: torch.Tensor, seed: int, flags: int = RQ_SIGNS_FIRST, *, q=Non
     randomized Hadamard R and quantize it to packed INT4.
 
     Returns ``(q, scales)`` or ``(q, scales, y)`` when ``want_y``: q is
-    (rows x n/2) uint8, scales (rows,) fp32, y (rows x n) fp32 = x R."""
+    (rows x n/2) uint8, scales (rows,) fp32, y (rows x n) fp32 = x R.  With
+    RQ_INT8_CODES in flags q is (rows x n) int8; with RQ_GROUP_SCALES scales is
+    (rows x n/128)."""
     lib = load_library()
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit stride in the last dimension")
@@ -108,9 +114,11 @@ def fwht_quant(x: torch.Tensor, seed: int, flags: int = RQ_SIGNS_FIRST, *, q=Non
         raise ValueError("x must be float32, bfloat16 or float16")
     rows, n = x.shape
     if q is None:
-        q = torch.empty(rows, n // 2, dtype=torch.uint8, device=x.device)
+        q = (torch.empty(rows, n, dtype=torch.int8, device=x.device) if flags & RQ_INT8_CODES
+             else torch.empty(rows, n // 2, dtype=torch.uint8, device=x.device))
     if scales is None:
-        scales = torch.empty(rows, dtype=torch.float32, device=x.device)
+        scales = (torch.empty(rows, n // 128, dtype=torch.float32, device=x.device) if flags & RQ_GROUP_SCALES
+                  else torch.empty(rows, dtype=torch.float32, device=x.device))
     if want_y and y is None:
         y = torch.empty(rows, n, dtype=torch.float32, device=x.device)
     _dev(x, q, scales, y)
@@ -224,6 +232,27 @@ def attn_decode(q: torch.Tensor, cache: dict, seed: int, flags: int = RQ_SIGNS_F
         st = lib.rq_attn_decode(_ptr(q), _DTYPES[q.dtype], M, H, D, _ptr(kq), _ptr(ks), _ptr(vq), _ptr(vs), T,
                                 seed, flags, float(softmax_scale), _ptr(out), _stream(stream))
     _check("rq_attn_decode", st)
+    return out
+
+
+def w4a8_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_dtype=torch.float16, out=None,
+              stream=None):
+    """a_q (M x K int8) x w_q (N x K/2 packed INT4): y (M x N).  w_scales of shape (N,)
+    are per channel, (N, K/128) per group of 128; out_dtype float16 / float32, or
+    int32 (raw exact sums, per-channel scales only)."""
+    lib = load_library()
+    M, K = a_q.shape
+    N, kb = w_q.shape
+    if kb * 2 != K or a_q.dtype != torch.int8 or w_q.dtype != torch.uint8:
+        raise ValueError("a_q must be int8 (M x K), w_q uint8 (N x K/2)")
+    group = K if w_scales is None or w_scales.dim() == 1 else K // w_scales.shape[1]
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
+    _dev(a_q, a_scales, w_q, w_scales, out)
+    with torch.cuda.device(a_q.device):
+        st = lib.rq_w4a8_gemm(_ptr(a_q), _ptr(a_scales), _ptr(w_q), _ptr(w_scales), M, N, K, group, _ptr(out),
+                              _DTYPES[out.dtype], _stream(stream))
+    _check("rq_w4a8_gemm", st)
     return out
 
 

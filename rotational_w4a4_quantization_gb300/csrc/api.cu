@@ -73,7 +73,9 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
     const bool kron = !rq::pow2(n) && rq::kron_block_of(n, &km, &klb);
     if (!kron && (!rq::pow2(n) || n < RQ_MIN_N || n > RQ_MAX_N)) return RQ_ERR_UNSUPPORTED;
     if (ld_x < n) return RQ_ERR_INVALID_ARG;
-    if (flags & ~uint32_t(RQ_SIGNS_FIRST)) return RQ_ERR_INVALID_ARG;
+    if (flags & ~uint32_t(RQ_SIGNS_FIRST | RQ_INT8_CODES | RQ_GROUP_SCALES)) return RQ_ERR_INVALID_ARG;
+    if ((flags & RQ_INT8_CODES) && (flags & RQ_GROUP_SCALES)) return RQ_ERR_INVALID_ARG;
+    if ((flags & (RQ_INT8_CODES | RQ_GROUP_SCALES)) && n != 4096) return RQ_ERR_UNSUPPORTED;
     if (rows == 0) return RQ_OK;
     if (!x || !q || !scales) return RQ_ERR_INVALID_ARG;
     if (!rq::aligned16(x) || !rq::aligned16(q) || !rq::aligned16(scales) || (y && !rq::aligned16(y)))
@@ -170,6 +172,24 @@ rq_status rq_attn_decode(const void *q, rq_dtype q_dtype, int64_t M, int64_t hea
     if (heads > 65535 / 8 || M > 65535) return RQ_ERR_UNSUPPORTED;   // grid limits: 8 CTAs per head, M rows
     cudaError_t e = rq::launch_attn_decode(q, (int)q_dtype, M, heads, head_dim, kq, ks, vq, vs, tokens, seed, flags,
                                            softmax_scale, out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+}
+
+rq_status rq_w4a8_gemm(const int8_t *a_q, const float *a_scales, const uint8_t *w_q, const float *w_scales,
+                       int64_t M, int64_t N, int64_t K, int64_t group, void *y, rq_dtype y_dtype, void *stream) {
+    if (M < 0 || N < 0 || K <= 0 || group <= 0) return RQ_ERR_INVALID_ARG;
+    if (K % 128 != 0 || (group != 128 && group != K)) return RQ_ERR_UNSUPPORTED;
+    if (y_dtype != RQ_F16 && y_dtype != RQ_F32 && !(y_dtype == RQ_I32 && group == K)) return RQ_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return RQ_OK;
+    if (!a_q || !w_q || !y || (y_dtype != RQ_I32 && (!a_scales || !w_scales))) return RQ_ERR_INVALID_ARG;
+    if (!rq::aligned16(a_q) || !rq::aligned16(w_q) || !rq::aligned16(y)) return RQ_ERR_MISALIGNED;
+    if ((a_scales && (reinterpret_cast<uintptr_t>(a_scales) & 3u)) ||
+        (w_scales && (reinterpret_cast<uintptr_t>(w_scales) & 3u)))
+        return RQ_ERR_MISALIGNED;
+    if ((M + 31) / 32 > 65535) return RQ_ERR_UNSUPPORTED;
+    const int y_mode = y_dtype == RQ_F16 ? 0 : (y_dtype == RQ_F32 ? 1 : 2);
+    cudaError_t e = rq::launch_w4a8_gemm(a_q, a_scales, w_q, w_scales, M, N, K, group, y, y_mode,
+                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }
 

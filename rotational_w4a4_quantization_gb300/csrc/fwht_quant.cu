@@ -47,6 +47,7 @@
 //    input copies are in flight, and then walks groups of rows.
 //  * n = 4096 (the activation size of the serving path) has its own variant
 //    with 64 values per thread and three butterfly phases (see below).
+#include "rq.h"
 #include "rq_internal.h"
 #include "rot_device.cuh"
 
@@ -673,6 +674,8 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
 
         // ---------------- row absmax (two warps) ----------------
         float amax = pairs_absmax<NP>(v);
+        // a group of 128 elements (per-group scales) is the 64 of threads t and t ^ 1
+        const float amax_grp = fmaxf(amax, __shfl_xor_sync(full, amax, 1));
 #pragma unroll
         for (int k = 0; k < 5; ++k) amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1 << k));
         if (lane == 0) red[row_in_cta * 2 + half] = aborted ? __int_as_float(-1) : amax;
@@ -685,10 +688,18 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
 
         // ---------------- quantize, pack, store: 64 consecutive elements ----------------
         if (active) {
-            const float inv = amax > 0.f ? 7.0f / amax : 0.f;
+            // codes: INT4 per row (default), INT8 per row, or INT4 per group of 128
+            const bool i8 = (prm.flags & RQ_INT8_CODES) != 0, grp = (prm.flags & RQ_GROUP_SCALES) != 0;
+            const float am = grp ? amax_grp : amax;
+            const float qmax = i8 ? 127.0f : 7.0f;
+            const float inv = am > 0.f ? qmax / am : 0.f;
             const pair_t inv2 = mk2(inv, inv);
             const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
-            if (t == 0) job.scales[row] = (amax / 7.0f) * inv_sqrt_n;
+            if (grp) {
+                if ((t & 1) == 0) job.scales[row * (int64_t)(n / 128) + (t >> 1)] = (am / 7.0f) * inv_sqrt_n;
+            } else if (t == 0) {
+                job.scales[row] = (am / qmax) * inv_sqrt_n;
+            }
             // the thread's 64 consecutive elements are chunks 8t + s; one branch per
             // row for each option (signs after the transform, fp32 output)
             if (!signs_first) {
@@ -710,21 +721,45 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
                     yp[2 * s + 1] = make_ulonglong2(fma2(v[4 * s + 2], sc2, z2), fma2(v[4 * s + 3], sc2, z2));
                 }
             }
-            uint32_t words[8];
+            if (i8) {
+                // one byte per code (the low byte of the biased float is the
+                // two's-complement code): 64 bytes, four 16-byte stores
+                uint32_t words[16];
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                uint32_t code[8];
+                for (int s = 0; s < 8; ++s) {
+                    uint32_t code[8];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const pair_t qq = fma2(v[4 * s + k], inv2, bias2);
-                    code[2 * k] = (uint32_t)qq;
-                    code[2 * k + 1] = (uint32_t)(qq >> 32);
+                    for (int k = 0; k < 4; ++k) {
+                        const pair_t qq = fma2(v[4 * s + k], inv2, bias2);
+                        code[2 * k] = (uint32_t)qq;
+                        code[2 * k + 1] = (uint32_t)(qq >> 32);
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        words[2 * s + h] = __byte_perm(__byte_perm(code[4 * h], code[4 * h + 1], 0x0040u),
+                                                       __byte_perm(code[4 * h + 2], code[4 * h + 3], 0x0040u), 0x5410u);
                 }
-                words[s] = pack8(code);
+                uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)n + 64 * t);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    qp[c] = make_uint4(words[4 * c], words[4 * c + 1], words[4 * c + 2], words[4 * c + 3]);
+            } else {
+                uint32_t words[8];
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    uint32_t code[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const pair_t qq = fma2(v[4 * s + k], inv2, bias2);
+                        code[2 * k] = (uint32_t)qq;
+                        code[2 * k + 1] = (uint32_t)(qq >> 32);
+                    }
+                    words[s] = pack8(code);
+                }
+                uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)(n / 2) + 32 * t);
+                qp[0] = make_uint4(words[0], words[1], words[2], words[3]);
+                qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
             }
-            uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)(n / 2) + 32 * t);
-            qp[0] = make_uint4(words[0], words[1], words[2], words[3]);
-            qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
         }
     }
     if (aborted) {

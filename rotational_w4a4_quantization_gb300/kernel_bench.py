@@ -7,6 +7,7 @@
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel fused --workload decode
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel unfused --workload decode
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel attn
+    python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel w4a8 --workload decode
 
 Runs `--warmup` untimed launches, then `--reps` launches each timed with CUDA events on the
 current stream (L2 flushed before each launch unless `--no-flush`; a GPU-side pause lets
@@ -18,6 +19,8 @@ result from the rotation kernel followed by the GEMM kernel (two launches, one t
 region); both count the bytes of x, the packed weights and scales, and y.  `attn`
 times one decode query per head over the KV workload's cache (written by the KV
 kernel, 8192 tokens x 32 heads x 128) and counts the cache, the query and the output.
+`w4a8` times the W4A8 product (INT8 activations, INT4 weights, one scale per group of
+128) of the workload's GEMM shape and counts 2MNK.
 """
 from __future__ import annotations
 
@@ -37,7 +40,7 @@ from rotational_w4a4_quantization_gb300 import synth  # noqa: E402
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["fwht", "kv", "gemm", "fused", "unfused", "attn"], required=True)
+    ap.add_argument("--kernel", choices=["fwht", "kv", "gemm", "fused", "unfused", "attn", "w4a8"], required=True)
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="prefill")
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
@@ -74,6 +77,20 @@ def main(argv=None):
         T, H, D = k.shape
         work, unit = 2 * T * H * (D * 2 + D // 2 + 4), "GB/s"
         what = f"kv_rotate_quant {T}x{H}x{D} bf16"
+    elif args.kernel == "w4a8":
+        if not w.gemm_n:
+            raise SystemExit(f"workload {w.name} has no GEMM")
+        M, K, N = w.rows, w.n, w.gemm_n
+        g8 = torch.Generator().manual_seed(1000 + w.data_seed)
+        a8 = torch.randint(-128, 128, (M, K), dtype=torch.int8, generator=g8).to(dev)
+        s8 = (torch.rand(M, generator=g8) + 0.05).to(dev)
+        wq, _ = synth.random_codes(N, K, 1001 + w.data_seed)
+        sg = (torch.rand(N, K // 128, generator=g8) + 0.05).to(dev)
+        wq = wq.to(dev)
+        y = torch.empty(M, N, dtype=torch.float16, device=dev)
+        fn = lambda: rq.w4a8_gemm(a8, s8, wq, sg, out=y)
+        work, unit = 2 * M * N * K, "TOPS"
+        what = f"w4a8_gemm {M}x{K}x{N} per-group-128 fp16"
     elif args.kernel == "attn":
         kw = synth.KV
         k, v = synth.kv_pair(kw.kv_tokens, kw.kv_heads, kw.kv_head_dim, kw.data_seed,

@@ -170,3 +170,37 @@ def attn(lib, q=A16, dt=1, M=1, H=32, D=128, kq=A16, ks=A16, vq=A16, vs=A16, T=8
 ])
 def test_attn_argument_checks(lib, kw, expect):
     assert attn(lib, **kw) == expect
+
+
+def w8(lib, a=A16, sa=A16, w=A16, sw=A16, M=16, N=4096, K=4096, group=128, y=A16, ydt=2):
+    return lib.rq_w4a8_gemm(a, sa, w, sw, M, N, K, group, y, ydt, NULL)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(M=-1), 1),
+    (dict(K=0), 1),
+    (dict(group=0), 1),
+    (dict(K=4000), 2),                # K not a multiple of 128
+    (dict(group=64), 2),              # groups of 128 or one per channel only
+    (dict(ydt=3), 2),                 # raw int32 sums need per-channel scales
+    (dict(ydt=1), 2),                 # bf16 output not offered
+    (dict(a=NULL), 1),
+    (dict(sw=NULL), 1),
+    (dict(w=A1), 3),
+    (dict(sa=A1), 3),                 # scales need 4-byte alignment
+    (dict(M=0, a=NULL), 0),
+    (dict(N=0), 0),
+])
+def test_w4a8_argument_checks(lib, kw, expect):
+    assert w8(lib, **kw) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(n=4096, ld=4096, flags=1 | 4, rows=0), 0),     # INT8 codes at n = 4096
+    (dict(n=4096, ld=4096, flags=8, rows=0), 0),         # per-group scales at n = 4096
+    (dict(n=2048, ld=2048, flags=4, rows=0), 2),         # INT8 codes only for n = 4096
+    (dict(n=4096, ld=4096, flags=4 | 8, rows=0), 1),     # one mode at a time
+    (dict(n=4096, ld=4096, flags=16, rows=0), 1),        # unknown flag bit
+])
+def test_fwht_code_mode_checks(lib, kw, expect):
+    assert fq(lib, **kw) == expect

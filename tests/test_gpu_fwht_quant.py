@@ -13,7 +13,7 @@ import oracle
 import rotational_w4a4_quantization_gb300 as rq
 from rotational_w4a4_quantization_gb300 import synth
 
-from parity import compare_codes, compare_rows, compare_scales, to_np
+from parity import compare_codes, compare_rows, compare_scales, to_np, unpack_codes
 
 pytestmark = pytest.mark.gpu
 
@@ -73,7 +73,7 @@ def test_degenerate_rows(n):
     q, s, y = rq.fwht_quant(x.to(DEV), 3, rq.RQ_SIGNS_FIRST, want_y=True)
     qn, sn = to_np(q), to_np(s)
     assert sn[0] == 0.0 and sn[5] == 0.0 and not qn[0].any() and not qn[5].any()
-    codes1 = oracle.unpack(qn[1:2], n)[0]
+    codes1 = unpack_codes(qn[1:2], n)[0]
     assert set(np.unique(np.abs(codes1)).tolist()) == {7}
     np.testing.assert_allclose(np.abs(to_np(y)[1]), 100.0 / np.sqrt(n), rtol=1e-6)
     _run_and_compare(x, seed=3, flags=rq.RQ_SIGNS_FIRST)

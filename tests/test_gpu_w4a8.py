@@ -1,0 +1,117 @@
+"""GPU parity of the W4A8 path ([SQ] §The architecture, §End-to-end flow):
+INT8 activation codes and per-group INT4 weight codes from rq_fwht_quant
+(n = 4096), and rq_w4a8_gemm with per-channel or per-group weight scales.
+
+Bars: codes identical to the oracle's except in the tie window (a difference of
+one allowed there), scales within 1e-5; the product on the oracle's codes:
+int32 sums bit-exact (per-channel), fp32 within 1e-5 relative, fp16 within one
+ulp.  The end-to-end decode case compares the GPU's output with the oracle's
+computed entirely from the oracle's own codes, within the bound that the tie
+window allows: per row, (codes in the tie window) x a_scale x 8 x w_scale.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rotational_w4a4_quantization_gb300 as rq
+from rotational_w4a4_quantization_gb300 import synth
+
+from parity import compare_codes, compare_f16, compare_scales, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+K4 = 4096
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _compare_int8(gpu_q, ref_q, ratio):
+    g, r = gpu_q.astype(np.int16), ref_q.astype(np.int16)
+    diff = g != r
+    tie = oracle.tie_mask(ratio)
+    bad = diff & ~(tie & (np.abs(g - r) == 1))
+    assert not bad.any(), f"{int(bad.sum())} INT8 codes differ outside the tie window"
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
+def test_int8_activation_codes(dt, flags):
+    x = synth.activations(21, K4, dt, 5, 4, 100.0)
+    q, s = rq.fwht_quant(x.to(DEV), synth.SIGN_SEED, flags | rq.RQ_INT8_CODES)
+    assert q.dtype == torch.int8 and q.shape == (21, K4)
+    ref = oracle.fwht_quant8(x.double().numpy(), synth.SIGN_SEED, flags, want_ratio=True)
+    _compare_int8(to_np(q), ref["q"], ref["ratio"])
+    compare_scales(to_np(s), ref["scales"])
+
+
+@pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
+def test_group_weight_codes(flags):
+    wt = synth.weights_t(37, K4, 7, 0.02)
+    q, s = rq.fwht_quant(wt.to(DEV), synth.SIGN_SEED, flags | rq.RQ_GROUP_SCALES)
+    assert s.shape == (37, K4 // 128)
+    ref = oracle.fwht_quant_groups(wt.double().numpy(), synth.SIGN_SEED, flags, 128, want_ratio=True)
+    compare_codes(to_np(q), ref["q"], ref["ratio"], K4)
+    compare_scales(to_np(s), ref["scales"])
+
+
+def _random_operands(M, N, K, group, seed):
+    g = np.random.default_rng(seed)
+    qa = g.integers(-128, 128, size=(M, K)).astype(np.int8)
+    qw = g.integers(0, 256, size=(N, K // 2)).astype(np.uint8)
+    sa = (g.random(M) + 0.05).astype(np.float32)
+    sw = (g.random((N, K // group) if group != K else N) + 0.05).astype(np.float32)
+    return qa, sa, qw, sw
+
+
+def _gpu(qa, sa, qw, sw, out_dtype):
+    d = [torch.from_numpy(np.ascontiguousarray(a)).to(DEV) for a in (qa, sa, qw, sw)]
+    y = rq.w4a8_gemm(*d, out_dtype=out_dtype)
+    assert rq.sync_status() == 0
+    return to_np(y)
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33, 64])
+@pytest.mark.parametrize("N,K", [(16, 128), (40, 512), (256, 4096)])
+def test_product_per_channel(M, N, K):
+    qa, sa, qw, sw = _random_operands(M, N, K, K, 1000 + M + N + K)
+    acc, yref = oracle.w4a8_gemm(qa, sa, qw, sw.reshape(N, 1), M, N, K, K)
+    np.testing.assert_array_equal(_gpu(qa, sa, qw, sw, torch.int32).astype(np.int64), acc)
+    np.testing.assert_allclose(_gpu(qa, sa, qw, sw, torch.float32), yref, rtol=1e-5, atol=0)
+    compare_f16(_gpu(qa, sa, qw, sw, torch.float16), yref)
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 40])
+@pytest.mark.parametrize("N,K", [(16, 128), (48, 1024), (128, 4096)])
+def test_product_per_group(M, N, K):
+    qa, sa, qw, sw = _random_operands(M, N, K, 128, 2000 + M + N + K)
+    _, yref = oracle.w4a8_gemm(qa, sa, qw, sw, M, N, K, 128)
+    y = _gpu(qa, sa, qw, sw, torch.float32)
+    # fp32 sums of K/128 scaled group partials: relative to the row's magnitude
+    err = np.abs(y - yref).max(axis=1)
+    assert np.all(err <= 1e-5 * np.abs(yref).max(axis=1))
+    compare_f16(_gpu(qa, sa, qw, sw, torch.float16), yref, atol=1e-5 * np.abs(yref).max(axis=1, keepdims=True))
+
+
+def test_decode_workload_end_to_end():
+    """16 tokens x 4096 -> 4096: INT8 activations and the product on the GPU,
+    weights folded per group of 128 by the oracle (the offline step), against the
+    oracle computed from its own codes."""
+    w = synth.WORKLOADS["decode"]
+    x = synth.activations(w.rows, w.n, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor)
+    wt = synth.weights_t(w.gemm_n, w.n, w.weight_seed, w.w_std)
+    fold = oracle.fwht_quant_groups(wt.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, 128)
+    ref_a = oracle.fwht_quant8(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, want_ratio=True)
+    _, yref = oracle.w4a8_gemm(ref_a["q"], ref_a["scales"], fold["q"], fold["scales"], w.rows, w.gemm_n, w.n, 128)
+    qa, sa = rq.fwht_quant(x.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST | rq.RQ_INT8_CODES)
+    y = to_np(rq.w4a8_gemm(qa, sa, torch.from_numpy(fold["q"]).to(DEV), torch.from_numpy(fold["scales"]).to(DEV),
+                           out_dtype=torch.float32))
+    ties = oracle.tie_mask(ref_a["ratio"]).sum(axis=1)            # per row
+    bound = (ties[:, None] * ref_a["scales"].astype(np.float64)[:, None] * 8.0
+             * fold["scales"].astype(np.float64).max(axis=1)[None, :])
+    bound += 1e-5 * np.abs(yref).max(axis=1, keepdims=True)
+    assert np.all(np.abs(y - yref) <= bound)
