@@ -115,3 +115,21 @@ def test_decode_workload_end_to_end():
              * fold["scales"].astype(np.float64).max(axis=1)[None, :])
     bound += 1e-5 * np.abs(yref).max(axis=1, keepdims=True)
     assert np.all(np.abs(y - yref) <= bound)
+
+
+def test_int8_codes_prefill_batch():
+    """2048 rows: the 512-thread CTAs of the n = 4096 kernel."""
+    x = synth.activations(2048, K4, torch.bfloat16, 3, 4, 100.0)
+    q, s = rq.fwht_quant(x.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST | rq.RQ_INT8_CODES)
+    ref = oracle.fwht_quant8(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, want_ratio=True)
+    _compare_int8(to_np(q), ref["q"], ref["ratio"])
+    compare_scales(to_np(s), ref["scales"])
+
+
+def test_group_codes_large_fold():
+    """1300 weight rows (fp32): the 256-thread CTAs of the n = 4096 kernel."""
+    wt = synth.weights_t(1300, K4, 9, 0.02)
+    q, s = rq.fwht_quant(wt.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST | rq.RQ_GROUP_SCALES)
+    ref = oracle.fwht_quant_groups(wt.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, 128, want_ratio=True)
+    compare_codes(to_np(q), ref["q"], ref["ratio"], K4)
+    compare_scales(to_np(s), ref["scales"])
