@@ -282,8 +282,13 @@ rq_status rq_attn_decode(const void *q, rq_dtype q_dtype, int64_t M, int64_t hea
  *   K         a multiple of 128.  group: 128 or K.
  *   y, y_dtype  [M][N]: RQ_F16, RQ_F32, or RQ_I32 (raw exact sums, group == K
  *             only).
- *   Decode-oriented: every M goes through one kernel of legacy tensor-core MMAs
- *   (int8 x int8 -> int32), CTAs of 16 channels x 32 tokens.
+ *   Kernels: per-channel scales with M > 64, K <= 65536 and rows of y a
+ *   multiple of 16 bytes run on the 5th-generation tensor cores (each INT8 code
+ *   split exactly into two 4-bit halves, a = 16 (a >> 4) + (a & 15), both
+ *   multiplied as FP8 into separate exact accumulators, CTA pairs, 128 x 256
+ *   output tiles); everything else goes through legacy tensor-core MMAs
+ *   (int8 x int8 -> int32), CTAs of 16 channels x 32 tokens.  Either way the
+ *   integer sums are exact.
  *   Errors: RQ_ERR_INVALID_ARG (negative sizes, NULL pointers),
  *   RQ_ERR_UNSUPPORTED (K, group, y_dtype), RQ_ERR_MISALIGNED (a_q, w_q, y not
  *   16-byte aligned; scales not 4-byte aligned).  M == 0 or N == 0 returns

@@ -59,8 +59,12 @@ cudaError_t launch_attn_decode(const void *q, int in_type, int64_t M, int64_t he
                                int64_t tokens, uint64_t seed, uint32_t flags, float softmax_scale, float *out,
                                cudaStream_t stream);
 
-// W4A8 product for few tokens: INT8 activations, INT4 weights, per-channel
-// (group == K) or per-group (group == 128) weight scales.
+// W4A8 product: INT8 activations, INT4 weights, per-channel (group == K) or
+// per-group (group == 128) weight scales.  Per-channel scales with more than 64
+// tokens run on the tensor cores (launch_w4a8_gemm_tc), the rest on mma.sync.
+bool w4a8_gemm_tc_supported(int64_t M, int64_t N, int64_t K, int y_mode);
+cudaError_t launch_w4a8_gemm_tc(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,
+                                int64_t N, int64_t K, void *y, int y_mode, cudaStream_t stream);
 cudaError_t launch_w4a8_gemm(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,
                              int64_t N, int64_t K, int64_t group, void *y, int y_mode, cudaStream_t stream);
 

@@ -59,6 +59,20 @@
 // (even codes, then odd codes), which leaves every dot product unchanged.
 // Every mbarrier wait is bounded: on expiry the CTA raises the library's error
 // word, stops, releases its tensor memory and returns.
+//
+// W4A8 variant (A8; "SpinQuant" page, The architecture: INT8 activations, INT4
+// weights, one scale per output channel).  An INT8 code a splits exactly into
+// a = 16 h + l with h = a >> 4 in [-8, 7] and l = a & 15 in [0, 15].  Each
+// activation row becomes two operand rows of 4-bit values: row 2i holds
+// u = h + 8, row 2i+1 holds u = l, both exact E4M3 bytes as above, so an
+// operand tile of 128 rows carries 64 activation rows and both accumulators
+// stay exact (sum u u_w <= 225 K).  The epilogue combines the two TMEM lanes of
+// a row (adjacent lanes of one warp):
+//   sum a q_w = 16 (acc_h - 8 sum u_h + c) + (acc_l - 8 sum u_l),
+//   c = 64 K - 8 sum u_w (the W4A4 column term),
+// which is sum a u_w - 8 sum a with sum a = sum (16 u_h - 128 + l).  The packed
+// A tile of a K block is 64 rows x 128 bytes of int8 codes, the same 8 KB as
+// 128 rows x 64 bytes of packed nibbles, so the rings are unchanged.
 #include "rq_internal.h"
 
 #include <cuda.h>
@@ -324,12 +338,53 @@ __device__ __forceinline__ void cluster_sync() {
     }
 }
 
-template <int YMODE, bool PAIR>
+// Store NV consecutive outputs of row m from column nb on: raw sums (YMODE 2),
+// or acc * sa * sw in fp32 (1) or fp16 (0); groups that would cross N are
+// skipped (N * element size is a multiple of 16 bytes).
+template <int YMODE, int NV>
+__device__ __forceinline__ void store_outputs(void *y, int64_t N, int64_t m, int64_t nb, const int (&acc)[NV],
+                                              const float *ws, float sa) {
+    const float4 *ws4 = reinterpret_cast<const float4 *>(ws);
+    if (YMODE == 2) {
+        int *yr = static_cast<int *>(y) + m * N + nb;
+#pragma unroll
+        for (int j = 0; j < NV; j += 4)
+            if (nb + j + 3 < N) *reinterpret_cast<int4 *>(yr + j) = make_int4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+    } else if (YMODE == 1) {
+        float *yr = static_cast<float *>(y) + m * N + nb;
+#pragma unroll
+        for (int j = 0; j < NV; j += 4) {
+            if (nb + j + 3 >= N) continue;
+            const float4 w4 = ws4[j / 4];
+            float4 o;
+            o.x = ((float)acc[j] * sa) * w4.x;
+            o.y = ((float)acc[j + 1] * sa) * w4.y;
+            o.z = ((float)acc[j + 2] * sa) * w4.z;
+            o.w = ((float)acc[j + 3] * sa) * w4.w;
+            *reinterpret_cast<float4 *>(yr + j) = o;
+        }
+    } else {
+        __half *yr = static_cast<__half *>(y) + m * N + nb;
+#pragma unroll
+        for (int j = 0; j < NV; j += 8) {
+            if (nb + j + 7 >= N) continue;
+            __align__(16) __half h[8];
+            const float4 wa = ws4[j / 4], wb = ws4[j / 4 + 1];
+            const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int e2 = 0; e2 < 8; ++e2) h[e2] = __float2half_rn(((float)acc[j + e2] * sa) * wv[e2]);
+            *reinterpret_cast<uint4 *>(yr + j) = *reinterpret_cast<const uint4 *>(h);
+        }
+    }
+}
+
+template <int YMODE, bool PAIR, bool A8>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                const __grid_constant__ TcParams prm) {
     using C = Cfg<PAIR>;
     using S = Smem<PAIR>;
+    static_assert(!A8 || PAIR, "the W4A8 variant runs on CTA pairs");
     extern __shared__ uint8_t smem_raw[];
     // align by offsetting the shared array itself, so the compiler keeps the
     // shared address space (plain LDS/STS instead of generic accesses)
@@ -339,7 +394,8 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t rank = PAIR ? cluster_rank() : 0;
     const int kblocks = (int)(prm.K / BK);
     const int64_t n_tiles_n = (prm.N + BN - 1) / BN;
-    const int64_t n_tiles = n_tiles_n * ((prm.M + C::TILE_M - 1) / C::TILE_M);
+    const int64_t m_op = A8 ? 2 * prm.M : prm.M;     // operand rows (two per INT8 activation row)
+    const int64_t n_tiles = n_tiles_n * ((m_op + C::TILE_M - 1) / C::TILE_M);
     const int64_t first_tile = blockIdx.x / C::NCTA, tile_step = gridDim.x / C::NCTA;
 
     if (threadIdx.x == 0) {
@@ -389,13 +445,15 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int64_t g = 0;                                   // global K-block counter
             bool ok = true;
             for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step) {
-                const int m0 = (int)(tile / n_tiles_n) * C::TILE_M + (int)rank * BM;
+                // A rows of this CTA: 128 packed rows, or (A8) 64 INT8 rows
+                const int m0 = A8 ? (int)(tile / n_tiles_n) * (C::TILE_M / 2) + (int)rank * (BM / 2)
+                                  : (int)(tile / n_tiles_n) * C::TILE_M + (int)rank * BM;
                 const int n0 = (int)(tile % n_tiles_n) * BN + (int)rank * C::WROWS;
                 for (int kb = 0; kb < kblocks; ++kb, ++g) {
                     const int st = (int)(g % C::PK_STAGES);
                     if (!mbar_wait<false, true>(s, &s.pk_empty[st], (uint32_t)((g / C::PK_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
                     mbar_expect_tx(&s.pk_full[st], C::PK_A + C::PK_W);
-                    tma_load_2d(s.pkA[st], &tmA, &s.pk_full[st], kb * (BK / 2), m0);
+                    tma_load_2d(s.pkA[st], &tmA, &s.pk_full[st], kb * (A8 ? BK : BK / 2), m0);
                     tma_load_2d(s.pkW[st], &tmW, &s.pk_full[st], kb * (BK / 2), n0);
                 }
             }
@@ -440,9 +498,12 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // the tile's weight scale for column tc, loaded now so that its latency
             // is not on the converters' path at the end of the tile
             const float wsc = (YMODE != 2 && tc < BN && n0 + tc < prm.N) ? prm.sw[n0 + tc] : 0.f;
-            uint32_t sumA[C::NACH], sumW[C::NWCH];
+            // A8: sumA holds the rows' sum of u_h, sumL their sum of u_l
+            uint32_t sumA[C::NACH], sumL[A8 ? C::NACH : 1], sumW[C::NWCH];
 #pragma unroll
             for (int j = 0; j < C::NACH; ++j) sumA[j] = 0;
+#pragma unroll
+            for (int j = 0; j < (A8 ? C::NACH : 1); ++j) sumL[j] = 0;
 #pragma unroll
             for (int j = 0; j < C::NWCH; ++j) sumW[j] = 0;
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
@@ -468,8 +529,34 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     *reinterpret_cast<uint4 *>(rowp + 16 * g0) = make_uint4(lo[0], hi[0], lo[1], hi[1]);
                     *reinterpret_cast<uint4 *>(rowp + 16 * g1) = make_uint4(lo[2], hi[2], lo[3], hi[3]);
                 };
+                if constexpr (A8) {
+                    // INT8 chunk tt + 128 j = row (tt >> 3) + 16 j, codes 16 c .. 16 c + 15
+                    // with c = tt & 7 -> granule c of operand rows 2 row (u_h) and
+                    // 2 row + 1 (u_l), in the even-then-odd order of the W side
+                    const int c = tt & 7;
 #pragma unroll
-                for (int j = 0; j < C::NACH; ++j) emit(s.opA[os], rq + 32 * j, a[j], sumA[j]);
+                    for (int j = 0; j < C::NACH; ++j) {
+                        const uint4 &v = a[j];
+                        const uint32_t p[4] = {__byte_perm(v.x, v.y, 0x6420u), __byte_perm(v.x, v.y, 0x7531u),
+                                               __byte_perm(v.z, v.w, 0x6420u), __byte_perm(v.z, v.w, 0x7531u)};
+                        uint32_t h[4], l[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            h[i] = ((p[i] >> 4) & 0x0f0f0f0fu) ^ 0x08080808u;   // h + 8 = top nibble, sign bit flipped
+                            l[i] = p[i] & 0x0f0f0f0fu;
+                        }
+                        sumA[j] = __dp4a(h[0] + h[1] + h[2] + h[3], 0x01010101u, sumA[j]);   // byte lanes <= 60
+                        sumL[j] = __dp4a(l[0] + l[1] + l[2] + l[3], 0x01010101u, sumL[j]);
+                        const int r2 = 2 * ((tt >> 3) + 16 * j);
+                        uint8_t *rowp = s.opA[os] + r2 * 128;
+                        *reinterpret_cast<uint4 *>(rowp + 16 * (c ^ (r2 & 7))) = make_uint4(h[0], h[1], h[2], h[3]);
+                        *reinterpret_cast<uint4 *>(rowp + 128 + 16 * (c ^ ((r2 + 1) & 7))) =
+                            make_uint4(l[0], l[1], l[2], l[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < C::NACH; ++j) emit(s.opA[os], rq + 32 * j, a[j], sumA[j]);
+                }
 #pragma unroll
                 for (int j = 0; j < C::NWCH; ++j) emit(s.opW[os], rq + 32 * j, w[j], sumW[j]);
                 // One proxy fence per thread orders its generic reads of the packed
@@ -486,11 +573,18 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
             }
             if (!ok) break;
-            // row sums: the four lanes sharing a row hold its four chunks
+            // row sums: the four lanes sharing a row hold its four chunks (A8: the
+            // eight lanes sharing an INT8 row hold its eight chunks)
 #pragma unroll
             for (int j = 0; j < C::NACH; ++j) {
                 sumA[j] += __shfl_xor_sync(0xffffffffu, sumA[j], 1);
                 sumA[j] += __shfl_xor_sync(0xffffffffu, sumA[j], 2);
+                if constexpr (A8) {
+                    sumA[j] += __shfl_xor_sync(0xffffffffu, sumA[j], 4);
+                    sumL[j] += __shfl_xor_sync(0xffffffffu, sumL[j], 1);
+                    sumL[j] += __shfl_xor_sync(0xffffffffu, sumL[j], 2);
+                    sumL[j] += __shfl_xor_sync(0xffffffffu, sumL[j], 4);
+                }
             }
 #pragma unroll
             for (int j = 0; j < C::NWCH; ++j) {
@@ -502,9 +596,20 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // the column terms on to the peer)
             const int buf = it & 1;
             if (!mbar_wait(s, &s.sum_empty[buf], (uint32_t)((it >> 1) & 1) ^ 1, prm.err)) { ok = false; break; }
-            if (ch == 0) {
+            if constexpr (A8) {
+                if ((tt & 7) == 0) {
+#pragma unroll
+                    for (int j = 0; j < C::NACH; ++j) {
+                        const int r2 = 2 * ((tt >> 3) + 16 * j);
+                        atomicAdd(&s.rowsum[buf][r2], (int)sumA[j]);
+                        atomicAdd(&s.rowsum[buf][r2 + 1], (int)sumL[j]);
+                    }
+                }
+            } else if (ch == 0) {
 #pragma unroll
                 for (int j = 0; j < C::NACH; ++j) atomicAdd(&s.rowsum[buf][rq + 32 * j], (int)sumA[j]);
+            }
+            if (ch == 0) {
 #pragma unroll
                 for (int j = 0; j < C::NWCH; ++j) atomicAdd(&s.colsum[buf][rq + 32 * j], (int)sumW[j]);
             }
@@ -548,64 +653,48 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             if (!mbar_wait<PAIR, true>(s, &s.col_full[buf], par, prm.err)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            // operand rows of this CTA; output row m (A8: two operand rows per row)
             const int64_t m0 = (tile / n_tiles_n) * C::TILE_M + (int64_t)rank * BM, n0 = (tile % n_tiles_n) * BN;
             const int mr = 32 * q + lane;
-            const int64_t m = m0 + mr;
+            const int64_t m = A8 ? (m0 + mr) >> 1 : m0 + mr;
             const int rowt = -8 * s.rowsum[buf][mr];
             s.rowsum[buf][mr] = 0;
             const float sa = (YMODE != 2 && m < prm.M) ? prm.sa[m] : 0.f;
+            // A8: the u_l lane (odd) takes no column term; its partner adds 16 x its own
+            const bool odd = A8 && (lane & 1);
+            const int cmask = odd ? 0 : -1;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 const int col0 = 32 * c;
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + col0), r);
-                if (m < prm.M) {
+                if (A8 || m < prm.M) {
                     int acc[32];
                     const int4 *ct = reinterpret_cast<const int4 *>(&s.colterm[buf][col0]);
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
                         const int4 c4 = ct[j / 4];
-                        const int cv[4] = {c4.x, c4.y, c4.z, c4.w};
+                        const int cv[4] = {c4.x & cmask, c4.y & cmask, c4.z & cmask, c4.w & cmask};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int u = __float2int_rn(__uint_as_float(r[j + i]) * 262144.0f);   // exact: x 2^18
                             acc[j + i] = u + rowt + cv[i];
                         }
                     }
-                    const float4 *ws4 = reinterpret_cast<const float4 *>(&s.wscale[buf][col0]);
-                    const int64_t nb = n0 + col0;
-                    if (YMODE == 2) {
-                        int *yr = static_cast<int *>(prm.y) + m * prm.N + nb;
+                    if constexpr (A8) {
+                        // the even lane outputs columns col0 .. col0 + 15, the odd lane
+                        // the next 16: each sends the partner the half it outputs
+                        int out[16];
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            if (nb + j + 3 < prm.N)
-                                *reinterpret_cast<int4 *>(yr + j) = make_int4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                    } else if (YMODE == 1) {
-                        float *yr = static_cast<float *>(prm.y) + m * prm.N + nb;
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            if (nb + j + 3 >= prm.N) continue;
-                            const float4 w4 = ws4[j / 4];
-                            float4 o;
-                            o.x = ((float)acc[j] * sa) * w4.x;
-                            o.y = ((float)acc[j + 1] * sa) * w4.y;
-                            o.z = ((float)acc[j + 2] * sa) * w4.z;
-                            o.w = ((float)acc[j + 3] * sa) * w4.w;
-                            *reinterpret_cast<float4 *>(yr + j) = o;
+                        for (int j = 0; j < 16; ++j) {
+                            const int mine = odd ? acc[j + 16] : acc[j];
+                            const int recv = __shfl_xor_sync(0xffffffffu, odd ? acc[j] : acc[j + 16], 1);
+                            out[j] = odd ? 16 * recv + mine : 16 * mine + recv;
                         }
+                        const int cb = col0 + (odd ? 16 : 0);
+                        if (m < prm.M) store_outputs<YMODE, 16>(prm.y, prm.N, m, n0 + cb, out, &s.wscale[buf][cb], sa);
                     } else {
-                        __half *yr = static_cast<__half *>(prm.y) + m * prm.N + nb;
-#pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            if (nb + j + 7 >= prm.N) continue;
-                            __align__(16) __half h[8];
-                            const float4 wa = ws4[j / 4], wb = ws4[j / 4 + 1];
-                            const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-                            for (int e2 = 0; e2 < 8; ++e2)
-                                h[e2] = __float2half_rn(((float)acc[j + e2] * sa) * wv[e2]);
-                            *reinterpret_cast<uint4 *>(yr + j) = *reinterpret_cast<const uint4 *>(h);
-                        }
+                        store_outputs<YMODE, 32>(prm.y, prm.N, m, n0 + col0, acc, &s.wscale[buf][col0], sa);
                     }
                 }
             }
@@ -654,13 +743,13 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row_bytes, int box_rows,
+bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row_bytes, int box_bytes, int box_rows,
               CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    const cuuint32_t box[2] = {BK / 2, (cuuint32_t)box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -677,14 +766,17 @@ int sm_count() {
     return sms;
 }
 
-template <int YMODE, bool PAIR>
+// A8: a_q holds M rows of K int8 codes (TMA boxes of 64 rows x 128 bytes), and a
+// tile spans 128 activation rows.
+template <int YMODE, bool PAIR, bool A8 = false>
 cudaError_t launch_mode(const GemmArgs &g, const TcParams &p, cudaStream_t stream) {
     using C = Cfg<PAIR>;
     CUtensorMap ta, tw;
-    if (!make_map(&ta, g.a_q, g.M, g.K / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&tw, g.w_q, g.N, g.K / 2, C::WROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
+    const bool a_ok = A8 ? make_map(&ta, g.a_q, g.M, g.K, BK, BM / 2, CU_TENSOR_MAP_SWIZZLE_NONE)
+                         : make_map(&ta, g.a_q, g.M, g.K / 2, BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!a_ok || !make_map(&tw, g.w_q, g.N, g.K / 2, BK / 2, C::WROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    auto kern = w4a4_tc_kernel<YMODE, PAIR>;
+    auto kern = w4a4_tc_kernel<YMODE, PAIR, A8>;
     const size_t smem = sizeof(Smem<PAIR>) + 1024;
     static bool attr_set = false;
     if (!attr_set) {
@@ -694,7 +786,8 @@ cudaError_t launch_mode(const GemmArgs &g, const TcParams &p, cudaStream_t strea
     }
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorUnknown;
-    const int64_t tiles = ((p.N + BN - 1) / BN) * ((p.M + C::TILE_M - 1) / C::TILE_M);
+    const int64_t m_op = A8 ? 2 * p.M : p.M;
+    const int64_t tiles = ((p.N + BN - 1) / BN) * ((m_op + C::TILE_M - 1) / C::TILE_M);
     // persistent: one CTA per SM (one pair per two SMs)
     const int64_t units = tiles < sms / C::NCTA ? tiles : sms / C::NCTA;
     cudaLaunchConfig_t cfg = {};
@@ -727,6 +820,23 @@ cudaError_t launch_w4a4_gemm_tc(const GemmArgs &g, cudaStream_t stream) {
         case 3: return launch_mode<1, true>(g, p, stream);
         case 4: return launch_mode<2, false>(g, p, stream);
         default: return launch_mode<2, true>(g, p, stream);
+    }
+}
+
+bool w4a8_gemm_tc_supported(int64_t M, int64_t N, int64_t K, int y_mode) {
+    const int64_t elem = y_mode == 0 ? 2 : 4;
+    return M > 64 && K % BK == 0 && K <= 65536 && (N * elem) % 16 == 0;
+}
+
+cudaError_t launch_w4a8_gemm_tc(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,
+                                int64_t N, int64_t K, void *y, int y_mode, cudaStream_t stream) {
+    const GemmArgs g{reinterpret_cast<const uint8_t *>(aq), sa, wq, sw, M, N, K, y, y_mode};
+    TcParams p{sa, sw, y, M, N, K, error_word_device_ptr()};
+    if (!p.err) return cudaErrorUnknown;
+    switch (y_mode) {   // M > 64: at least 130 operand rows, so always CTA pairs
+        case 0: return launch_mode<0, true, true>(g, p, stream);
+        case 1: return launch_mode<1, true, true>(g, p, stream);
+        default: return launch_mode<2, true, true>(g, p, stream);
     }
 }
 

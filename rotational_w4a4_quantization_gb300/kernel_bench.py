@@ -8,6 +8,7 @@
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel unfused --workload decode
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel attn
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel w4a8 --workload decode
+    python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel w4a8 --workload prefill --group channel
 
 Runs `--warmup` untimed launches, then `--reps` launches each timed with CUDA events on the
 current stream (L2 flushed before each launch unless `--no-flush`; a GPU-side pause lets
@@ -20,7 +21,8 @@ region); both count the bytes of x, the packed weights and scales, and y.  `attn
 times one decode query per head over the KV workload's cache (written by the KV
 kernel, 8192 tokens x 32 heads x 128) and counts the cache, the query and the output.
 `w4a8` times the W4A8 product (INT8 activations, INT4 weights, one scale per group of
-128) of the workload's GEMM shape and counts 2MNK.
+128, or per output channel with `--group channel`) of the workload's GEMM shape and
+counts 2MNK.
 """
 from __future__ import annotations
 
@@ -45,6 +47,8 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--group", choices=["128", "channel"], default="128",
+                    help="w4a8: weight scales per group of 128 or per output channel")
     ap.add_argument("--n", type=int, default=0,
                     help="fwht: row length instead of the workload's (e.g. 14336 = 28 x 512), same rows and recipe")
     args = ap.parse_args(argv)
@@ -85,12 +89,13 @@ def main(argv=None):
         a8 = torch.randint(-128, 128, (M, K), dtype=torch.int8, generator=g8).to(dev)
         s8 = (torch.rand(M, generator=g8) + 0.05).to(dev)
         wq, _ = synth.random_codes(N, K, 1001 + w.data_seed)
-        sg = (torch.rand(N, K // 128, generator=g8) + 0.05).to(dev)
-        wq = wq.to(dev)
+        per_channel = args.group == "channel"
+        sg = (torch.rand(N, generator=g8) if per_channel else torch.rand(N, K // 128, generator=g8)) + 0.05
+        sg, wq = sg.to(dev), wq.to(dev)
         y = torch.empty(M, N, dtype=torch.float16, device=dev)
         fn = lambda: rq.w4a8_gemm(a8, s8, wq, sg, out=y)
         work, unit = 2 * M * N * K, "TOPS"
-        what = f"w4a8_gemm {M}x{K}x{N} per-group-128 fp16"
+        what = f"w4a8_gemm {M}x{K}x{N} {'per-channel' if per_channel else 'per-group-128'} fp16"
     elif args.kernel == "attn":
         kw = synth.KV
         k, v = synth.kv_pair(kw.kv_tokens, kw.kv_heads, kw.kv_head_dim, kw.data_seed,

@@ -133,3 +133,62 @@ def test_group_codes_large_fold():
     ref = oracle.fwht_quant_groups(wt.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, 128, want_ratio=True)
     compare_codes(to_np(q), ref["q"], ref["ratio"], K4)
     compare_scales(to_np(s), ref["scales"])
+
+
+# ---- per-channel products of more than 64 tokens: the tensor-core kernel ----
+
+@pytest.mark.parametrize("M", [65, 130, 257, 600])
+@pytest.mark.parametrize("N,K", [(256, 128), (520, 1024), (1024, 4096)])
+def test_product_tensor_cores(M, N, K):
+    """CTA-pair tiles of 128 rows x 256 channels; ragged M (65 -> one half-empty
+    tile, 600 -> 5 tiles) and ragged N (520 = 2 x 256 + 8)."""
+    qa, sa, qw, sw = _random_operands(M, N, K, K, 3000 + M + N + K)
+    acc, yref = oracle.w4a8_gemm(qa, sa, qw, sw.reshape(N, 1), M, N, K, K)
+    np.testing.assert_array_equal(_gpu(qa, sa, qw, sw, torch.int32).astype(np.int64), acc)
+    np.testing.assert_allclose(_gpu(qa, sa, qw, sw, torch.float32), yref, rtol=1e-5, atol=0)
+    compare_f16(_gpu(qa, sa, qw, sw, torch.float16), yref)
+
+
+def test_product_row_length_off_the_vector_width():
+    """N = 100 fp16 outputs (200-byte rows) with 200 tokens: the mma.sync kernel."""
+    M, N, K = 200, 100, 512
+    qa, sa, qw, sw = _random_operands(M, N, K, K, 3999)
+    acc, yref = oracle.w4a8_gemm(qa, sa, qw, sw.reshape(N, 1), M, N, K, K)
+    compare_f16(_gpu(qa, sa, qw, sw, torch.float16), yref)
+    np.testing.assert_array_equal(_gpu(qa, sa, qw, sw, torch.int32).astype(np.int64), acc)
+
+
+def test_extreme_codes_at_max_k():
+    """K = 65536 with constant rows and columns: every sum is K a w in closed
+    form, up to 2^26 in magnitude; a = 127 against w = 7 drives both 4-bit
+    accumulators to their largest value (225 K)."""
+    M, N, K = 130, 256, 65536
+    a_vals = np.array([-128, 127, -1, 0, 1, -7, 64, -65], dtype=np.int64)
+    w_vals = np.array([-8, 7, -1, 0, 3, -5], dtype=np.int64)
+    ar = a_vals[np.arange(M) % len(a_vals)]
+    wc = w_vals[np.arange(N) % len(w_vals)]
+    qa = np.repeat(ar.astype(np.int8)[:, None], K, axis=1)
+    nib = (wc & 15).astype(np.uint8)
+    qw = np.repeat((nib | (nib << 4))[:, None], K // 2, axis=1)
+    sa = np.ones(M, dtype=np.float32)
+    sw = np.ones(N, dtype=np.float32)
+    y = _gpu(qa, sa, qw, sw, torch.int32).astype(np.int64)
+    np.testing.assert_array_equal(y, K * ar[:, None] * wc[None, :])
+
+
+def test_prefill_shape_sampled_rows():
+    """2048 x 4096 -> 14336: INT8 codes of the prefill activations (from the
+    oracle) against random INT4 weights; int32 sums and fp16 outputs of 27 rows,
+    spread over every tile row and both CTAs of a pair, against the oracle."""
+    w = synth.WORKLOADS["prefill"]
+    M, K, N = w.rows, w.n, w.gemm_n
+    x = synth.activations(M, K, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor)
+    ref_a = oracle.fwht_quant8(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+    qw, sw = synth.random_codes(N, K, 4001)
+    qw, sw = qw.numpy(), sw.numpy()
+    y32 = _gpu(ref_a["q"], ref_a["scales"], qw, sw, torch.int32)
+    y16 = _gpu(ref_a["q"], ref_a["scales"], qw, sw, torch.float16)
+    rows = np.unique(np.concatenate([np.arange(0, M, 97), [63, 64, 127, 128, M - 1]]))
+    acc, yref = oracle.w4a8_gemm(ref_a["q"][rows], ref_a["scales"][rows], qw, sw.reshape(N, 1), len(rows), N, K, K)
+    np.testing.assert_array_equal(y32[rows].astype(np.int64), acc)
+    compare_f16(y16[rows], yref)
