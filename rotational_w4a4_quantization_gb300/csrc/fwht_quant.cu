@@ -390,7 +390,34 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
         }
 
         // ---------------- row absmax ----------------
-        float amax = pairs_absmax<NP>(v);
+        // Two-phase plans end with chunks chunk_of(t, s, phase 2).  From n = 1024
+        // on, slot bits 2, 3 are chunk bits C-2, C-1 and row-thread bits 0, 1 chunk
+        // bits 2, 3, so a group of 128 elements (16 chunks) is four slots of each
+        // of four threads, and a thread's outputs touch four groups (gmax[q], q =
+        // slot bits 2, 3).  For n = 256, 512 a thread holds 16 consecutive chunks:
+        // one group.
+        constexpr bool kGroups4 = PL::kTwoPhase && C >= 7;
+        const bool i8 = PL::kTwoPhase && (prm.flags & RQ_INT8_CODES) != 0;
+        const bool per_group = PL::kTwoPhase && (prm.flags & RQ_GROUP_SCALES) != 0;
+        float gmax[kGroups4 ? 4 : 1];
+        float amax;
+        if constexpr (kGroups4) {
+            static_assert(NP == 64, "16 slots of 4 pairs");
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                gmax[q4] = pairs_absmax<16>(*reinterpret_cast<const pair_t(*)[16]>(&v[16 * q4]));
+            amax = fmaxf(fmaxf(gmax[0], gmax[1]), fmaxf(gmax[2], gmax[3]));
+            if (per_group) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    gmax[q4] = fmaxf(gmax[q4], __shfl_xor_sync(full, gmax[q4], 1));
+                    gmax[q4] = fmaxf(gmax[q4], __shfl_xor_sync(full, gmax[q4], 2));
+                }
+            }
+        } else {
+            amax = pairs_absmax<NP>(v);
+            gmax[0] = amax;                                    // n = 256, 512: the thread's group
+        }
         if constexpr (P > 1) {
 #pragma unroll
             for (int k = 0; k < (PL::T < 5 ? PL::T : 5); ++k)
@@ -405,7 +432,13 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
         }
 
         // ---------------- quantize, pack, store ----------------
-        const float inv = amax > 0.f ? 7.0f / amax : 0.f;
+        // codes: INT4 per row (default), INT8 per row, or INT4 per group of 128
+        // (the last two for two-phase plans only; the host rejects the others)
+        const float qmax = i8 ? 127.0f : 7.0f;
+        const float inv = amax > 0.f ? qmax / amax : 0.f;
+        float ginv[kGroups4 ? 4 : 1];
+#pragma unroll
+        for (int q4 = 0; q4 < (kGroups4 ? 4 : 1); ++q4) ginv[q4] = per_group ? (gmax[q4] > 0.f ? 7.0f / gmax[q4] : 0.f) : inv;
         const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
         uint8_t *stg = ostage + (warp * 2 + obuf) * OSTG;
         if constexpr (!PL::kTwoPhase) {
@@ -414,7 +447,20 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
             __syncwarp();
         }
         if (active) {
-            if (t == 0) job.scales[row] = (amax / 7.0f) * inv_sqrt_n;
+            if (PL::kTwoPhase && per_group) {
+                if constexpr (kGroups4) {
+                    if ((t & 3) == 0) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            job.scales[row * (int64_t)(n / 128) + ((t >> 2) | ((q4 & 1) << (C - 6)) | ((q4 >> 1) << (C - 5)))] =
+                                (gmax[q4] / 7.0f) * inv_sqrt_n;
+                    }
+                } else {
+                    job.scales[row * (int64_t)(n / 128) + t] = (gmax[0] / 7.0f) * inv_sqrt_n;
+                }
+            } else if (t == 0) {
+                job.scales[row] = (amax / qmax) * inv_sqrt_n;
+            }
             uint8_t *qrow = PL::kTwoPhase ? job.q + row * (int64_t)(n / 2) : stg + (lane / P) * (n / 2);
             // output chunk of slot s: phase-2 map, or natural order for one row per thread
             auto out_chunk = [&](int s) { return PL::kTwoPhase ? chunk_of<C>(t, s, true) : (chunk_t<C>(t, false) | s); };
@@ -442,14 +488,43 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
                     yp[1] = make_ulonglong2(fma2(v[4 * s + 2], sc2, z2), fma2(v[4 * s + 3], sc2, z2));
                 }
             }
+            if (PL::kTwoPhase && i8) {
+                // one byte per code (the low byte of the biased float is the
+                // two's-complement code): chunks c0 .. c0 + 3 are 32 bytes
+                const pair_t inv2 = mk2(inv, inv);
+#pragma unroll
+                for (int s4 = 0; s4 < NSLOT; s4 += 4) {
+                    uint32_t words[8];
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int s = s4 + cc;
+                        uint32_t code[8];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const pair_t qq = fma2(v[4 * s + k], inv2, bias2);
+                            code[2 * k] = (uint32_t)qq;
+                            code[2 * k + 1] = (uint32_t)(qq >> 32);
+                        }
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            words[2 * cc + h] = __byte_perm(__byte_perm(code[4 * h], code[4 * h + 1], 0x0040u),
+                                                            __byte_perm(code[4 * h + 2], code[4 * h + 3], 0x0040u), 0x5410u);
+                    }
+                    uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)n + 8 * out_chunk(s4));
+                    qp[0] = make_uint4(words[0], words[1], words[2], words[3]);
+                    qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
+                }
+            } else {
 #pragma unroll
             for (int s4 = 0; s4 < NSLOT; s4 += 4) {
                 uint32_t words[4];
                 const int c0 = out_chunk(s4);
+                // the row's multiplier, or (groups) that of the group of slots s4 .. s4 + 3
+                const float ginv_s = ginv[kGroups4 ? (s4 >> 2) : 0];
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int s = s4 + cc;
-                    const float sinv = out_neg(s) ? -inv : inv;
+                    const float sinv = out_neg(s) ? -ginv_s : ginv_s;
                     const pair_t inv2 = mk2(sinv, sinv);
                     uint32_t code[8];
 #pragma unroll
@@ -462,6 +537,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
                 }
                 // chunks c0..c0+3 are consecutive (slot bits 0,1 = chunk bits 0,1)
                 *reinterpret_cast<uint4 *>(qrow + 4 * c0) = make_uint4(words[0], words[1], words[2], words[3]);
+            }
             }
         }
         if constexpr (!PL::kTwoPhase) {

@@ -1,6 +1,7 @@
 """GPU parity of the W4A8 path ([SQ] §The architecture, §End-to-end flow):
 INT8 activation codes and per-group INT4 weight codes from rq_fwht_quant
-(n = 4096), and rq_w4a8_gemm with per-channel or per-group weight scales.
+(n = 4096, and the other powers of two from 256 to 8192), and rq_w4a8_gemm
+with per-channel or per-group weight scales.
 
 Bars: codes identical to the oracle's except in the tie window (a difference of
 one allowed there), scales within 1e-5; the product on the oracle's codes:
@@ -56,6 +57,69 @@ def test_group_weight_codes(flags):
     assert s.shape == (37, K4 // 128)
     ref = oracle.fwht_quant_groups(wt.double().numpy(), synth.SIGN_SEED, flags, 128, want_ratio=True)
     compare_codes(to_np(q), ref["q"], ref["ratio"], K4)
+    compare_scales(to_np(s), ref["scales"])
+
+
+# ---- the two code modes at the other power-of-two row lengths ----
+
+SIZES = [256, 512, 1024, 2048, 8192]
+
+
+@pytest.mark.parametrize("n", SIZES)
+@pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
+def test_int8_codes_other_sizes(n, flags):
+    x = synth.activations(13, n, torch.bfloat16, 40 + n % 97, max(1, n // 1000), 100.0)
+    q, s = rq.fwht_quant(x.to(DEV), synth.SIGN_SEED, flags | rq.RQ_INT8_CODES)
+    assert q.dtype == torch.int8 and q.shape == (13, n)
+    ref = oracle.fwht_quant8(x.double().numpy(), synth.SIGN_SEED, flags, want_ratio=True)
+    _compare_int8(to_np(q), ref["q"], ref["ratio"])
+    compare_scales(to_np(s), ref["scales"])
+
+
+@pytest.mark.parametrize("n", SIZES)
+@pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
+def test_group_codes_other_sizes(n, flags):
+    """Groups of 128: one per thread for n = 256, 512; from n = 1024 on four
+    threads share a group and each thread touches four groups."""
+    wt = synth.weights_t(19, n, 7 + n % 13, 0.02)
+    q, s = rq.fwht_quant(wt.to(DEV), synth.SIGN_SEED, flags | rq.RQ_GROUP_SCALES)
+    assert s.shape == (19, n // 128)
+    ref = oracle.fwht_quant_groups(wt.double().numpy(), synth.SIGN_SEED, flags, 128, want_ratio=True)
+    compare_codes(to_np(q), ref["q"], ref["ratio"], n)
+    compare_scales(to_np(s), ref["scales"])
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.float16])
+@pytest.mark.parametrize("mode", ["int8", "group"])
+def test_code_modes_input_dtypes(dt, mode):
+    n = 1024
+    x = synth.activations(9, n, dt, 77, 2, 100.0)
+    if mode == "int8":
+        q, s = rq.fwht_quant(x.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST | rq.RQ_INT8_CODES)
+        ref = oracle.fwht_quant8(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, want_ratio=True)
+        _compare_int8(to_np(q), ref["q"], ref["ratio"])
+    else:
+        q, s = rq.fwht_quant(x.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST | rq.RQ_GROUP_SCALES)
+        ref = oracle.fwht_quant_groups(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, 128, want_ratio=True)
+        compare_codes(to_np(q), ref["q"], ref["ratio"], n)
+    compare_scales(to_np(s), ref["scales"])
+
+
+def test_int8_codes_large_batch_8192():
+    """1000 rows of 8192 (two warps per row, CTAs looping over row groups)."""
+    x = synth.activations(1000, 8192, torch.bfloat16, 5, 8, 100.0)
+    q, s = rq.fwht_quant(x.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST | rq.RQ_INT8_CODES)
+    ref = oracle.fwht_quant8(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, want_ratio=True)
+    _compare_int8(to_np(q), ref["q"], ref["ratio"])
+    compare_scales(to_np(s), ref["scales"])
+
+
+def test_group_codes_large_fold_8192():
+    """700 weight rows of 8192 (fp32): the per-group fold of a W4A8 layer with K = 8192."""
+    wt = synth.weights_t(700, 8192, 11, 0.02)
+    q, s = rq.fwht_quant(wt.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST | rq.RQ_GROUP_SCALES)
+    ref = oracle.fwht_quant_groups(wt.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, 128, want_ratio=True)
+    compare_codes(to_np(q), ref["q"], ref["ratio"], 8192)
     compare_scales(to_np(s), ref["scales"])
 
 
