@@ -89,7 +89,7 @@ typedef enum {
 enum { RQ_SIGNS_FIRST = 1u };
 /* rq_attn_decode: leave the output in the rotated basis (o~ instead of o~ R^T). */
 enum { RQ_ATTN_ROTATED_OUT = 2u };
-/* rq_fwht_quant (n a power of two, 256..8192): INT8 codes per row (activations of the W4A8 layer),
+/* rq_fwht_quant (n = m 2^k, or a power of two from 256 to 8192): INT8 codes per row (activations of the W4A8 layer),
  * or INT4 codes with one scale per group of 128 elements (weights of the W4A8
  * layer with per-group scales). */
 enum { RQ_INT8_CODES = 4u, RQ_GROUP_SCALES = 8u };
@@ -127,8 +127,8 @@ enum { RQ_INT8_CODES = 4u, RQ_GROUP_SCALES = 8u };
  *            y = x diag(s) (H_m (x) H_{2^k}) / sqrt(n) (or diag(s) after).
  *   ld_x     row stride in elements, >= n, ld_x * sizeof(x_dtype) % 16 == 0.
  *   seed     sign-vector seed.
- *   flags    RQ_SIGNS_FIRST or 0, plus at most one of (n a power of two,
- *            256 <= n <= 8192; RQ_ERR_UNSUPPORTED otherwise):
+ *   flags    RQ_SIGNS_FIRST or 0, plus at most one of (n = m 2^k, or a
+ *            power of two from 256 to 8192; RQ_ERR_UNSUPPORTED for n <= 128):
  *            RQ_INT8_CODES: per-row INT8 codes for the W4A8 layer's
  *              activations ([SQ] §End-to-end flow): q is [rows][n] int8,
  *              scale = max|y| / 127, q = clamp(round_half_even(y / scale),

@@ -75,9 +75,9 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
     if (ld_x < n) return RQ_ERR_INVALID_ARG;
     if (flags & ~uint32_t(RQ_SIGNS_FIRST | RQ_INT8_CODES | RQ_GROUP_SCALES)) return RQ_ERR_INVALID_ARG;
     if ((flags & RQ_INT8_CODES) && (flags & RQ_GROUP_SCALES)) return RQ_ERR_INVALID_ARG;
-    // INT8 and per-group codes: powers of two from 256 on (the plans whose threads
-    // end with whole 32-element runs of a row)
-    if ((flags & (RQ_INT8_CODES | RQ_GROUP_SCALES)) && (kron || n < 256)) return RQ_ERR_UNSUPPORTED;
+    // INT8 and per-group codes: n = m 2^k, and powers of two from 256 on (the plans
+    // whose threads end with whole 32-element runs of a row)
+    if ((flags & (RQ_INT8_CODES | RQ_GROUP_SCALES)) && !kron && n < 256) return RQ_ERR_UNSUPPORTED;
     if (rows == 0) return RQ_OK;
     if (!x || !q || !scales) return RQ_ERR_INVALID_ARG;
     if (!rq::aligned16(x) || !rq::aligned16(q) || !rq::aligned16(scales) || (y && !rq::aligned16(y)))

@@ -28,14 +28,21 @@
 //    tracks the row's absmax;
 //  * a block reduction gives the scale; the same threads quantize (one f32x2 FMA
 //    against a 1.5 * 2^23 bias per pair, round half to even, as the power-of-two
-//    kernels) and store one byte per column pair and segment.
+//    kernels) and store one byte per column pair and segment;
+//  * code modes as in the power-of-two kernels: INT8 codes per row (two bytes
+//    per column pair and segment), or INT4 with one scale per group of 128
+//    consecutive elements (n is a multiple of 128: a warp per group reads the
+//    finished row buffer, and the quantizer takes its group's multiplier).
 // Bound: issue (per element ~20 instructions for the shuffled stages and m/2
 // FMAs for H_m), not HBM.
+#include "rq.h"
 #include "rq_internal.h"
 #include "rot_device.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 namespace rq {
 namespace {
@@ -120,8 +127,11 @@ __global__ void __launch_bounds__(kKThreads, 2) fwht_kron_kernel(const __grid_co
     float *row = reinterpret_cast<float *>(kraw);                       // N floats
     uint32_t *sgn = reinterpret_cast<uint32_t *>(row + N);               // N / 2 sign words
     float *red = reinterpret_cast<float *>(sgn + N / 2);                 // kKWarps
+    float *ginv = red + kKWarps;                                          // N / 128 (per-group codes)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool signs_first = (p.flags & 1u) != 0;
+    const bool i8 = (p.flags & RQ_INT8_CODES) != 0, per_group = (p.flags & RQ_GROUP_SCALES) != 0;
+    static_assert(N % 128 == 0, "m is a multiple of 4 and 2^k >= 32");
     const uint32_t msel = signs_first ? 0xffffffffu : 0u;
 
     // sign word j: bit 15 / bit 31 set when element 2j / 2j + 1 takes -1 (top bit of
@@ -269,24 +279,56 @@ __global__ void __launch_bounds__(kKThreads, 2) fwht_kron_kernel(const __grid_co
 #pragma unroll
         for (int w = 1; w < kKWarps; ++w) amax = fmaxf(amax, red[w]);
 
-        // ---- quantize, pack, store (the same column pairs) ----
-        const float inv = amax > 0.f ? 7.0f / amax : 0.f;
-        const pair_t inv2 = mk2(inv, inv), bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
-        if (threadIdx.x == 0) p.scales[r] = (amax / 7.0f) * p.inv_sqrt_n;
-        uint8_t *qrow = p.q + r * (int64_t)(N / 2);
-        float *yrow = p.y ? p.y + r * (int64_t)N : nullptr;
-        for (int j = 2 * threadIdx.x; j < B; j += 2 * kKThreads) {
+        // per-group codes: the max of each 128 consecutive elements of the rotated
+        // row (complete in the row buffer after the barrier above), a warp per group
+        if (per_group) {
+            for (int g = warp; g < N / 128; g += kKWarps) {
+                const float4 v4 = reinterpret_cast<const float4 *>(row + g * 128)[lane];
+                float gm = fmaxf(fmaxf(fabsf(v4.x), fabsf(v4.y)), fmaxf(fabsf(v4.z), fabsf(v4.w)));
 #pragma unroll
-            for (int a2 = 0; a2 < M; ++a2) {
-                const pair_t v2 = *reinterpret_cast<const pair_t *>(row + a2 * B + j);
-                const pair_t qq = fma2(v2, inv2, bias2);
-                const uint32_t c0 = (uint32_t)qq & 0xfu, c1 = (uint32_t)(qq >> 32) & 0xfu;
-                qrow[(a2 * B + j) / 2] = (uint8_t)(c0 | (c1 << 4));
-                if (yrow)
-                    *reinterpret_cast<pair_t *>(yrow + a2 * B + j) =
-                        fma2(v2, mk2(p.inv_sqrt_n, p.inv_sqrt_n), 0ull);
+                for (int k = 0; k < 5; ++k) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1 << k));
+                if (lane == 0) {
+                    ginv[g] = gm > 0.f ? 7.0f / gm : 0.f;
+                    p.scales[r * (int64_t)(N / 128) + g] = (gm / 7.0f) * p.inv_sqrt_n;
+                }
             }
+            __syncthreads();
         }
+
+        // ---- quantize, pack, store (the same column pairs) ----
+        // INT4 per row (default), INT8 per row, or INT4 per group of 128
+        const float qmax = i8 ? 127.0f : 7.0f;
+        const float inv = amax > 0.f ? qmax / amax : 0.f;
+        const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
+        if (!per_group && threadIdx.x == 0) p.scales[r] = (amax / qmax) * p.inv_sqrt_n;
+        uint8_t *qrow = p.q + r * (int64_t)(i8 ? N : N / 2);
+        float *yrow = p.y ? p.y + r * (int64_t)N : nullptr;
+        // one loop per code mode, so the default path carries no per-pair mode tests
+        auto quantize = [&](auto i8_tag, auto grp_tag) {
+            constexpr bool I8 = decltype(i8_tag)::value, GRP = decltype(grp_tag)::value;
+            for (int j = 2 * threadIdx.x; j < B; j += 2 * kKThreads) {
+#pragma unroll
+                for (int a2 = 0; a2 < M; ++a2) {
+                    const int e = a2 * B + j;                       // e, e + 1: one group (e even)
+                    const pair_t v2 = *reinterpret_cast<const pair_t *>(row + e);
+                    const float ie = GRP ? ginv[e >> 7] : inv;
+                    const pair_t qq = fma2(v2, mk2(ie, ie), bias2);
+                    if constexpr (I8) {
+                        // the low byte of the biased float is the two's-complement code
+                        const uint32_t c0 = (uint32_t)qq & 0xffu, c1 = (uint32_t)(qq >> 32) & 0xffu;
+                        *reinterpret_cast<uint16_t *>(qrow + e) = (uint16_t)(c0 | (c1 << 8));
+                    } else {
+                        const uint32_t c0 = (uint32_t)qq & 0xfu, c1 = (uint32_t)(qq >> 32) & 0xfu;
+                        qrow[e / 2] = (uint8_t)(c0 | (c1 << 4));
+                    }
+                    if (yrow)
+                        *reinterpret_cast<pair_t *>(yrow + e) = fma2(v2, mk2(p.inv_sqrt_n, p.inv_sqrt_n), 0ull);
+                }
+            }
+        };
+        if (i8) quantize(std::true_type{}, std::false_type{});
+        else if (per_group) quantize(std::false_type{}, std::true_type{});
+        else quantize(std::false_type{}, std::false_type{});
         __syncthreads();   // the row buffer is rewritten by the next row
     }
 }
@@ -295,7 +337,7 @@ template <int IN, int M, int LOGB>
 cudaError_t launch_kron_t(const KronParams &p, cudaStream_t stream) {
     constexpr int N = M << LOGB;
     auto kern = fwht_kron_kernel<IN, M, LOGB>;
-    const size_t smem = (size_t)N * 4 + (size_t)(N / 2) * 4 + kKWarps * 4;
+    const size_t smem = (size_t)N * 4 + (size_t)(N / 2) * 4 + kKWarps * 4 + (size_t)(N / 128) * 4;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, per_sm = 0;

@@ -6,7 +6,9 @@ largest magnitude, scales within 1e-5, codes identical outside the tie window.
 Cases: every block size with the smallest and largest power-of-two factor, the
 FFN widths 14336 = 28 x 512 and 28672 = 28 x 1024, three input dtypes, both
 sign sides, strided rows, degenerate rows, a prefill-sized batch of 14336-wide
-activations, and the fold of 14336-wide weight rows.
+activations, the fold of 14336-wide weight rows, and the two code modes of the
+W4A8 layer (INT8 per row; INT4 per group of 128, groups spanning several
+segments or lying inside one).
 """
 import numpy as np
 import pytest
@@ -89,3 +91,54 @@ def test_weight_fold_of_width_14336():
     K = 14336
     wt = synth.weights_t(64, K, 105, 0.02)
     _run_and_compare(wt, synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+
+
+def _compare_int8(gpu_q, ref_q, ratio):
+    g, r = gpu_q.astype(np.int16), ref_q.astype(np.int16)
+    bad = (g != r) & ~(oracle.tie_mask(ratio) & (np.abs(g - r) == 1))
+    assert not bad.any(), f"{int(bad.sum())} INT8 codes differ outside the tie window"
+
+
+@pytest.mark.parametrize("m", [12, 20, 28])
+@pytest.mark.parametrize("b", [32, 1024])
+@pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
+def test_int8_codes(m, b, flags):
+    """INT8 codes per row (the W4A8 activations) at n = m 2^k."""
+    n = m * b
+    x = synth.activations(6, n, torch.bfloat16, 3 * m + b, max(1, n // 1000), 100.0)
+    q, s = rq.fwht_quant(x.to(DEV), synth.SIGN_SEED, flags | rq.RQ_INT8_CODES)
+    assert q.dtype == torch.int8 and q.shape == (6, n)
+    ref = oracle.fwht_quant8(x.double().numpy(), synth.SIGN_SEED, flags, want_ratio=True)
+    _compare_int8(to_np(q), ref["q"], ref["ratio"])
+    compare_scales(to_np(s), ref["scales"])
+
+
+@pytest.mark.parametrize("m", [12, 20, 28])
+@pytest.mark.parametrize("b", [32, 64, 512])
+@pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
+def test_group_codes(m, b, flags):
+    """INT4 with one scale per 128 elements: groups span 4 (b = 32) or 2 (b = 64)
+    segments, or lie inside one (b = 512)."""
+    n = m * b
+    wt = synth.weights_t(5, n, m + b, 0.02)
+    q, s = rq.fwht_quant(wt.to(DEV), synth.SIGN_SEED, flags | rq.RQ_GROUP_SCALES)
+    assert s.shape == (5, n // 128)
+    ref = oracle.fwht_quant_groups(wt.double().numpy(), synth.SIGN_SEED, flags, 128, want_ratio=True)
+    compare_codes(to_np(q), ref["q"], ref["ratio"], n)
+    compare_scales(to_np(s), ref["scales"])
+
+
+def test_w4a8_codes_of_width_14336():
+    """The W4A8 down projection's inputs: 600 INT8 activation rows and 300
+    per-group weight rows of width 14336 (fp16 activations, fp32 weights)."""
+    n = 14336
+    x = synth.activations(600, n, torch.float16, 8, synth._n_outliers(n), 100.0)
+    q, s = rq.fwht_quant(x.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST | rq.RQ_INT8_CODES)
+    ref = oracle.fwht_quant8(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, want_ratio=True)
+    _compare_int8(to_np(q), ref["q"], ref["ratio"])
+    compare_scales(to_np(s), ref["scales"])
+    wt = synth.weights_t(300, n, 12, 0.02)
+    q, s = rq.fwht_quant(wt.to(DEV), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST | rq.RQ_GROUP_SCALES)
+    ref = oracle.fwht_quant_groups(wt.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, 128, want_ratio=True)
+    compare_codes(to_np(q), ref["q"], ref["ratio"], n)
+    compare_scales(to_np(s), ref["scales"])
