@@ -51,8 +51,9 @@
 //             and stores that takes several MMA periods).  A team widens all of
 //             its block's A and W chunks.  Each team keeps partial per-row code
 //             sums and hands them, and the weight scales, to the epilogue through
-//             shared memory;
-//   warps 14-17 epilogue (one per TMEM lane quarter): tcgen05.ld of the fp32
+//             shared memory.  CTA pairs whose packed operands fit in L2 run four
+//             teams (warps 2-17, four MMA periods per block; 4 + 4 stages);
+//   last 4 warps epilogue (one per TMEM lane quarter): tcgen05.ld of the fp32
 //             accumulator, offset removal, scales (broadcast from shared memory),
 //             16-byte stores.
 // The order of k inside each 8-code group is permuted the same way for A and W
@@ -85,16 +86,18 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;      // per-CTA A rows, tile columns, K block (codes)
 constexpr int kTeamWarps = 4;                     // one per TMEM lane quarter
-constexpr int kTeams = 3;                         // team t converts the K blocks g with g % 3 == t
-constexpr int kConvWarps = kTeams * kTeamWarps;
 constexpr int kTeamThreads = 32 * kTeamWarps;
 constexpr int kEpiWarps = 4;                      // one per TMEM lane quarter
-constexpr int kThreadsTC = 32 * (2 + kConvWarps + kEpiWarps);
+// producer and MMA warps, `teams` converter teams, epilogue warps
+constexpr int threads_tc(int teams) { return 32 * (2 + teams * kTeamWarps + kEpiWarps); }
 constexpr uint32_t kTmemCols = 2 * BN;            // two 128 x 256 fp32 accumulators
 constexpr long long kWaitLimitCycles = 4000000000ll;    // ~2 s at 2 GHz
 
-template <bool PAIR>
+// TEAMS converter teams: team t converts the K blocks g with g % TEAMS == t.
+template <bool PAIR, int TEAMS = 3>
 struct Cfg {
+    static_assert(TEAMS == 3 || (TEAMS == 4 && PAIR), "four teams only fit the shared memory of CTA pairs");
+    static constexpr int kTeams = TEAMS, kConvWarps = TEAMS * kTeamWarps, kThreads = threads_tc(TEAMS);
     static constexpr int NCTA = PAIR ? 2 : 1;
     static constexpr int WROWS = BN / NCTA;         // W rows (output channels) per CTA
     static constexpr int TILE_M = BM * NCTA;        // output rows per tile
@@ -104,8 +107,9 @@ struct Cfg {
     // for is its own finished block), and MMA commits complete in order, so an
     // operand-ring wait is safe with OP_STAGES >= kTeams.
     // The packed ring is the deeper one: it covers the TMA latency from L2/HBM
-    // (6 + 3 stages ran the prefill GEMM ~7% faster than 3 + 5).
-    static constexpr int PK_STAGES = PAIR ? 2 * kTeams : kTeams, OP_STAGES = 3;
+    // (6 + 3 stages ran the prefill GEMM ~7% faster than 3 + 5).  Four teams need
+    // four operand stages, which leaves room for only four packed ones.
+    static constexpr int PK_STAGES = TEAMS == 4 ? 4 : (PAIR ? 2 * kTeams : kTeams), OP_STAGES = TEAMS;
     static constexpr int PK_A = BM * BK / 2, PK_W = WROWS * BK / 2;   // packed bytes per stage
     static constexpr int OP_A = BM * BK, OP_W = WROWS * BK;           // e4m3 bytes per stage
     static constexpr int NACH = BM * (BK / 32) / kTeamThreads;       // A chunks per thread and K block
@@ -114,9 +118,10 @@ struct Cfg {
     static_assert(PK_STAGES % kTeams == 0 && OP_STAGES >= kTeams, "parity waits stay one phase ahead at most");
 };
 
-template <bool PAIR>
+template <bool PAIR, int TEAMS = 3>
 struct Smem {
-    using C = Cfg<PAIR>;
+    using C = Cfg<PAIR, TEAMS>;
+    static constexpr bool kPair = PAIR;
     alignas(1024) uint8_t opA[C::OP_STAGES][C::OP_A];
     alignas(1024) uint8_t opW[C::OP_STAGES][C::OP_W];
     alignas(128) uint8_t pkA[C::PK_STAGES][C::PK_A];
@@ -215,8 +220,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *b, uint32_t parity) {
 // off with __nanosleep between polls: for the roles with slack (the producer,
 // the epilogue), whose polling would otherwise take issue and shared-memory pipe
 // slots from the converter warps of the same SM sub-partition.
-template <bool CLUSTER = false, bool SLEEP = false, bool PAIR>
-__device__ __forceinline__ bool mbar_wait(Smem<PAIR> &s, uint64_t *b, uint32_t parity, int *err) {
+template <bool CLUSTER = false, bool SLEEP = false, class S>
+__device__ __forceinline__ bool mbar_wait(S &s, uint64_t *b, uint32_t parity, int *err) {
     if (mbar_try_wait<CLUSTER>(b, parity)) return true;
     const long long t0 = clock64();
     while (true) {
@@ -233,9 +238,9 @@ __device__ __forceinline__ bool mbar_wait(Smem<PAIR> &s, uint64_t *b, uint32_t p
 
 // Warp-wide wait on a barrier that the pair's multicast MMA commit releases: one
 // cluster-scope acquire per warp, and __syncwarp orders the other lanes after it.
-template <bool PAIR>
-__device__ __forceinline__ bool warp_wait_commit(Smem<PAIR> &s, uint64_t *b, uint32_t parity, int lane, int *err) {
-    if constexpr (PAIR) {
+template <class S>
+__device__ __forceinline__ bool warp_wait_commit(S &s, uint64_t *b, uint32_t parity, int lane, int *err) {
+    if constexpr (S::kPair) {
         int got = 1;
         if (lane == 0) got = mbar_wait<true>(s, b, parity, err);
         __syncwarp();
@@ -378,12 +383,13 @@ __device__ __forceinline__ void store_outputs(void *y, int64_t N, int64_t m, int
     }
 }
 
-template <int YMODE, bool PAIR, bool A8>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+template <int YMODE, bool PAIR, bool A8, int TEAMS>
+__global__ void __launch_bounds__(threads_tc(TEAMS), 1)
 w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                const __grid_constant__ TcParams prm) {
-    using C = Cfg<PAIR>;
-    using S = Smem<PAIR>;
+    using C = Cfg<PAIR, TEAMS>;
+    using S = Smem<PAIR, TEAMS>;
+    constexpr int kTeams = C::kTeams, kConvWarps = C::kConvWarps;
     static_assert(!A8 || PAIR, "the W4A8 variant runs on CTA pairs");
     extern __shared__ uint8_t smem_raw[];
     // align by offsetting the shared array itself, so the compiler keeps the
@@ -768,16 +774,16 @@ int sm_count() {
 
 // A8: a_q holds M rows of K int8 codes (TMA boxes of 64 rows x 128 bytes), and a
 // tile spans 128 activation rows.
-template <int YMODE, bool PAIR, bool A8 = false>
+template <int YMODE, bool PAIR, bool A8 = false, int TEAMS = 3>
 cudaError_t launch_mode(const GemmArgs &g, const TcParams &p, cudaStream_t stream) {
-    using C = Cfg<PAIR>;
+    using C = Cfg<PAIR, TEAMS>;
     CUtensorMap ta, tw;
     const bool a_ok = A8 ? make_map(&ta, g.a_q, g.M, g.K, BK, BM / 2, CU_TENSOR_MAP_SWIZZLE_NONE)
                          : make_map(&ta, g.a_q, g.M, g.K / 2, BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!a_ok || !make_map(&tw, g.w_q, g.N, g.K / 2, BK / 2, C::WROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    auto kern = w4a4_tc_kernel<YMODE, PAIR, A8>;
-    const size_t smem = sizeof(Smem<PAIR>) + 1024;
+    auto kern = w4a4_tc_kernel<YMODE, PAIR, A8, TEAMS>;
+    const size_t smem = sizeof(Smem<PAIR, TEAMS>) + 1024;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -792,7 +798,7 @@ cudaError_t launch_mode(const GemmArgs &g, const TcParams &p, cudaStream_t strea
     const int64_t units = tiles < sms / C::NCTA ? tiles : sms / C::NCTA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(units * C::NCTA));
-    cfg.blockDim = dim3(kThreadsTC);
+    cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -805,6 +811,15 @@ cudaError_t launch_mode(const GemmArgs &g, const TcParams &p, cudaStream_t strea
     return cudaLaunchKernelEx(&cfg, kern, ta, tw, p);
 }
 
+// Converter teams for CTA pairs.  Four teams give each warp four MMA periods per
+// K block but leave room for only four packed stages; that ring depth covers the
+// TMA latency while the operands stay in L2.  Measured: 2048 x 4096 -> 14336
+// (34 MB of packed operands) 110.6 -> 106.5 us with four teams, 4096 x 8192 ->
+// 28672 (134 MB) 745 -> 830 us.  The threshold lies between the two.
+constexpr int64_t kFourTeamsMaxOperandBytes = 64ll << 20;
+
+bool four_teams(int64_t a_bytes, int64_t w_bytes) { return a_bytes + w_bytes <= kFourTeamsMaxOperandBytes; }
+
 }  // namespace
 
 bool w4a4_gemm_tc_supported(const GemmArgs &g) { return g.M > 64 && g.K % BK == 0 && g.K <= 65536; }
@@ -813,13 +828,17 @@ cudaError_t launch_w4a4_gemm_tc(const GemmArgs &g, cudaStream_t stream) {
     TcParams p{g.a_scales, g.w_scales, g.y, g.M, g.N, g.K, error_word_device_ptr()};
     if (!p.err) return cudaErrorUnknown;
     const bool pair = g.M > BM;   // tiles of 256 rows on SM pairs; one SM for M <= 128
-    switch (g.y_mode * 2 + (pair ? 1 : 0)) {
+    const bool t4 = pair && four_teams(g.M * g.K / 2, g.N * g.K / 2);
+    switch (g.y_mode * 3 + (pair ? (t4 ? 2 : 1) : 0)) {
         case 0: return launch_mode<0, false>(g, p, stream);
         case 1: return launch_mode<0, true>(g, p, stream);
-        case 2: return launch_mode<1, false>(g, p, stream);
-        case 3: return launch_mode<1, true>(g, p, stream);
-        case 4: return launch_mode<2, false>(g, p, stream);
-        default: return launch_mode<2, true>(g, p, stream);
+        case 2: return launch_mode<0, true, false, 4>(g, p, stream);
+        case 3: return launch_mode<1, false>(g, p, stream);
+        case 4: return launch_mode<1, true>(g, p, stream);
+        case 5: return launch_mode<1, true, false, 4>(g, p, stream);
+        case 6: return launch_mode<2, false>(g, p, stream);
+        case 7: return launch_mode<2, true>(g, p, stream);
+        default: return launch_mode<2, true, false, 4>(g, p, stream);
     }
 }
 
@@ -833,10 +852,15 @@ cudaError_t launch_w4a8_gemm_tc(const int8_t *aq, const float *sa, const uint8_t
     const GemmArgs g{reinterpret_cast<const uint8_t *>(aq), sa, wq, sw, M, N, K, y, y_mode};
     TcParams p{sa, sw, y, M, N, K, error_word_device_ptr()};
     if (!p.err) return cudaErrorUnknown;
-    switch (y_mode) {   // M > 64: at least 130 operand rows, so always CTA pairs
+    // M > 64: at least 130 operand rows, so always CTA pairs
+    const bool t4 = four_teams(M * K, N * K / 2);
+    switch (y_mode * 2 + (t4 ? 1 : 0)) {
         case 0: return launch_mode<0, true, true>(g, p, stream);
-        case 1: return launch_mode<1, true, true>(g, p, stream);
-        default: return launch_mode<2, true, true>(g, p, stream);
+        case 1: return launch_mode<0, true, true, 4>(g, p, stream);
+        case 2: return launch_mode<1, true, true>(g, p, stream);
+        case 3: return launch_mode<1, true, true, 4>(g, p, stream);
+        case 4: return launch_mode<2, true, true>(g, p, stream);
+        default: return launch_mode<2, true, true, 4>(g, p, stream);
     }
 }
 

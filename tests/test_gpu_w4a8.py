@@ -256,3 +256,16 @@ def test_prefill_shape_sampled_rows():
     acc, yref = oracle.w4a8_gemm(ref_a["q"][rows], ref_a["scales"][rows], qw, sw.reshape(N, 1), len(rows), N, K, K)
     np.testing.assert_array_equal(y32[rows].astype(np.int64), acc)
     compare_f16(y16[rows], yref)
+
+
+def test_product_operands_beyond_l2_sampled_rows():
+    """4160 x 8192 -> 8192: 66 MB of operands, past the size up to which the
+    tensor-core kernel runs four converter teams, so this case takes the
+    three-team configuration.  int32 sums of 30 rows (every tile row and both
+    CTAs of a pair) against the oracle."""
+    M, N, K = 4160, 8192, 8192
+    qa, sa, qw, sw = _random_operands(M, N, K, K, 4242)
+    y32 = _gpu(qa, sa, qw, sw, torch.int32)
+    rows = np.unique(np.concatenate([np.arange(0, M, 173), [127, 128, 255, 256, M - 1]]))
+    acc, _ = oracle.w4a8_gemm(qa[rows], sa[rows], qw, sw.reshape(N, 1), len(rows), N, K, K)
+    np.testing.assert_array_equal(y32[rows].astype(np.int64), acc)
