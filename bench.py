@@ -51,7 +51,7 @@ SLEEP_CYCLES = 400_000       # ~0.2 ms GPU-side pause between timed steps
 # DRAM bytes (read + write) per launch from one ncu capture of the current kernel
 # on the prefill shapes (see the summaries in profiles/); None once a kernel changes.
 NCU_TRAFFIC = {
-    "w4a4_gemm": None,
+    "w4a4_gemm": 33_695_744 + 6_113_024,
     "fwht_quant": None,
     "kv_rotate_quant": None,
 }
