@@ -305,6 +305,20 @@ rq_status rq_w4a8_gemm(const int8_t *a_q, const float *a_scales, const uint8_t *
  */
 rq_status rq_sync_status(void *stream);
 
+/*
+ * rq_selftest_wait_timeout -- exercise the failure-detection path on the device.
+ *
+ *   Launches one thread that waits, through the same bounded mbarrier wait the
+ *   rotation kernels use for their bulk copies, on a barrier that nothing
+ *   arrives on.  After `limit_cycles` SM clock cycles the wait gives up, raises
+ *   the device error word and the kernel returns; no memory is touched and the
+ *   context stays usable.  The next rq_sync_status(stream) returns
+ *   RQ_ERR_TIMEOUT (and clears the word).
+ *   limit_cycles  1000 .. 4e9 (the production kernels use ~4e9, about 2 s).
+ *   Errors: RQ_ERR_INVALID_ARG (limit out of range), RQ_ERR_CUDA (launch).
+ */
+rq_status rq_selftest_wait_timeout(int64_t limit_cycles, void *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *rq_status_string(rq_status status);
 

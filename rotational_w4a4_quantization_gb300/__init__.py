@@ -32,11 +32,13 @@ from ._binding import (  # noqa: F401
     kv_rotate_quant,
     library_path,
     load_library,
+    selftest_wait_timeout,
     sync_status,
     w4a4_gemm,
     w4a8_gemm,
 )
 
 __all__ = ["RQ_ATTN_ROTATED_OUT", "RQ_GROUP_SCALES", "RQ_INT8_CODES", "RQ_SIGNS_FIRST", "RQError", "attn_decode",
-           "fwht_quant", "fwht_quant_gemm", "kv_rotate_quant", "library_path", "load_library", "sync_status",
+           "fwht_quant", "fwht_quant_gemm", "kv_rotate_quant", "library_path", "load_library", "selftest_wait_timeout",
+           "sync_status",
            "w4a4_gemm", "w4a8_gemm"]

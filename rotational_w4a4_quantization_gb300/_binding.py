@@ -62,6 +62,8 @@ def load_library() -> ctypes.CDLL:
     lib.rq_attn_decode.argtypes = [P, i32, i64, i64, i64, P, P, P, P, i64, u64, u32, ctypes.c_float, P, P]
     lib.rq_sync_status.restype = i32
     lib.rq_sync_status.argtypes = [P]
+    lib.rq_selftest_wait_timeout.restype = i32
+    lib.rq_selftest_wait_timeout.argtypes = [i64, P]
     lib.rq_status_string.restype = ctypes.c_char_p
     lib.rq_status_string.argtypes = [i32]
     lib.rq_version.restype = u32
@@ -259,3 +261,9 @@ def w4a8_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_d
 def sync_status(stream=None) -> int:
     """Drain the stream and return the library's status word (0 = OK)."""
     return int(load_library().rq_sync_status(_stream(stream)))
+
+
+def selftest_wait_timeout(limit_cycles: int, stream=None) -> None:
+    """Launch the failure-detection self-test: a bounded device wait on a barrier
+    that nothing arrives on.  The next :func:`sync_status` returns RQ_ERR_TIMEOUT."""
+    _check("rq_selftest_wait_timeout", load_library().rq_selftest_wait_timeout(int(limit_cycles), _stream(stream)))

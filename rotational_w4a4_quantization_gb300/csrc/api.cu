@@ -195,6 +195,12 @@ rq_status rq_w4a8_gemm(const int8_t *a_q, const float *a_scales, const uint8_t *
     return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }
 
+rq_status rq_selftest_wait_timeout(int64_t limit_cycles, void *stream) {
+    if (limit_cycles < 1000 || limit_cycles > 4000000000ll) return RQ_ERR_INVALID_ARG;
+    cudaError_t e = rq::launch_wait_timeout_selftest((long long)limit_cycles, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+}
+
 rq_status rq_sync_status(void *stream) {
     int word = 0;
     cudaError_t e = rq::read_and_clear_error_word(&word, static_cast<cudaStream_t>(stream));

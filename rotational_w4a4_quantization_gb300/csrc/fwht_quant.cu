@@ -141,11 +141,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *b, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait for a bulk copy; on expiry raise the error word and report failure.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *b, uint32_t parity, int *err) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *b, uint32_t parity, int *err,
+                                                  long long limit = kWaitLimitCycles) {
     if (mbar_try_wait(b, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(b, parity)) {
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             atomicExch(err, 1);
             return false;
         }
@@ -919,7 +920,26 @@ cudaError_t launch_n(const KParams &p, int in_type, cudaStream_t stream) {
     }
 }
 
+// Failure-detection self-test: one thread waits, through the rotation kernels'
+// bounded wait, on a barrier that nothing arrives on.  After `limit` cycles the
+// wait gives up and raises the error word, and the kernel returns normally.
+__global__ void wait_timeout_selftest_kernel(int *err, long long limit) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_wait_bounded(&bar, 0, err, limit);   // phase 0 never completes
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(long long limit_cycles, cudaStream_t stream) {
+    int *err = error_word_device_ptr();
+    if (!err) return cudaErrorUnknown;
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_cycles);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_type, uint64_t seed,
                               uint32_t flags, cudaStream_t stream) {

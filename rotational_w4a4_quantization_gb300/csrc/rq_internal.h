@@ -68,6 +68,10 @@ cudaError_t launch_w4a8_gemm_tc(const int8_t *aq, const float *sa, const uint8_t
 cudaError_t launch_w4a8_gemm(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,
                              int64_t N, int64_t K, int64_t group, void *y, int y_mode, cudaStream_t stream);
 
+// One thread waits on a barrier that nothing arrives on, with the rotation
+// kernels' bounded wait and the given limit: raises the error word on expiry.
+cudaError_t launch_wait_timeout_selftest(long long limit_cycles, cudaStream_t stream);
+
 // Device-resident error word set by bounded waits that gave up.
 cudaError_t read_and_clear_error_word(int *value, cudaStream_t stream);
 int *error_word_device_ptr();

@@ -209,3 +209,12 @@ def test_w4a8_argument_checks(lib, kw, expect):
 ])
 def test_fwht_code_mode_checks(lib, kw, expect):
     assert fq(lib, **kw) == expect
+
+
+@pytest.mark.parametrize("limit,expect", [(0, 1), (999, 1), (4_000_000_001, 1), (-5, 1)])
+def test_selftest_limit_checks(lib, limit, expect):
+    """The failure-detection self-test rejects limits outside 1000 .. 4e9 cycles
+    before it launches anything."""
+    lib.rq_selftest_wait_timeout.restype = ctypes.c_int32
+    lib.rq_selftest_wait_timeout.argtypes = [ctypes.c_int64, ctypes.c_void_p]
+    assert lib.rq_selftest_wait_timeout(limit, NULL) == expect
