@@ -85,6 +85,15 @@ def test_zero_rows_is_a_no_op():
     assert q.shape == (0, 128) and s.shape == (0,)
 
 
+@pytest.mark.parametrize("rows", [1212, 1300, 4100, 8192])
+def test_n4096_cta_sizes_for_batches(rows):
+    """n = 4096 batches around the CTA-size choice on 152 SMs: 1212 rows (8-row
+    CTAs, one round), 1300 and 4100 rows (7-row CTAs: fewer rows per SM in all),
+    8192 rows (8-row CTAs again)."""
+    x = synth.activations(rows, 4096, torch.bfloat16, seed=rows, n_outliers=4, factor=100.0)
+    _run_and_compare(x, seed=0x5EED, flags=rq.RQ_SIGNS_FIRST)
+
+
 @pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large"])
 def test_workload_activations_full_size(name):
     w = synth.WORKLOADS[name]
