@@ -149,7 +149,7 @@ def test_product_per_channel(M, N, K):
     compare_f16(_gpu(qa, sa, qw, sw, torch.float16), yref)
 
 
-@pytest.mark.parametrize("M", [1, 7, 16, 40])
+@pytest.mark.parametrize("M", [1, 7, 16, 40, 65, 300])
 @pytest.mark.parametrize("N,K", [(16, 128), (48, 1024), (128, 4096)])
 def test_product_per_group(M, N, K):
     qa, sa, qw, sw = _random_operands(M, N, K, 128, 2000 + M + N + K)
