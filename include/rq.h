@@ -287,9 +287,12 @@ rq_status rq_attn_decode(const void *q, rq_dtype q_dtype, int64_t M, int64_t hea
  *   multiple of 16 bytes run on the 5th-generation tensor cores (each INT8 code
  *   split exactly into two 4-bit halves, a = 16 (a >> 4) + (a & 15), both
  *   multiplied as FP8 into separate exact accumulators, CTA pairs, 128 x 256
- *   output tiles); everything else goes through legacy tensor-core MMAs
- *   (int8 x int8 -> int32), CTAs of 16 channels x 32 tokens.  Either way the
- *   integer sums are exact.
+ *   output tiles).  Per-group scales with M > 64, N a multiple of 128 and
+ *   K <= 8192 also run on the tensor cores: one exact partial per group in
+ *   tensor memory, scaled and summed in fp32 by the epilogue (128 x 128 tiles).
+ *   Everything else goes through legacy tensor-core MMAs (int8 x int8 ->
+ *   int32), CTAs of 16 channels x 32 tokens.  The integer sums of a group are
+ *   exact in every kernel.
  *   Errors: RQ_ERR_INVALID_ARG (negative sizes, NULL pointers),
  *   RQ_ERR_UNSUPPORTED (K, group, y_dtype), RQ_ERR_MISALIGNED (a_q, w_q, y not
  *   16-byte aligned; scales not 4-byte aligned).  M == 0 or N == 0 returns

@@ -65,6 +65,11 @@ cudaError_t launch_attn_decode(const void *q, int in_type, int64_t M, int64_t he
 bool w4a8_gemm_tc_supported(int64_t M, int64_t N, int64_t K, int y_mode);
 cudaError_t launch_w4a8_gemm_tc(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,
                                 int64_t N, int64_t K, void *y, int y_mode, cudaStream_t stream);
+// Per-group (128) weight scales with more than 64 tokens on the tensor cores:
+// N a multiple of 128, K <= 8192, fp16 or fp32 out.
+bool w4a8_group_tc_supported(int64_t M, int64_t N, int64_t K, int y_mode);
+cudaError_t launch_w4a8_group_tc(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,
+                                 int64_t N, int64_t K, void *y, int y_mode, cudaStream_t stream);
 cudaError_t launch_w4a8_gemm(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,
                              int64_t N, int64_t K, int64_t group, void *y, int y_mode, cudaStream_t stream);
 

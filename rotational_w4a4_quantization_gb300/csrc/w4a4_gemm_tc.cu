@@ -729,6 +729,392 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------------------
+// W4A8 with one weight scale per group of 128 codes along K ("SpinQuant" page,
+// The architecture: per-group scales), for more than 64 tokens:
+//   y[m][c] = sa[m] * sum_g sw[c][g] * sum_{k in g} a[m][k] q[c][k].
+// The group scale multiplies each K block's exact partial, so a block's product
+// cannot stay in one running accumulator as in the per-channel kernel.  Here:
+//  * codes widen to E4M3 with their sign (sign bit plus |q| <= 8 as u 2^-9, all
+//    exact), so a partial needs no offset terms; INT8 activations split as in
+//    the A8 variant (a = 16 h + l: row 2i holds h with its sign, row 2i+1 l);
+//  * the MMA (CTA pairs, M256 N128 K32) writes each K block into a fresh
+//    partial in a 3-deep TMEM ring (columns 0..383);
+//  * the epilogue warps (two per TMEM lane quarter, 64 columns each) read a
+//    partial and the running sum kept in TMEM (columns 384..511) with one wait,
+//    add sw[c][g] x partial, store the sum back and release the partial.  The
+//    round trips to TMEM, not the MMAs, set the pace, so the epilogue gets eight
+//    warps and the widening two teams.  After the last block the two rows of an
+//    activation row (adjacent TMEM lanes) combine as 16 S_h + S_l, times 2^18
+//    and sa[m];
+//  * the tile's group scales (128 columns x K/128 groups, K <= 8192) are staged
+//    in shared memory by the epilogue threads with cp.async, one tile ahead,
+//    transposed to [group][column] so that a block's 32 columns are 8 vector
+//    loads.  Barriers sc_full (the copies landed) and sc_empty (every epilogue
+//    warp is done with a buffer) order the two buffers; every wait is bounded.
+// ---------------------------------------------------------------------------
+constexpr int GBN = 128;                   // tile columns
+constexpr int GWROWS = GBN / 2;            // W rows (output channels) per CTA of the pair
+constexpr int GPK = 6, GOP = 3, GPR = 3;   // packed stages, operand stages, TMEM partial ring
+constexpr int GTEAMS = 2;                  // converter teams (the epilogue, not the widening, sets the pace)
+constexpr int GEPI = 8;                    // epilogue warps: two per TMEM lane quarter, 64 columns each
+constexpr int GTHREADS = 32 * (2 + GTEAMS * kTeamWarps + GEPI);
+constexpr int GMAXG = 64;                  // groups staged per column: K <= 8192
+constexpr uint32_t GSCOL = GPR * GBN;      // first TMEM column of the running sum
+static_assert(GSCOL + GBN <= 512, "TMEM budget");
+static_assert(GPK % GTEAMS == 0 && GOP >= GTEAMS, "parity waits stay one phase ahead at most");
+
+struct GSmem {
+    static constexpr bool kPair = true;
+    alignas(1024) uint8_t opA[GOP][BM * BK];            // 128 operand rows of E4M3
+    alignas(1024) uint8_t opW[GOP][GWROWS * BK];        // 64 W rows of E4M3
+    alignas(128) uint8_t pkA[GPK][(BM / 2) * BK];       // 64 INT8 rows x 128 bytes
+    alignas(128) uint8_t pkW[GPK][GWROWS * BK / 2];     // 64 packed W rows x 64 bytes
+    alignas(16) float gsc[2][GMAXG * GBN];              // group scales [g][column], two tiles
+    alignas(8) uint64_t pk_full[GPK], pk_empty[GPK];
+    uint64_t op_full[GOP], op_empty[GOP];               // op_full at the leader: both CTAs' teams
+    uint64_t p_full[GPR], p_empty[GPR];                 // p_empty at the leader: both CTAs' epilogues
+    uint64_t sc_full[2], sc_empty[2];                   // own epilogue threads / warps
+    uint32_t tmem_base;
+    volatile int abort_flag;
+};
+
+struct GParams {
+    const float *sa, *sw;   // sw: [N][K/128]
+    void *y;
+    int64_t M, N, K;
+    int *err;
+};
+
+// kind::f8f6f4, E4M3 x E4M3 -> F32, K-major, M = 256 (CTA pair), N = 128.
+constexpr uint32_t idesc_pair_n128() { return (1u << 4) | ((uint32_t)(GBN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24); }
+
+__device__ __forceinline__ void mma_f8_pair_n128(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc_pair_n128()), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+// Two 32-column TMEM loads (a partial and the running sum) behind one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t (&a)[32], uint32_t tb, uint32_t (&b)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+          "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+          "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]),
+          "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
+          "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
+          "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]),
+          "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]),
+          "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+        : "r"(ta), "r"(tb)
+        : "memory");
+}
+
+// Byte lanes holding 4-bit two's-complement codes (0..15) -> E4M3 bytes of the
+// same signed value times 2^-9: |q| <= 8 in bits 0..3, the sign in bit 7.
+__device__ __forceinline__ uint32_t nib_to_e4m3_signed(uint32_t x) {
+    const uint32_t neg = x & 0x08080808u;
+    const uint32_t msk = (neg >> 3) * 0xffu;                       // 0xff in the negative lanes
+    const uint32_t mag = x ^ ((x ^ (0x10101010u - x)) & msk);      // 16 - x there
+    return mag | (neg << 4);
+}
+
+// Store 16 final values of row m from column nb on (fp16 or fp32); N is a
+// multiple of 128.
+template <int YMODE>
+__device__ __forceinline__ void store16_f(void *y, int64_t N, int64_t m, int64_t nb, const float (&v)[16]) {
+    if (YMODE == 1) {
+        float4 *yr = reinterpret_cast<float4 *>(static_cast<float *>(y) + m * N + nb);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) yr[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    } else {
+        uint4 *yr = reinterpret_cast<uint4 *>(static_cast<__half *>(y) + m * N + nb);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            __align__(16) __half h[8];
+#pragma unroll
+            for (int e2 = 0; e2 < 8; ++e2) h[e2] = __float2half_rn(v[8 * j + e2]);
+            yr[j] = *reinterpret_cast<const uint4 *>(h);
+        }
+    }
+}
+
+template <int YMODE>
+__global__ void __launch_bounds__(GTHREADS, 1)
+w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                     const __grid_constant__ GParams prm) {
+    constexpr int kConvWarps = GTEAMS * kTeamWarps;
+    constexpr int PK_A = (BM / 2) * BK, PK_W = GWROWS * BK / 2;
+    extern __shared__ uint8_t smem_raw[];
+    GSmem &s = *reinterpret_cast<GSmem *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int kblocks = (int)(prm.K / BK);                    // = groups
+    const int64_t n_tiles_n = prm.N / GBN;
+    const int64_t n_tiles = n_tiles_n * ((prm.M + BM - 1) / BM);   // 128 activation rows per tile
+    const int64_t first_tile = blockIdx.x / 2, tile_step = gridDim.x / 2;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < GPK; ++i) {
+            mbar_init(&s.pk_full[i], 1);
+            mbar_init(&s.pk_empty[i], kTeamWarps);
+        }
+        for (int i = 0; i < GOP; ++i) {
+            mbar_init(&s.op_full[i], kTeamWarps * 2);
+            mbar_init(&s.op_empty[i], 1);
+        }
+        for (int i = 0; i < GPR; ++i) {
+            mbar_init(&s.p_full[i], 1);
+            mbar_init(&s.p_empty[i], GEPI * 2);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.sc_full[i], GBN);      // the 128 staging threads
+            mbar_init(&s.sc_empty[i], GEPI);
+        }
+        s.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s.tmem_base)),
+                     "r"(512u)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    cluster_sync<true>();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = s.tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int64_t g = 0;
+            bool ok = true;
+            for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step) {
+                const int m0 = (int)(tile / n_tiles_n) * BM + (int)rank * (BM / 2);   // INT8 rows
+                const int n0 = (int)(tile % n_tiles_n) * GBN + (int)rank * GWROWS;
+                for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                    const int st = (int)(g % GPK);
+                    if (!mbar_wait<false, true>(s, &s.pk_empty[st], (uint32_t)((g / GPK) & 1) ^ 1, prm.err)) { ok = false; break; }
+                    mbar_expect_tx(&s.pk_full[st], PK_A + PK_W);
+                    tma_load_2d(s.pkA[st], &tmA, &s.pk_full[st], kb * BK, m0);
+                    tma_load_2d(s.pkW[st], &tmW, &s.pk_full[st], kb * (BK / 2), n0);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (leader CTA): one fresh partial per K block ----------------
+        if (lane == 0 && rank == 0) {
+            int64_t g = 0;
+            bool ok = true;
+            for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step) {
+                for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                    const int pr = (int)(g % GPR), st = (int)(g % GOP);
+                    if (!mbar_wait<true>(s, &s.p_empty[pr], (uint32_t)((g / GPR) & 1) ^ 1, prm.err)) { ok = false; break; }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    if (!mbar_wait<true>(s, &s.op_full[st], (uint32_t)((g / GOP) & 1), prm.err)) { ok = false; break; }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t d = tmem + (uint32_t)(pr * GBN);
+                    const uint32_t a0 = smem_u32(s.opA[st]), w0 = smem_u32(s.opW[st]);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_f8_pair_n128(d, sw128_desc(a0 + 32 * k), sw128_desc(w0 + 32 * k), k != 0);
+                    mma_commit<true>(&s.op_empty[st]);
+                    mma_commit<true>(&s.p_full[pr]);
+                }
+            }
+        }
+    } else if (warp < 2 + kConvWarps) {
+        // ---------------- converters: signed E4M3 ----------------
+        const int tc = threadIdx.x - 64;
+        const int team = (warp - 2) / kTeamWarps;
+        const int tt = tc - kTeamThreads * team;
+        const int ch = tt & 3, rq = tt >> 2;        // W: row rq + 32 j (j < 2), 16-byte chunk ch
+        const int c8 = tt & 7, r8 = tt >> 3;        // A: INT8 row r8 + 16 j (j < 4), 16-code chunk c8
+        int64_t g = 0;
+        bool ok = true;
+        for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step) {
+            for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                if ((int)(g % GTEAMS) != team) continue;
+                const int ps = (int)(g % GPK), os = (int)(g % GOP);
+                if (!mbar_wait(s, &s.pk_full[ps], (uint32_t)((g / GPK) & 1), prm.err)) { ok = false; break; }
+                uint4 a[4], w[2];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) a[j] = reinterpret_cast<const uint4 *>(s.pkA[ps])[tt + kTeamThreads * j];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) w[j] = reinterpret_cast<const uint4 *>(s.pkW[ps])[tt + kTeamThreads * j];
+                if (!warp_wait_commit(s, &s.op_empty[os], (uint32_t)((g / GOP) & 1) ^ 1, lane, prm.err)) { ok = false; break; }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 &v = a[j];
+                    const uint32_t p[4] = {__byte_perm(v.x, v.y, 0x6420u), __byte_perm(v.x, v.y, 0x7531u),
+                                           __byte_perm(v.z, v.w, 0x6420u), __byte_perm(v.z, v.w, 0x7531u)};
+                    uint32_t h[4], l[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        h[i] = nib_to_e4m3_signed((p[i] >> 4) & 0x0f0f0f0fu);   // h = a >> 4, a 4-bit code
+                        l[i] = p[i] & 0x0f0f0f0fu;                              // l = a & 15 >= 0
+                    }
+                    const int r2 = 2 * (r8 + 16 * j);
+                    uint8_t *rowp = s.opA[os] + r2 * 128;
+                    *reinterpret_cast<uint4 *>(rowp + 16 * (c8 ^ (r2 & 7))) = make_uint4(h[0], h[1], h[2], h[3]);
+                    *reinterpret_cast<uint4 *>(rowp + 128 + 16 * (c8 ^ ((r2 + 1) & 7))) = make_uint4(l[0], l[1], l[2], l[3]);
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t wv[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+                    uint32_t lo[4], hi[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        lo[i] = nib_to_e4m3_signed(wv[i] & 0x0f0f0f0fu);          // even codes
+                        hi[i] = nib_to_e4m3_signed((wv[i] >> 4) & 0x0f0f0f0fu);   // odd codes
+                    }
+                    const int row = rq + 32 * j;
+                    uint8_t *rowp = s.opW[os] + row * 128;
+                    const int g0 = (2 * ch) ^ (row & 7), g1 = (2 * ch + 1) ^ (row & 7);
+                    *reinterpret_cast<uint4 *>(rowp + 16 * g0) = make_uint4(lo[0], hi[0], lo[1], hi[1]);
+                    *reinterpret_cast<uint4 *>(rowp + 16 * g1) = make_uint4(lo[2], hi[2], lo[3], hi[3]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&s.pk_empty[ps]);
+                    if (rank == 0) mbar_arrive(&s.op_full[os]);
+                    else mbar_arrive_remote_cta_scope(&s.op_full[os], 0);
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue: scale and add the partials, then combine and store ----------------
+        const int e = threadIdx.x - 64 - 32 * kConvWarps;   // 0..255; threads e < 128 stage column e's scales
+        const int q = warp & 3;                              // TMEM lane quarter
+        const int half = e >> 7;                             // columns 64 half .. 64 half + 63
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const bool odd = (lane & 1) != 0;
+        const int G = kblocks;
+        // copy the group scales of `tile`'s column e into buffer b (transposed to [g][column]);
+        // the thread's arrival on sc_full[b] fires when its copies have landed
+        auto stage = [&](int64_t tile, int b) {
+            const float *src = prm.sw + ((tile % n_tiles_n) * GBN + e) * (int64_t)G;
+            float *dst = s.gsc[b] + e;
+            for (int gg = 0; gg < G; ++gg)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst + gg * GBN)), "l"(src + gg)
+                             : "memory");
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&s.sc_full[b]))
+                         : "memory");
+        };
+        int64_t g = 0;
+        int it = 0;
+        bool ok = true;
+        if (first_tile < n_tiles && e < GBN) {
+            if (!mbar_wait<false, true>(s, &s.sc_empty[0], 1u, prm.err)) ok = false;   // fresh: passes at once
+            else stage(first_tile, 0);
+        }
+        for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step, ++it) {
+            const int b = it & 1;
+            if (!mbar_wait<false, true>(s, &s.sc_full[b], (uint32_t)((it >> 1) & 1), prm.err)) break;
+            // stage the next tile into the other buffer once every epilogue warp is done with it
+            const int64_t nt = tile + tile_step;
+            if (nt < n_tiles && e < GBN) {
+                if (!mbar_wait<false, true>(s, &s.sc_empty[b ^ 1], (uint32_t)(((it + 1) >> 1) & 1) ^ 1, prm.err)) break;
+                stage(nt, b ^ 1);
+            }
+            const int64_t m0 = (tile / n_tiles_n) * (2 * BM) + (int64_t)rank * BM;   // operand rows
+            const int64_t m = (m0 + 32 * q + lane) >> 1;                             // activation row
+            const int64_t n0 = (tile % n_tiles_n) * GBN;
+            const float sa = m < prm.M ? prm.sa[m] * 262144.0f : 0.f;               // x 2^18: partials are 2^-18 units
+            for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                const int pr = (int)(g % GPR);
+                if (!mbar_wait<true, true>(s, &s.p_full[pr], (uint32_t)((g / GPR) & 1), prm.err)) { ok = false; break; }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                // the previous block's stores of the running sum are complete before it is read
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                const float4 *sc4 = reinterpret_cast<const float4 *>(s.gsc[b] + kb * GBN);
+                const bool last = kb + 1 == kblocks;
+#pragma unroll 1
+                for (int c = 2 * half; c < 2 * half + 2; ++c) {
+                    uint32_t pv[32], sv[32];
+                    const uint32_t tp = tmem + lane_base + (uint32_t)(pr * GBN + 32 * c);
+                    const uint32_t ts = tmem + lane_base + GSCOL + (uint32_t)(32 * c);
+                    if (kb > 0) {
+                        tmem_ld32x2(tp, pv, ts, sv);
+                    } else {
+                        tmem_ld32(tp, pv);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) sv[j] = 0u;
+                    }
+                    float acc[32];
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 w4 = sc4[8 * c + j / 4];
+                        const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            acc[j + i] = fmaf(wv[i], __uint_as_float(pv[j + i]), __uint_as_float(sv[j + i]));
+                    }
+                    if (!last) {
+                        uint32_t st[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) st[j] = __float_as_uint(acc[j]);
+                        tmem_st32(ts, st);
+                    } else {
+                        // rows 2i (h) and 2i+1 (l) are lanes 2i, 2i+1: the even lane outputs the
+                        // chunk's first 16 columns, the odd lane the next 16
+                        float out[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float mine = odd ? acc[j + 16] : acc[j];
+                            const float recv = __shfl_xor_sync(0xffffffffu, odd ? acc[j] : acc[j + 16], 1);
+                            out[j] = (odd ? fmaf(16.f, recv, mine) : fmaf(16.f, mine, recv)) * sa;
+                        }
+                        if (m < prm.M) store16_f<YMODE>(prm.y, prm.N, m, n0 + 32 * c + (odd ? 16 : 0), out);
+                    }
+                }
+                // the partial may be overwritten (it was only read)
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cta(&s.p_empty[pr], 0);
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.sc_empty[b]);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("cp.async.wait_all;" ::: "memory");   // no copy into shared memory outlives the CTA
+    }
+
+    __syncwarp();
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    cluster_sync<true>();
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
@@ -820,6 +1206,35 @@ constexpr int64_t kFourTeamsMaxOperandBytes = 64ll << 20;
 
 bool four_teams(int64_t a_bytes, int64_t w_bytes) { return a_bytes + w_bytes <= kFourTeamsMaxOperandBytes; }
 
+template <int YMODE>
+cudaError_t launch_group_mode(const CUtensorMap &ta, const CUtensorMap &tw, const GParams &p, cudaStream_t stream) {
+    auto kern = w4a8_group_tc_kernel<YMODE>;
+    const size_t smem = sizeof(GSmem) + 1024;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorUnknown;
+    const int64_t tiles = (p.N / GBN) * ((p.M + BM - 1) / BM);
+    const int64_t units = tiles < sms / 2 ? tiles : sms / 2;   // persistent CTA pairs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units * 2));
+    cfg.blockDim = dim3(GTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tw, p);
+}
+
 }  // namespace
 
 bool w4a4_gemm_tc_supported(const GemmArgs &g) { return g.M > 64 && g.K % BK == 0 && g.K <= 65536; }
@@ -845,6 +1260,21 @@ cudaError_t launch_w4a4_gemm_tc(const GemmArgs &g, cudaStream_t stream) {
 bool w4a8_gemm_tc_supported(int64_t M, int64_t N, int64_t K, int y_mode) {
     const int64_t elem = y_mode == 0 ? 2 : 4;
     return M > 64 && K % BK == 0 && K <= 65536 && (N * elem) % 16 == 0;
+}
+
+bool w4a8_group_tc_supported(int64_t M, int64_t N, int64_t K, int y_mode) {
+    return M > 64 && K % BK == 0 && K / BK <= GMAXG && N % GBN == 0 && y_mode != 2;
+}
+
+cudaError_t launch_w4a8_group_tc(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,
+                                 int64_t N, int64_t K, void *y, int y_mode, cudaStream_t stream) {
+    const GParams p{sa, sw, y, M, N, K, error_word_device_ptr()};
+    if (!p.err) return cudaErrorUnknown;
+    CUtensorMap ta, tw;
+    if (!make_map(&ta, aq, M, K, BK, BM / 2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tw, wq, N, K / 2, BK / 2, GWROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    return y_mode == 1 ? launch_group_mode<1>(ta, tw, p, stream) : launch_group_mode<0>(ta, tw, p, stream);
 }
 
 cudaError_t launch_w4a8_gemm_tc(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,

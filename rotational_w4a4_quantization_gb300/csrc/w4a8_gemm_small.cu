@@ -1,6 +1,7 @@
 // w4a8_gemm_small.cu -- W4A8 linear layer for few tokens, with per-channel or
-// per-group weight scales (sm_103a).  Per-channel products of more than 64
-// tokens are dispatched to the tensor-core kernel (w4a4_gemm_tc.cu, A8 variant).
+// per-group weight scales (sm_103a).  Products of more than 64 tokens are
+// dispatched to the tensor-core kernels of w4a4_gemm_tc.cu where their shapes
+// allow (per channel: the A8 variant; per group: the group kernel).
 //
 // "SpinQuant" page, The architecture: the rotated weights go to INT4 and the
 // activations to INT8, with per-channel or per-group scales; End-to-end flow:
@@ -195,6 +196,8 @@ cudaError_t launch_w4a8_gemm(const int8_t *aq, const float *sa, const uint8_t *w
     if (group == K && w4a8_gemm_tc_supported(M, N, K, y_mode))
         return launch_w4a8_gemm_tc(aq, sa, wq, sw, M, N, K, y, y_mode, stream);
     if (group == K) return launch_w8_g<false>(aq, sa, wq, sw, M, N, K, y, y_mode, stream);
+    if (group == 128 && w4a8_group_tc_supported(M, N, K, y_mode))
+        return launch_w4a8_group_tc(aq, sa, wq, sw, M, N, K, y, y_mode, stream);
     if (group == 128) return launch_w8_g<true>(aq, sa, wq, sw, M, N, K, y, y_mode, stream);
     return cudaErrorInvalidValue;
 }

@@ -269,3 +269,50 @@ def test_product_operands_beyond_l2_sampled_rows():
     rows = np.unique(np.concatenate([np.arange(0, M, 173), [127, 128, 255, 256, M - 1]]))
     acc, _ = oracle.w4a8_gemm(qa[rows], sa[rows], qw, sw.reshape(N, 1), len(rows), N, K, K)
     np.testing.assert_array_equal(y32[rows].astype(np.int64), acc)
+
+
+# ---- per-group scales with more than 64 tokens: the tensor-core kernel ----
+
+def _check_per_group(y, yref):
+    err = np.abs(y.astype(np.float64) - yref).max(axis=1)
+    assert np.all(err <= 1e-5 * np.abs(yref).max(axis=1)), float((err / np.abs(yref).max(axis=1)).max())
+
+
+@pytest.mark.parametrize("M", [65, 130, 600])
+@pytest.mark.parametrize("N,K", [(128, 128), (384, 2048), (256, 8192)])
+def test_product_per_group_tensor_cores(M, N, K):
+    """N a multiple of 128 and K <= 8192: CTA pairs with 128 x 128 tiles, one
+    TMEM partial per group; one group (K = 128) up to the 64 groups staged per
+    column (K = 8192); ragged M."""
+    qa, sa, qw, sw = _random_operands(M, N, K, 128, 5000 + M + N + K)
+    _, yref = oracle.w4a8_gemm(qa, sa, qw, sw, M, N, K, 128)
+    _check_per_group(_gpu(qa, sa, qw, sw, torch.float32), yref)
+    compare_f16(_gpu(qa, sa, qw, sw, torch.float16), yref, atol=1e-5 * np.abs(yref).max(axis=1, keepdims=True))
+
+
+def test_per_group_more_groups_than_staged():
+    """K = 8320 (65 groups) is past the tensor-core kernel's staging: the mma.sync
+    kernel takes it."""
+    M, N, K = 100, 128, 8320
+    qa, sa, qw, sw = _random_operands(M, N, K, 128, 5999)
+    _, yref = oracle.w4a8_gemm(qa, sa, qw, sw, M, N, K, 128)
+    _check_per_group(_gpu(qa, sa, qw, sw, torch.float32), yref)
+
+
+def test_per_group_prefill_shape_sampled_rows():
+    """2048 x 4096 -> 14336 with per-group weight scales: INT8 codes of the
+    prefill activations (oracle) against random per-group INT4 weights; 27 rows
+    over every tile row and both CTAs of a pair, fp32 and fp16, against the oracle."""
+    w = synth.WORKLOADS["prefill"]
+    M, K, N = w.rows, w.n, w.gemm_n
+    x = synth.activations(M, K, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor)
+    ref_a = oracle.fwht_quant8(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+    g = np.random.default_rng(6001)
+    qw = g.integers(0, 256, size=(N, K // 2)).astype(np.uint8)
+    sw = (g.random((N, K // 128)) + 0.05).astype(np.float32)
+    y32 = _gpu(ref_a["q"], ref_a["scales"], qw, sw, torch.float32)
+    y16 = _gpu(ref_a["q"], ref_a["scales"], qw, sw, torch.float16)
+    rows = np.unique(np.concatenate([np.arange(0, M, 97), [63, 64, 127, 128, M - 1]]))
+    _, yref = oracle.w4a8_gemm(ref_a["q"][rows], ref_a["scales"][rows], qw, sw, len(rows), N, K, 128)
+    _check_per_group(y32[rows], yref)
+    compare_f16(y16[rows], yref, atol=1e-5 * np.abs(yref).max(axis=1, keepdims=True))
