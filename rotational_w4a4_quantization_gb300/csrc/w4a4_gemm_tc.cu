@@ -834,10 +834,8 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t (&a)[32], uint
 // Byte lanes holding 4-bit two's-complement codes (0..15) -> E4M3 bytes of the
 // same signed value times 2^-9: |q| <= 8 in bits 0..3, the sign in bit 7.
 __device__ __forceinline__ uint32_t nib_to_e4m3_signed(uint32_t x) {
-    const uint32_t neg = x & 0x08080808u;
-    const uint32_t msk = (neg >> 3) * 0xffu;                       // 0xff in the negative lanes
-    const uint32_t mag = x ^ ((x ^ (0x10101010u - x)) & msk);      // 16 - x there
-    return mag | (neg << 4);
+    const uint32_t one = (x >> 3) & 0x01010101u;                  // 1 in the negative lanes
+    return (x ^ (one * 0x8fu)) + one;                              // 0x80 | (15 - x) + 1 there
 }
 
 // Store 16 final values of row m from column nb on (fp16 or fp32); N is a
@@ -1047,7 +1045,7 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             const float sa = m < prm.M ? prm.sa[m] * 262144.0f : 0.f;               // x 2^18: partials are 2^-18 units
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
                 const int pr = (int)(g % GPR);
-                if (!mbar_wait<true, true>(s, &s.p_full[pr], (uint32_t)((g / GPR) & 1), prm.err)) { ok = false; break; }
+                if (!mbar_wait<true, false>(s, &s.p_full[pr], (uint32_t)((g / GPR) & 1), prm.err)) { ok = false; break; }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 // the previous block's stores of the running sum are complete before it is read
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
