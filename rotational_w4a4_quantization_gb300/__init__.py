@@ -18,7 +18,10 @@ Entry points (same names as the C ABI):
   cache;
 * :func:`w4a8_gemm` -- the W4A8 linear layer (INT8 activations from
   :func:`fwht_quant` with ``RQ_INT8_CODES``), per-channel or per-group weight
-  scales.
+  scales;
+* :func:`sync_status` -- drain a stream and read (and clear) the device error
+  word that bounded waits raise; :func:`selftest_wait_timeout` makes one such
+  wait run out on purpose, to exercise that path.
 """
 from ._binding import (  # noqa: F401
     RQ_ATTN_ROTATED_OUT,
