@@ -1146,13 +1146,11 @@ bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row_byte
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// SM count of the current device (0 on error).
 int sm_count() {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 0;
-    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     return sms;
 }
 
@@ -1168,12 +1166,9 @@ cudaError_t launch_mode(const GemmArgs &g, const TcParams &p, cudaStream_t strea
         return cudaErrorInvalidValue;
     auto kern = w4a4_tc_kernel<YMODE, PAIR, A8, TEAMS>;
     const size_t smem = sizeof(Smem<PAIR, TEAMS>) + 1024;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // set on every launch: the attribute is per device, and a process may use several
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorUnknown;
     const int64_t m_op = A8 ? 2 * p.M : p.M;
@@ -1208,12 +1203,9 @@ template <int YMODE>
 cudaError_t launch_group_mode(const CUtensorMap &ta, const CUtensorMap &tw, const GParams &p, cudaStream_t stream) {
     auto kern = w4a8_group_tc_kernel<YMODE>;
     const size_t smem = sizeof(GSmem) + 1024;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // set on every launch: the attribute is per device, and a process may use several
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorUnknown;
     const int64_t tiles = (p.N / GBN) * ((p.M + BM - 1) / BM);
