@@ -1,8 +1,8 @@
 /*
  * rq.h -- C ABI of the rotation-based W4A4 inference kernels (GB300, sm_103a).
  *
- * Three operations make up the online hot path of rotation-based 4-bit
- * inference:
+ * The online hot path of rotation-based 4-bit inference, and the operations
+ * around it:
  *
  *   rq_fwht_quant       randomized fast Walsh-Hadamard transform of each row,
  *                       fused with per-row symmetric INT4 quantization and
@@ -49,7 +49,7 @@
  *   +-1/sqrt(n)), and s in {-1,+1}^n is a Rademacher vector drawn from `seed`:
  *   s_i = +1 when the top bit of output i (0-based) of SplitMix64 seeded with
  *   `seed` is 0, else -1.  flags bit 0 (RQ_SIGNS_FIRST) selects the form:
- *     RQ_SIGNS_FIRST set:   y = (x diag(s)) H_n     ("x·diag(±1)·H_n/√n")
+ *     RQ_SIGNS_FIRST set:   y = (x diag(s)) H_n     (the signs act first)
  *     RQ_SIGNS_FIRST clear: y = (x H_n) diag(s)     (R = H_d·diag(s), [ROT] eq.)
  *   The two forms are transposes of each other; use the same flags for the
  *   activations and for the offline weight fold.
@@ -103,9 +103,9 @@ enum { RQ_INT8_CODES = 4u, RQ_GROUP_SCALES = 8u };
  *
  *   [ROT] §Weight Absorption and Online Fast Walsh-Hadamard Transforms,
  *   2. Online FWHT (n log2 n additions/subtractions, one global 1/sqrt(n)
- *   scale); [ROT] §Incoherence (R = H_d·diag(s)); [QR] §End-to-end flow
- *   ("an online Hadamard transform rotates the activation ... The rotated
- *   activation is quantized to INT4").  The same call performs the offline
+ *   scale); [ROT] §Incoherence (R = H_d·diag(s)); [QR] §End-to-end flow (the
+ *   activation is rotated on the fly by a Hadamard transform, then quantized to
+ *   INT4).  The same call performs the offline
  *   weight fold W~ = R^T W of [ROT] §Weight Absorption, 1. when given the rows
  *   of W^T (one output channel per row): each output channel is then quantized
  *   with its own scale.
@@ -181,8 +181,8 @@ rq_status rq_w4a4_gemm(const uint8_t *a_q, const float *a_scales, const uint8_t 
  * rq_kv_rotate_quant -- rotate each (token, head) vector of K and V by the
  * randomized Hadamard of size head_dim and quantize it per (token, head).
  *
- *   [QR] §The architecture ("The KV-cache rotation box ... keys and values
- *   stored per token are themselves rotated before being quantized") and
+ *   [QR] §The architecture (the KV-cache rotation box: each token's keys and
+ *   values are rotated, then quantized, before they are stored) and
  *   §End-to-end flow, "The KV cache"; [ROT] §Hardware Execution, 2. End-to-End
  *   KV Cache Footprint Reduction.  One sign vector of length head_dim (from
  *   `seed`) is shared by every head and by K and V.

@@ -58,8 +58,8 @@ uint64_t rqo_splitmix64(uint64_t seed, uint64_t i)
     return z ^ (z >> 31);
 }
 
-/* Rademacher vector s in {-1,+1}^n: [ROT] §Incoherence ("s ... sampled uniformly
- * from ±1").  Reading: s_i = +1 when the top bit of SplitMix64 output i is 0,
+/* Rademacher vector s in {-1,+1}^n: [ROT] §Incoherence (each sign drawn at
+ * random, +1 or -1 alike).  Reading: s_i = +1 when the top bit of SplitMix64 output i is 0,
  * else -1.  The pages fix no generator; this one is ours. */
 void rqo_signs(uint64_t seed, int64_t n, int8_t *s)
 {
@@ -320,8 +320,8 @@ void rqo_unpack_row(const uint8_t *in, int64_t n, int8_t *q)
  * per-row INT4 quantizer and packing.  Outputs: q (rows x n/2 bytes, row stride
  * n/2), scales (rows, fp32, rounded from the fp64 scale), and optionally the
  * fp64 rotated rows y (rows x n) and the ratios y/scale (rows x n).
- * [QR] §End-to-end flow ("an online Hadamard transform rotates the activation
- * ... The rotated activation is quantized to INT4"); [ROT] §Weight Absorption,
+ * [QR] §End-to-end flow (the activation is rotated on the fly by a Hadamard
+ * transform, then quantized to INT4); [ROT] §Weight Absorption,
  * 2. Online Fast Walsh-Hadamard Transform. */
 int rqo_fwht_quant(const double *x, int64_t rows, int64_t n, int64_t ld_x, uint64_t seed,
                    uint32_t flags, uint8_t *q, float *scales, double *y_out, double *ratio_out)
@@ -363,7 +363,8 @@ int rqo_fwht_quant(const double *x, int64_t rows, int64_t n, int64_t ld_x, uint6
  * K-major, W holding one output channel per row.  The integer form of the
  * rotated product Q(XR)·Q(R^T W) of [ROT] §Learned Orthogonal Rotations
  * (loss L(S)) and §The Principle of Computational Invariance (Y = (XR)(R^T W));
- * [QR] §End-to-end flow ("multiplied against the INT4 folded weights").
+ * [QR] §End-to-end flow (the INT4 activation meets the INT4 weights that carry
+ * the folded rotation).
  * Either output may be NULL.  Returns RQO_ERR_OVERFLOW if an accumulator
  * leaves the int32 range. */
 int rqo_w4a4_gemm(const uint8_t *aq, const float *sa, const uint8_t *wq, const float *sw,
@@ -441,8 +442,8 @@ int rqo_w4a4_gemm_entries(const uint8_t *aq, const float *sa, const uint8_t *wq,
 
 /* K and V, each [tokens][heads][head_dim] (fp64 here), are rotated per (token,
  * head) vector by the randomized Hadamard of size head_dim and quantized per
- * (token, head): [QR] §The architecture ("The KV-cache rotation box ... keys and
- * values stored per token are themselves rotated before being quantized") and
+ * (token, head): [QR] §The architecture (the KV-cache rotation box: each
+ * token's keys and values are rotated, then quantized, before they are stored) and
  * §End-to-end flow, "The KV cache"; [ROT] §Hardware Execution, 2. End-to-End KV
  * Cache Footprint Reduction.  Reading: one sign vector of length head_dim drawn
  * from `seed`, shared by every head and by K and V.  Either tensor may be NULL
@@ -552,9 +553,9 @@ int rqo_attn_decode(const double *q, int64_t M, int64_t heads, int64_t head_dim,
 /* W4A8 and per-group weight scales.                                          */
 /* ------------------------------------------------------------------------- */
 
-/* Per-row symmetric INT8 for activations: [SQ] §The architecture ("maps them to
- * INT4 (weights) and INT8 (activations) with ordinary per-channel or per-group
- * scales"), §End-to-end flow ("quantizes the rotated activation to INT8").
+/* Per-row symmetric INT8 for activations: [SQ] §The architecture (after the
+ * rotations, weights go to INT4 and activations to INT8, with per-channel or
+ * per-group scales), §End-to-end flow (the rotated activation becomes INT8).
  * Reading: scale = max|y| / 127, q = clamp(round_half_even(y / scale), -128, 127)
  * (-128 never occurs with this scale); an all-zero row gets scale 0, codes 0.
  * `ratio` (nullable) receives y / scale. */
@@ -646,8 +647,8 @@ int rqo_fwht_quant_groups(const double *x, int64_t rows, int64_t n, int64_t ld_x
  * scales sw (N x K/group; group == K is per-channel):
  *   acc_g[m][c] = sum_{k in group g} qa[m][k] qw[c][k]   (exact integers)
  *   y[m][c]     = sa[m] * sum_g sw[c][g] * acc_g[m][c]    (fp64)
- * [SQ] §End-to-end flow ("quantizes the rotated activation to INT8, and
- * multiplies it against the INT4 rotated weights"), §The architecture.
+ * [SQ] §End-to-end flow (the INT8 rotated activation is multiplied with the INT4
+ * rotated weights), §The architecture.
  * acc (nullable, per-channel only): the whole-K integer sums. */
 int rqo_w4a8_gemm(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M, int64_t N,
                   int64_t K, int64_t group, int64_t *acc, double *y)
