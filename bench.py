@@ -388,8 +388,7 @@ def run_gpu(args, work, kvw):
         "vs_baseline": None,
         "dtype": "int4",
         "data": "synthetic",
-        "config": {"workload": f"{work.name}: X {M}x{K} bf16 -> fwht+int4 -> W4A4 GEMM {M}x{K}x{N} fp16; "
-                               f"kv {T}x{H}x{D} bf16 K,V",
+        "config": {"workload": workload_desc(work, kvw),
                    "l2": "flushed between timed steps (2x L2 write, outside timed events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kernels": kernels,
@@ -445,6 +444,12 @@ def cpu_baseline(work, kvw, budget_s=15.0):
             "step_seconds_extrapolated": step_s, "parts_s": parts}
 
 
+def workload_desc(work, kvw):
+    """The step's workload, named the same way by both arms."""
+    return (f"{work.name}: X {work.rows}x{work.n} bf16 -> fwht+int4 -> W4A4 GEMM "
+            f"{work.rows}x{work.n}x{work.gemm_n} fp16; kv {kvw.kv_tokens}x{kvw.kv_heads}x{kvw.kv_head_dim} bf16 K,V")
+
+
 def run_reference(args, work, kvw):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -467,8 +472,7 @@ def run_reference(args, work, kvw):
         "full_step_ms_extrapolated": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4",
         "data": "synthetic",
-        "config": {"workload": f"{work.name}: X {work.rows}x{work.n} -> W4A4 GEMM "
-                               f"{work.rows}x{work.n}x{work.gemm_n}; kv {kvw.kv_tokens}x{kvw.kv_heads}x{kvw.kv_head_dim}"},
+        "config": {"workload": workload_desc(work, kvw), "parallelism": "host cores (oracle)"},
         "cpu_baseline": {"value": value, "unit": "TOPS", "cores": 1, "kind": "oracle",
                          "sample": f"each step: {gemm_rows} GEMM rows, 16 rotation rows, 64 KV tokens, "
                                    "scaled by rows to one full step"},
