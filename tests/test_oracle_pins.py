@@ -574,6 +574,41 @@ def test_group_quant_reduces_to_per_row_and_group_scales():
     np.testing.assert_allclose(g["scales"], (np.abs(y).max(axis=2) / 7.0).astype(np.float32), rtol=0, atol=0)
 
 
+@pytest.mark.parametrize("flags", [0, oracle.SIGNS_FIRST])
+def test_group_quant_codes_and_scales_group_by_group(flags):
+    """Per-group INT4 of the fold with groups of 128 inside rows of 1024: every
+    code of every group equals the brute-force nearest code of y_g / (max|y_g|/7),
+    with y = x R formed from scipy's explicit Sylvester matrix and the signs, and
+    the packed bytes decoded by plain bit arithmetic.  The rotated rows are built
+    with group magnitudes three orders apart (x = y R^T), so a code written at
+    another group's offset, or a scale paired with the neighbouring group, fails."""
+    n, group, seed = 1024, 128, 0x5EED
+    ng = n // group
+    rng = np.random.default_rng(44 + flags)
+    mags = np.array([1e-3, 1.0, 30.0, 0.02, 5.0, 400.0, 0.5, 2e-2])
+    y_target = rng.standard_normal((3, n)) * np.repeat(mags, group)[None, :]
+    y_target[1] = y_target[1][::-1].copy()          # another magnitude order per row
+    y_target[2] *= np.repeat(rng.permutation(mags), group)
+    s = oracle.signs(seed, n).astype(np.float64)
+    h = scipy.linalg.hadamard(n).astype(np.float64) / np.sqrt(n)
+    r = np.diag(s) @ h if flags == oracle.SIGNS_FIRST else h @ np.diag(s)
+    x = y_target @ r.T
+    y = x @ r                                        # what the oracle should rotate x to
+    out = oracle.fwht_quant_groups(x, seed, flags, group)
+    assert out["q"].shape == (3, n // 2) and out["scales"].shape == (3, ng)
+    codes = _unpack_np(out["q"], n)
+    for row in range(3):
+        for g in range(ng):
+            yg = y[row, g * group:(g + 1) * group]
+            sc = np.abs(yg).max() / 7.0
+            assert out["scales"][row, g] == np.float32(sc)
+            for j in range(group):
+                rr = yg[j] / sc
+                if abs(abs(rr - np.floor(rr)) - 0.5) < 1e-9:
+                    continue                         # rounding-order tie: either code is right
+                assert codes[row, g * group + j] == _brute_force_code(rr), (row, g, j)
+
+
 def _unpack_np(packed, K):
     b = packed.astype(np.int64)
     nib = np.stack([b & 15, b >> 4], axis=-1).reshape(packed.shape[0], K)
