@@ -100,6 +100,28 @@ def _dev(*tensors):
     return dev
 
 
+def _expect(t, name: str, shape, dtypes, *, optional: bool = False):
+    """Check a tensor the caller passes in (an output buffer, a scale vector):
+    exact shape, dtype and contiguity, so that no kernel reads or writes past the
+    end of a buffer the C side cannot size-check."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    dtypes = dtypes if isinstance(dtypes, (tuple, list)) else (dtypes,)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: expected dtype {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_OUT_DTYPES = (torch.float16, torch.float32, torch.int32)
+
+
 def fwht_quant(x: torch.Tensor, seed: int, flags: int = RQ_SIGNS_FIRST, *, q=None, scales=None,
                y=None, want_y: bool = False, stream=None):
     """Rotate each row of ``x`` (rows x n; row stride may exceed n) by the
@@ -115,14 +137,17 @@ def fwht_quant(x: torch.Tensor, seed: int, flags: int = RQ_SIGNS_FIRST, *, q=Non
     if x.dtype not in (torch.float32, torch.bfloat16, torch.float16):
         raise ValueError("x must be float32, bfloat16 or float16")
     rows, n = x.shape
+    q_shape, q_dtype = ((rows, n), torch.int8) if flags & RQ_INT8_CODES else ((rows, n // 2), torch.uint8)
+    s_shape = (rows, n // 128) if flags & RQ_GROUP_SCALES else (rows,)
     if q is None:
-        q = (torch.empty(rows, n, dtype=torch.int8, device=x.device) if flags & RQ_INT8_CODES
-             else torch.empty(rows, n // 2, dtype=torch.uint8, device=x.device))
+        q = torch.empty(q_shape, dtype=q_dtype, device=x.device)
     if scales is None:
-        scales = (torch.empty(rows, n // 128, dtype=torch.float32, device=x.device) if flags & RQ_GROUP_SCALES
-                  else torch.empty(rows, dtype=torch.float32, device=x.device))
+        scales = torch.empty(s_shape, dtype=torch.float32, device=x.device)
     if want_y and y is None:
         y = torch.empty(rows, n, dtype=torch.float32, device=x.device)
+    _expect(q, "q", q_shape, q_dtype)
+    _expect(scales, "scales", s_shape, torch.float32)
+    _expect(y, "y", (rows, n), torch.float32, optional=True)
     _dev(x, q, scales, y)
     with torch.cuda.device(x.device):
         st = lib.rq_fwht_quant(_ptr(x), _DTYPES[x.dtype], rows, n, x.stride(0), seed, flags,
@@ -146,6 +171,10 @@ def w4a4_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_d
     K = 2 * kb
     if out is None:
         out = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
+    _expect(out, "out", (M, N), _OUT_DTYPES)
+    raw = out.dtype == torch.int32       # raw accumulators: the scales are not read
+    _expect(a_scales, "a_scales", (M,), torch.float32, optional=raw)
+    _expect(w_scales, "w_scales", (N,), torch.float32, optional=raw)
     _dev(a_q, w_q, a_scales, w_scales, out)
     with torch.cuda.device(a_q.device):
         st = lib.rq_w4a4_gemm(_ptr(a_q), _ptr(a_scales), _ptr(w_q), _ptr(w_scales), M, N, K, seed, 0,
@@ -173,6 +202,10 @@ def kv_rotate_quant(k, v, seed: int, flags: int = RQ_SIGNS_FIRST, *, out=None, s
         if v is not None:
             out["vq"] = torch.empty(T, H, D // 2, dtype=torch.uint8, device=ref.device)
             out["vs"] = torch.empty(T, H, dtype=torch.float32, device=ref.device)
+    for src, qk, sk in ((k, "kq", "ks"), (v, "vq", "vs")):
+        if src is not None:
+            _expect(out.get(qk), f"out[{qk!r}]", (T, H, D // 2), torch.uint8)
+            _expect(out.get(sk), f"out[{sk!r}]", (T, H), torch.float32)
     _dev(k, v, *out.values())
     with torch.cuda.device(ref.device):
         st = lib.rq_kv_rotate_quant(_ptr(k), _ptr(v), _DTYPES[ref.dtype], T, H, D, seed, flags,
@@ -197,8 +230,14 @@ def fwht_quant_gemm(x: torch.Tensor, seed: int, flags: int, w_q: torch.Tensor, w
     N, kb = w_q.shape
     if kb * 2 != K or w_q.dtype != torch.uint8 or not w_q.is_contiguous():
         raise ValueError("w_q must be contiguous uint8 with K/2 columns")
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("x must be bfloat16 or float16")
     if out is None:
         out = torch.empty(M, N, dtype=out_dtype, device=x.device)
+    _expect(out, "out", (M, N), _OUT_DTYPES)
+    _expect(w_scales, "w_scales", (N,), torch.float32, optional=out.dtype == torch.int32)
+    _expect(a_q, "a_q", (M, K // 2), torch.uint8, optional=True)
+    _expect(a_scales, "a_scales", (M,), torch.float32, optional=True)
     _dev(x, w_q, w_scales, out, a_q, a_scales)
     with torch.cuda.device(x.device):
         st = lib.rq_fwht_quant_gemm(_ptr(x), _DTYPES[x.dtype], M, K, x.stride(0), seed, flags, _ptr(w_q),
@@ -227,8 +266,11 @@ def attn_decode(q: torch.Tensor, cache: dict, seed: int, flags: int = RQ_SIGNS_F
             raise ValueError("cache tensors must be contiguous with the kv_rotate_quant layout")
     if softmax_scale is None:
         softmax_scale = D ** -0.5
+    if q.dtype not in (torch.float32, torch.bfloat16, torch.float16):
+        raise ValueError("q must be float32, bfloat16 or float16")
     if out is None:
         out = torch.empty(M, H, D, dtype=torch.float32, device=q.device)
+    _expect(out, "out", (M, H, D), torch.float32)
     _dev(q, kq, ks, vq, vs, out)
     with torch.cuda.device(q.device):
         st = lib.rq_attn_decode(_ptr(q), _DTYPES[q.dtype], M, H, D, _ptr(kq), _ptr(ks), _ptr(vq), _ptr(vs), T,
@@ -247,9 +289,17 @@ def w4a8_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_d
     N, kb = w_q.shape
     if kb * 2 != K or a_q.dtype != torch.int8 or w_q.dtype != torch.uint8:
         raise ValueError("a_q must be int8 (M x K), w_q uint8 (N x K/2)")
-    group = K if w_scales is None or w_scales.dim() == 1 else K // w_scales.shape[1]
+    if not (a_q.is_contiguous() and w_q.is_contiguous()):
+        raise ValueError("a_q and w_q must be contiguous")
+    per_group = w_scales is not None and w_scales.dim() == 2 and w_scales.shape[1] != 1
+    group = 128 if per_group else K
     if out is None:
         out = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
+    _expect(out, "out", (M, N), _OUT_DTYPES)
+    raw = out.dtype == torch.int32
+    _expect(a_scales, "a_scales", (M,), torch.float32, optional=raw)
+    sw_shape = (N, K // 128) if per_group else ((N, 1) if w_scales is not None and w_scales.dim() == 2 else (N,))
+    _expect(w_scales, "w_scales", sw_shape, torch.float32, optional=raw)
     _dev(a_q, a_scales, w_q, w_scales, out)
     with torch.cuda.device(a_q.device):
         st = lib.rq_w4a8_gemm(_ptr(a_q), _ptr(a_scales), _ptr(w_q), _ptr(w_scales), M, N, K, group, _ptr(out),

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import rotational_w4a4_quantization_gb300 as rq
 from rotational_w4a4_quantization_gb300 import build as rq_build
@@ -218,3 +219,128 @@ def test_selftest_limit_checks(lib, limit, expect):
     lib.rq_selftest_wait_timeout.restype = ctypes.c_int32
     lib.rq_selftest_wait_timeout.argtypes = [ctypes.c_int64, ctypes.c_void_p]
     assert lib.rq_selftest_wait_timeout(limit, NULL) == expect
+
+
+# --------------------------------------------------------------------------
+# The Python binding checks every buffer the caller passes in (shape, dtype,
+# contiguity) before it reaches the C side, which cannot size-check a pointer.
+# These run on CPU tensors: the buffer checks come before the device check.
+# --------------------------------------------------------------------------
+
+def _t(shape, dtype):
+    return torch.zeros(shape, dtype=dtype)
+
+
+@pytest.mark.parametrize("kw,match", [
+    (dict(q=("rows", "half", torch.uint8, -1)), "q: expected shape"),
+    (dict(q=("rows", "half", torch.int8, 0)), "q: expected dtype"),
+    (dict(scales=("rows+1", torch.float32)), "scales: expected shape"),
+    (dict(scales=("rows", torch.float16)), "scales: expected dtype"),
+    (dict(y=("rows", "n", torch.float16)), "y: expected dtype"),
+])
+def test_binding_checks_fwht_quant_buffers(lib, kw, match):
+    rows, n = 8, 256
+    x = _t((rows, n), torch.bfloat16)
+    args = {}
+    if "q" in kw:
+        _, _, dt, extra = kw["q"]
+        args["q"] = _t((rows, n // 2 + extra), dt)
+    if "scales" in kw:
+        r, dt = kw["scales"]
+        args["scales"] = _t((rows + (1 if r == "rows+1" else 0),), dt)
+    if "y" in kw:
+        args["y"] = _t((rows, n), kw["y"][2])
+    with pytest.raises(ValueError, match=match):
+        rq.fwht_quant(x, 1, rq.RQ_SIGNS_FIRST, **args)
+
+
+def test_binding_checks_fwht_quant_code_modes(lib):
+    x = _t((4, 512), torch.bfloat16)
+    with pytest.raises(ValueError, match="q: expected shape"):     # INT8 codes take n bytes per row
+        rq.fwht_quant(x, 1, rq.RQ_INT8_CODES, q=_t((4, 256), torch.int8))
+    with pytest.raises(ValueError, match="scales: expected shape"):  # one scale per group of 128
+        rq.fwht_quant(x, 1, rq.RQ_GROUP_SCALES, scales=_t((4,), torch.float32))
+    with pytest.raises(ValueError, match="q must be contiguous"):
+        rq.fwht_quant(x, 1, 1, q=_t((4, 512), torch.uint8)[:, ::2])
+
+
+@pytest.mark.parametrize("which,bad,match", [
+    ("a_scales", _t((15,), torch.float32), "a_scales: expected shape"),
+    ("a_scales", _t((16,), torch.float16), "a_scales: expected dtype"),
+    ("w_scales", _t((64, 2), torch.float32)[:, 0], "w_scales must be contiguous"),
+    ("w_scales", None, "w_scales is required"),
+    ("out", _t((16, 63), torch.float16), "out: expected shape"),
+    ("out", _t((16, 64), torch.bfloat16), "out: expected dtype"),
+])
+def test_binding_checks_gemm_buffers(lib, which, bad, match):
+    M, N, K = 16, 64, 256
+    args = dict(a_q=_t((M, K // 2), torch.uint8), a_scales=_t((M,), torch.float32),
+                w_q=_t((N, K // 2), torch.uint8), w_scales=_t((N,), torch.float32))
+    out = None
+    if which == "out":
+        out = bad
+    else:
+        args[which] = bad
+    with pytest.raises(ValueError, match=match):
+        rq.w4a4_gemm(args["a_q"], args["a_scales"], args["w_q"], args["w_scales"], out=out)
+
+
+def test_binding_gemm_raw_mode_needs_no_scales(lib):
+    # int32 accumulators do not read the scales: None passes the buffer checks
+    # and stops at the device check (CPU tensors)
+    with pytest.raises(ValueError, match="CUDA"):
+        rq.w4a4_gemm(_t((16, 128), torch.uint8), None, _t((64, 128), torch.uint8), None,
+                     out=_t((16, 64), torch.int32))
+
+
+@pytest.mark.parametrize("key,shape,dtype,match", [
+    ("kq", (4, 2, 63), torch.uint8, "out\\['kq'\\]: expected shape"),
+    ("ks", (4, 2), torch.float64, "out\\['ks'\\]: expected dtype"),
+    ("vq", (4, 2, 64), torch.int8, "out\\['vq'\\]: expected dtype"),
+    ("vs", (4, 3), torch.float32, "out\\['vs'\\]: expected shape"),
+])
+def test_binding_checks_kv_buffers(lib, key, shape, dtype, match):
+    T, H, D = 4, 2, 128
+    k, v = _t((T, H, D), torch.bfloat16), _t((T, H, D), torch.bfloat16)
+    out = {"kq": _t((T, H, D // 2), torch.uint8), "ks": _t((T, H), torch.float32),
+           "vq": _t((T, H, D // 2), torch.uint8), "vs": _t((T, H), torch.float32)}
+    out[key] = _t(shape, dtype)
+    with pytest.raises(ValueError, match=match):
+        rq.kv_rotate_quant(k, v, 1, out=out)
+    del out["kq"]
+    with pytest.raises(ValueError, match="is required"):
+        rq.kv_rotate_quant(k, None if key.startswith("v") else v, 1, out=out)
+
+
+@pytest.mark.parametrize("which,bad,match", [
+    ("out", _t((4, 127), torch.float16), "out: expected shape"),
+    ("a_q", _t((4, 2047), torch.uint8), "a_q: expected shape"),
+    ("a_scales", _t((4,), torch.int32), "a_scales: expected dtype"),
+    ("w_scales", _t((129,), torch.float32), "w_scales: expected shape"),
+])
+def test_binding_checks_fused_buffers(lib, which, bad, match):
+    M, K, N = 4, 4096, 128
+    kw = dict(out=None, a_q=None, a_scales=None)
+    ws = _t((N,), torch.float32)
+    if which == "w_scales":
+        ws = bad
+    else:
+        kw[which] = bad
+    with pytest.raises(ValueError, match=match):
+        rq.fwht_quant_gemm(_t((M, K), torch.bfloat16), 1, 1, _t((N, K // 2), torch.uint8), ws, **kw)
+
+
+def test_binding_checks_attn_and_w4a8_buffers(lib):
+    M, H, D, T = 2, 4, 128, 16
+    cache = {"kq": _t((T, H, D // 2), torch.uint8), "ks": _t((T, H), torch.float32),
+             "vq": _t((T, H, D // 2), torch.uint8), "vs": _t((T, H), torch.float32)}
+    with pytest.raises(ValueError, match="out: expected shape"):
+        rq.attn_decode(_t((M, H, D), torch.bfloat16), cache, 1, out=_t((M, H, D - 1), torch.float32))
+    Mw, N, K = 8, 256, 512
+    aq, wq = _t((Mw, K), torch.int8), _t((N, K // 2), torch.uint8)
+    with pytest.raises(ValueError, match="w_scales: expected shape"):      # per-group: (N, K/128)
+        rq.w4a8_gemm(aq, _t((Mw,), torch.float32), wq, _t((N, K // 128 + 1), torch.float32))
+    with pytest.raises(ValueError, match="a_scales: expected shape"):
+        rq.w4a8_gemm(aq, _t((Mw + 1,), torch.float32), wq, _t((N,), torch.float32))
+    with pytest.raises(ValueError, match="out: expected dtype"):
+        rq.w4a8_gemm(aq, _t((Mw,), torch.float32), wq, _t((N,), torch.float32), out=_t((Mw, N), torch.int64))
