@@ -6,14 +6,22 @@ One step = one pass of the whole online path over one batch of synthetic input:
   3. rq_kv_rotate_quant K, V ([tokens][heads][head_dim] bf16) -> packed INT4 cache
 The weights are folded and quantized once, before timing (the offline step).
 
-Default workload: "prefill" -- X 2048 x 4096 bf16 (0.1% outlier channels x100),
-GEMM 2048 x 4096 -> 14336, plus the KV write of 8192 tokens x 32 heads x 128.
+Default workload: "large" -- X 4096 x 8192 bf16 (0.1% outlier channels x100),
+GEMM 4096 x 8192 -> 28672, plus the KV write of 8192 tokens x 32 heads x 128 (the
+largest configuration that runs on one GPU).  "prefill" (2048 x 4096 -> 14336),
+"decode" and "tiny" are also available.
 
 Output: one JSON line.  `value` is the W4A4 layer's integer-op throughput over
 the whole step (2*M*N*K per step / step time, TOPS); the per-kernel figures
 (GB/s of the rotation kernels, TOPS of the GEMM, roofline fractions) are in
 `kernels`.  L2 is flushed (a 2x-L2 buffer is written) between timed steps,
-outside the timed events.
+outside the timed events.  Before the timed steps the same step runs back to back
+for about a second (a clock soak) while nvidia-smi samples the clocks, so that the
+clock record covers the GPU under this load; the timed steps are sampled too.
+
+`parity` reports, on a sample of the step's rows, the codes that differ from the
+oracle's (all inside the half-integer tie window, or the run fails) and the worst
+per-row relative error of the rotated rows.
 
 `--impl reference` times the CPU oracle instead (on a bounded sample of each
 step's work, scaled to the same unit); it is the reference arm of this repo.
@@ -48,13 +56,35 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 4.5 / 2.25   # nominal dense ratio (fp8 / bf16) on GB300
 SLEEP_CYCLES = 400_000       # ~0.2 ms GPU-side pause between timed steps
 
-# DRAM bytes (read + write) per launch from one ncu capture of the current kernel
-# on the prefill shapes (see the summaries in profiles/); None once a kernel changes.
+# DRAM bytes (read + write) per launch of each kernel at each workload, from one
+# ncu capture of the kernel as it is now (dram__bytes_read.sum +
+# dram__bytes_write.sum); None where no capture of the current kernel exists.
 NCU_TRAFFIC = {
-    "w4a4_gemm": 33_695_744 + 6_113_024,
-    "fwht_quant": None,
-    "kv_rotate_quant": None,
+    ("w4a4_gemm", "prefill"): None,
+    ("w4a4_gemm", "large"): None,
+    ("fwht_quant", "prefill"): None,
+    ("fwht_quant", "large"): None,
+    ("kv_rotate_quant", "kv"): None,
 }
+PROBE_MMAS_PER_SM = 200_000   # FP8 tensor-pipe probe: ~0.1 s of back-to-back MMAs
+
+
+def host_info():
+    """Host cores and CPU model (the oracle's baseline is quoted with them)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except AttributeError:
+        usable = os.cpu_count()
+    return {"host_cores": os.cpu_count(), "host_cores_usable": usable, "host_cpu": model}
 
 
 # --------------------------------------------------------------------------
@@ -135,7 +165,7 @@ def gpu_selector(dev, local):
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -150,7 +180,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                 "--format=csv,noheader,nounits", "-lms", "50", "-f", self.path],
                 stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -165,29 +195,42 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, timed=None):
+        """Median SM clock, max clock and throttle reasons over every sample; with
+        `timed` = (t0, t1) wall-clock seconds, also how many samples fell inside."""
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return None
-        sm, mx, reasons = [], [], set()
+        import datetime
+        sm, mx, reasons, stamps = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
+                    sm.append(float(parts[2]))
+                    mx.append(float(parts[3]))
                 except ValueError:
                     continue
-                for name, val in zip(names, parts[5:9]):
+                try:
+                    stamps.append(datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp())
+                except ValueError:
+                    stamps.append(None)
+                for name, val in zip(names, parts[6:10]):
                     if val.lower() == "active":
                         reasons.add(name)
         os.unlink(self.path)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if timed is not None:
+            inside = [c for c, t in zip(sm, stamps) if t is not None and timed[0] <= t <= timed[1]]
+            out["samples_in_timed_steps"] = len(inside)
+            if inside:
+                out["sm_mhz_timed_steps"] = statistics.median(inside)
+        return out
 
 
 # --------------------------------------------------------------------------
@@ -263,7 +306,17 @@ def run_gpu(args, work, kvw):
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(gpu_selector(dev, local)) as clk:
+        # clock soak: the same step back to back for about args.soak seconds, so
+        # that the clocks are sampled under this load (untimed)
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < args.soak:
+            for _ in range(8):
+                step()
+            torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
         t0 = time.perf_counter()
+        w0 = time.time()
         for i in range(args.steps):
             flush.fill_(float(i))
             # keep the GPU busy while the host enqueues the step, so the step's
@@ -272,8 +325,10 @@ def run_gpu(args, work, kvw):
             step(events[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        w1 = time.time()
+        time.sleep(0.15)                     # let the sampler write its last sample
     barrier()
-    clocks = clk.summary()
+    clocks = clk.summary(timed=(w0, w1))
 
     per = {"fwht": [], "gemm": [], "kv": [], "step": []}
     for ev in events:
@@ -342,6 +397,10 @@ def run_gpu(args, work, kvw):
     e2e_ops, e2e_max = aggregate(ops_step * args.steps, e2e_s)
     assert rq.sync_status() == 0
 
+    # the FP8 tensor pipe alone, at this run's clocks (after the timed steps)
+    probe = probe_f8_pipe(stream)
+    parity = parity_sample(work, kvw, x_cpu, k_cpu, v_cpu, x, k, v, aq, as_, kv_out) if rank == 0 else None
+
     if rank != 0:
         return None
 
@@ -362,17 +421,23 @@ def run_gpu(args, work, kvw):
     }
     # dominant kernel by time
     dom = max(("fwht", "gemm", "kv"), key=lambda key: avg[key])
+    kernels["w4a4_gemm"]["frac_fp8_pipe_probe"] = (gb_ops / avg["gemm"] / 1e12 / probe["tflops"]
+                                                   if probe else None)
     if dom == "gemm":
         ach = gb_ops / avg["gemm"] / 1e12
         roof = {"kernel": "w4a4_gemm", "bound": "tensor", "achieved": ach, "peak": fp8_peak,
-                "unit": "TFLOP/s", "frac": ach / fp8_peak, "traffic": NCU_TRAFFIC["w4a4_gemm"],
-                "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (fp8 dense ratio)"}
+                "unit": "TFLOP/s", "frac": ach / fp8_peak,
+                "traffic": NCU_TRAFFIC.get(("w4a4_gemm", work.name)),
+                "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (fp8 dense ratio)",
+                "fp8_pipe_probe": probe,
+                "frac_fp8_pipe_probe": ach / probe["tflops"] if probe else None}
     else:
         key = "fwht_quant" if dom == "fwht" else "kv_rotate_quant"
         b = fb if dom == "fwht" else kb
         ach = b / avg[dom] / 1e9
         roof = {"kernel": key, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC[key],
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                "traffic": NCU_TRAFFIC.get((key, work.name if key == "fwht_quant" else "kv")),
                 "peak_source": f"{peaks['source']} hbm copy"}
 
     line = {
@@ -388,10 +453,9 @@ def run_gpu(args, work, kvw):
         "vs_baseline": None,
         "dtype": "int4",
         "data": "synthetic",
-        "config": {"workload": workload_desc(work, kvw),
-                   "l2": "flushed between timed steps (2x L2 write, outside timed events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": bench_config(work, kvw, world),
         "kernels": kernels,
+        "parity": parity,
         "roofline": roof,
         "e2e": {"value": e2e_ops / e2e_max / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -402,6 +466,83 @@ def run_gpu(args, work, kvw):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(work, kvw, budget_s=args.cpu_budget)
     return line
+
+
+def probe_f8_pipe(stream):
+    """Rate of the FP8 tensor pipe alone (M128 N256 K32 MMAs back to back on every
+    SM), timed with events on `stream`: the ceiling of the pipe the GEMM runs on,
+    at this run's clocks.  Median of 3 after one warm-up."""
+    import rotational_w4a4_quantization_gb300 as rq
+    ctas = rq.probe_f8_mma(1000, stream=stream)
+    times = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ctas = rq.probe_f8_mma(PROBE_MMAS_PER_SM, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    if rq.sync_status() != 0:
+        return None
+    t = statistics.median(times)
+    flops = 2 * 128 * 256 * 32 * PROBE_MMAS_PER_SM * ctas
+    return {"tflops": flops / t / 1e12, "mmas_per_sm": PROBE_MMAS_PER_SM, "ctas": ctas,
+            "shape": "M128 N256 K32 kind::f8f6f4 (e4m3), zeros in shared memory"}
+
+
+def parity_sample(work, kvw, x_cpu, k_cpu, v_cpu, x, k, v, aq, as_, kv_out, rows=64, kv_tokens=64):
+    """Codes of a sample of the step's rows against the oracle's (first and last
+    `rows` activation rows, first and last `kv_tokens` tokens of K and V): the
+    number of codes that differ (each must lie in the half-integer tie window and
+    differ by one, else this raises), and the worst per-row relative error of the
+    rotated rows, read back through the fp32 output of a separate call."""
+    import oracle
+    import rotational_w4a4_quantization_gb300 as rq
+
+    def decode(packed):
+        b = packed.astype(np.int16)
+        nib = np.stack([b & 15, b >> 4], axis=-1).reshape(packed.shape[0], -1)
+        return np.where(nib >= 8, nib - 16, nib)
+
+    def diff_count(gq, ref):
+        g, r = decode(gq), decode(ref["q"])
+        d = g != r
+        tie = oracle.tie_mask(ref["ratio"])
+        bad = d & ~(tie & (np.abs(g - r) == 1))
+        if bad.any():
+            raise AssertionError(f"{int(bad.sum())} sampled codes differ outside the tie window")
+        return int(d.sum()), int(tie.sum())
+
+    oracle.build()
+    seed, flags = synth.SIGN_SEED, 1
+    M, n = x_cpu.shape
+    sel = np.unique(np.r_[np.arange(min(rows, M)), np.arange(max(0, M - rows), M)])
+    ref = oracle.fwht_quant(x_cpu[sel].double().numpy(), seed, flags, want_y=True, want_ratio=True)
+    a_diff, a_tie = diff_count(aq[torch.from_numpy(sel).to(aq.device)].cpu().numpy(), ref)
+    _, _, ygpu = rq.fwht_quant(x[torch.from_numpy(sel).to(x.device)].contiguous(), seed, flags, want_y=True)
+    yg = ygpu.cpu().double().numpy()
+    err = (np.abs(yg - ref["y"]).max(axis=1) / np.abs(ref["y"]).max(axis=1)).max()
+    T, H, D = k_cpu.shape
+    tsel = np.unique(np.r_[np.arange(min(kv_tokens, T)), np.arange(max(0, T - kv_tokens), T)])
+    kv_diff, kv_tie = 0, 0
+    for src, qk in ((k_cpu, "kq"), (v_cpu, "vq")):
+        rr = oracle.fwht_quant(src[tsel].reshape(-1, D).double().numpy(), seed, flags, want_ratio=True)
+        dd, tt = diff_count(kv_out[qk][torch.from_numpy(tsel).to(k.device)].reshape(-1, D // 2).cpu().numpy(), rr)
+        kv_diff += dd
+        kv_tie += tt
+    return {"activation_rows": int(sel.size), "activation_codes": int(sel.size) * n,
+            "activation_codes_differing": a_diff, "activation_codes_in_tie_window": a_tie,
+            "fwht_max_row_rel_err": float(err), "fwht_tolerance": 1e-5,
+            "kv_vectors": int(tsel.size) * H * 2, "kv_codes_differing": kv_diff, "kv_codes_in_tie_window": kv_tie,
+            "tie_window": 1e-4,
+            "gemm": "bit-exact int32 on the full output of every workload: GPU tests (oracle over row blocks)"}
+
+
+def bench_config(work, kvw, world):
+    """The `config` object, the same for both arms."""
+    return {"workload": workload_desc(work, kvw),
+            "l2": "flushed between timed steps (2x L2 write, outside timed events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "none (one process)"}
 
 
 # --------------------------------------------------------------------------
@@ -441,7 +582,7 @@ def cpu_baseline(work, kvw, budget_s=15.0):
     return {"value": ops / step_s / 1e12, "unit": "TOPS", "cores": 1, "kind": "oracle",
             "sample": f"oracle (fp64 C, 1 thread) on {gemm_rows} GEMM rows, 64 rotation rows, "
                       f"256 KV tokens; scaled by rows to one full step",
-            "step_seconds_extrapolated": step_s, "parts_s": parts}
+            "step_seconds_extrapolated": step_s, "parts_s": parts, **host_info()}
 
 
 def workload_desc(work, kvw):
@@ -472,10 +613,11 @@ def run_reference(args, work, kvw):
         "full_step_ms_extrapolated": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4",
         "data": "synthetic",
-        "config": {"workload": workload_desc(work, kvw), "parallelism": "host cores (oracle)"},
+        "config": bench_config(work, kvw, world),
         "cpu_baseline": {"value": value, "unit": "TOPS", "cores": 1, "kind": "oracle",
                          "sample": f"each step: {gemm_rows} GEMM rows, 16 rotation rows, 64 KV tokens, "
-                                   "scaled by rows to one full step"},
+                                   "scaled by rows to one full step; one host core",
+                         **host_info()},
         "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -486,7 +628,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["rq", "reference"], default="rq")
-    ap.add_argument("--workload", choices=["prefill", "large", "decode", "tiny"], default="prefill")
+    ap.add_argument("--workload", choices=["prefill", "large", "decode", "tiny"], default="large")
+    ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed steps while clocks are sampled")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args(argv)

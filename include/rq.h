@@ -322,6 +322,23 @@ rq_status rq_sync_status(void *stream);
  */
 rq_status rq_selftest_wait_timeout(int64_t limit_cycles, void *stream);
 
+/*
+ * rq_probe_f8_mma -- measure the tensor pipe that the W4A4 products run on.
+ *
+ *   Not an operation of the method (the pages have no counterpart): a
+ *   measurement aid for reporting the GEMMs against their own pipe.  One CTA per
+ *   SM issues `mmas_per_sm` back-to-back tcgen05.mma kind::f8f6f4 instructions
+ *   of shape M128 N256 K32 (E4M3 operands of zeros in shared memory, fp32
+ *   accumulator in tensor memory), each 2 * 128 * 256 * 32 = 2,097,152
+ *   floating-point operations, then waits (bounded) for them.  Time the call on
+ *   `stream` with events: rate = 2097152 * mmas_per_sm * (*ctas) / time.
+ *   mmas_per_sm  1 .. 2^30.
+ *   ctas         out (may be NULL): CTAs launched (the SM count).
+ *   Errors: RQ_ERR_INVALID_ARG (count out of range), RQ_ERR_CUDA (launch); a
+ *   wait that gives up sets the error word that rq_sync_status reads.
+ */
+rq_status rq_probe_f8_mma(int64_t mmas_per_sm, int32_t *ctas, void *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *rq_status_string(rq_status status);
 

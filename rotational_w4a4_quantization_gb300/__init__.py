@@ -21,7 +21,9 @@ Entry points (same names as the C ABI):
   scales;
 * :func:`sync_status` -- drain a stream and read (and clear) the device error
   word that bounded waits raise; :func:`selftest_wait_timeout` makes one such
-  wait run out on purpose, to exercise that path.
+  wait run out on purpose, to exercise that path;
+* :func:`probe_f8_mma` -- a measurement aid: back-to-back FP8 MMAs on every SM,
+  the rate of the tensor pipe the W4A4 products run on.
 """
 from ._binding import (  # noqa: F401
     RQ_ATTN_ROTATED_OUT,
@@ -35,6 +37,7 @@ from ._binding import (  # noqa: F401
     kv_rotate_quant,
     library_path,
     load_library,
+    probe_f8_mma,
     selftest_wait_timeout,
     sync_status,
     w4a4_gemm,
@@ -42,6 +45,6 @@ from ._binding import (  # noqa: F401
 )
 
 __all__ = ["RQ_ATTN_ROTATED_OUT", "RQ_GROUP_SCALES", "RQ_INT8_CODES", "RQ_SIGNS_FIRST", "RQError", "attn_decode",
-           "fwht_quant", "fwht_quant_gemm", "kv_rotate_quant", "library_path", "load_library", "selftest_wait_timeout",
+           "fwht_quant", "fwht_quant_gemm", "kv_rotate_quant", "library_path", "load_library", "probe_f8_mma", "selftest_wait_timeout",
            "sync_status",
            "w4a4_gemm", "w4a8_gemm"]

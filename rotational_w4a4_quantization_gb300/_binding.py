@@ -64,6 +64,8 @@ def load_library() -> ctypes.CDLL:
     lib.rq_sync_status.argtypes = [P]
     lib.rq_selftest_wait_timeout.restype = i32
     lib.rq_selftest_wait_timeout.argtypes = [i64, P]
+    lib.rq_probe_f8_mma.restype = i32
+    lib.rq_probe_f8_mma.argtypes = [i64, P, P]
     lib.rq_status_string.restype = ctypes.c_char_p
     lib.rq_status_string.argtypes = [i32]
     lib.rq_version.restype = u32
@@ -317,3 +319,11 @@ def selftest_wait_timeout(limit_cycles: int, stream=None) -> None:
     """Launch the failure-detection self-test: a bounded device wait on a barrier
     that nothing arrives on.  The next :func:`sync_status` returns RQ_ERR_TIMEOUT."""
     _check("rq_selftest_wait_timeout", load_library().rq_selftest_wait_timeout(int(limit_cycles), _stream(stream)))
+
+
+def probe_f8_mma(mmas_per_sm: int, stream=None) -> int:
+    """Enqueue the tensor-pipe probe (back-to-back M128 N256 K32 FP8 MMAs, one CTA
+    per SM); returns the number of CTAs.  Each MMA is 2,097,152 operations."""
+    ctas = ctypes.c_int32(0)
+    _check("rq_probe_f8_mma", load_library().rq_probe_f8_mma(int(mmas_per_sm), ctypes.byref(ctas), _stream(stream)))
+    return int(ctas.value)

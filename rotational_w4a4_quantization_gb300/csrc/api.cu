@@ -201,6 +201,14 @@ rq_status rq_selftest_wait_timeout(int64_t limit_cycles, void *stream) {
     return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }
 
+rq_status rq_probe_f8_mma(int64_t mmas_per_sm, int32_t *ctas, void *stream) {
+    if (mmas_per_sm < 1 || mmas_per_sm > (int64_t(1) << 30)) return RQ_ERR_INVALID_ARG;
+    int n = 0;
+    cudaError_t e = rq::launch_f8_mma_probe((long long)mmas_per_sm, &n, static_cast<cudaStream_t>(stream));
+    if (ctas) *ctas = n;
+    return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+}
+
 rq_status rq_sync_status(void *stream) {
     int word = 0;
     cudaError_t e = rq::read_and_clear_error_word(&word, static_cast<cudaStream_t>(stream));

@@ -77,6 +77,10 @@ cudaError_t launch_w4a8_gemm(const int8_t *aq, const float *sa, const uint8_t *w
 // kernels' bounded wait and the given limit: raises the error word on expiry.
 cudaError_t launch_wait_timeout_selftest(long long limit_cycles, cudaStream_t stream);
 
+// Tensor-pipe rate probe: one CTA per SM issues `mmas_per_sm` M128 N256 K32
+// kind::f8f6f4 MMAs; *ctas receives the grid size.
+cudaError_t launch_f8_mma_probe(long long mmas_per_sm, int *ctas, cudaStream_t stream);
+
 // Device-resident error word set by bounded waits that gave up.
 cudaError_t read_and_clear_error_word(int *value, cudaStream_t stream);
 int *error_word_device_ptr();

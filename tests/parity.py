@@ -12,6 +12,10 @@ Tolerances (stated by the acceptance criteria of the hot path):
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -81,3 +85,42 @@ def compare_f16(gpu: np.ndarray, ref: np.ndarray, atol=0.0):
     big = np.abs(ref) > 65504
     ok |= big & np.isinf(g) & (np.sign(g) == np.sign(ref))
     assert ok.all(), f"{int((~ok).sum())} fp16 outputs off by more than one ulp"
+
+
+def host_threads() -> int:
+    """Threads for oracle runs split over row blocks: every core this process may use."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def oracle_gemm_row_blocks(aq, sa, wq, sw, M: int, N: int, K: int, threads: int | None = None):
+    """The oracle's whole W4A4 product, computed as disjoint row blocks on several
+    host threads (the oracle is single-threaded C; ctypes releases the GIL while
+    it runs, so the blocks run in parallel).  Yields (row0, acc int64, y fp64) per
+    block, in row order; the union is exactly oracle.w4a4_gemm on all M rows."""
+    threads = threads or host_threads()
+    rows_per = max(1, -(-M // threads))
+    bounds = [(r, min(M, r + rows_per)) for r in range(0, M, rows_per)]
+
+    def run(b):
+        r0, r1 = b
+        acc, y = oracle.w4a4_gemm(aq[r0:r1], sa[r0:r1], wq, sw, r1 - r0, N, K)
+        return r0, acc, y
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        for out in ex.map(run, bounds):
+            yield out
+
+
+def record(name: str, **fields):
+    """Append one JSON line to the file named by RQ_PARITY_RECORD (if set): the
+    counts a run of the parity tests is asked to report (tie-window codes, worst
+    per-row rotation error, host threads used by the oracle)."""
+    path = os.environ.get("RQ_PARITY_RECORD")
+    if not path:
+        return
+    os.makedirs(os.path.dirname(os.path.abspath(path)), exist_ok=True)
+    with open(path, "a") as f:
+        f.write(json.dumps({"test": name, **fields}) + "\n")

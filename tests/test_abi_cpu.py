@@ -344,3 +344,9 @@ def test_binding_checks_attn_and_w4a8_buffers(lib):
         rq.w4a8_gemm(aq, _t((Mw + 1,), torch.float32), wq, _t((N,), torch.float32))
     with pytest.raises(ValueError, match="out: expected dtype"):
         rq.w4a8_gemm(aq, _t((Mw,), torch.float32), wq, _t((N,), torch.float32), out=_t((Mw, N), torch.int64))
+
+
+@pytest.mark.parametrize("count,expect", [(0, 1), (-5, 1), ((1 << 30) + 1, 1)])
+def test_probe_argument_checks(lib, count, expect):
+    ctas = ctypes.c_int32(-1)
+    assert lib.rq_probe_f8_mma(count, ctypes.byref(ctas), NULL) == expect

@@ -4,7 +4,7 @@ The GEMM is fed the oracle's (or seeded random) codes, so the comparison is of
 the product alone: int32 accumulators bit-exact, fp32 dequant within 1e-5
 relative, fp16 within one ulp.  Shapes cover decode-sized and prefill-sized M,
 ragged M / N, every output mode, extreme codes, and the full-size workloads
-(checked on sampled entries against the oracle and, over the whole output, on
+(every output against the oracle, run over row blocks on all host cores, plus
 row and column sums that hold at any size).
 """
 import numpy as np
@@ -15,7 +15,7 @@ import oracle
 import rotational_w4a4_quantization_gb300 as rq
 from rotational_w4a4_quantization_gb300 import synth
 
-from parity import compare_f16, to_dev, to_np
+from parity import compare_f16, host_threads, oracle_gemm_row_blocks, record, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -113,38 +113,58 @@ def test_pipeline_codes_from_oracle_fold():
     compare_f16(out[torch.float16], y)
 
 
-def _sample_positions(M, N, count, seed):
-    rng = np.random.default_rng(seed)
-    ms = list(rng.integers(0, M, count)) + [0, M - 1, 0, M - 1, min(127, M - 1), min(128, M - 1)]
-    cs = list(rng.integers(0, N, count)) + [0, N - 1, N - 1, 0, min(255, N - 1), min(256, N - 1)]
-    return np.array(ms, np.int64), np.array(cs, np.int64)
-
-
 @pytest.mark.parametrize("name", ["decode", "prefill", "large"])
-def test_workload_full_size(name):
+def test_workload_full_output(name):
+    """Every output of the full-size decode, prefill and large products against
+    the oracle: int32 accumulators bit-exact, fp32 within 1e-5 relative, fp16
+    within one ulp.  The oracle runs over disjoint row blocks on all host cores."""
+    import time
     w = synth.WORKLOADS[name]
     M, N, K = w.rows, w.gemm_n, w.n
     aq, sa, wq, sw = _codes(M, N, K, 1000 + w.data_seed)
     d = [t.to(DEV) for t in (aq, sa, wq, sw)]
-    acc = rq.w4a4_gemm(*d, out_dtype=torch.int32)
+    acc_np = to_np(rq.w4a4_gemm(*d, out_dtype=torch.int32)).astype(np.int64)
     yf = to_np(rq.w4a4_gemm(*d, out_dtype=torch.float32))
     yh = to_np(rq.w4a4_gemm(*d, out_dtype=torch.float16))
-    ms, cs = _sample_positions(M, N, 2000, w.data_seed)
-    r_acc, r_y = oracle.w4a4_gemm_entries(aq.numpy(), sa.numpy(), wq.numpy(), sw.numpy(), K, ms, cs)
-    acc_np = to_np(acc).astype(np.int64)
-    np.testing.assert_array_equal(acc_np[ms, cs], r_acc)
-    np.testing.assert_allclose(yf[ms, cs], r_y, rtol=1e-5, atol=0)
-    compare_f16(yh[ms, cs], r_y)
-    # Whole-output properties: sum_c acc[m,c] = a_m . (sum_c w_c) and
+    assert rq.sync_status() == 0
+    a_np, sa_np, w_np, sw_np = aq.numpy(), sa.numpy(), wq.numpy(), sw.numpy()
+    threads = host_threads()
+    t0 = time.perf_counter()
+    for r0, r_acc, r_y in oracle_gemm_row_blocks(a_np, sa_np, w_np, sw_np, M, N, K, threads):
+        r1 = r0 + r_acc.shape[0]
+        np.testing.assert_array_equal(acc_np[r0:r1], r_acc)
+        np.testing.assert_allclose(yf[r0:r1], r_y, rtol=1e-5, atol=0)
+        compare_f16(yh[r0:r1], r_y)
+    record("gemm_full_output", workload=name, M=M, N=N, K=K, outputs=M * N, host_threads=threads,
+           oracle_seconds=round(time.perf_counter() - t0, 2))
+    # Whole-output properties as well: sum_c acc[m,c] = a_m . (sum_c w_c) and
     # sum_m acc[m,c] = (sum_m a_m) . w_c, from the oracle's code decoding.
-    a = oracle.unpack(aq.numpy(), K)
-    wc = oracle.unpack(wq.numpy(), K)
+    a = oracle.unpack(a_np, K)
+    wc = oracle.unpack(w_np, K)
     a_sum = a.sum(axis=0, dtype=np.int64)
     w_sum = wc.sum(axis=0, dtype=np.int64)
     row_ref = np.concatenate([a[i:i + 512].astype(np.int64) @ w_sum for i in range(0, M, 512)])
     col_ref = np.concatenate([wc[i:i + 512].astype(np.int64) @ a_sum for i in range(0, N, 512)])
     np.testing.assert_array_equal(acc_np.sum(axis=1), row_ref)
     np.testing.assert_array_equal(acc_np.sum(axis=0), col_ref)
+
+
+def test_full_output_on_oracle_codes_prefill():
+    """The prefill product on the oracle's own codes of the workload (rotated and
+    quantized activations, folded and quantized weights), every output compared."""
+    w = synth.PREFILL
+    M, N, K = w.rows, w.gemm_n, w.n
+    x = synth.activations(M, K, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor)
+    wt = synth.weights_t(N, K, w.weight_seed, w.w_std)
+    xa = oracle.fwht_quant(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+    wf = oracle.fwht_quant(wt.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+    d = [torch.from_numpy(a).to(DEV) for a in (xa["q"], xa["scales"], wf["q"], wf["scales"])]
+    acc_np = to_np(rq.w4a4_gemm(*d, out_dtype=torch.int32)).astype(np.int64)
+    yf = to_np(rq.w4a4_gemm(*d, out_dtype=torch.float32))
+    for r0, r_acc, r_y in oracle_gemm_row_blocks(xa["q"], xa["scales"], wf["q"], wf["scales"], M, N, K):
+        r1 = r0 + r_acc.shape[0]
+        np.testing.assert_array_equal(acc_np[r0:r1], r_acc)
+        np.testing.assert_allclose(yf[r0:r1], r_y, rtol=1e-5, atol=0)
 
 
 def test_repeatable_bitwise():
