@@ -63,8 +63,8 @@ NCU_TRAFFIC = {
     ("w4a4_gemm", "prefill"): None,
     ("w4a4_gemm", "large"): None,
     ("fwht_quant", "prefill"): None,
-    ("fwht_quant", "large"): None,
-    ("kv_rotate_quant", "kv"): None,
+    ("fwht_quant", "large"): 67_167_232 + 1_138_688,      # codes mostly still in L2 at kernel end
+    ("kv_rotate_quant", "kv"): 134_263_040 + 14_430_720,
 }
 PROBE_MMAS_PER_SM = 200_000   # FP8 tensor-pipe probe: ~0.1 s of back-to-back MMAs
 

@@ -172,6 +172,13 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
  *             RQ_F32  the dequantized product in fp32;
  *             RQ_I32  the raw int32 accumulators (scales unused, may be NULL).
  *             N * sizeof(y_dtype) must be a multiple of 16 bytes.
+ *   Kernels (all on tensor cores, the integer sums exact in each):
+ *     M > 64: persistent CTA pairs, 256 x 256 tiles, codes widened to FP8
+ *       (tcgen05 kind::f8f6f4), tiles walked M-fastest for L2 reuse of W;
+ *     M <= 64, N a multiple of 128, K <= 8192: weights in tensor memory as
+ *       the MMA's 128-row side, tokens as its N side, K split over thread-block
+ *       clusters of up to 8 CTAs reduced in distributed shared memory;
+ *     other shapes: legacy FP8 mma.sync, CTAs of 16 channels x 64 tokens.
  */
 rq_status rq_w4a4_gemm(const uint8_t *a_q, const float *a_scales, const uint8_t *w_q,
                        const float *w_scales, int64_t M, int64_t N, int64_t K, uint64_t seed,
@@ -212,7 +219,8 @@ rq_status rq_kv_rotate_quant(const void *k, const void *v, rq_dtype dtype, int64
  *
  *   x         [M][ld_x] activation rows, bf16 or fp16 (x_dtype), ld_x >= K.
  *   M         1 <= M <= 16 (decode batches).
- *   K         the row length; 4096 only (RQ_ERR_UNSUPPORTED otherwise).
+ *   K         the row length: 1024, 2048, 4096 or 8192 (RQ_ERR_UNSUPPORTED
+ *             otherwise).
  *   seed, flags   as for rq_fwht_quant; must match the fold of w_q.
  *   w_q, w_scales, N   as for rq_w4a4_gemm; N a multiple of 128.
  *   y, y_dtype as for rq_w4a4_gemm (RQ_F16, RQ_F32, or RQ_I32 raw accumulators).
@@ -221,9 +229,12 @@ rq_status rq_kv_rotate_quant(const void *k, const void *v, rq_dtype dtype, int64
  *   Errors: as for rq_fwht_quant and rq_w4a4_gemm (RQ_ERR_INVALID_ARG,
  *   RQ_ERR_UNSUPPORTED for a shape or dtype outside the above,
  *   RQ_ERR_MISALIGNED for pointers or a row stride off their 16-byte rules);
- *   M == 0 or N == 0 returns RQ_OK without a launch.  The launch has N/32
- *   CTAs in thread-block clusters of 4, ~186 KB of shared memory each; a
- *   bounded wait that gives up sets the error word that rq_sync_status reads.
+ *   M == 0 or N == 0 returns RQ_OK without a launch.  The launch has N/128
+ *   thread-block clusters of S = 1, 2, 4 or 8 CTAs (S >= K/1024), one CTA per
+ *   SM: the CTAs of a cluster split K, rotate the tokens between them and
+ *   exchange the codes in distributed shared memory; the product runs on the
+ *   5th-generation tensor cores (weights in tensor memory).  A bounded wait that
+ *   gives up sets the error word that rq_sync_status reads.
  */
 rq_status rq_fwht_quant_gemm(const void *x, rq_dtype x_dtype, int64_t M, int64_t K, int64_t ld_x,
                              uint64_t seed, uint32_t flags, const uint8_t *w_q, const float *w_scales,

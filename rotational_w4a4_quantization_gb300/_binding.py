@@ -220,7 +220,8 @@ def kv_rotate_quant(k, v, seed: int, flags: int = RQ_SIGNS_FIRST, *, out=None, s
 def fwht_quant_gemm(x: torch.Tensor, seed: int, flags: int, w_q: torch.Tensor, w_scales, *,
                     out_dtype=torch.float16, out=None, a_q=None, a_scales=None, stream=None):
     """Decode-sized fusion of :func:`fwht_quant` and :func:`w4a4_gemm`: x (M x K,
-    bf16/fp16, unit stride in the last dimension; M <= 16, K = 4096) is rotated,
+    bf16/fp16, unit stride in the last dimension; M <= 16, K = 1024, 2048, 4096 or
+    8192) is rotated,
     quantized and multiplied by w_q (N x K/2 packed codes, N a multiple of 128)
     in one launch.  Returns y (M x N, out_dtype float16 / float32 / int32 raw
     accumulators); a_q (M x K/2) and a_scales (M,), when given, receive the

@@ -56,8 +56,9 @@ cudaError_t read_and_clear_error_word(int *value, cudaStream_t stream) {
 }
 
 cudaError_t launch_w4a4_gemm(const GemmArgs &g, cudaStream_t stream) {
-    if (w4a4_gemm_tc_supported(g)) return launch_w4a4_gemm_tc(g, stream);
-    return launch_w4a4_gemm_small(g, stream);
+    if (w4a4_gemm_tc_supported(g)) return launch_w4a4_gemm_tc(g, stream);                 // M > 64
+    if (w4a4_gemm_decode_tc_supported(g)) return launch_w4a4_gemm_decode_tc(g, stream);   // M <= 64
+    return launch_w4a4_gemm_small(g, stream);   // N not a multiple of 128, or K > 8192
 }
 
 }  // namespace rq
@@ -153,7 +154,7 @@ rq_status rq_fwht_quant_gemm(const void *x, rq_dtype x_dtype, int64_t M, int64_t
     if ((ld_x * rq::elem_size(x_dtype)) % 16 != 0) return RQ_ERR_MISALIGNED;
     if ((N * rq::elem_size(y_dtype)) % 16 != 0) return RQ_ERR_MISALIGNED;
     const int y_mode = y_dtype == RQ_F16 ? 0 : (y_dtype == RQ_F32 ? 1 : 2);
-    cudaError_t e = rq::launch_fused_decode(x, (int)x_dtype, M, ld_x, seed, flags, w_q, w_scales, N, y, y_mode,
+    cudaError_t e = rq::launch_fused_decode(x, (int)x_dtype, M, ld_x, seed, flags, w_q, w_scales, N, K, y, y_mode,
                                             a_q, a_scales, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace rq {
@@ -46,11 +47,25 @@ struct GemmArgs {
 
 cudaError_t launch_w4a4_gemm(const GemmArgs &args, cudaStream_t stream);
 
-// Fused decode path (rotation + quantization + W4A4 product in one launch).
+// Decode-sized products on the tensor cores (M <= 64 tokens, N a multiple of
+// 128, K a multiple of 128 up to 8192): weights in tensor memory, split along K
+// over a thread-block cluster.
+bool w4a4_gemm_decode_tc_supported(const GemmArgs &args);
+cudaError_t launch_w4a4_gemm_decode_tc(const GemmArgs &args, cudaStream_t stream);
+
+// Host helpers shared by the tensor-core kernels: a 2-D TMA map over a byte
+// matrix (rows x row_bytes, row stride row_bytes) with boxes of box_rows x
+// box_bytes; the SM count of the current device (0 on error).
+bool make_tma_map_u8(CUtensorMap *map, const void *base, int64_t rows, int64_t row_bytes, int box_bytes, int box_rows,
+                     CUtensorMapSwizzle swizzle);
+int device_sm_count();
+
+// Fused decode path (rotation + quantization + W4A4 product in one launch):
+// M <= 16 tokens, K in {1024, 2048, 4096, 8192}, N a multiple of 128.
 bool fused_decode_supported(int64_t M, int64_t K, int64_t N);
 cudaError_t launch_fused_decode(const void *x, int in_type, int64_t M, int64_t ldx, uint64_t seed, uint32_t flags,
-                                const uint8_t *wq, const float *sw, int64_t N, void *y, int y_mode, uint8_t *aq,
-                                float *as, cudaStream_t stream);
+                                const uint8_t *wq, const float *sw, int64_t N, int64_t K, void *y, int y_mode,
+                                uint8_t *aq, float *as, cudaStream_t stream);
 
 // Attention of decode queries over the rotated INT4 KV cache.
 bool attn_decode_supported(int64_t head_dim);

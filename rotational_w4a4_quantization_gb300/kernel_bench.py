@@ -6,6 +6,7 @@
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel kv
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel fused --workload decode
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel unfused --workload decode
+    python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel fused --workload large --rows 16
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel attn
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel w4a8 --workload decode
     python -m rotational_w4a4_quantization_gb300.kernel_bench --kernel w4a8 --workload prefill --group channel
@@ -49,6 +50,9 @@ def main(argv=None):
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--group", choices=["128", "channel"], default="128",
                     help="w4a8: weight scales per group of 128 or per output channel")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="gemm, fused, unfused: token rows instead of the workload's (e.g. 16 decode tokens "
+                         "through the large workload's 8192 -> 28672 layer)")
     ap.add_argument("--n", type=int, default=0,
                     help="fwht: row length instead of the workload's (e.g. 14336 = 28 x 512), same rows and recipe")
     args = ap.parse_args(argv)
@@ -110,7 +114,7 @@ def main(argv=None):
     elif args.kernel in ("fused", "unfused"):
         if not w.gemm_n or not w.rows:
             raise SystemExit(f"workload {w.name} has no activation GEMM")
-        M, K, N = w.rows, w.n, w.gemm_n
+        M, K, N = args.rows or w.rows, w.n, w.gemm_n
         x = synth.activations(M, K, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor).to(dev)
         wq, sw = synth.random_codes(N, K, 1001 + w.data_seed)
         wq, sw = wq.to(dev), sw.to(dev)
@@ -129,7 +133,7 @@ def main(argv=None):
     else:
         if not w.gemm_n:
             raise SystemExit(f"workload {w.name} has no GEMM")
-        M, K, N = w.rows, w.n, w.gemm_n
+        M, K, N = args.rows or w.rows, w.n, w.gemm_n
         aq, sa = synth.random_codes(M, K, 1000 + w.data_seed)
         wq, sw = synth.random_codes(N, K, 1001 + w.data_seed)
         d = [t.to(dev) for t in (aq, sa, wq, sw)]

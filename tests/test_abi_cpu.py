@@ -136,7 +136,9 @@ def fused(lib, x=A16, dt=1, M=16, K=4096, ld=4096, flags=1, w=A16, ws=A16, N=409
     (dict(dt=0), 2),                  # fp32 activations not offered by the fused path
     (dict(ydt=1), 2),                 # bf16 output not offered
     (dict(M=17), 2),                  # more than one m16 tile of tokens
-    (dict(K=2048, ld=2048), 2),       # the fused rotation is 4096 long
+    (dict(K=512, ld=512), 2),         # the fused rotation takes K = 1024, 2048, 4096, 8192
+    (dict(K=3072, ld=3072), 2),
+    (dict(K=16384, ld=16384), 2),
     (dict(N=4000), 2),                # N not a multiple of 128
     (dict(x=NULL), 1),
     (dict(ws=NULL), 1),

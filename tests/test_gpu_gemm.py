@@ -173,3 +173,56 @@ def test_repeatable_bitwise():
     r1 = rq.w4a4_gemm(*d, out_dtype=torch.float16)
     r2 = rq.w4a4_gemm(*d, out_dtype=torch.float16)
     assert torch.equal(r1, r2)
+
+
+# Decode-sized products (M <= 64, N a multiple of 128, K <= 8192) run on the
+# tensor-core decode kernel: weights in tensor memory, K split over a cluster of
+# 1, 2, 4 or 8 CTAs (chosen from K and the number of 128-channel tiles) whose
+# exact partials meet in distributed shared memory.  The shapes below reach
+# every split, uneven K slices (K blocks not a multiple of the split), every
+# token-tile count (16, 32, 48, 64 padded rows) and the largest slice.
+@pytest.mark.parametrize("M,N,K", [
+    (1, 128, 128),       # one CTA, one K block
+    (5, 256, 384),       # split 2, slices of 1 and 2 blocks
+    (16, 128, 1152),     # split 8, slices of 1 and 2 blocks
+    (17, 512, 4096),     # split 8, 4 blocks each, two token tiles
+    (33, 1024, 2048),    # three token tiles
+    (48, 4096, 8192),    # split 8, 8 blocks each (the largest slice)
+    (64, 2048, 1024),    # four token tiles, split 8 of one block
+    (7, 19200, 512),     # 150 channel tiles, split 1
+])
+def test_decode_tensor_core_shapes(M, N, K):
+    aq, sa, wq, sw = _codes(M, N, K, 77 + M + K)
+    out = _all_modes(aq, sa, wq, sw)
+    assert rq.sync_status() == 0
+    acc, y = oracle.w4a4_gemm(aq.numpy(), sa.numpy(), wq.numpy(), sw.numpy(), M, N, K)
+    np.testing.assert_array_equal(out[torch.int32].astype(np.int64), acc)
+    np.testing.assert_allclose(out[torch.float32], y, rtol=1e-5, atol=0)
+    compare_f16(out[torch.float16], y)
+
+
+@pytest.mark.parametrize("ba,bw", [(0x77, 0x77), (0x88, 0x88), (0x88, 0x77), (0x78, 0x87)])
+def test_decode_tensor_core_extreme_codes(ba, bw):
+    """All-extreme codes at the decode kernel's largest K (8192): every partial
+    and the cluster's integer sum stay exact."""
+    M, N, K = 16, 256, 8192
+    aq = synth.extreme_codes(M, K, ba)
+    wq = synth.extreme_codes(N, K, bw)
+    one_m, one_n = torch.ones(M), torch.ones(N)
+    acc = to_np(rq.w4a4_gemm(aq.to(DEV), one_m.to(DEV), wq.to(DEV), one_n.to(DEV), out_dtype=torch.int32))
+    ref, _ = oracle.w4a4_gemm(aq[:1].numpy(), one_m[:1].numpy(), wq[:1].numpy(), one_n[:1].numpy(), 1, 1, K)
+    assert (acc.astype(np.int64) == ref[0, 0]).all()
+
+
+def test_decode_tensor_core_large_model_width():
+    """16 tokens through the large workload's 8192 -> 28672 weights (224 channel
+    tiles, split 8: several waves of clusters), every output against the oracle."""
+    M, N, K = 16, 28672, 8192
+    aq, sa, wq, sw = _codes(M, N, K, 4242)
+    d = [t.to(DEV) for t in (aq, sa, wq, sw)]
+    acc_np = to_np(rq.w4a4_gemm(*d, out_dtype=torch.int32)).astype(np.int64)
+    yf = to_np(rq.w4a4_gemm(*d, out_dtype=torch.float32))
+    for r0, r_acc, r_y in oracle_gemm_row_blocks(aq.numpy(), sa.numpy(), wq.numpy(), sw.numpy(), M, N, K):
+        r1 = r0 + r_acc.shape[0]
+        np.testing.assert_array_equal(acc_np[r0:r1], r_acc)
+        np.testing.assert_allclose(yf[r0:r1], r_y, rtol=1e-5, atol=0)
