@@ -51,8 +51,8 @@
 //             and stores that takes several MMA periods).  A team widens all of
 //             its block's A and W chunks.  Each team keeps partial per-row code
 //             sums and hands them, and the weight scales, to the epilogue through
-//             shared memory.  CTA pairs whose packed operands fit in L2 run four
-//             teams (warps 2-17, four MMA periods per block; 4 + 4 stages);
+//             shared memory.  CTA pairs run four teams (warps 2-17, four MMA
+//             periods per block; 4 + 4 stages), single CTAs three;
 //   last 4 warps epilogue (one per TMEM lane quarter): tcgen05.ld of the fp32
 //             accumulator, offset removal, scales (broadcast from shared memory),
 //             16-byte stores.
@@ -401,7 +401,11 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int kblocks = (int)(prm.K / BK);
     const int64_t n_tiles_n = (prm.N + BN - 1) / BN;
     const int64_t m_op = A8 ? 2 * prm.M : prm.M;     // operand rows (two per INT8 activation row)
-    const int64_t n_tiles = n_tiles_n * ((m_op + C::TILE_M - 1) / C::TILE_M);
+    // Tiles run M-fastest: the CTAs working at the same time cover every row tile
+    // of a few column tiles, so those weight columns and all of A stay in L2
+    // (row-major order streamed W from DRAM once per row tile).
+    const int64_t n_tiles_m = (m_op + C::TILE_M - 1) / C::TILE_M;
+    const int64_t n_tiles = n_tiles_n * n_tiles_m;
     const int64_t first_tile = blockIdx.x / C::NCTA, tile_step = gridDim.x / C::NCTA;
 
     if (threadIdx.x == 0) {
@@ -452,9 +456,9 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             bool ok = true;
             for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step) {
                 // A rows of this CTA: 128 packed rows, or (A8) 64 INT8 rows
-                const int m0 = A8 ? (int)(tile / n_tiles_n) * (C::TILE_M / 2) + (int)rank * (BM / 2)
-                                  : (int)(tile / n_tiles_n) * C::TILE_M + (int)rank * BM;
-                const int n0 = (int)(tile % n_tiles_n) * BN + (int)rank * C::WROWS;
+                const int m0 = A8 ? (int)(tile % n_tiles_m) * (C::TILE_M / 2) + (int)rank * (BM / 2)
+                                  : (int)(tile % n_tiles_m) * C::TILE_M + (int)rank * BM;
+                const int n0 = (int)(tile / n_tiles_m) * BN + (int)rank * C::WROWS;
                 for (int kb = 0; kb < kblocks; ++kb, ++g) {
                     const int st = (int)(g % C::PK_STAGES);
                     if (!mbar_wait<false, true>(s, &s.pk_empty[st], (uint32_t)((g / C::PK_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
@@ -500,7 +504,7 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int it = 0;
         bool ok = true;
         for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step, ++it) {
-            const int n0 = (int)(tile % n_tiles_n) * BN;
+            const int n0 = (int)(tile / n_tiles_m) * BN;
             // the tile's weight scale for column tc, loaded now so that its latency
             // is not on the converters' path at the end of the tile
             const float wsc = (YMODE != 2 && tc < BN && n0 + tc < prm.N) ? prm.sw[n0 + tc] : 0.f;
@@ -660,7 +664,7 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!mbar_wait<PAIR, true>(s, &s.col_full[buf], par, prm.err)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             // operand rows of this CTA; output row m (A8: two operand rows per row)
-            const int64_t m0 = (tile / n_tiles_n) * C::TILE_M + (int64_t)rank * BM, n0 = (tile % n_tiles_n) * BN;
+            const int64_t m0 = (tile % n_tiles_m) * C::TILE_M + (int64_t)rank * BM, n0 = (tile / n_tiles_m) * BN;
             const int mr = 32 * q + lane;
             const int64_t m = A8 ? (m0 + mr) >> 1 : m0 + mr;
             const int rowt = -8 * s.rowsum[buf][mr];
@@ -871,7 +875,8 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const uint32_t rank = cluster_rank();
     const int kblocks = (int)(prm.K / BK);                    // = groups
     const int64_t n_tiles_n = prm.N / GBN;
-    const int64_t n_tiles = n_tiles_n * ((prm.M + BM - 1) / BM);   // 128 activation rows per tile
+    const int64_t n_tiles_m = (prm.M + BM - 1) / BM;                // 128 activation rows per tile
+    const int64_t n_tiles = n_tiles_n * n_tiles_m;                  // run M-fastest (L2 reuse of W)
     const int64_t first_tile = blockIdx.x / 2, tile_step = gridDim.x / 2;
 
     if (threadIdx.x == 0) {
@@ -911,8 +916,8 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             int64_t g = 0;
             bool ok = true;
             for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step) {
-                const int m0 = (int)(tile / n_tiles_n) * BM + (int)rank * (BM / 2);   // INT8 rows
-                const int n0 = (int)(tile % n_tiles_n) * GBN + (int)rank * GWROWS;
+                const int m0 = (int)(tile % n_tiles_m) * BM + (int)rank * (BM / 2);   // INT8 rows
+                const int n0 = (int)(tile / n_tiles_m) * GBN + (int)rank * GWROWS;
                 for (int kb = 0; kb < kblocks; ++kb, ++g) {
                     const int st = (int)(g % GPK);
                     if (!mbar_wait<false, true>(s, &s.pk_empty[st], (uint32_t)((g / GPK) & 1) ^ 1, prm.err)) { ok = false; break; }
@@ -1015,7 +1020,7 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         // copy the group scales of `tile`'s column e into buffer b (transposed to [g][column]);
         // the thread's arrival on sc_full[b] fires when its copies have landed
         auto stage = [&](int64_t tile, int b) {
-            const float *src = prm.sw + ((tile % n_tiles_n) * GBN + e) * (int64_t)G;
+            const float *src = prm.sw + ((tile / n_tiles_m) * GBN + e) * (int64_t)G;
             float *dst = s.gsc[b] + e;
             for (int gg = 0; gg < G; ++gg)
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst + gg * GBN)), "l"(src + gg)
@@ -1039,9 +1044,9 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 if (!mbar_wait<false, true>(s, &s.sc_empty[b ^ 1], (uint32_t)(((it + 1) >> 1) & 1) ^ 1, prm.err)) break;
                 stage(nt, b ^ 1);
             }
-            const int64_t m0 = (tile / n_tiles_n) * (2 * BM) + (int64_t)rank * BM;   // operand rows
+            const int64_t m0 = (tile % n_tiles_m) * (2 * BM) + (int64_t)rank * BM;   // operand rows
             const int64_t m = (m0 + 32 * q + lane) >> 1;                             // activation row
-            const int64_t n0 = (tile % n_tiles_n) * GBN;
+            const int64_t n0 = (tile / n_tiles_m) * GBN;
             const float sa = m < prm.M ? prm.sa[m] * 262144.0f : 0.f;               // x 2^18: partials are 2^-18 units
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
                 const int pr = (int)(g % GPR);
@@ -1190,14 +1195,12 @@ cudaError_t launch_mode(const GemmArgs &g, const TcParams &p, cudaStream_t strea
     return cudaLaunchKernelEx(&cfg, kern, ta, tw, p);
 }
 
-// Converter teams for CTA pairs.  Four teams give each warp four MMA periods per
-// K block but leave room for only four packed stages; that ring depth covers the
-// TMA latency while the operands stay in L2.  Measured: 2048 x 4096 -> 14336
-// (34 MB of packed operands) 110.6 -> 106.5 us with four teams, 4096 x 8192 ->
-// 28672 (134 MB) 745 -> 830 us.  The threshold lies between the two.
-constexpr int64_t kFourTeamsMaxOperandBytes = 64ll << 20;
-
-bool four_teams(int64_t a_bytes, int64_t w_bytes) { return a_bytes + w_bytes <= kFourTeamsMaxOperandBytes; }
+// Converter teams for CTA pairs: four.  Four teams give each warp four MMA
+// periods per K block but leave room for only four packed stages, a ring depth
+// that covers the TMA latency while the operands come from L2.  With tiles walked
+// M-fastest the CTAs working at once share their weight columns in L2 at every
+// size measured: 2048 x 4096 -> 14336 102.4 us (three teams ~106 us), 4096 x
+// 8192 -> 28672 676 us (three teams 739 us).
 
 template <int YMODE>
 cudaError_t launch_group_mode(const CUtensorMap &ta, const CUtensorMap &tw, const GParams &p, cudaStream_t stream) {
@@ -1227,13 +1230,20 @@ cudaError_t launch_group_mode(const CUtensorMap &ta, const CUtensorMap &tw, cons
 
 }  // namespace
 
+bool make_tma_map_u8(CUtensorMap *map, const void *base, int64_t rows, int64_t row_bytes, int box_bytes, int box_rows,
+                     CUtensorMapSwizzle swizzle) {
+    return make_map(map, base, rows, row_bytes, box_bytes, box_rows, swizzle);
+}
+
+int device_sm_count() { return sm_count(); }
+
 bool w4a4_gemm_tc_supported(const GemmArgs &g) { return g.M > 64 && g.K % BK == 0 && g.K <= 65536; }
 
 cudaError_t launch_w4a4_gemm_tc(const GemmArgs &g, cudaStream_t stream) {
     TcParams p{g.a_scales, g.w_scales, g.y, g.M, g.N, g.K, error_word_device_ptr()};
     if (!p.err) return cudaErrorUnknown;
     const bool pair = g.M > BM;   // tiles of 256 rows on SM pairs; one SM for M <= 128
-    const bool t4 = pair && four_teams(g.M * g.K / 2, g.N * g.K / 2);
+    const bool t4 = pair;         // four converter teams on pairs (single CTAs: no room)
     switch (g.y_mode * 3 + (pair ? (t4 ? 2 : 1) : 0)) {
         case 0: return launch_mode<0, false>(g, p, stream);
         case 1: return launch_mode<0, true>(g, p, stream);
@@ -1272,8 +1282,8 @@ cudaError_t launch_w4a8_gemm_tc(const int8_t *aq, const float *sa, const uint8_t
     const GemmArgs g{reinterpret_cast<const uint8_t *>(aq), sa, wq, sw, M, N, K, y, y_mode};
     TcParams p{sa, sw, y, M, N, K, error_word_device_ptr()};
     if (!p.err) return cudaErrorUnknown;
-    // M > 64: at least 130 operand rows, so always CTA pairs
-    const bool t4 = four_teams(M * K, N * K / 2);
+    // M > 64: at least 130 operand rows, so always CTA pairs, with four teams
+    const bool t4 = true;
     switch (y_mode * 2 + (t4 ? 1 : 0)) {
         case 0: return launch_mode<0, true, true>(g, p, stream);
         case 1: return launch_mode<0, true, true, 4>(g, p, stream);
