@@ -56,8 +56,9 @@ constexpr int DCH = 128;                 // output channels per CTA (MMA M, TMEM
 constexpr int DTHREADS = 256;            // eight warps: two per TMEM lane quarter
 constexpr int DMAXB = 8;                 // K blocks per CTA: KS <= 1024 codes
 constexpr int DMAXS = 8;                 // CTAs per cluster
-constexpr uint32_t DTMEM_COLS = 512;     // weights: 32 columns per K block (<= 256); accumulator after
+constexpr uint32_t DTMEM_COLS = 512;     // weights: 32 columns per K block (<= 256); accumulators after
 constexpr uint32_t DACC_COL = 256;
+constexpr int DNACC = 4;                 // independent accumulators: K step j goes to accumulator j % 4
 constexpr long long kDecodeWaitLimit = 4000000000ll;   // ~2 s at 2 GHz
 constexpr size_t kOneCtaPerSmBytes = 116 * 1024;        // dynamic shared memory that keeps one CTA per SM
 
@@ -73,6 +74,8 @@ struct DSmem {
     // share of the channels: [source CTA][token][channel - 128 rank / S]
     alignas(16) int recv[16 * MT * DCH];
     int aborts[DMAXS];                                  // abort flags the cluster's CTAs push here
+    float wsc[DCH];                                     // weight scales of the channels this CTA stores
+    float tsc[16 * MT];                                 // token scales (decode product: loaded at the start)
     int qsum[16 * MT];                                  // sum of each token's activation codes over the slice
     // fused only: the slice's packed activation codes and every token's scale, as
     // the CTAs of the cluster that rotate the tokens write them; the rotation
@@ -178,6 +181,7 @@ __device__ __forceinline__ void d_tmem_st8(uint32_t taddr, const uint32_t (&v)[8
                  : "memory");
 }
 
+// 16 columns of the warp's 32 lanes; completes at the next d_tmem_wait_ld.
 __device__ __forceinline__ void d_tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -185,8 +189,8 @@ __device__ __forceinline__ void d_tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void d_tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Split cluster barrier at the start: every CTA of the cluster has started (its
 // shared memory exists) before any CTA writes into another's.
@@ -218,15 +222,32 @@ __device__ __forceinline__ uint32_t d_e4m3_signed(uint32_t x) {
 // Phases shared by the decode product and the fused rotation + product
 // ---------------------------------------------------------------------------
 
-// Barriers, tensor memory (512 columns), zeroed token sums.
+// At entry, warp 0: lane 0 initializes the barriers, then lane b requests K
+// block b of the weight slice (the layer is bound by this stream, so it starts
+// before anything else).  A block is one box of 64 bytes x 128 channels with the
+// 64-byte swizzle: chunk j of channel r lands at 16-byte position
+// j ^ ((r >> 1) & 3) of the channel's 64 bytes, so the lanes reading chunk j of
+// 32 consecutive channels hit distinct bank groups.
 template <class S_>
-__device__ __forceinline__ uint32_t d_setup(S_ &s, int tid, int warp, int mp) {
-    if (tid == 0) {
+__device__ __forceinline__ void d_start_weights(S_ &s, const CUtensorMap *tm, int lane, int b0, int nb, int64_t c0) {
+    if (lane == 0) {
         for (int b = 0; b < DMAXB; ++b) d_mbar_init(&s.wfull[b], 1);
         d_mbar_init(&s.mma_done, 1);
         s.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncwarp();
+    if (lane < nb) {
+        d_expect_tx(&s.wfull[lane], DCH * DBK / 2);
+        d_tma_2d(s.pkw[lane], tm, &s.wfull[lane], (b0 + lane) * (DBK / 2), (int)c0);
+    }
+    __syncwarp();
+}
+
+// Tensor memory (512 columns), zeroed token sums; every thread then sees the
+// barriers warp 0 initialized.
+template <class S_>
+__device__ __forceinline__ uint32_t d_setup(S_ &s, int tid, int warp, int mp) {
     if (tid < mp) s.qsum[tid] = 0;
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(d_smem(&s.tmem_base)),
@@ -241,51 +262,48 @@ __device__ __forceinline__ uint32_t d_setup(S_ &s, int tid, int warp, int mp) {
     return s.tmem_base;
 }
 
-// The whole weight slice is requested at once: the layer is bound by this stream.
-// A K block arrives as four boxes of 16 bytes x 128 channels, so that shared
-// memory holds it as [chunk][channel][16 bytes] and the 32 lanes reading chunk j
-// of their channels read 512 contiguous bytes.
-template <class S_>
-__device__ __forceinline__ void d_issue_weights(S_ &s, const CUtensorMap *tm, int b0, int nb, int64_t c0) {
-    for (int b = 0; b < nb; ++b) {
-        d_expect_tx(&s.wfull[b], DCH * DBK / 2);
+// Activation codes of the slice -> signed E4M3 operand (tokens >= M stay zero
+// codes) and each token's code sum.  d_load_acts issues every load of the
+// thread (load(m, off) returns the 16 packed bytes at byte offset off of token
+// m's slice: 32 codes = operand granules 2 ch, 2 ch + 1), d_store_acts widens
+// and stores them once they have landed.
+template <int MT>
+struct ActChunks {
+    static constexpr int MAXC = 16 * MT * DMAXB * 4 / DTHREADS;   // chunks per thread at most (1 .. 8)
+    uint4 v[MAXC];
+};
+
+template <int MT, class Load>
+__device__ __forceinline__ void d_load_acts(ActChunks<MT> &a, int tid, int nb, int M, Load load) {
+    constexpr int MP = 16 * MT;
+    const int per_row = nb * 4;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            d_tma_2d(s.pkw[b] + j * (DCH * 16), tm, &s.wfull[b], (b0 + b) * (DBK / 2) + 16 * j, (int)c0);
+    for (int i = 0; i < ActChunks<MT>::MAXC; ++i) {
+        const int e = tid + DTHREADS * i;
+        const int m = e / per_row, rem = e - m * per_row;
+        a.v[i] = (e < MP * per_row && m < M) ? load(m, (rem >> 2) * (DBK / 2) + 16 * (rem & 3))
+                                              : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
-// Activation codes of the slice -> signed E4M3 operand (tokens >= M stay zero
-// codes) and each token's code sum.  load(m, off) returns the 16 packed bytes at
-// byte offset off of token m's slice (32 codes = operand granules 2 ch, 2 ch + 1).
-template <int MT, class S_, class Load>
-__device__ __forceinline__ void d_widen_acts(S_ &s, int tid, int nb, int M, Load load) {
+template <int MT, class S_>
+__device__ __forceinline__ void d_store_acts(S_ &s, const ActChunks<MT> &a, int tid, int nb, int M) {
     constexpr int MP = 16 * MT;
-    constexpr int MAXC = MP * DMAXB * 4 / DTHREADS;   // chunks per thread at most (1 .. 8)
     const int per_row = nb * 4;
-    // every load first, so that their latencies overlap
-    uint4 vin[MAXC];
 #pragma unroll
-    for (int i = 0; i < MAXC; ++i) {
-        const int e = tid + DTHREADS * i;
-        const int m = e / per_row, rem = e - m * per_row;
-        vin[i] = (e < MP * per_row && m < M) ? load(m, (rem >> 2) * (DBK / 2) + 16 * (rem & 3))
-                                              : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int i = 0; i < MAXC; ++i) {
+    for (int i = 0; i < ActChunks<MT>::MAXC; ++i) {
         const int e = tid + DTHREADS * i;
         if (e >= MP * per_row) break;
         const int m = e / per_row, rem = e - m * per_row, b = rem >> 2, ch = rem & 3;
-        const uint4 v = vin[i];
+        const uint4 v = a.v[i];
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[8], usum = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            o[2 * i] = d_e4m3_signed(wv[i] & 0x0f0f0f0fu);
-            o[2 * i + 1] = d_e4m3_signed((wv[i] >> 4) & 0x0f0f0f0fu);
+        for (int k = 0; k < 4; ++k) {
+            o[2 * k] = d_e4m3_signed(wv[k] & 0x0f0f0f0fu);
+            o[2 * k + 1] = d_e4m3_signed((wv[k] >> 4) & 0x0f0f0f0fu);
             uint32_t ul, uh;
-            d_widen_u(wv[i], ul, uh);
+            d_widen_u(wv[k], ul, uh);
             usum = __dp4a(ul + uh, 0x01010101u, usum);   // byte lanes <= 30
         }
         uint8_t *rowp = s.opb[b] + m * DBK;
@@ -314,8 +332,8 @@ __device__ __forceinline__ void d_widen_weights(S_ &s, uint32_t tmem, int nb, in
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            // chunk j (codes 32 j .. 32 j + 31) of this thread's channel
-            const uint4 v = *reinterpret_cast<const uint4 *>(s.pkw[b] + j * (DCH * 16) + r * 16);
+            // chunk j (codes 32 j .. 32 j + 31) of this thread's channel (64-byte swizzle)
+            const uint4 v = *reinterpret_cast<const uint4 *>(s.pkw[b] + r * (DBK / 2) + 16 * (j ^ ((r >> 1) & 3)));
             uint32_t o[8];
             d_widen_u(v.x, o[0], o[1]);
             d_widen_u(v.y, o[2], o[3]);
@@ -335,6 +353,30 @@ __device__ __forceinline__ void d_st_cluster(const void *local, uint32_t rank, i
     asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
 
+// The weight scale of one channel this CTA stores (thread tid < 128 / S), and a
+// token scale (tid < M): loaded at entry into registers, stored into shared
+// memory after the widening, so that their latency overlaps everything before.
+struct ScalePrefetch {
+    float w, t;
+};
+__device__ __forceinline__ ScalePrefetch d_load_scales(int tid, uint32_t rank, int nsplit, int64_t c0, const float *sw,
+                                                       const float *sa, int M, int y_mode) {
+    const int cw = DCH / nsplit;
+    ScalePrefetch p{0.f, 0.f};
+    if (y_mode != 2) {
+        if (tid < cw) p.w = __ldg(sw + c0 + (int)rank * cw + tid);
+        if (sa && tid < M) p.t = __ldg(sa + tid);
+    }
+    return p;
+}
+template <class S_>
+__device__ __forceinline__ void d_store_scales(S_ &s, const ScalePrefetch &p, int tid, uint32_t rank, int nsplit,
+                                               int M, bool tokens) {
+    const int cw = DCH / nsplit;
+    if (tid < cw) s.wsc[(int)rank * cw + tid] = p.w;
+    if (tokens && tid < M) s.tsc[tid] = p.t;
+}
+
 // After every thread's operands are in place: one thread issues the slice's
 // MMAs; the four lane-quarter warps turn the accumulators into exact integer
 // partials acc 2^18 - 8 sum q_a and push each into the shared memory of the CTA
@@ -350,12 +392,13 @@ __device__ __forceinline__ bool d_product(S_ &s, uint32_t tmem, int nb, int tid,
     if constexpr (WAIT_STARTED) d_cluster_wait();   // every CTA of the cluster has started
     const bool aborted = s.abort_flag != 0;
     if (tid == 0 && !aborted) {
-        const uint32_t dacc = tmem + DACC_COL;
+        // K step 4 b + k accumulates into accumulator k: four independent chains
         for (int b = 0; b < nb; ++b) {
             const uint32_t bb = d_smem(s.opb[b]);
 #pragma unroll
             for (int k = 0; k < DBK / 32; ++k)
-                d_mma_ts<MT>(dacc, tmem + (uint32_t)(32 * b + 8 * k), d_sw128_desc(bb + 32 * k), (b | k) != 0);
+                d_mma_ts<MT>(tmem + DACC_COL + (uint32_t)(16 * MT * k), tmem + (uint32_t)(32 * b + 8 * k),
+                             d_sw128_desc(bb + 32 * k), b != 0);
         }
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                          d_smem(&s.mma_done))
@@ -372,14 +415,22 @@ __device__ __forceinline__ bool d_product(S_ &s, uint32_t tmem, int nb, int tid,
             int *dst = s.recv + (int)rank * (16 * MT) * cw + (r - (int)owner * cw);   // + m cw
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
-                uint32_t v[16];
-                d_tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + DACC_COL + 16 * t, v);
+                int acc[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] = 0;
+                uint32_t v[DNACC][16];   // the four accumulators' columns of token tile t, one wait
+#pragma unroll
+                for (int a = 0; a < DNACC; ++a)
+                    d_tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + DACC_COL + (uint32_t)(16 * MT * a + 16 * t), v[a]);
+                d_tmem_wait_ld();
+#pragma unroll
+                for (int a = 0; a < DNACC; ++a)   // each accumulator holds an exact multiple of 2^-18
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[j] += __float2int_rn(__uint_as_float(v[a][j]) * 262144.0f);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int m = 16 * t + j;
-                    if (m < M)
-                        d_st_cluster(dst + m * cw, owner,
-                                     __float2int_rn(__uint_as_float(v[j]) * 262144.0f) - 8 * s.qsum[m]);
+                    if (m < M) d_st_cluster(dst + m * cw, owner, acc[j] - 8 * s.qsum[m]);
                 }
             }
         } else if (lane == 0) {
@@ -393,10 +444,10 @@ __device__ __forceinline__ bool d_product(S_ &s, uint32_t tmem, int nb, int tid,
 
 // After a cluster barrier: CTA `rank` adds the partials that the slices pushed
 // for channels [128 rank / S, 128 (rank + 1) / S) and stores y (a token's scale
-// from sa(m)).
+// from sa(m), the channel's from s.wsc, loaded at the start).
 template <int MT, class S_, class Scale>
 __device__ __forceinline__ void d_reduce_store(S_ &s, int tid, uint32_t rank, int nsplit, int M, int64_t N, int64_t c0,
-                                               const float *sw, void *y, int y_mode, Scale sa) {
+                                               void *y, int y_mode, Scale sa) {
     const int cw = DCH / nsplit;
     bool any_abort = false;
     for (int j = 0; j < nsplit; ++j) any_abort |= s.aborts[j] != 0;
@@ -410,7 +461,7 @@ __device__ __forceinline__ void d_reduce_store(S_ &s, int tid, uint32_t rank, in
         if (y_mode == 2) {
             static_cast<int *>(y)[o] = tot;
         } else {
-            const float v = ((float)tot * sa(m)) * sw[col];
+            const float v = ((float)tot * sa(m)) * s.wsc[c];
             if (y_mode == 1) static_cast<float *>(y)[o] = v;
             else static_cast<__half *>(y)[o] = __float2half_rn(v);
         }
@@ -450,18 +501,21 @@ w4a4_decode_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     const int nb = (int)(((int64_t)(rank + 1) * kblocks) / nsplit) - b0;   // 1 .. DMAXB
     const int M = (int)prm.M;
 
-    const uint32_t tmem = d_setup(s, tid, warp, 16 * MT);
-    if (tid == 0) d_issue_weights(s, &tmW, b0, nb, c0);
+    if (warp == 0) d_start_weights(s, &tmW, lane, b0, nb, c0);
     const uint8_t *abase = prm.aq + (int64_t)b0 * (DBK / 2);
     const int64_t lda = prm.K / 2;
-    d_widen_acts<MT>(s, tid, nb, M, [&](int m, int off) {
+    ActChunks<MT> acts;
+    d_load_acts<MT>(acts, tid, nb, M, [&](int m, int off) {
         return __ldg(reinterpret_cast<const uint4 *>(abase + (int64_t)m * lda + off));
     });
-    d_widen_weights(s, tmem, nb, warp, lane, prm.err);
+    const ScalePrefetch sc = d_load_scales(tid, rank, nsplit, c0, prm.sw, prm.sa, M, prm.y_mode);
+    const uint32_t tmem = d_setup(s, tid, warp, 16 * MT);
+    d_widen_weights(s, tmem, nb, warp, lane, prm.err);   // each block as it lands
+    d_store_acts<MT>(s, acts, tid, nb, M);
+    d_store_scales(s, sc, tid, rank, nsplit, M, true);
     const bool aborted = d_product<MT, true>(s, tmem, nb, tid, warp, lane, M, rank, nsplit, prm.err);
     d_cluster_sync();   // every CTA's partials (and abort flag) are in place
-    d_reduce_store<MT>(s, tid, rank, nsplit, M, prm.N, c0, prm.sw, prm.y, prm.y_mode,
-                       [&](int m) { return prm.sa[m]; });
+    d_reduce_store<MT>(s, tid, rank, nsplit, M, prm.N, c0, prm.y, prm.y_mode, [&](int m) { return s.tsc[m]; });
     d_teardown(s, tmem, aborted, tid, warp, nb, prm.err);
 }
 
@@ -694,8 +748,9 @@ fused_decode_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
     const int M = (int)prm.M;
     const bool signs_first = (prm.flags & 1u) != 0;
 
+    if (warp == 0) d_start_weights(s, &tmW, lane, b0, nb, c0);
+    const ScalePrefetch sc = d_load_scales(tid, rank, nsplit, c0, prm.sw, nullptr, M, prm.y_mode);
     const uint32_t tmem = d_setup(s, tid, warp, 16);
-    if (tid == 0) d_issue_weights(s, &tmW, b0, nb, c0);
 
     // sign bits: word j holds elements 32 j .. 32 j + 31 (one SplitMix64 output each)
     for (int base = 0; base < n; base += DTHREADS) {
@@ -828,11 +883,16 @@ fused_decode_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_con
     }
     d_cluster_sync();   // every token's codes of this CTA's slice, and every scale, are in place
 
-    d_widen_acts<1>(s, tid, nb, M, [&](int m, int off) { return *reinterpret_cast<const uint4 *>(&s.apk[m][off]); });
+    {
+        ActChunks<1> acts;
+        d_load_acts<1>(acts, tid, nb, M, [&](int m, int off) { return *reinterpret_cast<const uint4 *>(&s.apk[m][off]); });
+        d_store_acts<1>(s, acts, tid, nb, M);
+    }
+    d_store_scales(s, sc, tid, rank, nsplit, M, false);
     d_widen_weights(s, tmem, nb, warp, lane, prm.err);
     const bool aborted = d_product<1, false>(s, tmem, nb, tid, warp, lane, M, rank, nsplit, prm.err);
     d_cluster_sync();
-    d_reduce_store<1>(s, tid, rank, nsplit, M, prm.N, c0, prm.sw, prm.y, prm.y_mode, [&](int m) { return s.asc[m]; });
+    d_reduce_store<1>(s, tid, rank, nsplit, M, prm.N, c0, prm.y, prm.y_mode, [&](int m) { return s.asc[m]; });
     d_teardown(s, tmem, aborted, tid, warp, nb, prm.err);
     (void)RPAD;
 }
@@ -880,7 +940,7 @@ cudaError_t launch_cluster(Kern kern, size_t smem, int nsplit, int64_t tiles, co
 template <int MT>
 cudaError_t launch_decode_mt(const GemmArgs &g, int nsplit, cudaStream_t stream) {
     CUtensorMap tw;
-    if (!make_tma_map_u8(&tw, g.w_q, g.N, g.K / 2, 16, DCH, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+    if (!make_tma_map_u8(&tw, g.w_q, g.N, g.K / 2, DBK / 2, DCH, CU_TENSOR_MAP_SWIZZLE_64B)) return cudaErrorInvalidValue;
     const DParams p{g.a_q, g.a_scales, g.w_scales, g.y, g.M, g.N, g.K, g.y_mode, error_word_device_ptr()};
     if (!p.err) return cudaErrorUnknown;
     return launch_cluster(w4a4_decode_tc_kernel<MT>, launch_smem<DSmem<MT, false>>(), nsplit, g.N / DCH, tw, p, stream);
@@ -934,7 +994,7 @@ cudaError_t launch_fused_decode(const void *x, int in_type, int64_t M, int64_t l
     const int nsplit = pick_split(K / DBK, N / DCH, sms);
     if (nsplit == 0) return cudaErrorInvalidValue;
     CUtensorMap tw;
-    if (!make_tma_map_u8(&tw, wq, N, K / 2, 16, DCH, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+    if (!make_tma_map_u8(&tw, wq, N, K / 2, DBK / 2, DCH, CU_TENSOR_MAP_SWIZZLE_64B)) return cudaErrorInvalidValue;
     const FParams p{x, ldx, in_type, seed, flags, sw, y, M, N, K, y_mode, aq, as, error_word_device_ptr()};
     if (!p.err) return cudaErrorUnknown;
     switch (K) {
