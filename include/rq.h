@@ -93,6 +93,10 @@ enum { RQ_ATTN_ROTATED_OUT = 2u };
  * or INT4 codes with one scale per group of 128 elements (weights of the W4A8
  * layer with per-group scales). */
 enum { RQ_INT8_CODES = 4u, RQ_GROUP_SCALES = 8u };
+/* rq_fwht_quant (powers of two from 256 to 8192): the INT4 codes written as the
+ * W4A4 product's operand, one byte per code (see rq_fwht_quant); rq_w4a4_gemm:
+ * the activation codes a_q are given in that form. */
+enum { RQ_E4M3_CODES = 16u, RQ_A_E4M3 = 16u };
 
 /* Smallest / largest supported Hadamard size (row length n, head_dim). */
 #define RQ_MIN_N 32
@@ -137,6 +141,14 @@ enum { RQ_INT8_CODES = 4u, RQ_GROUP_SCALES = 8u };
  *              consecutive elements ([SQ] §The architecture, per-group scales;
  *              the weight fold of the W4A8 layer): q as above, scales
  *              [rows][n/128] fp32.
+ *            RQ_E4M3_CODES (powers of two from 256 to 8192 only): the same
+ *              INT4 codes and scales as the default, each code stored as the
+ *              tensor-core operand of rq_w4a4_gemm (RQ_A_E4M3): q is
+ *              [rows][n] bytes; the byte of code q is q for q >= 0 and
+ *              0x80 | -q for q < 0 (the FP8 E4M3 encoding of q * 2^-9), and
+ *              within each group of 8 codes the bytes hold codes
+ *              0, 2, 4, 6, 1, 3, 5, 7 of the group.  Twice the bytes of the
+ *              packed form; the product then widens only the weights.
  *   q        out: [rows][n/2] bytes, packed codes (row stride n/2).
  *   scales   out: [rows] fp32 scales, max|y|/7 of each rotated row.
  *   y        out, may be NULL: [rows][n] fp32 rotated rows y = xR (parity
@@ -166,7 +178,9 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
  *             of 128 and at most 65536.
  *   seed      accepted for a uniform signature and ignored: the rotation is
  *             already folded into w_q.
- *   flags     must be 0.
+ *   flags     0, or RQ_A_E4M3: a_q is [M][K] bytes, the activation codes in
+ *             the operand form rq_fwht_quant writes with RQ_E4M3_CODES (M > 64
+ *             only; RQ_ERR_UNSUPPORTED otherwise).
  *   y         out: [M][N] row-major, of y_dtype:
  *             RQ_F16  the dequantized product rounded to fp16;
  *             RQ_F32  the dequantized product in fp32;

@@ -19,6 +19,8 @@ RQ_SIGNS_FIRST = 1
 RQ_ATTN_ROTATED_OUT = 2
 RQ_INT8_CODES = 4
 RQ_GROUP_SCALES = 8
+RQ_E4M3_CODES = 16      # rq_fwht_quant: INT4 codes as the product's E4M3 operand bytes
+RQ_A_E4M3 = 16          # rq_w4a4_gemm: a_q holds those bytes
 
 _STATUS = {0: "RQ_OK", 1: "RQ_ERR_INVALID_ARG", 2: "RQ_ERR_UNSUPPORTED", 3: "RQ_ERR_MISALIGNED",
            4: "RQ_ERR_CUDA", 5: "RQ_ERR_TIMEOUT"}
@@ -132,14 +134,20 @@ def fwht_quant(x: torch.Tensor, seed: int, flags: int = RQ_SIGNS_FIRST, *, q=Non
     Returns ``(q, scales)`` or ``(q, scales, y)`` when ``want_y``: q is
     (rows x n/2) uint8, scales (rows,) fp32, y (rows x n) fp32 = x R.  With
     RQ_INT8_CODES in flags q is (rows x n) int8; with RQ_GROUP_SCALES scales is
-    (rows x n/128)."""
+    (rows x n/128); with RQ_E4M3_CODES q is (rows x n) uint8, the same INT4 codes
+    as the product's operand bytes (see include/rq.h)."""
     lib = load_library()
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit stride in the last dimension")
     if x.dtype not in (torch.float32, torch.bfloat16, torch.float16):
         raise ValueError("x must be float32, bfloat16 or float16")
     rows, n = x.shape
-    q_shape, q_dtype = ((rows, n), torch.int8) if flags & RQ_INT8_CODES else ((rows, n // 2), torch.uint8)
+    if flags & RQ_INT8_CODES:
+        q_shape, q_dtype = (rows, n), torch.int8
+    elif flags & RQ_E4M3_CODES:
+        q_shape, q_dtype = (rows, n), torch.uint8
+    else:
+        q_shape, q_dtype = (rows, n // 2), torch.uint8
     s_shape = (rows, n // 128) if flags & RQ_GROUP_SCALES else (rows,)
     if q is None:
         q = torch.empty(q_shape, dtype=q_dtype, device=x.device)
@@ -162,15 +170,17 @@ def w4a4_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_d
               seed: int = 0, out=None, stream=None):
     """y = dequant(Q(XR) . Q(R^T W)): a_q (M x K/2), w_q (N x K/2) packed codes,
     a_scales (M,), w_scales (N,).  out_dtype float16 / float32, or int32 for the
-    raw accumulators."""
+    raw accumulators.  a_q of shape (M x K) holds the activation codes in the
+    operand form of fwht_quant(..., RQ_E4M3_CODES) (more than 64 rows)."""
     lib = load_library()
-    M, kb = a_q.shape
+    M, ka = a_q.shape
     N, kb2 = w_q.shape
-    if kb != kb2 or a_q.dtype != torch.uint8 or w_q.dtype != torch.uint8:
-        raise ValueError("a_q and w_q must be uint8 with the same K/2 columns")
+    if a_q.dtype != torch.uint8 or w_q.dtype != torch.uint8 or ka not in (kb2, 2 * kb2):
+        raise ValueError("a_q (M x K/2, or M x K operand bytes) and w_q (N x K/2) must be uint8")
     if not (a_q.is_contiguous() and w_q.is_contiguous()):
         raise ValueError("packed operands must be contiguous")
-    K = 2 * kb
+    K = 2 * kb2
+    flags = RQ_A_E4M3 if ka == K else 0
     if out is None:
         out = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
     _expect(out, "out", (M, N), _OUT_DTYPES)
@@ -179,7 +189,7 @@ def w4a4_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_d
     _expect(w_scales, "w_scales", (N,), torch.float32, optional=raw)
     _dev(a_q, w_q, a_scales, w_scales, out)
     with torch.cuda.device(a_q.device):
-        st = lib.rq_w4a4_gemm(_ptr(a_q), _ptr(a_scales), _ptr(w_q), _ptr(w_scales), M, N, K, seed, 0,
+        st = lib.rq_w4a4_gemm(_ptr(a_q), _ptr(a_scales), _ptr(w_q), _ptr(w_scales), M, N, K, seed, flags,
                               _ptr(out), _DTYPES[out.dtype], _stream(stream))
     _check("rq_w4a4_gemm", st)
     return out

@@ -74,11 +74,14 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
     const bool kron = !rq::pow2(n) && rq::kron_block_of(n, &km, &klb);
     if (!kron && (!rq::pow2(n) || n < RQ_MIN_N || n > RQ_MAX_N)) return RQ_ERR_UNSUPPORTED;
     if (ld_x < n) return RQ_ERR_INVALID_ARG;
-    if (flags & ~uint32_t(RQ_SIGNS_FIRST | RQ_INT8_CODES | RQ_GROUP_SCALES)) return RQ_ERR_INVALID_ARG;
-    if ((flags & RQ_INT8_CODES) && (flags & RQ_GROUP_SCALES)) return RQ_ERR_INVALID_ARG;
+    if (flags & ~uint32_t(RQ_SIGNS_FIRST | RQ_INT8_CODES | RQ_GROUP_SCALES | RQ_E4M3_CODES)) return RQ_ERR_INVALID_ARG;
+    const uint32_t modes = flags & uint32_t(RQ_INT8_CODES | RQ_GROUP_SCALES | RQ_E4M3_CODES);
+    if (modes & (modes - 1)) return RQ_ERR_INVALID_ARG;   // at most one code mode
     // INT8 and per-group codes: n = m 2^k, and powers of two from 256 on (the plans
-    // whose threads end with whole 32-element runs of a row)
-    if ((flags & (RQ_INT8_CODES | RQ_GROUP_SCALES)) && !kron && n < 256) return RQ_ERR_UNSUPPORTED;
+    // whose threads end with whole 32-element runs of a row); E4M3 operand codes:
+    // powers of two from 256 on
+    if (modes && !kron && n < 256) return RQ_ERR_UNSUPPORTED;
+    if ((flags & RQ_E4M3_CODES) && kron) return RQ_ERR_UNSUPPORTED;
     if (rows == 0) return RQ_OK;
     if (!x || !q || !scales) return RQ_ERR_INVALID_ARG;
     if (!rq::aligned16(x) || !rq::aligned16(q) || !rq::aligned16(scales) || (y && !rq::aligned16(y)))
@@ -97,7 +100,9 @@ rq_status rq_w4a4_gemm(const uint8_t *a_q, const float *a_scales, const uint8_t 
                        uint32_t flags, void *y, rq_dtype y_dtype, void *stream) {
     (void)seed;  // the rotation is already folded into w_q
     if (M < 0 || N < 0 || K <= 0) return RQ_ERR_INVALID_ARG;
-    if (flags != 0) return RQ_ERR_INVALID_ARG;
+    if (flags & ~uint32_t(RQ_A_E4M3)) return RQ_ERR_INVALID_ARG;
+    const bool a_e4m3 = (flags & RQ_A_E4M3) != 0;
+    if (a_e4m3 && M > 0 && M <= 64) return RQ_ERR_UNSUPPORTED;   // the operand form feeds the tensor-core kernel
     if (K % 128 != 0 || K > 65536) return RQ_ERR_UNSUPPORTED;
     if (y_dtype != RQ_F16 && y_dtype != RQ_F32 && y_dtype != RQ_I32) return RQ_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return RQ_OK;
@@ -107,7 +112,7 @@ rq_status rq_w4a4_gemm(const uint8_t *a_q, const float *a_scales, const uint8_t 
     if (need_scales && (!rq::aligned16(a_scales) || !rq::aligned16(w_scales))) return RQ_ERR_MISALIGNED;
     if ((N * rq::elem_size(y_dtype)) % 16 != 0) return RQ_ERR_MISALIGNED;
     rq::GemmArgs g{a_q, a_scales, w_q, w_scales, M, N, K, y,
-                   y_dtype == RQ_F16 ? 0 : (y_dtype == RQ_F32 ? 1 : 2)};
+                   y_dtype == RQ_F16 ? 0 : (y_dtype == RQ_F32 ? 1 : 2), a_e4m3};
     cudaError_t e = rq::launch_w4a4_gemm(g, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
 }

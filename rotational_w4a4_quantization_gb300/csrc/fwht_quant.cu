@@ -400,6 +400,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
         constexpr bool kGroups4 = PL::kTwoPhase && C >= 7;
         const bool i8 = PL::kTwoPhase && (prm.flags & RQ_INT8_CODES) != 0;
         const bool per_group = PL::kTwoPhase && (prm.flags & RQ_GROUP_SCALES) != 0;
+        const bool e4 = PL::kTwoPhase && (prm.flags & RQ_E4M3_CODES) != 0;
         float gmax[kGroups4 ? 4 : 1];
         float amax;
         if constexpr (kGroups4) {
@@ -537,7 +538,14 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
                     words[cc] = pack8(code);
                 }
                 // chunks c0..c0+3 are consecutive (slot bits 0,1 = chunk bits 0,1)
-                *reinterpret_cast<uint4 *>(qrow + 4 * c0) = make_uint4(words[0], words[1], words[2], words[3]);
+                if (e4) {
+                    // one signed E4M3 byte per code, in the product's operand order
+                    uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)n + 8 * c0);
+                    qp[0] = make_uint4(e4m3_even(words[0]), e4m3_odd(words[0]), e4m3_even(words[1]), e4m3_odd(words[1]));
+                    qp[1] = make_uint4(e4m3_even(words[2]), e4m3_odd(words[2]), e4m3_even(words[3]), e4m3_odd(words[3]));
+                } else {
+                    *reinterpret_cast<uint4 *>(qrow + 4 * c0) = make_uint4(words[0], words[1], words[2], words[3]);
+                }
             }
             }
         }
@@ -774,6 +782,7 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
         if (active) {
             // codes: INT4 per row (default), INT8 per row, or INT4 per group of 128
             const bool i8 = (prm.flags & RQ_INT8_CODES) != 0, grp = (prm.flags & RQ_GROUP_SCALES) != 0;
+            const bool e4 = (prm.flags & RQ_E4M3_CODES) != 0;
             const float am = grp ? amax_grp : amax;
             const float qmax = i8 ? 127.0f : 7.0f;
             const float inv = am > 0.f ? qmax / am : 0.f;
@@ -840,9 +849,18 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
                     }
                     words[s] = pack8(code);
                 }
-                uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)(n / 2) + 32 * t);
-                qp[0] = make_uint4(words[0], words[1], words[2], words[3]);
-                qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
+                if (e4) {
+                    // one signed E4M3 byte per code, in the product's operand order: 64 bytes
+                    uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)n + 64 * t);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        qp[c] = make_uint4(e4m3_even(words[2 * c]), e4m3_odd(words[2 * c]), e4m3_even(words[2 * c + 1]),
+                                           e4m3_odd(words[2 * c + 1]));
+                } else {
+                    uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)(n / 2) + 32 * t);
+                    qp[0] = make_uint4(words[0], words[1], words[2], words[3]);
+                    qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
+                }
             }
         }
     }

@@ -145,6 +145,17 @@ __device__ __forceinline__ uint32_t pack8(const uint32_t *c) {
     return (ev & 0x0f0f0f0fu) | ((od << 4) & 0xf0f0f0f0u);
 }
 
+// The operand form of 8 packed codes (one word, code 2k in the low nibble of byte
+// k): one E4M3 byte per code with the code's sign and |q| <= 8 as |q| 2^-9,
+// the even codes in e4m3_even, the odd codes in e4m3_odd (this order within
+// each group of 8 is the W4A4 product's operand order).
+__device__ __forceinline__ uint32_t e4m3_signed_lanes(uint32_t x) {   // byte lanes 0..15 (two's complement)
+    const uint32_t neg = (x >> 3) & 0x01010101u;
+    return (x ^ (neg * 0x8fu)) + neg;
+}
+__device__ __forceinline__ uint32_t e4m3_even(uint32_t w) { return e4m3_signed_lanes(w & 0x0f0f0f0fu); }
+__device__ __forceinline__ uint32_t e4m3_odd(uint32_t w) { return e4m3_signed_lanes((w >> 4) & 0x0f0f0f0fu); }
+
 __device__ __forceinline__ int k4_chunk1(int t, int s) {
     return (t & 7) | (s << 3) | (((t >> 3) & 3) << 6) | ((t >> 5) << 8);
 }

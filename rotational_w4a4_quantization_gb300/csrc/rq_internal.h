@@ -43,6 +43,7 @@ struct GemmArgs {
     int64_t M, N, K;
     void *y;
     int y_mode;
+    bool a_e4m3;    // a_q holds one E4M3 operand byte per code ([M][K]), not packed nibbles
 };
 
 cudaError_t launch_w4a4_gemm(const GemmArgs &args, cudaStream_t stream);

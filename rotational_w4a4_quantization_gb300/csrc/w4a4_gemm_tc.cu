@@ -118,13 +118,13 @@ struct Cfg {
     static_assert(PK_STAGES % kTeams == 0 && OP_STAGES >= kTeams, "parity waits stay one phase ahead at most");
 };
 
-template <bool PAIR, int TEAMS = 3>
+template <bool PAIR, int TEAMS = 3, bool AE = false>
 struct Smem {
     using C = Cfg<PAIR, TEAMS>;
     static constexpr bool kPair = PAIR;
     alignas(1024) uint8_t opA[C::OP_STAGES][C::OP_A];
     alignas(1024) uint8_t opW[C::OP_STAGES][C::OP_W];
-    alignas(128) uint8_t pkA[C::PK_STAGES][C::PK_A];
+    alignas(128) uint8_t pkA[C::PK_STAGES][AE ? 16 : C::PK_A];   // AE: A goes straight into opA
     alignas(128) uint8_t pkW[C::PK_STAGES][C::PK_W];
     alignas(16) int rowsum[2][BM];       // per tile parity: sum_k u_a (the teams add in; the epilogue clears)
     alignas(16) int colsum[2][BN];       // the same for sum_k u_w, this CTA's W rows
@@ -137,6 +137,7 @@ struct Smem {
     uint64_t acc_full[2], acc_empty[2];  // acc_empty (leader): both CTAs' epilogues
     uint64_t sum_full[2], sum_empty[2];  // own converters -> own epilogue and back
     uint64_t col_full[2];                // colterm complete: own and (pair) the peer's epilogue warps
+    uint64_t a_full[C::OP_STAGES];       // AE: this CTA's operand tile of A landed (TMA)
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -334,6 +335,13 @@ __device__ __forceinline__ uint32_t widen(uint32_t w, uint32_t &lo, uint32_t &hi
     return lo + hi;   // four bytes, each <= 30
 }
 
+// Byte lanes holding 4-bit two's-complement codes (0..15) -> E4M3 bytes of the
+// same signed value times 2^-9: |q| <= 8 in bits 0..3, the sign in bit 7.
+__device__ __forceinline__ uint32_t tc_e4m3_lanes(uint32_t x) {
+    const uint32_t neg = (x >> 3) & 0x01010101u;
+    return (x ^ (neg * 0x8fu)) + neg;
+}
+
 template <bool PAIR>
 __device__ __forceinline__ void cluster_sync() {
     if constexpr (PAIR) {
@@ -383,14 +391,21 @@ __device__ __forceinline__ void store_outputs(void *y, int64_t N, int64_t m, int
     }
 }
 
-template <int YMODE, bool PAIR, bool A8, int TEAMS>
+// AE: the activation codes arrive in the operand form (one signed E4M3 byte per
+// code, rq_fwht_quant with RQ_E4M3_CODES): lane 1 of warp 0 loads each K block's
+// 128 x 128-byte A tile by TMA with the 128-byte swizzle straight into the
+// operand ring (completing on a_full), the converters widen only W, with its
+// sign (E4M3 of q 2^-9), and wait for a_full before releasing the operand
+// stage.  Products q_a q_w 2^-18 are exact, so no offset sums are kept.
+template <int YMODE, bool PAIR, bool A8, int TEAMS, bool AE = false>
 __global__ void __launch_bounds__(threads_tc(TEAMS), 1)
 w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                const __grid_constant__ TcParams prm) {
     using C = Cfg<PAIR, TEAMS>;
-    using S = Smem<PAIR, TEAMS>;
+    using S = Smem<PAIR, TEAMS, AE>;
     constexpr int kTeams = C::kTeams, kConvWarps = C::kConvWarps;
     static_assert(!A8 || PAIR, "the W4A8 variant runs on CTA pairs");
+    static_assert(!(A8 && AE), "one activation form");
     extern __shared__ uint8_t smem_raw[];
     // align by offsetting the shared array itself, so the compiler keeps the
     // shared address space (plain LDS/STS instead of generic accesses)
@@ -416,6 +431,7 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int i = 0; i < C::OP_STAGES; ++i) {
             mbar_init(&s.op_full[i], kTeamWarps * C::NCTA);
             mbar_init(&s.op_empty[i], 1);
+            mbar_init(&s.a_full[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.acc_full[i], 1);
@@ -462,9 +478,23 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int kb = 0; kb < kblocks; ++kb, ++g) {
                     const int st = (int)(g % C::PK_STAGES);
                     if (!mbar_wait<false, true>(s, &s.pk_empty[st], (uint32_t)((g / C::PK_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
-                    mbar_expect_tx(&s.pk_full[st], C::PK_A + C::PK_W);
-                    tma_load_2d(s.pkA[st], &tmA, &s.pk_full[st], kb * (A8 ? BK : BK / 2), m0);
+                    mbar_expect_tx(&s.pk_full[st], (AE ? 0 : C::PK_A) + C::PK_W);
+                    if constexpr (!AE) tma_load_2d(s.pkA[st], &tmA, &s.pk_full[st], kb * (A8 ? BK : BK / 2), m0);
                     tma_load_2d(s.pkW[st], &tmW, &s.pk_full[st], kb * (BK / 2), n0);
+                }
+            }
+        } else if (AE && lane == 1) {
+            // operand-form A: each K block's tile into the operand ring once the
+            // MMAs that last read that stage are done
+            int64_t g = 0;
+            bool ok = true;
+            for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step) {
+                const int m0 = (int)(tile % n_tiles_m) * C::TILE_M + (int)rank * BM;
+                for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                    const int os = (int)(g % C::OP_STAGES);
+                    if (!mbar_wait<PAIR, true>(s, &s.op_empty[os], (uint32_t)((g / C::OP_STAGES) & 1) ^ 1, prm.err)) { ok = false; break; }
+                    mbar_expect_tx(&s.a_full[os], C::OP_A);
+                    tma_load_2d(s.opA[os], &tmA, &s.a_full[os], kb * BK, m0);
                 }
             }
         }
@@ -521,9 +551,11 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int ps = (int)(g % C::PK_STAGES);
                 const int os = (int)(g % C::OP_STAGES);
                 if (!mbar_wait(s, &s.pk_full[ps], (uint32_t)((g / C::PK_STAGES) & 1), prm.err)) { ok = false; break; }
-                uint4 a[C::NACH], w[C::NWCH];
+                uint4 a[AE ? 1 : C::NACH], w[C::NWCH];
+                if constexpr (!AE) {
 #pragma unroll
-                for (int j = 0; j < C::NACH; ++j) a[j] = reinterpret_cast<const uint4 *>(s.pkA[ps])[tt + kTeamThreads * j];
+                    for (int j = 0; j < C::NACH; ++j) a[j] = reinterpret_cast<const uint4 *>(s.pkA[ps])[tt + kTeamThreads * j];
+                }
 #pragma unroll
                 for (int j = 0; j < C::NWCH; ++j) w[j] = reinterpret_cast<const uint4 *>(s.pkW[ps])[tt + kTeamThreads * j];
                 if (!warp_wait_commit(s, &s.op_empty[os], (uint32_t)((g / C::OP_STAGES) & 1) ^ 1, lane, prm.err)) { ok = false; break; }
@@ -539,7 +571,9 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     *reinterpret_cast<uint4 *>(rowp + 16 * g0) = make_uint4(lo[0], hi[0], lo[1], hi[1]);
                     *reinterpret_cast<uint4 *>(rowp + 16 * g1) = make_uint4(lo[2], hi[2], lo[3], hi[3]);
                 };
-                if constexpr (A8) {
+                if constexpr (AE) {
+                    // A is in place by TMA (a_full below)
+                } else if constexpr (A8) {
                     // INT8 chunk tt + 128 j = row (tt >> 3) + 16 j, codes 16 c .. 16 c + 15
                     // with c = tt & 7 -> granule c of operand rows 2 row (u_h) and
                     // 2 row + 1 (u_l), in the even-then-odd order of the W side
@@ -567,8 +601,30 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                     for (int j = 0; j < C::NACH; ++j) emit(s.opA[os], rq + 32 * j, a[j], sumA[j]);
                 }
+                if constexpr (AE) {
+                    // W with its sign: E4M3 of q 2^-9, the even codes of each word
+                    // first (the operand order of the activation bytes)
 #pragma unroll
-                for (int j = 0; j < C::NWCH; ++j) emit(s.opW[os], rq + 32 * j, w[j], sumW[j]);
+                    for (int j = 0; j < C::NWCH; ++j) {
+                        const int row = rq + 32 * j;
+                        uint8_t *rowp = s.opW[os] + row * 128;
+                        const uint4 &v = w[j];
+                        const int g0 = (2 * ch) ^ (row & 7), g1 = (2 * ch + 1) ^ (row & 7);
+                        *reinterpret_cast<uint4 *>(rowp + 16 * g0) =
+                            make_uint4(tc_e4m3_lanes(v.x & 0x0f0f0f0fu), tc_e4m3_lanes((v.x >> 4) & 0x0f0f0f0fu),
+                                       tc_e4m3_lanes(v.y & 0x0f0f0f0fu), tc_e4m3_lanes((v.y >> 4) & 0x0f0f0f0fu));
+                        *reinterpret_cast<uint4 *>(rowp + 16 * g1) =
+                            make_uint4(tc_e4m3_lanes(v.z & 0x0f0f0f0fu), tc_e4m3_lanes((v.z >> 4) & 0x0f0f0f0fu),
+                                       tc_e4m3_lanes(v.w & 0x0f0f0f0fu), tc_e4m3_lanes((v.w >> 4) & 0x0f0f0f0fu));
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < C::NWCH; ++j) emit(s.opW[os], rq + 32 * j, w[j], sumW[j]);
+                }
+                // AE: this CTA's A tile must be in place before the stage is released to the MMA
+                if constexpr (AE) {
+                    if (!mbar_wait(s, &s.a_full[os], (uint32_t)((g / C::OP_STAGES) & 1), prm.err)) { ok = false; break; }
+                }
                 // One proxy fence per thread orders its generic reads of the packed
                 // stage before the next TMA refill of it (or the refill can overtake
                 // them) and its operand stores before the tensor core's reads; then
@@ -606,7 +662,9 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // the column terms on to the peer)
             const int buf = it & 1;
             if (!mbar_wait(s, &s.sum_empty[buf], (uint32_t)((it >> 1) & 1) ^ 1, prm.err)) { ok = false; break; }
-            if constexpr (A8) {
+            if constexpr (AE) {
+                // no offset sums: the products are of signed codes
+            } else if constexpr (A8) {
                 if ((tt & 7) == 0) {
 #pragma unroll
                     for (int j = 0; j < C::NACH; ++j) {
@@ -619,7 +677,7 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                 for (int j = 0; j < C::NACH; ++j) atomicAdd(&s.rowsum[buf][rq + 32 * j], (int)sumA[j]);
             }
-            if (ch == 0) {
+            if (!AE && ch == 0) {
 #pragma unroll
                 for (int j = 0; j < C::NWCH; ++j) atomicAdd(&s.colsum[buf][rq + 32 * j], (int)sumW[j]);
             }
@@ -639,7 +697,7 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!mbar_wait<false, true>(s, &s.sum_full[buf], par, prm.err)) break;
             // this CTA's column terms (the sums are cleared for the tile after next)
             for (int cl = e; cl < C::WROWS; cl += 32 * kEpiWarps) {
-                const int v = 64 * (int)prm.K - 8 * s.colsum[buf][cl];
+                const int v = AE ? 0 : 64 * (int)prm.K - 8 * s.colsum[buf][cl];
                 s.colsum[buf][cl] = 0;
                 const int col = (int)rank * C::WROWS + cl;
                 s.colterm[buf][col] = v;
@@ -1161,16 +1219,19 @@ int sm_count() {
 
 // A8: a_q holds M rows of K int8 codes (TMA boxes of 64 rows x 128 bytes), and a
 // tile spans 128 activation rows.
-template <int YMODE, bool PAIR, bool A8 = false, int TEAMS = 3>
+template <int YMODE, bool PAIR, bool A8 = false, int TEAMS = 3, bool AE = false>
 cudaError_t launch_mode(const GemmArgs &g, const TcParams &p, cudaStream_t stream) {
     using C = Cfg<PAIR, TEAMS>;
     CUtensorMap ta, tw;
-    const bool a_ok = A8 ? make_map(&ta, g.a_q, g.M, g.K, BK, BM / 2, CU_TENSOR_MAP_SWIZZLE_NONE)
-                         : make_map(&ta, g.a_q, g.M, g.K / 2, BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+    // AE: 128 rows x 128 bytes of operand-form codes, with the 128-byte swizzle of
+    // the MMA's K-major operand layout
+    const bool a_ok = AE ? make_map(&ta, g.a_q, g.M, g.K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B)
+                         : (A8 ? make_map(&ta, g.a_q, g.M, g.K, BK, BM / 2, CU_TENSOR_MAP_SWIZZLE_NONE)
+                               : make_map(&ta, g.a_q, g.M, g.K / 2, BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE));
     if (!a_ok || !make_map(&tw, g.w_q, g.N, g.K / 2, BK / 2, C::WROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    auto kern = w4a4_tc_kernel<YMODE, PAIR, A8, TEAMS>;
-    const size_t smem = sizeof(Smem<PAIR, TEAMS>) + 1024;
+    auto kern = w4a4_tc_kernel<YMODE, PAIR, A8, TEAMS, AE>;
+    const size_t smem = sizeof(Smem<PAIR, TEAMS, AE>) + 1024;
     // set on every launch: the attribute is per device, and a process may use several
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1244,6 +1305,16 @@ cudaError_t launch_w4a4_gemm_tc(const GemmArgs &g, cudaStream_t stream) {
     if (!p.err) return cudaErrorUnknown;
     const bool pair = g.M > BM;   // tiles of 256 rows on SM pairs; one SM for M <= 128
     const bool t4 = pair;         // four converter teams on pairs (single CTAs: no room)
+    if (g.a_e4m3) {
+        switch (g.y_mode * 2 + (pair ? 1 : 0)) {
+            case 0: return launch_mode<0, false, false, 3, true>(g, p, stream);
+            case 1: return launch_mode<0, true, false, 4, true>(g, p, stream);
+            case 2: return launch_mode<1, false, false, 3, true>(g, p, stream);
+            case 3: return launch_mode<1, true, false, 4, true>(g, p, stream);
+            case 4: return launch_mode<2, false, false, 3, true>(g, p, stream);
+            default: return launch_mode<2, true, false, 4, true>(g, p, stream);
+        }
+    }
     switch (g.y_mode * 3 + (pair ? (t4 ? 2 : 1) : 0)) {
         case 0: return launch_mode<0, false>(g, p, stream);
         case 1: return launch_mode<0, true>(g, p, stream);

@@ -50,6 +50,9 @@ def main(argv=None):
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--group", choices=["128", "channel"], default="128",
                     help="w4a8: weight scales per group of 128 or per output channel")
+    ap.add_argument("--a-form", choices=["packed", "e4m3"], default="packed",
+                    help="fwht: write the codes packed or as the product's E4M3 operand bytes; gemm: feed the "
+                         "product activations in that form (made by the rotation kernel from the workload's X)")
     ap.add_argument("--rows", type=int, default=0,
                     help="gemm, fused, unfused: token rows instead of the workload's (e.g. 16 decode tokens "
                          "through the large workload's 8192 -> 28672 layer)")
@@ -70,11 +73,13 @@ def main(argv=None):
         n = args.n or w.n
         n_out = synth._n_outliers(n) if args.n else w.n_outliers
         x = synth.activations(w.rows, n, w.x_dtype, w.data_seed, n_out, w.outlier_factor).to(dev)
-        q = torch.empty(w.rows, n // 2, dtype=torch.uint8, device=dev)
+        e4 = args.a_form == "e4m3"
+        q = torch.empty(w.rows, n if e4 else n // 2, dtype=torch.uint8, device=dev)
         s = torch.empty(w.rows, dtype=torch.float32, device=dev)
-        fn = lambda: rq.fwht_quant(x, seed, flags, q=q, scales=s)
-        work, unit = w.rows * (n * x.element_size() + n // 2 + 4), "GB/s"
-        what = f"fwht_quant {w.rows}x{n} {str(x.dtype).split('.')[-1]}"
+        fl = flags | (rq.RQ_E4M3_CODES if e4 else 0)
+        fn = lambda: rq.fwht_quant(x, seed, fl, q=q, scales=s)
+        work, unit = w.rows * (n * x.element_size() + (n if e4 else n // 2) + 4), "GB/s"
+        what = f"fwht_quant {w.rows}x{n} {str(x.dtype).split('.')[-1]}{' e4m3 codes' if e4 else ''}"
     elif args.kernel == "kv":
         kw = synth.KV
         k, v = synth.kv_pair(kw.kv_tokens, kw.kv_heads, kw.kv_head_dim, kw.data_seed,
@@ -137,10 +142,13 @@ def main(argv=None):
         aq, sa = synth.random_codes(M, K, 1000 + w.data_seed)
         wq, sw = synth.random_codes(N, K, 1001 + w.data_seed)
         d = [t.to(dev) for t in (aq, sa, wq, sw)]
+        if args.a_form == "e4m3":
+            x = synth.activations(M, K, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor).to(dev)
+            d[0], d[1] = rq.fwht_quant(x, seed, flags | rq.RQ_E4M3_CODES)
         y = torch.empty(M, N, dtype=torch.float16, device=dev)
         fn = lambda: rq.w4a4_gemm(*d, out=y)
         work, unit = 2 * M * N * K, "TOPS"
-        what = f"w4a4_gemm {M}x{K}x{N} fp16"
+        what = f"w4a4_gemm {M}x{K}x{N} fp16{' (e4m3 activations)' if args.a_form == 'e4m3' else ''}"
 
     flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size, dtype=torch.uint8,
                         device=dev)

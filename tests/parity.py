@@ -125,3 +125,25 @@ def record(name: str, **fields):
     os.makedirs(os.path.dirname(os.path.abspath(path)), exist_ok=True)
     with open(path, "a") as f:
         f.write(json.dumps({"test": name, **fields}) + "\n")
+
+
+def operand_form(packed: np.ndarray) -> np.ndarray:
+    """Packed INT4 rows -> the W4A4 product's operand bytes (rq_fwht_quant with
+    RQ_E4M3_CODES): one byte per code, q for q >= 0 and 0x80 | -q for q < 0, and
+    within each group of 8 codes the order 0, 2, 4, 6, 1, 3, 5, 7.  Plain bit
+    arithmetic on the bytes (test-side re-encoding of the oracle's codes)."""
+    rows, half = packed.reshape(-1, packed.shape[-1]).shape
+    b = packed.reshape(rows, half // 4, 4).astype(np.int16)
+    nib = np.concatenate([b & 15, b >> 4], axis=-1)              # even codes, then odd codes
+    byte = np.where(nib >= 8, 0x80 | (16 - nib), nib)
+    return byte.astype(np.uint8).reshape(rows, 2 * half)
+
+
+def from_operand_form(e4: np.ndarray, n: int) -> np.ndarray:
+    """Inverse of operand_form: operand bytes -> int16 codes in natural order."""
+    b = e4.reshape(-1, n // 8, 8).astype(np.int16)
+    q = np.where(b & 0x80, -(b & 0x7F), b & 0x7F)
+    out = np.empty_like(q)
+    out[..., 0::2] = q[..., :4]
+    out[..., 1::2] = q[..., 4:]
+    return out.reshape(-1, n)

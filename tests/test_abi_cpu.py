@@ -86,6 +86,9 @@ def gemm(lib, M=16, N=64, K=256, a=A16, w=A16, sa=A16, sw=A16, y=A16, ydt=2, fla
     (dict(K=200), 2),                 # not a multiple of 128
     (dict(K=131072), 2),
     (dict(flags=1), 1),
+    (dict(flags=32), 1),
+    (dict(flags=16), 2),              # operand-form activations feed the M > 64 kernel only
+    (dict(flags=16, M=0, a=NULL), 0),  # empty: nothing to do
     (dict(ydt=1), 2),                 # bf16 output not offered
     (dict(a=NULL), 1),
     (dict(sa=NULL), 1),
@@ -208,7 +211,12 @@ def test_w4a8_argument_checks(lib, kw, expect):
     (dict(n=14336, ld=14336, flags=4, rows=0), 0),       # and for n = m 2^k (Paley blocks)
     (dict(n=12 * 32, ld=12 * 32, flags=8, rows=0), 0),
     (dict(n=4096, ld=4096, flags=4 | 8, rows=0), 1),     # one mode at a time
-    (dict(n=4096, ld=4096, flags=16, rows=0), 1),        # unknown flag bit
+    (dict(n=4096, ld=4096, flags=32, rows=0), 1),        # unknown flag bit
+    (dict(n=8192, ld=8192, flags=1 | 16, rows=0), 0),    # E4M3 operand codes at n = 8192
+    (dict(n=256, ld=256, flags=16, rows=0), 0),          # and from n = 256 on
+    (dict(n=128, ld=128, flags=16, rows=0), 2),          # not for n <= 128
+    (dict(n=14336, ld=14336, flags=16, rows=0), 2),      # nor for n = m 2^k
+    (dict(n=4096, ld=4096, flags=4 | 16, rows=0), 1),    # one mode at a time
 ])
 def test_fwht_code_mode_checks(lib, kw, expect):
     assert fq(lib, **kw) == expect

@@ -135,3 +135,26 @@ def test_output_guard_bands_untouched():
     rq.fwht_quant(x, 5, rq.RQ_SIGNS_FIRST, q=qbuf[2:2 + rows], scales=sbuf[4:4 + rows])
     assert bool((qbuf[:2] == 0xA5).all()) and bool((qbuf[2 + rows:] == 0xA5).all())
     assert bool((sbuf[:4] == -3.0).all()) and bool((sbuf[4 + rows:] == -3.0).all())
+
+
+
+@pytest.mark.parametrize("n", [256, 1024, 2048, 4096, 8192])
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
+def test_e4m3_operand_codes(n, dt, flags):
+    """RQ_E4M3_CODES: the same codes and scales as the packed INT4 output, one
+    operand byte per code (decoded here by bit arithmetic), and the oracle's codes
+    within the tie window."""
+    from parity import from_operand_form, unpack_codes
+    rows = 77
+    x = synth.activations(rows, n, dt, n + rows, 4, 100.0)
+    xd = x.to(DEV)
+    q_p, s_p = rq.fwht_quant(xd, 5, flags)
+    q_e, s_e = rq.fwht_quant(xd, 5, flags | rq.RQ_E4M3_CODES)
+    assert q_e.shape == (rows, n) and q_e.dtype == torch.uint8
+    assert torch.equal(s_e, s_p)
+    codes_e = from_operand_form(to_np(q_e), n)
+    assert np.array_equal(codes_e, unpack_codes(to_np(q_p), n))
+    assert np.abs(codes_e).max() <= 8
+    ref = oracle.fwht_quant(x.double().numpy(), 5, flags, want_ratio=True)
+    compare_codes(oracle.pack(codes_e.astype(np.int8)), ref["q"], ref["ratio"], n)

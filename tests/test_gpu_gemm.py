@@ -15,7 +15,7 @@ import oracle
 import rotational_w4a4_quantization_gb300 as rq
 from rotational_w4a4_quantization_gb300 import synth
 
-from parity import compare_f16, host_threads, oracle_gemm_row_blocks, record, to_dev, to_np
+from parity import compare_f16, host_threads, operand_form, oracle_gemm_row_blocks, record, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -226,3 +226,65 @@ def test_decode_tensor_core_large_model_width():
         r1 = r0 + r_acc.shape[0]
         np.testing.assert_array_equal(acc_np[r0:r1], r_acc)
         np.testing.assert_allclose(yf[r0:r1], r_y, rtol=1e-5, atol=0)
+
+
+
+# Activations in the operand form (RQ_A_E4M3, M > 64): the product reads the
+# codes as signed E4M3 bytes straight into its operand ring and widens only W.
+def _e4m3_all_modes(aq, sa, wq, sw):
+    ae = torch.from_numpy(operand_form(aq.numpy())).to(DEV)
+    d = [t.to(DEV) for t in (sa, wq, sw)]
+    return {dt: to_np(rq.w4a4_gemm(ae, d[0], d[1], d[2], out_dtype=dt)) for dt in (torch.int32, torch.float32, torch.float16)}
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (65, 256, 128), (100, 136, 512), (128, 256, 256), (130, 264, 512), (256, 512, 1024), (300, 392, 640),
+    (384, 20480, 640), (256, 40960, 384), (512, 1024, 4096),
+])
+def test_e4m3_activations_shapes(M, N, K):
+    aq, sa, wq, sw = _codes(M, N, K, 5 * M + N)
+    out = _e4m3_all_modes(aq, sa, wq, sw)
+    assert rq.sync_status() == 0
+    acc, y = oracle.w4a4_gemm(aq.numpy(), sa.numpy(), wq.numpy(), sw.numpy(), M, N, K)
+    np.testing.assert_array_equal(out[torch.int32].astype(np.int64), acc)
+    np.testing.assert_allclose(out[torch.float32], y, rtol=1e-5, atol=0)
+    compare_f16(out[torch.float16], y)
+
+
+@pytest.mark.parametrize("ba,bw", [(0x77, 0x77), (0x88, 0x88), (0x88, 0x77), (0x78, 0x87)])
+def test_e4m3_activations_extreme_codes_at_max_k(ba, bw):
+    M, N, K = 256, 256, 65536
+    aq = synth.extreme_codes(M, K, ba)
+    wq = synth.extreme_codes(N, K, bw)
+    one_m, one_n = torch.ones(M), torch.ones(N)
+    ae = torch.from_numpy(operand_form(aq.numpy())).to(DEV)
+    acc = to_np(rq.w4a4_gemm(ae, one_m.to(DEV), wq.to(DEV), one_n.to(DEV), out_dtype=torch.int32))
+    ref, _ = oracle.w4a4_gemm(aq[:1].numpy(), one_m[:1].numpy(), wq[:1].numpy(), one_n[:1].numpy(), 1, 1, K)
+    assert (acc.astype(np.int64) == ref[0, 0]).all()
+
+
+@pytest.mark.parametrize("name", ["prefill", "large"])
+def test_e4m3_activations_workload_full_output(name):
+    """Every output of the prefill and large products with operand-form activations."""
+    w = synth.WORKLOADS[name]
+    M, N, K = w.rows, w.gemm_n, w.n
+    aq, sa, wq, sw = _codes(M, N, K, 2000 + w.data_seed)
+    out = _e4m3_all_modes(aq, sa, wq, sw)
+    acc_np = out[torch.int32].astype(np.int64)
+    for r0, r_acc, r_y in oracle_gemm_row_blocks(aq.numpy(), sa.numpy(), wq.numpy(), sw.numpy(), M, N, K):
+        r1 = r0 + r_acc.shape[0]
+        np.testing.assert_array_equal(acc_np[r0:r1], r_acc)
+        np.testing.assert_allclose(out[torch.float32][r0:r1], r_y, rtol=1e-5, atol=0)
+        compare_f16(out[torch.float16][r0:r1], r_y)
+
+
+def test_e4m3_path_end_to_end_matches_packed_path():
+    """Rotation in operand form, then the product, equals the packed-code path bit for bit."""
+    M, N, K = 384, 1024, 4096
+    x = synth.activations(M, K, torch.bfloat16, 9, 4, 100.0).to(DEV)
+    wq, sw = synth.random_codes(N, K, 10)
+    wd, sd = wq.to(DEV), sw.to(DEV)
+    qp, sp = rq.fwht_quant(x, 7, rq.RQ_SIGNS_FIRST)
+    qe, se = rq.fwht_quant(x, 7, rq.RQ_SIGNS_FIRST | rq.RQ_E4M3_CODES)
+    for dt in (torch.int32, torch.float32, torch.float16):
+        assert torch.equal(rq.w4a4_gemm(qe, se, wd, sd, out_dtype=dt), rq.w4a4_gemm(qp, sp, wd, sd, out_dtype=dt))
