@@ -1,7 +1,9 @@
 """Benchmark of the rotation-based W4A4 hot path on GB300.
 
 One step = one pass of the whole online path over one batch of synthetic input:
-  1. rq_fwht_quant      X (tokens x hidden, bf16) -> packed INT4 codes + scales
+  1. rq_fwht_quant      X (tokens x hidden, bf16) -> INT4 codes + scales (the codes
+                        stored as the product's E4M3 operand bytes; --a-form packed
+                        writes them two per byte instead)
   2. rq_w4a4_gemm       codes x folded INT4 weights -> Y (tokens x out, fp16)
   3. rq_kv_rotate_quant K, V ([tokens][heads][head_dim] bf16) -> packed INT4 cache
 The weights are folded and quantized once, before timing (the offline step).
@@ -91,8 +93,10 @@ def host_info():
 # work accounting (algorithmic bytes / ops)
 # --------------------------------------------------------------------------
 
-def fwht_bytes(rows, n, in_bytes=2):
-    return rows * (n * in_bytes + n // 2 + 4)
+def fwht_bytes(rows, n, in_bytes=2, code_bytes_per_elem=0.5):
+    """Read the row once, write its codes (packed: n/2 bytes; operand form: n)
+    and scale once."""
+    return rows * (n * in_bytes + int(n * code_bytes_per_elem) + 4)
 
 
 def gemm_ops(M, N, K):
@@ -263,6 +267,8 @@ def run_gpu(args, work, kvw):
 
     seed, flags = synth.SIGN_SEED, rq.RQ_SIGNS_FIRST
     M, K, N = work.rows, work.n, work.gemm_n
+    e4 = args.a_form == "e4m3"                      # activation codes as the product's operand bytes
+    aflags = flags | (rq.RQ_E4M3_CODES if e4 else 0)
     T, H, D = kvw.kv_tokens, kvw.kv_heads, kvw.kv_head_dim
     x_cpu, wt_cpu, k_cpu, v_cpu = make_inputs(work, kvw, dev)
     x, k, v = x_cpu.to(dev), k_cpu.to(dev), v_cpu.to(dev)
@@ -272,7 +278,7 @@ def run_gpu(args, work, kvw):
     del wt_cpu
 
     # preallocated outputs
-    aq = torch.empty(M, K // 2, dtype=torch.uint8, device=dev)
+    aq = torch.empty(M, K if e4 else K // 2, dtype=torch.uint8, device=dev)
     as_ = torch.empty(M, dtype=torch.float32, device=dev)
     y = torch.empty(M, N, dtype=torch.float16, device=dev)
     kv_out = {"kq": torch.empty(T, H, D // 2, dtype=torch.uint8, device=dev),
@@ -286,7 +292,7 @@ def run_gpu(args, work, kvw):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        rq.fwht_quant(x, seed, flags, q=aq, scales=as_)
+        rq.fwht_quant(x, seed, aflags, q=aq, scales=as_)
         if ev:
             ev[1].record(stream)
         rq.w4a4_gemm(aq, as_, wq, ws, out=y)
@@ -372,7 +378,7 @@ def run_gpu(args, work, kvw):
         s_run.wait_event(ev_in[j])
         if i >= 2:
             s_run.wait_event(ev_out[j])     # step i-2's outputs have been copied out
-        rq.fwht_quant(b["x"], seed, flags, q=b["aq"], scales=b["as"], stream=s_run)
+        rq.fwht_quant(b["x"], seed, aflags, q=b["aq"], scales=b["as"], stream=s_run)
         rq.w4a4_gemm(b["aq"], b["as"], wq, ws, out=b["y"], stream=s_run)
         rq.kv_rotate_quant(b["k"], b["v"], seed, flags, out=b["kv"], stream=s_run)
         ev_run[j].record(s_run)
@@ -399,7 +405,7 @@ def run_gpu(args, work, kvw):
 
     # the FP8 tensor pipe alone, at this run's clocks (after the timed steps)
     probe = probe_f8_pipe(stream)
-    parity = parity_sample(work, kvw, x_cpu, k_cpu, v_cpu, x, k, v, aq, as_, kv_out) if rank == 0 else None
+    parity = parity_sample(work, kvw, x_cpu, k_cpu, v_cpu, x, k, v, aq, as_, kv_out, e4) if rank == 0 else None
 
     if rank != 0:
         return None
@@ -407,7 +413,7 @@ def run_gpu(args, work, kvw):
     peaks = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     avg = {key: sum(vals) / len(vals) for key, vals in per.items()}
-    fb = fwht_bytes(M, K)
+    fb = fwht_bytes(M, K, code_bytes_per_elem=1.0 if e4 else 0.5)
     gb_ops = gemm_ops(M, N, K)
     kb = kv_bytes(T, H, D)
     kernels = {
@@ -453,7 +459,7 @@ def run_gpu(args, work, kvw):
         "vs_baseline": None,
         "dtype": "int4",
         "data": "synthetic",
-        "config": bench_config(work, kvw, world),
+        "config": bench_config(work, kvw, world, args.a_form),
         "kernels": kernels,
         "parity": parity,
         "roofline": roof,
@@ -490,7 +496,7 @@ def probe_f8_pipe(stream):
             "shape": "M128 N256 K32 kind::f8f6f4 (e4m3), zeros in shared memory"}
 
 
-def parity_sample(work, kvw, x_cpu, k_cpu, v_cpu, x, k, v, aq, as_, kv_out, rows=64, kv_tokens=64):
+def parity_sample(work, kvw, x_cpu, k_cpu, v_cpu, x, k, v, aq, as_, kv_out, e4, rows=64, kv_tokens=64):
     """Codes of a sample of the step's rows against the oracle's (first and last
     `rows` activation rows, first and last `kv_tokens` tokens of K and V): the
     number of codes that differ (each must lie in the half-integer tie window and
@@ -504,8 +510,17 @@ def parity_sample(work, kvw, x_cpu, k_cpu, v_cpu, x, k, v, aq, as_, kv_out, rows
         nib = np.stack([b & 15, b >> 4], axis=-1).reshape(packed.shape[0], -1)
         return np.where(nib >= 8, nib - 16, nib)
 
-    def diff_count(gq, ref):
-        g, r = decode(gq), decode(ref["q"])
+    def decode_operand(ob):
+        # operand bytes: sign in bit 7, |q| in bits 0..3; codes 0,2,4,6,1,3,5,7 of each group of 8
+        b = ob.astype(np.int16).reshape(ob.shape[0], -1, 8)
+        q = np.where(b & 0x80, -(b & 0x7F), b & 0x7F)
+        out = np.empty_like(q)
+        out[..., 0::2] = q[..., :4]
+        out[..., 1::2] = q[..., 4:]
+        return out.reshape(ob.shape[0], -1)
+
+    def diff_count(gq, ref, operand=False):
+        g, r = (decode_operand(gq) if operand else decode(gq)), decode(ref["q"])
         d = g != r
         tie = oracle.tie_mask(ref["ratio"])
         bad = d & ~(tie & (np.abs(g - r) == 1))
@@ -518,7 +533,7 @@ def parity_sample(work, kvw, x_cpu, k_cpu, v_cpu, x, k, v, aq, as_, kv_out, rows
     M, n = x_cpu.shape
     sel = np.unique(np.r_[np.arange(min(rows, M)), np.arange(max(0, M - rows), M)])
     ref = oracle.fwht_quant(x_cpu[sel].double().numpy(), seed, flags, want_y=True, want_ratio=True)
-    a_diff, a_tie = diff_count(aq[torch.from_numpy(sel).to(aq.device)].cpu().numpy(), ref)
+    a_diff, a_tie = diff_count(aq[torch.from_numpy(sel).to(aq.device)].cpu().numpy(), ref, operand=e4)
     _, _, ygpu = rq.fwht_quant(x[torch.from_numpy(sel).to(x.device)].contiguous(), seed, flags, want_y=True)
     yg = ygpu.cpu().double().numpy()
     err = (np.abs(yg - ref["y"]).max(axis=1) / np.abs(ref["y"]).max(axis=1)).max()
@@ -538,9 +553,11 @@ def parity_sample(work, kvw, x_cpu, k_cpu, v_cpu, x, k, v, aq, as_, kv_out, rows
             "gemm": "bit-exact int32 on the full output of every workload: GPU tests (oracle over row blocks)"}
 
 
-def bench_config(work, kvw, world):
+def bench_config(work, kvw, world, a_form="e4m3"):
     """The `config` object, the same for both arms."""
     return {"workload": workload_desc(work, kvw),
+            "activation_codes": ("INT4 codes stored as the product's E4M3 operand bytes (1 byte per code)"
+                                 if a_form == "e4m3" else "INT4 codes packed two per byte"),
             "l2": "flushed between timed steps (2x L2 write, outside timed events)",
             "parallelism": f"replicas x{world}" if world > 1 else "none (one process)"}
 
@@ -613,7 +630,7 @@ def run_reference(args, work, kvw):
         "full_step_ms_extrapolated": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4",
         "data": "synthetic",
-        "config": bench_config(work, kvw, world),
+        "config": bench_config(work, kvw, world, args.a_form),
         "cpu_baseline": {"value": value, "unit": "TOPS", "cores": 1, "kind": "oracle",
                          "sample": f"each step: {gemm_rows} GEMM rows, 16 rotation rows, 64 KV tokens, "
                                    "scaled by rows to one full step; one host core",
@@ -630,6 +647,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["rq", "reference"], default="rq")
     ap.add_argument("--workload", choices=["prefill", "large", "decode", "tiny"], default="large")
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed steps while clocks are sampled")
+    ap.add_argument("--a-form", choices=["e4m3", "packed"], default="e4m3",
+                    help="activation codes between the rotation and the product: the product's E4M3 operand "
+                         "bytes (default) or packed INT4 nibbles")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args(argv)
