@@ -45,8 +45,10 @@
 //  * CTAs are persistent: each computes the sign masks of its n positions once
 //    (SplitMix64, one call per element) into shared memory, while its first
 //    input copies are in flight, and then walks groups of rows.
-//  * n = 4096 (the activation size of the serving path) has its own variant
-//    with 64 values per thread and three butterfly phases (see below).
+//  * n = 4096 and n = 8192 (the activation sizes of the serving paths) have
+//    their own variants with 64 values per thread and three butterfly phases
+//    joined by two shared-memory transposes, without shuffles (see below); the
+//    plans above serve n <= 2048.
 #include "rq.h"
 #include "rq_internal.h"
 #include "rot_device.cuh"
@@ -902,6 +904,316 @@ cudaError_t launch_k4(const KParams &p, int threads, cudaStream_t stream) {
     }
 }
 
+// --------------------------------------------------------------------------
+// n = 8192: three butterfly phases with two transposes, 64 values per thread,
+// four warps per row.  Element i = 8c + e (chunk c, 10 bits) = 4q + e' (quad q,
+// 11 bits); thread t = 0..127 of a row is lane + 32 wr:
+//   phase 1: chunk slots s = chunk bits 3,4,5 (8 chunks); lane bits 0..2 ->
+//            chunk bits 0..2, lane bits 3,4 -> 6,7, wr -> 8,9, so each warp
+//            copies and reads a contiguous quarter row (eight lanes read 128
+//            contiguous bytes); stages on element bits 0,1,2 and 6,7,8;
+//   phase 2: quad slots = quad bits 7..10 (16 quads); lane -> quad bits 0..4,
+//            wr -> 5,6; stages on element bits 9..12;
+//   phase 3: quad slots = quad bits 0..3; t -> quad bits 4..10; stages on
+//            element bits 3,4,5, and the thread ends with 64 consecutive
+//            elements (its 64 codes are 32 or 64 contiguous bytes).
+// Stage order 0,1,2,6,7,8,9,10,11,12,3,4,5 (the fused decode kernel runs the
+// same order for K = 8192, so its codes are these bit for bit).
+// Row buffer: fp32 quads in 16-byte granules.  The first transpose keeps quad q
+// at q ^ q3 (quad bit 3 into bit 0), the second at q ^ (q4, q5, q6) (bits 0..2):
+// every 8-lane phase of both sides of both transposes then touches 8 distinct
+// bank groups, and every access but the last transpose's reads is a thread base
+// plus a compile-time offset (checked exhaustively on the host for all t, s).
+// --------------------------------------------------------------------------
+constexpr int K8_LOGN = 13, K8_N = 8192;
+
+__host__ __device__ constexpr int k8_max_rows(int in_type) { return in_type == IN_F32 ? 2 : 4; }
+// Rows per CTA: the most that fit, or fewer for small batches so that they
+// spread over more SMs (16 decode rows: 16 CTAs instead of 4).
+inline int k8_pick_rows(int64_t rows, int in_type, int sms) {
+    for (int r = k8_max_rows(in_type); r > 1; r /= 2)
+        if ((rows + r - 1) / r >= sms) return r;
+    return 1;
+}
+
+template <int IN, int ROWS>
+size_t k8_smem_bytes() {
+    constexpr int ES = IN == IN_F32 ? 4 : 2;
+    // barriers | sign words | absmax exchange | per-warp input quarters | fp32 row buffers
+    return 128 + (size_t)K8_N * 2 + 128 + (size_t)(4 * ROWS) * (K8_N * ES / 4) + (size_t)ROWS * K8_N * 4;
+}
+
+template <int IN, int ROWS>
+__global__ void __launch_bounds__(128 * ROWS, 1)
+fwht_quant_k8_kernel(const __grid_constant__ KParams prm) {
+    constexpr int n = K8_N;
+    constexpr int THREADS = 128 * ROWS, NW = THREADS / 32;
+    constexpr int G = IN == IN_F32 ? 2 : 1;              // 16-byte granules per input chunk
+    constexpr int ES = IN == IN_F32 ? 4 : 2;
+    constexpr int QB = n * ES / 4;                        // input bytes of a quarter row (one warp)
+    constexpr int NP = 32;                                // fp32 pairs per thread
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw);                  // NW
+    uint32_t *sgn = reinterpret_cast<uint32_t *>(smem_raw + 128);             // n/2 words
+    float *red = reinterpret_cast<float *>(smem_raw + 128 + n * 2);          // ROWS*4
+    unsigned char *inbuf = smem_raw + 128 + n * 2 + 128;                      // NW quarters
+    ulonglong2 *rowbuf = reinterpret_cast<ulonglong2 *>(inbuf + NW * QB);    // ROWS rows
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row_in_cta = warp >> 2;
+    const int t = threadIdx.x & 127;
+    const int wr = t >> 5;
+    const bool signs_first = (prm.flags & 1u) != 0;
+    const uint32_t msel = signs_first ? 0xffffffffu : 0u;
+    const unsigned full = 0xffffffffu;
+    const int64_t total_groups = prm.groups_per_job * prm.njobs;
+    unsigned char *wbuf = inbuf + warp * QB;
+    ulonglong2 *buf = rowbuf + (size_t)row_in_cta * (n / 4);
+    const uint32_t rbar = 1 + row_in_cta;                  // named barrier of the row's four warps
+    // thread bases of every access (slot s adds a compile-time offset)
+    const int c1 = (lane & 7) | ((lane >> 3) << 6) | (wr << 8);                 // phase-1 chunk of slot s: c1 + 8 s
+    const uint4 *sg1 = reinterpret_cast<const uint4 *>(sgn) + c1;               // its sign words: sg1[8 s]
+    const uint4 *sg3 = reinterpret_cast<const uint4 *>(sgn) + 8 * t;            // output chunk 8 t + c: sg3[c]
+    const unsigned char *xb = wbuf + 16 * G * (c1 & 255);                       // its input: + 128 G s
+    const int w1 = (2 * c1) ^ ((c1 >> 2) & 1);
+    ulonglong2 *const bw1[2] = {buf + w1, buf + (w1 ^ 1)};                      // quad 2 chunk + h: bw1[h][16 s]
+    const int q2 = lane | (wr << 5);                                            // phase-2 quad of slot s: q2 + 128 s
+    const ulonglong2 *const br1 = buf + (q2 ^ ((q2 >> 3) & 1));                 // [128 s]
+    ulonglong2 *const bw2 = buf + (q2 ^ ((q2 >> 4) & 7));                       // [128 s]
+    const ulonglong2 *const br2 = buf + 16 * t;                                 // quad 16 t + s: [s ^ m3]
+    const int m3 = t & 7;
+
+    if (threadIdx.x < NW) mbar_init(&bars[threadIdx.x], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();    // barriers initialized before the warps issue their first copies
+
+    // This warp's quarter of row (group g, row_in_cta): chunks with bits 8,9 = wr.
+    auto issue = [&](int64_t g) {
+        const int jb = job_of(g, prm.groups_per_job);
+        const RotJob &job = prm.job[jb];
+        const int64_t row = (g - (int64_t)jb * prm.groups_per_job) * ROWS + row_in_cta;
+        const bool valid = row < job.rows;
+        mbar_expect_tx(&bars[warp], valid ? (uint32_t)QB : 0u);
+        if (valid)
+            bulk_copy(wbuf, static_cast<const char *>(job.x) + (row * job.ld) * ES + wr * QB, QB, &bars[warp]);
+    };
+    if (lane == 0 && (int64_t)blockIdx.x < total_groups) issue(blockIdx.x);
+    // Sign masks (computed while the first copies are in flight): word j covers
+    // elements 2j (bit 15) and 2j+1 (bit 31).
+    for (int j = threadIdx.x; j < n / 2; j += THREADS) {
+        const uint32_t s0 = (uint32_t)(splitmix64_at(prm.seed, 2ull * j) >> 63);
+        const uint32_t s1 = (uint32_t)(splitmix64_at(prm.seed, 2ull * j + 1) >> 63);
+        sgn[j] = (s0 << 15) | (s1 << 31);
+    }
+    __syncthreads();
+
+    const float inv_sqrt_n = 0.70710678118654752440f / 64.0f;
+    uint32_t phase = 0;
+    bool aborted = false;
+    for (int64_t grp = blockIdx.x; grp < total_groups; grp += gridDim.x) {
+        const int jb = job_of(grp, prm.groups_per_job);
+        const RotJob &job = prm.job[jb];
+        const int64_t row = (grp - (int64_t)jb * prm.groups_per_job) * ROWS + row_in_cta;
+
+        pair_t v[NP];
+        // ---------------- phase 1: input, signs, 6 stages ----------------
+        // A copy that never lands raises the error word; the iteration then runs
+        // on stale data with its stores disabled, so barriers stay matched.
+        if (!mbar_wait_bounded(&bars[warp], phase, prm.err)) aborted = true;
+        phase ^= 1u;
+        const bool active = row < job.rows && !aborted;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint4 m = sg1[8 * s];
+            uint4 g[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) g[h] = *reinterpret_cast<const uint4 *>(xb + 128 * G * s + 16 * h);
+            convert_chunk<IN>(g, m, msel, &v[4 * s]);   // includes the in-pair stage
+        }
+        // hand the quarter back to the copy engine (generic reads before the
+        // next bulk write) and fetch this warp's quarter of its next row
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0 && !aborted && grp + gridDim.x < total_groups) issue(grp + gridDim.x);
+#pragma unroll
+        for (int rb = 1; rb <= 5; ++rb) butterfly_pairs<NP>(v, rb);
+
+        // ---------------- transpose 1, phase 2 ----------------
+        // (the previous row's last reads of the buffer came before its absmax barrier)
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            bw1[0][16 * s] = make_ulonglong2(v[4 * s], v[4 * s + 1]);
+            bw1[1][16 * s] = make_ulonglong2(v[4 * s + 2], v[4 * s + 3]);
+        }
+        asm volatile("bar.sync %0, 128;" ::"r"(rbar) : "memory");
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            const ulonglong2 q = br1[128 * s];
+            v[2 * s] = q.x; v[2 * s + 1] = q.y;
+        }
+#pragma unroll
+        for (int rb = 2; rb <= 5; ++rb) butterfly_pairs<NP>(v, rb);
+
+        // ---------------- transpose 2, phase 3 ----------------
+        asm volatile("bar.sync %0, 128;" ::"r"(rbar) : "memory");   // every thread has read transpose 1
+#pragma unroll
+        for (int s = 0; s < 16; ++s) bw2[128 * s] = make_ulonglong2(v[2 * s], v[2 * s + 1]);
+        asm volatile("bar.sync %0, 128;" ::"r"(rbar) : "memory");
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            const ulonglong2 q = br2[s ^ m3];
+            v[2 * s] = q.x; v[2 * s + 1] = q.y;
+        }
+#pragma unroll
+        for (int rb = 3; rb <= 5; ++rb) butterfly_pairs<NP>(v, rb);
+
+        // ---------------- row absmax (four warps) ----------------
+        float amax = pairs_absmax<NP>(v);
+        // a group of 128 elements (per-group scales) is the 64 of threads t and t ^ 1
+        const float amax_grp = fmaxf(amax, __shfl_xor_sync(full, amax, 1));
+#pragma unroll
+        for (int k = 0; k < 5; ++k) amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1 << k));
+        if (lane == 0) red[row_in_cta * 4 + wr] = aborted ? __int_as_float(-1) : amax;
+        asm volatile("bar.sync %0, 128;" ::"r"(rbar) : "memory");
+        const float4 r4 = reinterpret_cast<const float4 *>(red)[row_in_cta];
+        // the four warps of a row leave together: share the abort decision
+        const bool any_abort = __float_as_int(r4.x) == -1 || __float_as_int(r4.y) == -1 ||
+                               __float_as_int(r4.z) == -1 || __float_as_int(r4.w) == -1;
+        amax = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
+        if (any_abort) { aborted = true; break; }
+
+        // ---------------- quantize, pack, store: 64 consecutive elements ----------------
+        if (active) {
+            // codes: INT4 per row (default), INT8 per row, or INT4 per group of 128
+            const bool i8 = (prm.flags & RQ_INT8_CODES) != 0, grp = (prm.flags & RQ_GROUP_SCALES) != 0;
+            const bool e4 = (prm.flags & RQ_E4M3_CODES) != 0;
+            const float am = grp ? amax_grp : amax;
+            const float qmax = i8 ? 127.0f : 7.0f;
+            const float inv = am > 0.f ? qmax / am : 0.f;
+            const pair_t inv2 = mk2(inv, inv);
+            const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
+            if (grp) {
+                if ((t & 1) == 0) job.scales[row * (int64_t)(n / 128) + (t >> 1)] = (am / 7.0f) * inv_sqrt_n;
+            } else if (t == 0) {
+                job.scales[row] = (am / qmax) * inv_sqrt_n;
+            }
+            // the thread's 64 consecutive elements are chunks 8t + c (pairs 4c .. 4c+3);
+            // one branch per row for each option (signs after the transform, fp32 output)
+            if (!signs_first) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 m = sg3[c];
+                    const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        v[4 * c + k] ^= ((pair_t)(mm[k] & 0x80000000u) << 32) | (pair_t)(mm[k] << 16);
+                }
+            }
+            if (job.y) {
+                const pair_t sc2 = mk2(inv_sqrt_n, inv_sqrt_n), z2 = 0ull;
+                ulonglong2 *yp = reinterpret_cast<ulonglong2 *>(job.y + row * (int64_t)n + 64 * t);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) yp[c] = make_ulonglong2(fma2(v[2 * c], sc2, z2), fma2(v[2 * c + 1], sc2, z2));
+            }
+            if (i8) {
+                // one byte per code (the low byte of the biased float is the
+                // two's-complement code): 64 bytes, four 16-byte stores
+                uint32_t words[16];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t code[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const pair_t qq = fma2(v[4 * c + k], inv2, bias2);
+                        code[2 * k] = (uint32_t)qq;
+                        code[2 * k + 1] = (uint32_t)(qq >> 32);
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        words[2 * c + h] = __byte_perm(__byte_perm(code[4 * h], code[4 * h + 1], 0x0040u),
+                                                       __byte_perm(code[4 * h + 2], code[4 * h + 3], 0x0040u), 0x5410u);
+                }
+                uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)n + 64 * t);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    qp[c] = make_uint4(words[4 * c], words[4 * c + 1], words[4 * c + 2], words[4 * c + 3]);
+            } else if (e4) {
+                // one signed E4M3 byte per code, in the product's operand order
+                // (even codes, then odd codes, of each chunk): 64 bytes
+                uint32_t words[16];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t code[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const pair_t qq = fma2(v[4 * c + k], inv2, bias2);
+                        code[2 * k] = (uint32_t)qq;
+                        code[2 * k + 1] = (uint32_t)(qq >> 32);
+                    }
+                    words[2 * c] = e4m3_word(code[0], code[2], code[4], code[6]);
+                    words[2 * c + 1] = e4m3_word(code[1], code[3], code[5], code[7]);
+                }
+                uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)n + 64 * t);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    qp[c] = make_uint4(words[4 * c], words[4 * c + 1], words[4 * c + 2], words[4 * c + 3]);
+            } else {
+                uint32_t words[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t code[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const pair_t qq = fma2(v[4 * c + k], inv2, bias2);
+                        code[2 * k] = (uint32_t)qq;
+                        code[2 * k + 1] = (uint32_t)(qq >> 32);
+                    }
+                    words[c] = pack8(code);
+                }
+                uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)(n / 2) + 32 * t);
+                qp[0] = make_uint4(words[0], words[1], words[2], words[3]);
+                qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
+            }
+        }
+    }
+    if (aborted) {
+        // wait (bounded) for this warp's copy still in flight before leaving
+        mbar_wait_bounded(&bars[warp], phase, prm.err);
+    }
+}
+
+template <int IN, int ROWS>
+cudaError_t launch_k8_t(const KParams &p, cudaStream_t stream) {
+    auto kern = fwht_quant_k8_kernel<IN, ROWS>;
+    const size_t smem = k8_smem_bytes<IN, ROWS>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128 * ROWS, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t total = p.groups_per_job * p.njobs;
+    int64_t grid = (int64_t)sms * per_sm;
+    if (grid > total) grid = total;
+    kern<<<(unsigned)grid, 128 * ROWS, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int IN>
+cudaError_t launch_k8(const KParams &p, int rows, cudaStream_t stream) {
+    switch (rows) {
+        case 1: return launch_k8_t<IN, 1>(p, stream);
+        case 2: return launch_k8_t<IN, 2>(p, stream);
+        default:
+            if constexpr (k8_max_rows(IN) >= 4) return launch_k8_t<IN, 4>(p, stream);
+            return cudaErrorInvalidValue;
+    }
+}
+
 template <int LOGN, int IN>
 size_t smem_bytes() {
     using PL = Plan<LOGN - 3>;
@@ -985,15 +1297,18 @@ cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_t
     if (!p.err) return cudaErrorUnknown;
     const int C = log_n - 3;
     const int S = C <= 3 ? C : (C == 4 ? 3 : 4);      // as in Plan<C>
-    int k4_threads = 0;
-    if (log_n == K4_LOGN) {
+    int k4_threads = 0, k8_rows = 0;
+    if (log_n == K4_LOGN || log_n == K8_LOGN) {
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return cudaErrorUnknown;
-        k4_threads = k4_pick_threads(max_rows, in_type, sms);
+        if (log_n == K4_LOGN) k4_threads = k4_pick_threads(max_rows, in_type, sms);
+        else k8_rows = k8_pick_rows(max_rows, in_type, sms);
     }
-    const int rows_per_group = log_n == K4_LOGN ? k4_threads / 64 : threads_for(log_n, in_type) >> (C - S);
+    const int rows_per_group = log_n == K4_LOGN   ? k4_threads / 64
+                               : log_n == K8_LOGN ? k8_rows
+                                                  : threads_for(log_n, in_type) >> (C - S);
     p.groups_per_job = (max_rows + rows_per_group - 1) / rows_per_group;
     if (p.groups_per_job == 0) return cudaSuccess;
     switch (log_n) {
@@ -1011,7 +1326,13 @@ cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_t
                 case IN_F16: return launch_k4<IN_F16>(p, k4_threads, stream);
                 default: return cudaErrorInvalidValue;
             }
-        case 13: return launch_n<13>(p, in_type, stream);
+        case 13:
+            switch (in_type) {
+                case IN_F32: return launch_k8<IN_F32>(p, k8_rows, stream);
+                case IN_BF16: return launch_k8<IN_BF16>(p, k8_rows, stream);
+                case IN_F16: return launch_k8<IN_F16>(p, k8_rows, stream);
+                default: return cudaErrorInvalidValue;
+            }
         default: return cudaErrorInvalidValue;
     }
 }

@@ -156,6 +156,21 @@ __device__ __forceinline__ uint32_t e4m3_signed_lanes(uint32_t x) {   // byte la
 __device__ __forceinline__ uint32_t e4m3_even(uint32_t w) { return e4m3_signed_lanes(w & 0x0f0f0f0fu); }
 __device__ __forceinline__ uint32_t e4m3_odd(uint32_t w) { return e4m3_signed_lanes((w >> 4) & 0x0f0f0f0fu); }
 
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+// The same operand bytes straight from four codes, each the low byte of a word
+// (two's complement, |q| <= 7): gather the bytes, then turn each negative one
+// into sign and magnitude (a selector nibble with bit 3 set replicates the sign
+// of its byte, so `neg` holds 0xff in the bytes of negative codes).
+__device__ __forceinline__ uint32_t e4m3_word(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
+    const uint32_t x = prmt_b32(prmt_b32(c0, c1, 0x0040u), prmt_b32(c2, c3, 0x0040u), 0x5410u);
+    const uint32_t neg = prmt_b32(x, 0u, 0xba98u);
+    return (x ^ (neg & 0x7f7f7f7fu)) + (neg & 0x01010101u);
+}
+
 __device__ __forceinline__ int k4_chunk1(int t, int s) {
     return (t & 7) | (s << 3) | (((t >> 3) & 3) << 6) | ((t >> 5) << 8);
 }

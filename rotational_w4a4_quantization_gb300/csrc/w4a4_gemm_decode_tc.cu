@@ -551,7 +551,7 @@ __host__ __device__ constexpr int stage_bit(int L, int k) {
     constexpr int o10[10] = {0, 1, 2, 5, 6, 7, 8, 3, 4, 9};
     constexpr int o11[11] = {0, 1, 2, 5, 6, 7, 8, 3, 4, 9, 10};
     constexpr int o12[12] = {0, 1, 2, 6, 7, 8, 9, 10, 11, 3, 4, 5};
-    constexpr int o13[13] = {0, 1, 2, 5, 6, 7, 8, 9, 10, 3, 4, 11, 12};
+    constexpr int o13[13] = {0, 1, 2, 6, 7, 8, 9, 10, 11, 12, 3, 4, 5};
     return L == 10 ? o10[k] : (L == 11 ? o11[k] : (L == 12 ? o12[k] : o13[k]));
 }
 
