@@ -94,6 +94,17 @@ def test_n4096_cta_sizes_for_batches(rows):
     _run_and_compare(x, seed=0x5EED, flags=rq.RQ_SIGNS_FIRST)
 
 
+@pytest.mark.parametrize("rows,dt", [(7, torch.bfloat16), (301, torch.bfloat16), (311, torch.float16),
+                                     (611, torch.bfloat16), (613, torch.float32), (1517, torch.bfloat16)])
+def test_n8192_rows_per_cta(rows, dt):
+    """n = 8192 batches around the rows-per-CTA choice on 152 SMs (one row per
+    CTA below 304 rows, two below 608, then four; fp32 input at most two), each
+    with a ragged last group, for both rotation forms."""
+    x = synth.activations(rows, 8192, dt, seed=rows, n_outliers=8, factor=100.0)
+    for flags in (rq.RQ_SIGNS_FIRST, 0):
+        _run_and_compare(x, seed=0x5EED, flags=flags)
+
+
 @pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large"])
 def test_workload_activations_full_size(name):
     w = synth.WORKLOADS[name]
