@@ -61,12 +61,14 @@ SLEEP_CYCLES = 400_000       # ~0.2 ms GPU-side pause between timed steps
 # DRAM bytes (read + write) per launch of each kernel at each workload, from one
 # ncu capture of the kernel as it is now (dram__bytes_read.sum +
 # dram__bytes_write.sum); None where no capture of the current kernel exists.
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch, from the ncu captures
+# summarized under profiles/ (kernel, workload, activation-code form); None where no
+# capture of the current kernel exists.  Writes still in L2 when a kernel ends are
+# not counted by the capture.
 NCU_TRAFFIC = {
-    ("w4a4_gemm", "prefill"): None,
-    ("w4a4_gemm", "large"): None,
-    ("fwht_quant", "prefill"): None,
-    ("fwht_quant", "large"): 67_167_232 + 1_138_688,      # codes mostly still in L2 at kernel end
-    ("kv_rotate_quant", "kv"): 134_263_040 + 14_430_720,
+    ("w4a4_gemm", "large", "e4m3"): 158_147_840 + 205_566_720,
+    ("fwht_quant", "large", "e4m3"): 67_146_240 + 3_233_792,
+    ("kv_rotate_quant", "kv", None): 134_283_008 + 14_740_224,
 }
 PROBE_MMAS_PER_SM = 200_000   # FP8 tensor-pipe probe: ~0.1 s of back-to-back MMAs
 
@@ -433,7 +435,7 @@ def run_gpu(args, work, kvw):
         ach = gb_ops / avg["gemm"] / 1e12
         roof = {"kernel": "w4a4_gemm", "bound": "tensor", "achieved": ach, "peak": fp8_peak,
                 "unit": "TFLOP/s", "frac": ach / fp8_peak,
-                "traffic": NCU_TRAFFIC.get(("w4a4_gemm", work.name)),
+                "traffic": NCU_TRAFFIC.get(("w4a4_gemm", work.name, args.a_form)),
                 "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (fp8 dense ratio)",
                 "fp8_pipe_probe": probe,
                 "frac_fp8_pipe_probe": ach / probe["tflops"] if probe else None}
@@ -443,7 +445,7 @@ def run_gpu(args, work, kvw):
         ach = b / avg[dom] / 1e9
         roof = {"kernel": key, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
-                "traffic": NCU_TRAFFIC.get((key, work.name if key == "fwht_quant" else "kv")),
+                "traffic": NCU_TRAFFIC.get((key, work.name, args.a_form) if key == "fwht_quant" else (key, "kv", None)),
                 "peak_source": f"{peaks['source']} hbm copy"}
 
     line = {
