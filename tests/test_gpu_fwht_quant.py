@@ -13,7 +13,7 @@ import oracle
 import rotational_w4a4_quantization_gb300 as rq
 from rotational_w4a4_quantization_gb300 import synth
 
-from parity import compare_codes, compare_rows, compare_scales, to_np, unpack_codes
+from parity import compare_codes, compare_rows, compare_scales, record, to_np, unpack_codes
 
 pytestmark = pytest.mark.gpu
 
@@ -27,16 +27,17 @@ def _built():
     __graft_entry__.build()
 
 
-def _run_and_compare(x_cpu: torch.Tensor, seed: int, flags: int, x_dev=None):
-    """x_cpu: rows x n (the exact values the GPU reads)."""
+def _run_and_compare(x_cpu: torch.Tensor, seed: int, flags: int, x_dev=None, with_err=False):
+    """x_cpu: rows x n (the exact values the GPU reads).  Returns the number of
+    tie-window code differences (and, with_err, the worst per-row error of y)."""
     rows, n = x_cpu.shape
     xd = x_cpu.to(DEV) if x_dev is None else x_dev
     q, s, y = rq.fwht_quant(xd, seed, flags, want_y=True)
     ref = oracle.fwht_quant(x_cpu.double().numpy(), seed, flags, want_y=True, want_ratio=True)
-    compare_rows(to_np(y), ref["y"])
+    err = compare_rows(to_np(y), ref["y"])
     compare_scales(to_np(s), ref["scales"])
     ties = compare_codes(to_np(q), ref["q"], ref["ratio"], n)
-    return ties
+    return (ties, err) if with_err else ties
 
 
 def _rows_for(n):
@@ -109,8 +110,10 @@ def test_n8192_rows_per_cta(rows, dt):
 def test_workload_activations_full_size(name):
     w = synth.WORKLOADS[name]
     x = synth.activations(w.rows, w.n, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor)
-    ties = _run_and_compare(x, synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+    ties, err = _run_and_compare(x, synth.SIGN_SEED, rq.RQ_SIGNS_FIRST, with_err=True)
     print(f"{name}: {ties} tie-window code differences out of {x.numel()}")
+    record("fwht_workload", workload=name, rows=w.rows, n=w.n, codes=x.numel(), tie_window_differences=ties,
+           max_row_rel_err=err, tolerance=1e-5)
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large"])

@@ -7,7 +7,7 @@ import oracle
 import rotational_w4a4_quantization_gb300 as rq
 from rotational_w4a4_quantization_gb300 import synth
 
-from parity import compare_codes, compare_scales, to_np
+from parity import compare_codes, compare_scales, record, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -61,6 +61,8 @@ def test_kv_workload_full_size():
                          w.kv_outliers_per_head, w.kv_outlier_factor)
     ties = _check(k, v, synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
     print(f"kv: {ties} tie-window code differences")
+    record("kv_workload", tokens=w.kv_tokens, heads=w.kv_heads, head_dim=w.kv_head_dim,
+           codes=2 * k.numel(), tie_window_differences=ties)
 
 
 def test_kv_equals_fwht_quant_on_flattened_rows():
