@@ -1214,6 +1214,268 @@ cudaError_t launch_k8(const KParams &p, int rows, cudaStream_t stream) {
     }
 }
 
+// --------------------------------------------------------------------------
+// n = 128 (one head of K or V, head_dim 128): a warp pair per 32 rows.
+//
+// Lane l of the pair's warp h holds half h of row l (64 values as fp32 pairs):
+// chunk slots s = element bits 3..5, read in the order s ^ (l & 7) so that the
+// eight lanes of a shared-memory phase read eight different 16-byte columns of
+// their rows (a Sylvester network on XOR-permuted input leaves output j in
+// place times (-1)^popcount(j & a), folded into the quantization multiplier).
+// Six stages run in registers; the seventh (element bit 6, across the halves)
+// goes through shared memory: warp 0 keeps output chunks 0..3 and warp 1 chunks
+// 4..7, each hands the other half of its values to its partner lane (16 pairs,
+// 64-bit stores, conflict-free) and forms y = A +- B for the chunks it keeps, i.e.
+// two runs of 32 consecutive outputs: 16 bytes of codes each.  Warp 1 runs its
+// last register stage (slot bit 2) with sum and difference swapped (the same
+// fused multiply-adds with the sign of b flipped), so in both warps registers
+// 0..15 hold the kept chunks and 16..31 the ones handed over: the two warps run
+// the same instructions, and warp 1's A - B comes out as B - A, a sign folded
+// into its multiplier like the read-order signs.  One named barrier per
+// pair orders the exchange (and frees the input slot for the next copy), a second
+// one the row-maximum exchange.  Compared with two lanes per row and a shuffle
+// stage this saves the shuffles' 1.5 instructions per element and most of the
+// per-group control, at 16 warps per SM.
+// --------------------------------------------------------------------------
+constexpr int KV_PAIRS = 2;    // warp pairs per CTA
+constexpr int KV_DEPTH = 2;    // input groups in flight per pair
+
+template <int IN>
+constexpr int kv_pair_bytes() {
+    // input ring (32 rows per group) | exchange [2][16][32] pairs | row maxima [2][32]
+    return KV_DEPTH * 32 * 128 * (IN == IN_F32 ? 4 : 2) + 2 * 16 * 32 * 8 + 2 * 32 * 4;
+}
+template <int IN>
+size_t kv_smem_bytes() {
+    return 256 + (size_t)KV_PAIRS * kv_pair_bytes<IN>() + 128 + 256;   // alignment | pairs | barriers | sign words
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+    return r;
+}
+
+template <int IN>
+__global__ void __launch_bounds__(64 * KV_PAIRS, 4)
+fwht_quant_kv128_kernel(const __grid_constant__ KParams prm) {
+    constexpr int n = 128, G = IN == IN_F32 ? 2 : 1, ES = IN == IN_F32 ? 4 : 2, RB = n * ES;
+    constexpr int NP = 32;                                 // fp32 pairs per thread
+    constexpr int PB = kv_pair_bytes<IN>();
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    // 256-byte aligned base: the XOR addressing below needs the chunk-offset bits
+    // (4..6, or 5..7 for fp32 rows) of the input rows and the sign table free.
+    // Each pair's block is a multiple of 256 bytes.
+    static_assert(PB % 256 == 0, "pair blocks keep 256-byte alignment");
+    unsigned char *base = smem_raw + ((256u - (smem_addr(smem_raw) & 255u)) & 255u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + KV_PAIRS * PB);      // KV_PAIRS * KV_DEPTH
+    uint32_t *sgn = reinterpret_cast<uint32_t *>(base + KV_PAIRS * PB + 128); // 64 words
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pair = warp >> 1, h = warp & 1;
+    const int a = lane & 7;
+    unsigned char *pbase = base + pair * PB;
+    unsigned char *ring = pbase;
+    pair_t *xch = reinterpret_cast<pair_t *>(pbase + KV_DEPTH * 32 * RB);
+    float *amx = reinterpret_cast<float *>(pbase + KV_DEPTH * 32 * RB + 2 * 16 * 32 * 8);
+    const uint32_t pbar = 1 + pair;                        // named barrier of the pair (64 threads)
+    const bool signs_first = (prm.flags & 1u) != 0;
+    const uint32_t msel = signs_first ? 0xffffffffu : 0u;
+    const int64_t total_groups = prm.groups_per_job * prm.njobs;
+    const int64_t first = (int64_t)blockIdx.x * KV_PAIRS + pair, step = (int64_t)gridDim.x * KV_PAIRS;
+    const float inv_sqrt_n = 0.70710678118654752440f / 8.0f;
+    // sign of the value in register chunk c of run r against y: (-1)^popcount(s & a)
+    // for the butterfly slot s = 4 h + c, and for warp 1's second run (B - A) -1
+    float fsg[2][4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        fsg[0][c] = (__popc(((h << 2) | c) & a) & 1) ? -1.f : 1.f;
+        fsg[1][c] = h ? -fsg[0][c] : fsg[0][c];
+    }
+    const float sig = h ? -1.f : 1.f;                      // warp 1: the last stage swapped
+
+    if (threadIdx.x < KV_PAIRS * KV_DEPTH) mbar_init(&bars[threadIdx.x], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
+
+    // The 32 rows of group g into ring slot `slot` (one lane of the pair's warp 0).
+    auto issue = [&](int64_t g, int slot) {
+        const int jb = job_of(g, prm.groups_per_job);
+        const RotJob &job = prm.job[jb];
+        const int64_t row0 = (g - (int64_t)jb * prm.groups_per_job) * 32;
+        int64_t valid = job.rows - row0;
+        valid = valid < 0 ? 0 : (valid > 32 ? 32 : valid);
+        uint64_t *bar = &bars[pair * KV_DEPTH + slot];
+        unsigned char *dst = ring + slot * 32 * RB;
+        const char *x = static_cast<const char *>(job.x);
+        mbar_expect_tx(bar, (uint32_t)(valid * RB));
+        if (job.ld * ES == RB) {
+            if (valid > 0) bulk_copy(dst, x + row0 * RB, (uint32_t)(valid * RB), bar);
+        } else {
+            for (int r = 0; r < valid; ++r) bulk_copy(dst + r * RB, x + (row0 + r) * job.ld * ES, RB, bar);
+        }
+    };
+    if (h == 0 && lane == 0) {
+#pragma unroll
+        for (int d = 0; d < KV_DEPTH; ++d)
+            if (first + d * step < total_groups) issue(first + d * step, d);
+    }
+    if (threadIdx.x < n / 2) {
+        const uint32_t s0 = (uint32_t)(splitmix64_at(prm.seed, 2ull * threadIdx.x) >> 63);
+        const uint32_t s1 = (uint32_t)(splitmix64_at(prm.seed, 2ull * threadIdx.x + 1) >> 63);
+        sgn[threadIdx.x] = (s0 << 15) | (s1 << 31);
+    }
+    __syncthreads();
+
+    // shared addresses with the lane's XOR order in bits 4..6 (chunk c ^ s is at base ^ 16 G s)
+    const uint32_t sg_in = smem_addr(sgn) + 128u * (uint32_t)h + 16u * (uint32_t)a;   // input-side masks
+    const uint32_t ring_lane = smem_addr(ring) + (uint32_t)(lane * RB + h * (RB / 2)) + 16u * G * (uint32_t)a;
+    pair_t *give = xch + h * 512 + lane;                   // [k]: stride 32 pairs
+    const pair_t *take = xch + (h ^ 1) * 512 + lane;
+    const uint4 *sg_out = reinterpret_cast<const uint4 *>(sgn);
+
+    int slot = 0;
+    uint32_t phase = 0;
+    bool aborted = false;
+    for (int64_t grp = first; grp < total_groups; grp += step) {
+        const int jb = job_of(grp, prm.groups_per_job);
+        const RotJob &job = prm.job[jb];
+        const int64_t row = (grp - (int64_t)jb * prm.groups_per_job) * 32 + lane;
+        if (!mbar_wait_bounded(&bars[pair * KV_DEPTH + slot], phase, prm.err)) aborted = true;
+        const bool active = row < job.rows && !aborted;
+
+        pair_t v[NP];
+        const uint32_t rl = ring_lane + (uint32_t)(slot * 32 * RB);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint4 m = lds128(sg_in ^ (16u * s));
+            uint4 g[G];
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) g[hh] = lds128((rl ^ (16u * G * s)) + 16u * hh);
+            convert_chunk<IN>(g, m, msel, &v[4 * s]);       // includes the in-pair stage
+        }
+#pragma unroll
+        for (int rb = 1; rb <= 4; ++rb) butterfly_pairs<NP>(v, rb);
+        {
+            // slot bit 2: (a + sig b, a - sig b), i.e. swapped in warp 1
+            const pair_t sp = mk2(sig, sig), sn = mk2(-sig, -sig);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const pair_t x = v[k], y = v[16 + k];
+                v[k] = fma2(y, sp, x);
+                v[16 + k] = fma2(y, sn, x);
+            }
+        }
+        // hand the partner the chunks it keeps
+#pragma unroll
+        for (int k = 0; k < 16; ++k) give[32 * k] = v[16 + k];
+        // the input slot's generic reads, ordered before its next bulk write
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("bar.sync %0, 64;" ::"r"(pbar) : "memory");
+        if (h == 0 && lane == 0 && !aborted && grp + KV_DEPTH * step < total_groups) issue(grp + KV_DEPTH * step, slot);
+        if (++slot == KV_DEPTH) {
+            slot = 0;
+            phase ^= 1u;
+        }
+        // y = A +- B for the kept chunks: two runs of 32 outputs in v[0..15], v[16..31]
+        // (warp 1: own - received = B - A for the second run)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const pair_t o = take[32 * k];
+            const pair_t s_ = add2(v[k], o), d_ = sub2(v[k], o);
+            v[k] = s_; v[16 + k] = d_;
+        }
+        float amax = pairs_absmax<NP>(v);
+        amx[h * 32 + lane] = aborted ? __int_as_float(-1) : amax;
+        asm volatile("bar.sync %0, 64;" ::"r"(pbar) : "memory");
+        const float m0 = amx[lane], m1 = amx[32 + lane];
+        // the two warps of the pair leave together: share the abort decision
+        const bool any_abort = __any_sync(0xffffffffu, __float_as_int(m0) == -1 || __float_as_int(m1) == -1);
+        if (any_abort) { aborted = true; break; }
+        amax = fmaxf(m0, m1);
+
+        if (active) {
+            const float inv = amax > 0.f ? 7.0f / amax : 0.f;
+            if (h == 0) job.scales[row] = (amax / 7.0f) * inv_sqrt_n;
+            // output chunk of run r, chunk c: 8 r + 4 h + c
+            if (!signs_first) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 m = sg_out[8 * r + 4 * h + c];
+                        const uint32_t mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            v[16 * r + 4 * c + k] ^= ((pair_t)(mm[k] & 0x80000000u) << 32) | (pair_t)(mm[k] << 16);
+                    }
+            }
+            if (job.y) {
+                float *yrow = job.y + row * (int64_t)n;
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float ys = fsg[r][c] * inv_sqrt_n;
+                        const pair_t sc2 = mk2(ys, ys), z2 = 0ull;
+                        ulonglong2 *yp = reinterpret_cast<ulonglong2 *>(yrow + 8 * (8 * r + 4 * h + c));
+                        yp[0] = make_ulonglong2(fma2(v[16 * r + 4 * c], sc2, z2), fma2(v[16 * r + 4 * c + 1], sc2, z2));
+                        yp[1] = make_ulonglong2(fma2(v[16 * r + 4 * c + 2], sc2, z2), fma2(v[16 * r + 4 * c + 3], sc2, z2));
+                    }
+            }
+            const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
+            uint8_t *qrow = job.q + row * (int64_t)(n / 2);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                uint32_t words[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float sv = fsg[r][c] * inv;
+                    const pair_t inv2 = mk2(sv, sv);
+                    uint32_t code[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const pair_t qq = fma2(v[16 * r + 4 * c + k], inv2, bias2);
+                        code[2 * k] = (uint32_t)qq;
+                        code[2 * k + 1] = (uint32_t)(qq >> 32);
+                    }
+                    words[c] = pack8(code);
+                }
+                *reinterpret_cast<uint4 *>(qrow + 32 * r + 16 * h) = make_uint4(words[0], words[1], words[2], words[3]);
+            }
+        }
+    }
+    if (aborted) {
+        // wait (bounded) for this pair's copies still in flight before leaving
+        for (int d = 0; d < KV_DEPTH; ++d) {
+            const uint32_t par = d >= slot ? phase : (phase ^ 1u);
+            mbar_wait_bounded(&bars[pair * KV_DEPTH + d], par, prm.err);
+        }
+    }
+}
+
+template <int IN>
+cudaError_t launch_kv128(const KParams &p, cudaStream_t stream) {
+    auto kern = fwht_quant_kv128_kernel<IN>;
+    const size_t smem = kv_smem_bytes<IN>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 64 * KV_PAIRS, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t total = p.groups_per_job * p.njobs;
+    int64_t grid = (int64_t)sms * per_sm;
+    const int64_t need = (total + KV_PAIRS - 1) / KV_PAIRS;
+    if (grid > need) grid = need;
+    kern<<<(unsigned)grid, 64 * KV_PAIRS, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <int LOGN, int IN>
 size_t smem_bytes() {
     using PL = Plan<LOGN - 3>;
@@ -1308,13 +1570,20 @@ cudaError_t launch_fwht_quant(const RotJob *jobs, int njobs, int log_n, int in_t
     }
     const int rows_per_group = log_n == K4_LOGN   ? k4_threads / 64
                                : log_n == K8_LOGN ? k8_rows
+                               : log_n == 7       ? 32                  // one warp pair per 32 rows
                                                   : threads_for(log_n, in_type) >> (C - S);
     p.groups_per_job = (max_rows + rows_per_group - 1) / rows_per_group;
     if (p.groups_per_job == 0) return cudaSuccess;
     switch (log_n) {
         case 5: return launch_n<5>(p, in_type, stream);
         case 6: return launch_n<6>(p, in_type, stream);
-        case 7: return launch_n<7>(p, in_type, stream);
+        case 7:
+            switch (in_type) {
+                case IN_F32: return launch_kv128<IN_F32>(p, stream);
+                case IN_BF16: return launch_kv128<IN_BF16>(p, stream);
+                case IN_F16: return launch_kv128<IN_F16>(p, stream);
+                default: return cudaErrorInvalidValue;
+            }
         case 8: return launch_n<8>(p, in_type, stream);
         case 9: return launch_n<9>(p, in_type, stream);
         case 10: return launch_n<10>(p, in_type, stream);
