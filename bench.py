@@ -614,7 +614,7 @@ def run_reference(args, work, kvw):
     world, rank, _ = dist_env()
     if rank != 0:
         return None
-    gemm_rows = 2
+    gemm_rows = 2 if args.steps <= 50 else 1     # keeps a long run within a few minutes
     for _ in range(args.warmup):
         _oracle_sample(work, kvw, gemm_rows, 16, 64)
     total = 0.0
@@ -644,7 +644,8 @@ def run_reference(args, work, kvw):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200,
+                    help="timed steps (200 large steps span ~0.15 s: several clock samples fall inside)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["rq", "reference"], default="rq")
     ap.add_argument("--workload", choices=["prefill", "large", "decode", "tiny"], default="large")
