@@ -925,6 +925,14 @@ cudaError_t launch_k4(const KParams &p, int threads, cudaStream_t stream) {
 // bank groups, and every access but the last transpose's reads is a thread base
 // plus a compile-time offset (checked exhaustively on the host for all t, s).
 // --------------------------------------------------------------------------
+// One fp32 pair from shared memory.  The transposes read their granules as two of
+// these (volatile, so they are issued where written): measured 41.2 -> 40.0 us (ncu)
+// against 128-bit loads into pairs for 4096 x 8192 rows.
+__device__ __forceinline__ pair_t lds64v(const void *p) {
+    pair_t r;
+    asm volatile("ld.shared.b64 %0, [%1];" : "=l"(r) : "r"(smem_addr(p)));
+    return r;
+}
 constexpr int K8_LOGN = 13, K8_N = 8192;
 
 __host__ __device__ constexpr int k8_max_rows(int in_type) { return in_type == IN_F32 ? 2 : 4; }
@@ -1048,8 +1056,8 @@ fwht_quant_k8_kernel(const __grid_constant__ KParams prm) {
         asm volatile("bar.sync %0, 128;" ::"r"(rbar) : "memory");
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
-            const ulonglong2 q = br1[128 * s];
-            v[2 * s] = q.x; v[2 * s + 1] = q.y;
+            v[2 * s] = lds64v(br1 + 128 * s);
+            v[2 * s + 1] = lds64v(reinterpret_cast<const pair_t *>(br1 + 128 * s) + 1);
         }
 #pragma unroll
         for (int rb = 2; rb <= 5; ++rb) butterfly_pairs<NP>(v, rb);
@@ -1061,8 +1069,8 @@ fwht_quant_k8_kernel(const __grid_constant__ KParams prm) {
         asm volatile("bar.sync %0, 128;" ::"r"(rbar) : "memory");
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
-            const ulonglong2 q = br2[s ^ m3];
-            v[2 * s] = q.x; v[2 * s + 1] = q.y;
+            v[2 * s] = lds64v(br2 + (s ^ m3));
+            v[2 * s + 1] = lds64v(reinterpret_cast<const pair_t *>(br2 + (s ^ m3)) + 1);
         }
 #pragma unroll
         for (int rb = 3; rb <= 5; ++rb) butterfly_pairs<NP>(v, rb);
