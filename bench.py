@@ -68,7 +68,7 @@ SLEEP_CYCLES = 400_000       # ~0.2 ms GPU-side pause between timed steps
 NCU_TRAFFIC = {
     ("w4a4_gemm", "large", "e4m3"): 158_147_840 + 205_566_720,
     ("fwht_quant", "large", "e4m3"): 67_145_728 + 2_708_992,
-    ("kv_rotate_quant", "kv", None): 134_263_296 + 14_614_528,
+    ("kv_rotate_quant", "kv", None): 134_277_120 + 13_850_112,
 }
 PROBE_MMAS_PER_SM = 200_000   # FP8 tensor-pipe probe: ~0.1 s of back-to-back MMAs
 

@@ -1243,9 +1243,12 @@ cudaError_t launch_k8(const KParams &p, int rows, cudaStream_t stream) {
 // pair orders the exchange (and frees the input slot for the next copy), a second
 // one the row-maximum exchange.  Compared with two lanes per row and a shuffle
 // stage this saves the shuffles' 1.5 instructions per element and most of the
-// per-group control, at 16 warps per SM.
+// per-group control, at 16 warps per SM (8 one-pair CTAs).
 // --------------------------------------------------------------------------
-constexpr int KV_PAIRS = 2;    // warp pairs per CTA
+// One warp pair per CTA; the launch bound of 9 CTAs per SM caps registers at 112
+// (96 used, no spills), and shared memory admits 8 (16 warps).  Against two pairs
+// per CTA at 128 registers: 37.6 -> 36.9 us median (K, V 8192 x 32 x 128).
+constexpr int KV_PAIRS = 1;    // warp pairs per CTA
 constexpr int KV_DEPTH = 2;    // input groups in flight per pair
 
 template <int IN>
@@ -1265,7 +1268,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 template <int IN>
-__global__ void __launch_bounds__(64 * KV_PAIRS, 4)
+__global__ void __launch_bounds__(64 * KV_PAIRS, 9)
 fwht_quant_kv128_kernel(const __grid_constant__ KParams prm) {
     constexpr int n = 128, G = IN == IN_F32 ? 2 : 1, ES = IN == IN_F32 ? 4 : 2, RB = n * ES;
     constexpr int NP = 32;                                 // fp32 pairs per thread
