@@ -98,6 +98,9 @@ enum { RQ_INT8_CODES = 4u, RQ_GROUP_SCALES = 8u };
  * the activation codes a_q are given in that form. */
 enum { RQ_E4M3_CODES = 16u, RQ_A_E4M3 = 16u };
 
+/* rq_fwht_quant code mode: the default INT4 codes, one int8 byte each. */
+enum { RQ_INT4_BYTES = 32u };
+
 /* Smallest / largest supported Hadamard size (row length n, head_dim). */
 #define RQ_MIN_N 32
 #define RQ_MAX_N 8192
@@ -149,6 +152,11 @@ enum { RQ_E4M3_CODES = 16u, RQ_A_E4M3 = 16u };
  *              within each group of 8 codes the bytes hold codes
  *              0, 2, 4, 6, 1, 3, 5, 7 of the group.  Twice the bytes of the
  *              packed form; the product then widens only the weights.
+ *            RQ_INT4_BYTES: the default INT4 codes and scales (max|y|/7),
+ *              each code stored as one int8 byte: q is [rows][n] int8.  This
+ *              is the activation operand of rq_w4a8_gemm, which then computes
+ *              the W4A4 product with per-channel or per-group (128) weight
+ *              scales ([SQ] §The architecture, per-group scales).
  *   q        out: [rows][n/2] bytes, packed codes (row stride n/2).
  *   scales   out: [rows] fp32 scales, max|y|/7 of each rotated row.
  *   y        out, may be NULL: [rows][n] fp32 rotated rows y = xR (parity

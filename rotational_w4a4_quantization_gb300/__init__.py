@@ -30,6 +30,7 @@ from ._binding import (  # noqa: F401
     RQ_ATTN_ROTATED_OUT,
     RQ_E4M3_CODES,
     RQ_GROUP_SCALES,
+    RQ_INT4_BYTES,
     RQ_INT8_CODES,
     RQ_SIGNS_FIRST,
     RQError,
@@ -46,7 +47,7 @@ from ._binding import (  # noqa: F401
     w4a8_gemm,
 )
 
-__all__ = ["RQ_A_E4M3", "RQ_ATTN_ROTATED_OUT", "RQ_E4M3_CODES", "RQ_GROUP_SCALES", "RQ_INT8_CODES", "RQ_SIGNS_FIRST", "RQError", "attn_decode",
+__all__ = ["RQ_A_E4M3", "RQ_ATTN_ROTATED_OUT", "RQ_E4M3_CODES", "RQ_GROUP_SCALES", "RQ_INT4_BYTES", "RQ_INT8_CODES", "RQ_SIGNS_FIRST", "RQError", "attn_decode",
            "fwht_quant", "fwht_quant_gemm", "kv_rotate_quant", "library_path", "load_library", "probe_f8_mma", "selftest_wait_timeout",
            "sync_status",
            "w4a4_gemm", "w4a8_gemm"]

@@ -20,6 +20,7 @@ RQ_ATTN_ROTATED_OUT = 2
 RQ_INT8_CODES = 4
 RQ_GROUP_SCALES = 8
 RQ_E4M3_CODES = 16      # rq_fwht_quant: INT4 codes as the product's E4M3 operand bytes
+RQ_INT4_BYTES = 32      # rq_fwht_quant: INT4 codes, one int8 byte each (the W4A8 product's A operand)
 RQ_A_E4M3 = 16          # rq_w4a4_gemm: a_q holds those bytes
 
 _STATUS = {0: "RQ_OK", 1: "RQ_ERR_INVALID_ARG", 2: "RQ_ERR_UNSUPPORTED", 3: "RQ_ERR_MISALIGNED",
@@ -135,14 +136,16 @@ def fwht_quant(x: torch.Tensor, seed: int, flags: int = RQ_SIGNS_FIRST, *, q=Non
     (rows x n/2) uint8, scales (rows,) fp32, y (rows x n) fp32 = x R.  With
     RQ_INT8_CODES in flags q is (rows x n) int8; with RQ_GROUP_SCALES scales is
     (rows x n/128); with RQ_E4M3_CODES q is (rows x n) uint8, the same INT4 codes
-    as the product's operand bytes (see include/rq.h)."""
+    as the product's operand bytes (see include/rq.h); with RQ_INT4_BYTES q is
+    (rows x n) int8, the INT4 codes one per byte (for w4a8_gemm: a W4A4 product
+    with per-group weight scales)."""
     lib = load_library()
     if x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be 2-D with unit stride in the last dimension")
     if x.dtype not in (torch.float32, torch.bfloat16, torch.float16):
         raise ValueError("x must be float32, bfloat16 or float16")
     rows, n = x.shape
-    if flags & RQ_INT8_CODES:
+    if flags & (RQ_INT8_CODES | RQ_INT4_BYTES):
         q_shape, q_dtype = (rows, n), torch.int8
     elif flags & RQ_E4M3_CODES:
         q_shape, q_dtype = (rows, n), torch.uint8

@@ -74,12 +74,13 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
     const bool kron = !rq::pow2(n) && rq::kron_block_of(n, &km, &klb);
     if (!kron && (!rq::pow2(n) || n < RQ_MIN_N || n > RQ_MAX_N)) return RQ_ERR_UNSUPPORTED;
     if (ld_x < n) return RQ_ERR_INVALID_ARG;
-    if (flags & ~uint32_t(RQ_SIGNS_FIRST | RQ_INT8_CODES | RQ_GROUP_SCALES | RQ_E4M3_CODES)) return RQ_ERR_INVALID_ARG;
-    const uint32_t modes = flags & uint32_t(RQ_INT8_CODES | RQ_GROUP_SCALES | RQ_E4M3_CODES);
+    if (flags & ~uint32_t(RQ_SIGNS_FIRST | RQ_INT8_CODES | RQ_GROUP_SCALES | RQ_E4M3_CODES | RQ_INT4_BYTES))
+        return RQ_ERR_INVALID_ARG;
+    const uint32_t modes = flags & uint32_t(RQ_INT8_CODES | RQ_GROUP_SCALES | RQ_E4M3_CODES | RQ_INT4_BYTES);
     if (modes & (modes - 1)) return RQ_ERR_INVALID_ARG;   // at most one code mode
-    // INT8 and per-group codes: n = m 2^k, and powers of two from 256 on (the plans
-    // whose threads end with whole 32-element runs of a row); E4M3 operand codes:
-    // powers of two from 256 on
+    // INT8, INT4-in-bytes and per-group codes: n = m 2^k, and powers of two from 256
+    // on (the plans whose threads end with whole 32-element runs of a row); E4M3
+    // operand codes: powers of two from 256 on
     if (modes && !kron && n < 256) return RQ_ERR_UNSUPPORTED;
     if ((flags & RQ_E4M3_CODES) && kron) return RQ_ERR_UNSUPPORTED;
     if (rows == 0) return RQ_OK;

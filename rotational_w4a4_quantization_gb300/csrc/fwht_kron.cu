@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kKThreads, 2) fwht_kron_kernel(const __grid_co
     float *ginv = red + kKWarps;                                          // N / 128 (per-group codes)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool signs_first = (p.flags & 1u) != 0;
-    const bool i8 = (p.flags & RQ_INT8_CODES) != 0, per_group = (p.flags & RQ_GROUP_SCALES) != 0;
+    const bool i8 = (p.flags & (RQ_INT8_CODES | RQ_INT4_BYTES)) != 0, per_group = (p.flags & RQ_GROUP_SCALES) != 0;
     static_assert(N % 128 == 0, "m is a multiple of 4 and 2^k >= 32");
     const uint32_t msel = signs_first ? 0xffffffffu : 0u;
 
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kKThreads, 2) fwht_kron_kernel(const __grid_co
 
         // ---- quantize, pack, store (the same column pairs) ----
         // INT4 per row (default), INT8 per row, or INT4 per group of 128
-        const float qmax = i8 ? 127.0f : 7.0f;
+        const float qmax = (p.flags & RQ_INT8_CODES) ? 127.0f : 7.0f;   // INT8, or INT4 (also in bytes)
         const float inv = amax > 0.f ? qmax / amax : 0.f;
         const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
         if (!per_group && threadIdx.x == 0) p.scales[r] = (amax / qmax) * p.inv_sqrt_n;

@@ -400,7 +400,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
         // slot bits 2, 3).  For n = 256, 512 a thread holds 16 consecutive chunks:
         // one group.
         constexpr bool kGroups4 = PL::kTwoPhase && C >= 7;
-        const bool i8 = PL::kTwoPhase && (prm.flags & RQ_INT8_CODES) != 0;
+        const bool i8 = PL::kTwoPhase && (prm.flags & (RQ_INT8_CODES | RQ_INT4_BYTES)) != 0;
         const bool per_group = PL::kTwoPhase && (prm.flags & RQ_GROUP_SCALES) != 0;
         const bool e4 = PL::kTwoPhase && (prm.flags & RQ_E4M3_CODES) != 0;
         float gmax[kGroups4 ? 4 : 1];
@@ -438,7 +438,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
         // ---------------- quantize, pack, store ----------------
         // codes: INT4 per row (default), INT8 per row, or INT4 per group of 128
         // (the last two for two-phase plans only; the host rejects the others)
-        const float qmax = i8 ? 127.0f : 7.0f;
+        const float qmax = (prm.flags & RQ_INT8_CODES) ? 127.0f : 7.0f;   // INT8, or INT4 (also in bytes)
         const float inv = amax > 0.f ? qmax / amax : 0.f;
         float ginv[kGroups4 ? 4 : 1];
 #pragma unroll
@@ -783,10 +783,10 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
         // ---------------- quantize, pack, store: 64 consecutive elements ----------------
         if (active) {
             // codes: INT4 per row (default), INT8 per row, or INT4 per group of 128
-            const bool i8 = (prm.flags & RQ_INT8_CODES) != 0, grp = (prm.flags & RQ_GROUP_SCALES) != 0;
+            const bool i8 = (prm.flags & (RQ_INT8_CODES | RQ_INT4_BYTES)) != 0, grp = (prm.flags & RQ_GROUP_SCALES) != 0;
             const bool e4 = (prm.flags & RQ_E4M3_CODES) != 0;
             const float am = grp ? amax_grp : amax;
-            const float qmax = i8 ? 127.0f : 7.0f;
+            const float qmax = (prm.flags & RQ_INT8_CODES) ? 127.0f : 7.0f;   // INT8, or INT4 (also in bytes)
             const float inv = am > 0.f ? qmax / am : 0.f;
             const pair_t inv2 = mk2(inv, inv);
             const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
@@ -1093,10 +1093,10 @@ fwht_quant_k8_kernel(const __grid_constant__ KParams prm) {
         // ---------------- quantize, pack, store: 64 consecutive elements ----------------
         if (active) {
             // codes: INT4 per row (default), INT8 per row, or INT4 per group of 128
-            const bool i8 = (prm.flags & RQ_INT8_CODES) != 0, grp = (prm.flags & RQ_GROUP_SCALES) != 0;
+            const bool i8 = (prm.flags & (RQ_INT8_CODES | RQ_INT4_BYTES)) != 0, grp = (prm.flags & RQ_GROUP_SCALES) != 0;
             const bool e4 = (prm.flags & RQ_E4M3_CODES) != 0;
             const float am = grp ? amax_grp : amax;
-            const float qmax = i8 ? 127.0f : 7.0f;
+            const float qmax = (prm.flags & RQ_INT8_CODES) ? 127.0f : 7.0f;   // INT8, or INT4 (also in bytes)
             const float inv = am > 0.f ? qmax / am : 0.f;
             const pair_t inv2 = mk2(inv, inv);
             const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23

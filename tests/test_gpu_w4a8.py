@@ -316,3 +316,47 @@ def test_per_group_prefill_shape_sampled_rows():
     _, yref = oracle.w4a8_gemm(ref_a["q"][rows], ref_a["scales"][rows], qw, sw, len(rows), N, K, 128)
     _check_per_group(y32[rows], yref)
     compare_f16(y16[rows], yref, atol=1e-5 * np.abs(yref).max(axis=1, keepdims=True))
+
+
+# ---------------------------------------------------------------------------
+# W4A4 with per-group weight scales: INT4 activation codes one per byte
+# (RQ_INT4_BYTES) into the W4A8 product.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [256, 1024, 4096, 8192, 3072])
+@pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
+def test_int4_byte_codes(n, flags):
+    """RQ_INT4_BYTES: the oracle's INT4 codes (tie window aside) and scales, one
+    int8 byte per code, and exactly the GPU's own packed codes and scales."""
+    x = synth.activations(37, n, torch.bfloat16, n + 9, 4, 100.0)
+    xd = x.to(DEV)
+    qb, sb = rq.fwht_quant(xd, 5, flags | rq.RQ_INT4_BYTES)
+    qp, sp = rq.fwht_quant(xd, 5, flags)
+    ref = oracle.fwht_quant(x.double().numpy(), 5, flags, want_ratio=True)
+    g = to_np(qb).astype(np.int16)
+    assert g.min() >= -8 and g.max() <= 7
+    # the same codes as the packed form (decoded by bit arithmetic), the same scales
+    b = to_np(qp).astype(np.int16)
+    nib = np.stack([b & 15, b >> 4], axis=-1).reshape(37, n)
+    np.testing.assert_array_equal(g, np.where(nib >= 8, nib - 16, nib))
+    np.testing.assert_array_equal(to_np(sb), to_np(sp))
+    _compare_int8(g, oracle.unpack(ref["q"], n), ref["ratio"].reshape(37, n))
+    compare_scales(to_np(sb), ref["scales"])
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 256, 4096), (130, 384, 2048), (600, 256, 8192)])
+def test_w4a4_per_group_product(M, N, K):
+    """The W4A4 product with per-group weight scales on the oracle's codes: INT4
+    activation codes as bytes, per-group INT4 weight codes, against the oracle's
+    per-group product (fp32 sums of group partials: 1e-5 of each row's largest)."""
+    x = synth.activations(M, K, torch.bfloat16, M + K, 4, 100.0)
+    wt = synth.weights_t(N, K, 7 + N)
+    ra = oracle.fwht_quant(x.double().numpy(), 5, rq.RQ_SIGNS_FIRST)
+    rw = oracle.fwht_quant_groups(wt.double().numpy(), 5, rq.RQ_SIGNS_FIRST, 128)
+    qa = oracle.unpack(ra["q"], K).astype(np.int8)
+    _, yref = oracle.w4a8_gemm(qa, ra["scales"], rw["q"], rw["scales"], M, N, K, 128)
+    _check_per_group(_gpu(qa, ra["scales"], rw["q"], rw["scales"], torch.float32), yref)
+    # and the GPU's own INT4 bytes are those codes within the tie window
+    qb, _ = rq.fwht_quant(x.to(DEV), 5, rq.RQ_SIGNS_FIRST | rq.RQ_INT4_BYTES)
+    ra2 = oracle.fwht_quant(x.double().numpy(), 5, rq.RQ_SIGNS_FIRST, want_ratio=True)
+    _compare_int8(to_np(qb).astype(np.int16), qa.astype(np.int16), ra2["ratio"].reshape(M, K))
