@@ -134,8 +134,9 @@ enum { RQ_INT4_BYTES = 32u };
  *            y = x diag(s) (H_m (x) H_{2^k}) / sqrt(n) (or diag(s) after).
  *   ld_x     row stride in elements, >= n, ld_x * sizeof(x_dtype) % 16 == 0.
  *   seed     sign-vector seed.
- *   flags    RQ_SIGNS_FIRST or 0, plus at most one of (n = m 2^k, or a
- *            power of two from 256 to 8192; RQ_ERR_UNSUPPORTED for n <= 128):
+ *   flags    RQ_SIGNS_FIRST or 0, plus at most one of (n = m 2^k, n = 128,
+ *            or a power of two from 256 to 8192; RQ_ERR_UNSUPPORTED for
+ *            n < 128; at n = 128 the one group of RQ_GROUP_SCALES is the row):
  *            RQ_INT8_CODES: per-row INT8 codes for the W4A8 layer's
  *              activations ([SQ] §End-to-end flow): q is [rows][n] int8,
  *              scale = max|y| / 127, q = clamp(round_half_even(y / scale),
@@ -144,7 +145,7 @@ enum { RQ_INT4_BYTES = 32u };
  *              consecutive elements ([SQ] §The architecture, per-group scales;
  *              the weight fold of the W4A8 layer): q as above, scales
  *              [rows][n/128] fp32.
- *            RQ_E4M3_CODES (powers of two from 256 to 8192 only): the same
+ *            RQ_E4M3_CODES (n = 128 and powers of two from 256 to 8192): the same
  *              INT4 codes and scales as the default, each code stored as the
  *              tensor-core operand of rq_w4a4_gemm (RQ_A_E4M3): q is
  *              [rows][n] bytes; the byte of code q is q for q >= 0 and

@@ -78,10 +78,10 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
         return RQ_ERR_INVALID_ARG;
     const uint32_t modes = flags & uint32_t(RQ_INT8_CODES | RQ_GROUP_SCALES | RQ_E4M3_CODES | RQ_INT4_BYTES);
     if (modes & (modes - 1)) return RQ_ERR_INVALID_ARG;   // at most one code mode
-    // INT8, INT4-in-bytes and per-group codes: n = m 2^k, and powers of two from 256
-    // on (the plans whose threads end with whole 32-element runs of a row); E4M3
-    // operand codes: powers of two from 256 on
-    if (modes && !kron && n < 256) return RQ_ERR_UNSUPPORTED;
+    // INT8, INT4-in-bytes and per-group codes: n = m 2^k, n = 128, and powers of two
+    // from 256 on (the kernels whose threads end with whole 32-element runs of a
+    // row); E4M3 operand codes: n = 128 and powers of two from 256 on
+    if (modes && !kron && n < 256 && n != 128) return RQ_ERR_UNSUPPORTED;   // n = 128: the head-sized kernel
     if ((flags & RQ_E4M3_CODES) && kron) return RQ_ERR_UNSUPPORTED;
     if (rows == 0) return RQ_OK;
     if (!x || !q || !scales) return RQ_ERR_INVALID_ARG;

@@ -1406,8 +1406,13 @@ fwht_quant_kv128_kernel(const __grid_constant__ KParams prm) {
         amax = fmaxf(m0, m1);
 
         if (active) {
-            const float inv = amax > 0.f ? 7.0f / amax : 0.f;
-            if (h == 0) job.scales[row] = (amax / 7.0f) * inv_sqrt_n;
+            // codes: INT4 packed (default; with RQ_GROUP_SCALES the one group of 128 is
+            // the row), INT8 or INT4 one per byte, or the product's E4M3 operand bytes
+            const uint32_t fl = prm.flags;
+            const bool bytes = (fl & (RQ_INT8_CODES | RQ_INT4_BYTES)) != 0, e4 = (fl & RQ_E4M3_CODES) != 0;
+            const float qmax = (fl & RQ_INT8_CODES) ? 127.0f : 7.0f;
+            const float inv = amax > 0.f ? qmax / amax : 0.f;
+            if (h == 0) job.scales[row] = (amax / qmax) * inv_sqrt_n;
             // output chunk of run r, chunk c: 8 r + 4 h + c
             if (!signs_first) {
 #pragma unroll
@@ -1435,24 +1440,59 @@ fwht_quant_kv128_kernel(const __grid_constant__ KParams prm) {
                     }
             }
             const pair_t bias2 = mk2(12582912.0f, 12582912.0f);   // 1.5 * 2^23
-            uint8_t *qrow = job.q + row * (int64_t)(n / 2);
+            if (!bytes && !e4) {
+                uint8_t *qrow = job.q + row * (int64_t)(n / 2);
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                uint32_t words[4];
+                for (int r = 0; r < 2; ++r) {
+                    uint32_t words[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float sv = fsg[r][c] * inv;
-                    const pair_t inv2 = mk2(sv, sv);
-                    uint32_t code[8];
+                    for (int c = 0; c < 4; ++c) {
+                        const float sv = fsg[r][c] * inv;
+                        const pair_t inv2 = mk2(sv, sv);
+                        uint32_t code[8];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const pair_t qq = fma2(v[16 * r + 4 * c + k], inv2, bias2);
-                        code[2 * k] = (uint32_t)qq;
-                        code[2 * k + 1] = (uint32_t)(qq >> 32);
+                        for (int k = 0; k < 4; ++k) {
+                            const pair_t qq = fma2(v[16 * r + 4 * c + k], inv2, bias2);
+                            code[2 * k] = (uint32_t)qq;
+                            code[2 * k + 1] = (uint32_t)(qq >> 32);
+                        }
+                        words[c] = pack8(code);
                     }
-                    words[c] = pack8(code);
+                    *reinterpret_cast<uint4 *>(qrow + 32 * r + 16 * h) = make_uint4(words[0], words[1], words[2], words[3]);
                 }
-                *reinterpret_cast<uint4 *>(qrow + 32 * r + 16 * h) = make_uint4(words[0], words[1], words[2], words[3]);
+            } else {
+                // one byte per code: run r is 32 bytes at 64 r + 32 h
+                uint8_t *qrow = job.q + row * (int64_t)n;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    uint32_t words[8];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float sv = fsg[r][c] * inv;
+                        const pair_t inv2 = mk2(sv, sv);
+                        uint32_t code[8];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const pair_t qq = fma2(v[16 * r + 4 * c + k], inv2, bias2);
+                            code[2 * k] = (uint32_t)qq;
+                            code[2 * k + 1] = (uint32_t)(qq >> 32);
+                        }
+                        if (e4) {
+                            // signed E4M3 bytes, even codes then odd codes of the chunk
+                            words[2 * c] = e4m3_word(code[0], code[2], code[4], code[6]);
+                            words[2 * c + 1] = e4m3_word(code[1], code[3], code[5], code[7]);
+                        } else {
+                            // two's-complement bytes in element order
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh)
+                                words[2 * c + hh] = __byte_perm(__byte_perm(code[4 * hh], code[4 * hh + 1], 0x0040u),
+                                                                __byte_perm(code[4 * hh + 2], code[4 * hh + 3], 0x0040u), 0x5410u);
+                        }
+                    }
+                    uint4 *qp = reinterpret_cast<uint4 *>(qrow + 64 * r + 32 * h);
+                    qp[0] = make_uint4(words[0], words[1], words[2], words[3]);
+                    qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
+                }
             }
         }
     }

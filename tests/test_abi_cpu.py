@@ -206,19 +206,22 @@ def test_w4a8_argument_checks(lib, kw, expect):
     (dict(n=4096, ld=4096, flags=8, rows=0), 0),         # per-group scales at n = 4096
     (dict(n=2048, ld=2048, flags=4, rows=0), 0),         # INT8 codes at n = 2048
     (dict(n=256, ld=256, flags=8, rows=0), 0),           # per-group scales from n = 256 on
-    (dict(n=128, ld=128, flags=4, rows=0), 2),           # not for n <= 128
-    (dict(n=128, ld=128, flags=8, rows=0), 2),
+    (dict(n=128, ld=128, flags=4, rows=0), 0),           # n = 128: the head-sized kernel
+    (dict(n=128, ld=128, flags=8, rows=0), 0),
+    (dict(n=64, ld=64, flags=4, rows=0), 2),             # not below 128
     (dict(n=14336, ld=14336, flags=4, rows=0), 0),       # and for n = m 2^k (Paley blocks)
     (dict(n=12 * 32, ld=12 * 32, flags=8, rows=0), 0),
     (dict(n=4096, ld=4096, flags=4 | 8, rows=0), 1),     # one mode at a time
     (dict(n=4096, ld=4096, flags=64, rows=0), 1),        # unknown flag bit
     (dict(n=4096, ld=4096, flags=1 | 32, rows=0), 0),    # INT4 codes one per byte at n = 4096
     (dict(n=14336, ld=14336, flags=32, rows=0), 0),      # and for n = m 2^k
-    (dict(n=128, ld=128, flags=32, rows=0), 2),          # not for n <= 128
+    (dict(n=128, ld=128, flags=32, rows=0), 0),          # n = 128 too
+    (dict(n=32, ld=32, flags=32, rows=0), 2),            # not below 128
     (dict(n=4096, ld=4096, flags=4 | 32, rows=0), 1),    # one mode at a time
     (dict(n=8192, ld=8192, flags=1 | 16, rows=0), 0),    # E4M3 operand codes at n = 8192
     (dict(n=256, ld=256, flags=16, rows=0), 0),          # and from n = 256 on
-    (dict(n=128, ld=128, flags=16, rows=0), 2),          # not for n <= 128
+    (dict(n=128, ld=128, flags=16, rows=0), 0),          # and at n = 128
+    (dict(n=64, ld=64, flags=16, rows=0), 2),            # not below
     (dict(n=14336, ld=14336, flags=16, rows=0), 2),      # nor for n = m 2^k
     (dict(n=4096, ld=4096, flags=4 | 16, rows=0), 1),    # one mode at a time
 ])

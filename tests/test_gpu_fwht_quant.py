@@ -152,7 +152,7 @@ def test_output_guard_bands_untouched():
 
 
 
-@pytest.mark.parametrize("n", [256, 1024, 2048, 4096, 8192])
+@pytest.mark.parametrize("n", [128, 256, 1024, 2048, 4096, 8192])
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
 def test_e4m3_operand_codes(n, dt, flags):

@@ -62,7 +62,7 @@ def test_group_weight_codes(flags):
 
 # ---- the two code modes at the other power-of-two row lengths ----
 
-SIZES = [256, 512, 1024, 2048, 8192]
+SIZES = [128, 256, 512, 1024, 2048, 8192]   # 128: the head-sized kernel
 
 
 @pytest.mark.parametrize("n", SIZES)
@@ -323,7 +323,7 @@ def test_per_group_prefill_shape_sampled_rows():
 # (RQ_INT4_BYTES) into the W4A8 product.
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("n", [256, 1024, 4096, 8192, 3072])
+@pytest.mark.parametrize("n", [128, 256, 1024, 4096, 8192, 3072])
 @pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
 def test_int4_byte_codes(n, flags):
     """RQ_INT4_BYTES: the oracle's INT4 codes (tie window aside) and scales, one
