@@ -58,16 +58,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 4.5 / 2.25   # nominal dense ratio (fp8 / bf16) on GB300
 SLEEP_CYCLES = 400_000       # ~0.2 ms GPU-side pause between timed steps
 
-# DRAM bytes (read + write) per launch of each kernel at each workload, from one
-# ncu capture of the kernel as it is now (dram__bytes_read.sum +
-# dram__bytes_write.sum); None where no capture of the current kernel exists.
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch, from the ncu captures
 # summarized under profiles/ (kernel, workload, activation-code form); None where no
 # capture of the current kernel exists.  Writes still in L2 when a kernel ends are
 # not counted by the capture.
 NCU_TRAFFIC = {
-    ("w4a4_gemm", "large", "e4m3"): 158_147_840 + 205_566_720,
-    ("fwht_quant", "large", "e4m3"): 67_145_728 + 2_708_992,
+    ("w4a4_gemm", "large", "e4m3"): 161_607_168 + 202_691_584,
+    ("fwht_quant", "large", "e4m3"): 67_176_960 + 3_142_912,
     ("kv_rotate_quant", "kv", None): 134_277_120 + 13_850_112,
 }
 PROBE_MMAS_PER_SM = 200_000   # FP8 tensor-pipe probe: ~0.1 s of back-to-back MMAs
@@ -97,8 +94,8 @@ def host_info():
 
 def fwht_bytes(rows, n, in_bytes=2, code_bytes_per_elem=0.5):
     """Read the row once, write its codes (packed: n/2 bytes; operand form: n)
-    and scale once."""
-    return rows * (n * in_bytes + int(n * code_bytes_per_elem) + 4)
+    and its scale (operand form: the scale and the row's code sum)."""
+    return rows * (n * in_bytes + int(n * code_bytes_per_elem) + (8 if code_bytes_per_elem == 1.0 else 4))
 
 
 def gemm_ops(M, N, K):
@@ -281,7 +278,7 @@ def run_gpu(args, work, kvw):
 
     # preallocated outputs
     aq = torch.empty(M, K if e4 else K // 2, dtype=torch.uint8, device=dev)
-    as_ = torch.empty(M, dtype=torch.float32, device=dev)
+    as_ = torch.empty((M, 2) if e4 else (M,), dtype=torch.float32, device=dev)   # e4m3: (scale, code sum) per row
     y = torch.empty(M, N, dtype=torch.float16, device=dev)
     kv_out = {"kq": torch.empty(T, H, D // 2, dtype=torch.uint8, device=dev),
               "ks": torch.empty(T, H, dtype=torch.float32, device=dev),
@@ -535,7 +532,13 @@ def parity_sample(work, kvw, x_cpu, k_cpu, v_cpu, x, k, v, aq, as_, kv_out, e4, 
     M, n = x_cpu.shape
     sel = np.unique(np.r_[np.arange(min(rows, M)), np.arange(max(0, M - rows), M)])
     ref = oracle.fwht_quant(x_cpu[sel].double().numpy(), seed, flags, want_y=True, want_ratio=True)
-    a_diff, a_tie = diff_count(aq[torch.from_numpy(sel).to(aq.device)].cpu().numpy(), ref, operand=e4)
+    gq = aq[torch.from_numpy(sel).to(aq.device)].cpu().numpy()
+    a_diff, a_tie = diff_count(gq, ref, operand=e4)
+    if e4:
+        # the code sum beside each scale, exact for the codes written
+        sums = as_[torch.from_numpy(sel).to(as_.device), 1].cpu().numpy()
+        if not np.array_equal(sums, decode_operand(gq).astype(np.int64).sum(axis=1).astype(np.float32)):
+            raise AssertionError("sampled row code sums differ from the codes written")
     _, _, ygpu = rq.fwht_quant(x[torch.from_numpy(sel).to(x.device)].contiguous(), seed, flags, want_y=True)
     yg = ygpu.cpu().double().numpy()
     err = (np.abs(yg - ref["y"]).max(axis=1) / np.abs(ref["y"]).max(axis=1)).max()

@@ -151,15 +151,19 @@ enum { RQ_INT4_BYTES = 32u };
  *              [rows][n] bytes; the byte of code q is q for q >= 0 and
  *              0x80 | -q for q < 0 (the FP8 E4M3 encoding of q * 2^-9), and
  *              within each group of 8 codes the bytes hold codes
- *              0, 2, 4, 6, 1, 3, 5, 7 of the group.  Twice the bytes of the
- *              packed form; the product then widens only the weights.
+ *              0, 2, 4, 6, 1, 3, 5, 7 of the group.  scales is [rows][2]
+ *              fp32: the row's scale (max|y|/7, as the default) and the sum
+ *              of its n codes (an integer, exact in fp32), the product's
+ *              offset term.  Twice the bytes of the packed form; the product
+ *              then widens only the weights.
  *            RQ_INT4_BYTES: the default INT4 codes and scales (max|y|/7),
  *              each code stored as one int8 byte: q is [rows][n] int8.  This
  *              is the activation operand of rq_w4a8_gemm, which then computes
  *              the W4A4 product with per-channel or per-group (128) weight
  *              scales ([SQ] §The architecture, per-group scales).
  *   q        out: [rows][n/2] bytes, packed codes (row stride n/2).
- *   scales   out: [rows] fp32 scales, max|y|/7 of each rotated row.
+ *   scales   out: [rows] fp32 scales, max|y|/7 of each rotated row (the
+ *            shapes above for RQ_GROUP_SCALES and RQ_E4M3_CODES).
  *   y        out, may be NULL: [rows][n] fp32 rotated rows y = xR (parity
  *            checks only; writing it adds 4n bytes of traffic per row).
  */
@@ -189,11 +193,14 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
  *             already folded into w_q.
  *   flags     0, or RQ_A_E4M3: a_q is [M][K] bytes, the activation codes in
  *             the operand form rq_fwht_quant writes with RQ_E4M3_CODES (M > 64
- *             only; RQ_ERR_UNSUPPORTED otherwise).
+ *             only; RQ_ERR_UNSUPPORTED otherwise), and a_scales is [M][2]
+ *             (scale, sum of the row's codes) as it writes them; a_scales is
+ *             then required for RQ_I32 too.
  *   y         out: [M][N] row-major, of y_dtype:
  *             RQ_F16  the dequantized product rounded to fp16;
  *             RQ_F32  the dequantized product in fp32;
- *             RQ_I32  the raw int32 accumulators (scales unused, may be NULL).
+ *             RQ_I32  the raw int32 accumulators (scales unused, may be NULL,
+ *                     but for the code sums of RQ_A_E4M3).
  *             N * sizeof(y_dtype) must be a multiple of 16 bytes.
  *   Kernels (all on tensor cores, the integer sums exact in each):
  *     M > 64: persistent CTA pairs, 256 x 256 tiles, codes widened to FP8

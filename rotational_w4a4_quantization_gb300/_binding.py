@@ -136,7 +136,8 @@ def fwht_quant(x: torch.Tensor, seed: int, flags: int = RQ_SIGNS_FIRST, *, q=Non
     (rows x n/2) uint8, scales (rows,) fp32, y (rows x n) fp32 = x R.  With
     RQ_INT8_CODES in flags q is (rows x n) int8; with RQ_GROUP_SCALES scales is
     (rows x n/128); with RQ_E4M3_CODES q is (rows x n) uint8, the same INT4 codes
-    as the product's operand bytes (see include/rq.h); with RQ_INT4_BYTES q is
+    as the product's operand bytes (see include/rq.h), and scales (rows x 2)
+    holds each row's scale and code sum; with RQ_INT4_BYTES q is
     (rows x n) int8, the INT4 codes one per byte (for w4a8_gemm: a W4A4 product
     with per-group weight scales)."""
     lib = load_library()
@@ -151,7 +152,7 @@ def fwht_quant(x: torch.Tensor, seed: int, flags: int = RQ_SIGNS_FIRST, *, q=Non
         q_shape, q_dtype = (rows, n), torch.uint8
     else:
         q_shape, q_dtype = (rows, n // 2), torch.uint8
-    s_shape = (rows, n // 128) if flags & RQ_GROUP_SCALES else (rows,)
+    s_shape = (rows, n // 128) if flags & RQ_GROUP_SCALES else ((rows, 2) if flags & RQ_E4M3_CODES else (rows,))
     if q is None:
         q = torch.empty(q_shape, dtype=q_dtype, device=x.device)
     if scales is None:
@@ -174,7 +175,8 @@ def w4a4_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_d
     """y = dequant(Q(XR) . Q(R^T W)): a_q (M x K/2), w_q (N x K/2) packed codes,
     a_scales (M,), w_scales (N,).  out_dtype float16 / float32, or int32 for the
     raw accumulators.  a_q of shape (M x K) holds the activation codes in the
-    operand form of fwht_quant(..., RQ_E4M3_CODES) (more than 64 rows)."""
+    operand form of fwht_quant(..., RQ_E4M3_CODES) (more than 64 rows); a_scales
+    is then the (M x 2) scales-and-code-sums it returns, needed for int32 too."""
     lib = load_library()
     M, ka = a_q.shape
     N, kb2 = w_q.shape
@@ -188,7 +190,10 @@ def w4a4_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_d
         out = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
     _expect(out, "out", (M, N), _OUT_DTYPES)
     raw = out.dtype == torch.int32       # raw accumulators: the scales are not read
-    _expect(a_scales, "a_scales", (M,), torch.float32, optional=raw)
+    if flags & RQ_A_E4M3:
+        _expect(a_scales, "a_scales", (M, 2), torch.float32)   # (scale, code sum) per row
+    else:
+        _expect(a_scales, "a_scales", (M,), torch.float32, optional=raw)
     _expect(w_scales, "w_scales", (N,), torch.float32, optional=raw)
     _dev(a_q, w_q, a_scales, w_scales, out)
     with torch.cuda.device(a_q.device):

@@ -108,9 +108,10 @@ rq_status rq_w4a4_gemm(const uint8_t *a_q, const float *a_scales, const uint8_t 
     if (y_dtype != RQ_F16 && y_dtype != RQ_F32 && y_dtype != RQ_I32) return RQ_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return RQ_OK;
     const bool need_scales = y_dtype != RQ_I32;
-    if (!a_q || !w_q || !y || (need_scales && (!a_scales || !w_scales))) return RQ_ERR_INVALID_ARG;
+    const bool need_a = need_scales || a_e4m3;   // the operand form's row code sums sit in a_scales
+    if (!a_q || !w_q || !y || (need_a && !a_scales) || (need_scales && !w_scales)) return RQ_ERR_INVALID_ARG;
     if (!rq::aligned16(a_q) || !rq::aligned16(w_q) || !rq::aligned16(y)) return RQ_ERR_MISALIGNED;
-    if (need_scales && (!rq::aligned16(a_scales) || !rq::aligned16(w_scales))) return RQ_ERR_MISALIGNED;
+    if ((need_a && !rq::aligned16(a_scales)) || (need_scales && !rq::aligned16(w_scales))) return RQ_ERR_MISALIGNED;
     if ((N * rq::elem_size(y_dtype)) % 16 != 0) return RQ_ERR_MISALIGNED;
     rq::GemmArgs g{a_q, a_scales, w_q, w_scales, M, N, K, y,
                    y_dtype == RQ_F16 ? 0 : (y_dtype == RQ_F32 ? 1 : 2), a_e4m3};

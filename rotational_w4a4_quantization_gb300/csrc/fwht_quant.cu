@@ -463,7 +463,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
                     job.scales[row * (int64_t)(n / 128) + t] = (gmax[0] / 7.0f) * inv_sqrt_n;
                 }
             } else if (t == 0) {
-                job.scales[row] = (amax / qmax) * inv_sqrt_n;
+                job.scales[e4 ? 2 * row : row] = (amax / qmax) * inv_sqrt_n;   // E4M3: (scale, code sum) per row
             }
             uint8_t *qrow = PL::kTwoPhase ? job.q + row * (int64_t)(n / 2) : stg + (lane / P) * (n / 2);
             // output chunk of slot s: phase-2 map, or natural order for one row per thread
@@ -519,6 +519,7 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
                     qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
                 }
             } else {
+            int csum = 0;   // E4M3: this thread's part of the row's code sum
 #pragma unroll
             for (int s4 = 0; s4 < NSLOT; s4 += 4) {
                 uint32_t words[4];
@@ -537,16 +538,26 @@ fwht_quant_kernel(const __grid_constant__ KParams prm) {
                         code[2 * k] = (uint32_t)qq;
                         code[2 * k + 1] = (uint32_t)(qq >> 32);
                     }
-                    words[cc] = pack8(code);
+                    if (e4) {
+                        // one signed E4M3 byte per code, in the product's operand
+                        // order (even codes, then odd codes, of each chunk)
+                        *reinterpret_cast<uint2 *>(job.q + row * (int64_t)n + 8 * (c0 + cc)) =
+                            make_uint2(e4m3_word_sum(code[0], code[2], code[4], code[6], csum),
+                                       e4m3_word_sum(code[1], code[3], code[5], code[7], csum));
+                    } else {
+                        words[cc] = pack8(code);
+                    }
                 }
                 // chunks c0..c0+3 are consecutive (slot bits 0,1 = chunk bits 0,1)
+                if (!e4) *reinterpret_cast<uint4 *>(qrow + 4 * c0) = make_uint4(words[0], words[1], words[2], words[3]);
+            }
+            if constexpr (PL::kTwoPhase && P <= 32) {
                 if (e4) {
-                    // one signed E4M3 byte per code, in the product's operand order
-                    uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)n + 8 * c0);
-                    qp[0] = make_uint4(e4m3_even(words[0]), e4m3_odd(words[0]), e4m3_even(words[1]), e4m3_odd(words[1]));
-                    qp[1] = make_uint4(e4m3_even(words[2]), e4m3_odd(words[2]), e4m3_even(words[3]), e4m3_odd(words[3]));
-                } else {
-                    *reinterpret_cast<uint4 *>(qrow + 4 * c0) = make_uint4(words[0], words[1], words[2], words[3]);
+                    // the row's P threads are consecutive lanes, all active or all not
+                    const unsigned rmask = (full >> (32 - P)) << (lane & ~(P - 1));
+#pragma unroll
+                    for (int k = 0; k < PL::T; ++k) csum += __shfl_xor_sync(rmask, csum, 1 << k);
+                    if (t == 0) job.scales[2 * row + 1] = (float)csum;
                 }
             }
             }
@@ -773,6 +784,8 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
 #pragma unroll
         for (int k = 0; k < 5; ++k) amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1 << k));
         if (lane == 0) red[row_in_cta * 2 + half] = aborted ? __int_as_float(-1) : amax;
+        // E4M3: the row's code sum is added up in global memory by its warps
+        if ((prm.flags & RQ_E4M3_CODES) && active && t == 0) job.scales[2 * row + 1] = 0.f;
         asm volatile("bar.sync %0, 64;" ::"r"(rbar) : "memory");
         const float r0 = red[row_in_cta * 2], r1 = red[row_in_cta * 2 + 1];
         // the two warps of a row leave together: share the abort decision
@@ -793,7 +806,7 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
             if (grp) {
                 if ((t & 1) == 0) job.scales[row * (int64_t)(n / 128) + (t >> 1)] = (am / 7.0f) * inv_sqrt_n;
             } else if (t == 0) {
-                job.scales[row] = (am / qmax) * inv_sqrt_n;
+                job.scales[e4 ? 2 * row : row] = (am / qmax) * inv_sqrt_n;   // E4M3: (scale, code sum) per row
             }
             // the thread's 64 consecutive elements are chunks 8t + s; one branch per
             // row for each option (signs after the transform, fp32 output)
@@ -838,6 +851,30 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     qp[c] = make_uint4(words[4 * c], words[4 * c + 1], words[4 * c + 2], words[4 * c + 3]);
+            } else if (e4) {
+                // one signed E4M3 byte per code, in the product's operand order
+                // (even codes, then odd codes, of each chunk): 64 bytes
+                uint32_t words[16];
+                int csum = 0;
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    uint32_t code[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const pair_t qq = fma2(v[4 * s + k], inv2, bias2);
+                        code[2 * k] = (uint32_t)qq;
+                        code[2 * k + 1] = (uint32_t)(qq >> 32);
+                    }
+                    words[2 * s] = e4m3_word_sum(code[0], code[2], code[4], code[6], csum);
+                    words[2 * s + 1] = e4m3_word_sum(code[1], code[3], code[5], code[7], csum);
+                }
+                uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)n + 64 * t);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    qp[c] = make_uint4(words[4 * c], words[4 * c + 1], words[4 * c + 2], words[4 * c + 3]);
+                // the warp's part of the code sum (the slot was zeroed before the barrier)
+                csum = __reduce_add_sync(full, csum);
+                if (lane == 0) atomicAdd(&job.scales[2 * row + 1], (float)csum);
             } else {
                 uint32_t words[8];
 #pragma unroll
@@ -851,18 +888,9 @@ fwht_quant_k4_kernel(const __grid_constant__ KParams prm) {
                     }
                     words[s] = pack8(code);
                 }
-                if (e4) {
-                    // one signed E4M3 byte per code, in the product's operand order: 64 bytes
-                    uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)n + 64 * t);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        qp[c] = make_uint4(e4m3_even(words[2 * c]), e4m3_odd(words[2 * c]), e4m3_even(words[2 * c + 1]),
-                                           e4m3_odd(words[2 * c + 1]));
-                } else {
-                    uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)(n / 2) + 32 * t);
-                    qp[0] = make_uint4(words[0], words[1], words[2], words[3]);
-                    qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
-                }
+                uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)(n / 2) + 32 * t);
+                qp[0] = make_uint4(words[0], words[1], words[2], words[3]);
+                qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
             }
         }
     }
@@ -1082,6 +1110,8 @@ fwht_quant_k8_kernel(const __grid_constant__ KParams prm) {
 #pragma unroll
         for (int k = 0; k < 5; ++k) amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1 << k));
         if (lane == 0) red[row_in_cta * 4 + wr] = aborted ? __int_as_float(-1) : amax;
+        // E4M3: the row's code sum is added up in global memory by its warps
+        if ((prm.flags & RQ_E4M3_CODES) && active && t == 0) job.scales[2 * row + 1] = 0.f;
         asm volatile("bar.sync %0, 128;" ::"r"(rbar) : "memory");
         const float4 r4 = reinterpret_cast<const float4 *>(red)[row_in_cta];
         // the four warps of a row leave together: share the abort decision
@@ -1103,7 +1133,7 @@ fwht_quant_k8_kernel(const __grid_constant__ KParams prm) {
             if (grp) {
                 if ((t & 1) == 0) job.scales[row * (int64_t)(n / 128) + (t >> 1)] = (am / 7.0f) * inv_sqrt_n;
             } else if (t == 0) {
-                job.scales[row] = (am / qmax) * inv_sqrt_n;
+                job.scales[e4 ? 2 * row : row] = (am / qmax) * inv_sqrt_n;   // E4M3: (scale, code sum) per row
             }
             // the thread's 64 consecutive elements are chunks 8t + c (pairs 4c .. 4c+3);
             // one branch per row for each option (signs after the transform, fp32 output)
@@ -1149,6 +1179,7 @@ fwht_quant_k8_kernel(const __grid_constant__ KParams prm) {
                 // one signed E4M3 byte per code, in the product's operand order
                 // (even codes, then odd codes, of each chunk): 64 bytes
                 uint32_t words[16];
+                int csum = 0;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint32_t code[8];
@@ -1158,13 +1189,16 @@ fwht_quant_k8_kernel(const __grid_constant__ KParams prm) {
                         code[2 * k] = (uint32_t)qq;
                         code[2 * k + 1] = (uint32_t)(qq >> 32);
                     }
-                    words[2 * c] = e4m3_word(code[0], code[2], code[4], code[6]);
-                    words[2 * c + 1] = e4m3_word(code[1], code[3], code[5], code[7]);
+                    words[2 * c] = e4m3_word_sum(code[0], code[2], code[4], code[6], csum);
+                    words[2 * c + 1] = e4m3_word_sum(code[1], code[3], code[5], code[7], csum);
                 }
                 uint4 *qp = reinterpret_cast<uint4 *>(job.q + row * (int64_t)n + 64 * t);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     qp[c] = make_uint4(words[4 * c], words[4 * c + 1], words[4 * c + 2], words[4 * c + 3]);
+                // the warp's part of the code sum (the slot was zeroed before the barrier)
+                csum = __reduce_add_sync(full, csum);
+                if (lane == 0) atomicAdd(&job.scales[2 * row + 1], (float)csum);
             } else {
                 uint32_t words[8];
 #pragma unroll
@@ -1398,6 +1432,8 @@ fwht_quant_kv128_kernel(const __grid_constant__ KParams prm) {
         }
         float amax = pairs_absmax<NP>(v);
         amx[h * 32 + lane] = aborted ? __int_as_float(-1) : amax;
+        // E4M3: the row's code sum is added up in global memory by its two threads
+        if ((prm.flags & RQ_E4M3_CODES) && active && h == 0) job.scales[2 * row + 1] = 0.f;
         asm volatile("bar.sync %0, 64;" ::"r"(pbar) : "memory");
         const float m0 = amx[lane], m1 = amx[32 + lane];
         // the two warps of the pair leave together: share the abort decision
@@ -1412,7 +1448,7 @@ fwht_quant_kv128_kernel(const __grid_constant__ KParams prm) {
             const bool bytes = (fl & (RQ_INT8_CODES | RQ_INT4_BYTES)) != 0, e4 = (fl & RQ_E4M3_CODES) != 0;
             const float qmax = (fl & RQ_INT8_CODES) ? 127.0f : 7.0f;
             const float inv = amax > 0.f ? qmax / amax : 0.f;
-            if (h == 0) job.scales[row] = (amax / qmax) * inv_sqrt_n;
+            if (h == 0) job.scales[e4 ? 2 * row : row] = (amax / qmax) * inv_sqrt_n;   // E4M3: (scale, code sum)
             // output chunk of run r, chunk c: 8 r + 4 h + c
             if (!signs_first) {
 #pragma unroll
@@ -1463,6 +1499,7 @@ fwht_quant_kv128_kernel(const __grid_constant__ KParams prm) {
             } else {
                 // one byte per code: run r is 32 bytes at 64 r + 32 h
                 uint8_t *qrow = job.q + row * (int64_t)n;
+                int csum = 0;
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     uint32_t words[8];
@@ -1479,8 +1516,8 @@ fwht_quant_kv128_kernel(const __grid_constant__ KParams prm) {
                         }
                         if (e4) {
                             // signed E4M3 bytes, even codes then odd codes of the chunk
-                            words[2 * c] = e4m3_word(code[0], code[2], code[4], code[6]);
-                            words[2 * c + 1] = e4m3_word(code[1], code[3], code[5], code[7]);
+                            words[2 * c] = e4m3_word_sum(code[0], code[2], code[4], code[6], csum);
+                            words[2 * c + 1] = e4m3_word_sum(code[1], code[3], code[5], code[7], csum);
                         } else {
                             // two's-complement bytes in element order
 #pragma unroll
@@ -1493,6 +1530,8 @@ fwht_quant_kv128_kernel(const __grid_constant__ KParams prm) {
                     qp[0] = make_uint4(words[0], words[1], words[2], words[3]);
                     qp[1] = make_uint4(words[4], words[5], words[6], words[7]);
                 }
+                // this thread's half of the code sum (the slot was zeroed before the barrier)
+                if (e4) atomicAdd(&job.scales[2 * row + 1], (float)csum);
             }
         }
     }

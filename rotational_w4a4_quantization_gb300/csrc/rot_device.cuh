@@ -145,28 +145,21 @@ __device__ __forceinline__ uint32_t pack8(const uint32_t *c) {
     return (ev & 0x0f0f0f0fu) | ((od << 4) & 0xf0f0f0f0u);
 }
 
-// The operand form of 8 packed codes (one word, code 2k in the low nibble of byte
-// k): one E4M3 byte per code with the code's sign and |q| <= 8 as |q| 2^-9,
-// the even codes in e4m3_even, the odd codes in e4m3_odd (this order within
-// each group of 8 is the W4A4 product's operand order).
-__device__ __forceinline__ uint32_t e4m3_signed_lanes(uint32_t x) {   // byte lanes 0..15 (two's complement)
-    const uint32_t neg = (x >> 3) & 0x01010101u;
-    return (x ^ (neg * 0x8fu)) + neg;
-}
-__device__ __forceinline__ uint32_t e4m3_even(uint32_t w) { return e4m3_signed_lanes(w & 0x0f0f0f0fu); }
-__device__ __forceinline__ uint32_t e4m3_odd(uint32_t w) { return e4m3_signed_lanes((w >> 4) & 0x0f0f0f0fu); }
-
 __device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
     return r;
 }
-// The same operand bytes straight from four codes, each the low byte of a word
-// (two's complement, |q| <= 7): gather the bytes, then turn each negative one
-// into sign and magnitude (a selector nibble with bit 3 set replicates the sign
-// of its byte, so `neg` holds 0xff in the bytes of negative codes).
-__device__ __forceinline__ uint32_t e4m3_word(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
+// The operand form of four codes, each the low byte of a word (two's complement,
+// |q| <= 7): one E4M3 byte per code with the code's sign and |q| as |q| 2^-9.
+// Gather the bytes, then turn each negative one into sign and magnitude (a
+// selector nibble with bit 3 set replicates the sign of its byte, so `neg`
+// holds 0xff in the bytes of negative codes).  The four codes are also added to
+// `sum` (a signed byte dot product with ones): the operand form carries each
+// row's code sum, the offset term of the W4A4 product.
+__device__ __forceinline__ uint32_t e4m3_word_sum(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, int &sum) {
     const uint32_t x = prmt_b32(prmt_b32(c0, c1, 0x0040u), prmt_b32(c2, c3, 0x0040u), 0x5410u);
+    sum = __dp4a((int)x, 0x01010101, sum);
     const uint32_t neg = prmt_b32(x, 0u, 0xba98u);
     return (x ^ (neg & 0x7f7f7f7fu)) + (neg & 0x01010101u);
 }

@@ -335,13 +335,6 @@ __device__ __forceinline__ uint32_t widen(uint32_t w, uint32_t &lo, uint32_t &hi
     return lo + hi;   // four bytes, each <= 30
 }
 
-// Byte lanes holding 4-bit two's-complement codes (0..15) -> E4M3 bytes of the
-// same signed value times 2^-9: |q| <= 8 in bits 0..3, the sign in bit 7.
-__device__ __forceinline__ uint32_t tc_e4m3_lanes(uint32_t x) {
-    const uint32_t neg = (x >> 3) & 0x01010101u;
-    return (x ^ (neg * 0x8fu)) + neg;
-}
-
 template <bool PAIR>
 __device__ __forceinline__ void cluster_sync() {
     if constexpr (PAIR) {
@@ -392,11 +385,12 @@ __device__ __forceinline__ void store_outputs(void *y, int64_t N, int64_t m, int
 }
 
 // AE: the activation codes arrive in the operand form (one signed E4M3 byte per
-// code, rq_fwht_quant with RQ_E4M3_CODES): lane 1 of warp 0 loads each K block's
-// 128 x 128-byte A tile by TMA with the 128-byte swizzle straight into the
-// operand ring (completing on a_full), the converters widen only W, with its
-// sign (E4M3 of q 2^-9), and wait for a_full before releasing the operand
-// stage.  Products q_a q_w 2^-18 are exact, so no offset sums are kept.
+// code, rq_fwht_quant with RQ_E4M3_CODES, whose scales carry each row's code sum
+// S_a): lane 1 of warp 0 loads each K block's 128 x 128-byte A tile by TMA with
+// the 128-byte swizzle straight into the operand ring (completing on a_full),
+// the converters widen only W, to u_w = q_w + 8 as for the packed path, and wait
+// for a_full before releasing the operand stage.  Products q_a u_w 2^-18 and
+// their sums (|.| <= 120 K 2^-18) are exact; the epilogue subtracts 8 S_a.
 template <int YMODE, bool PAIR, bool A8, int TEAMS, bool AE = false>
 __global__ void __launch_bounds__(threads_tc(TEAMS), 1)
 w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
@@ -602,20 +596,21 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     for (int j = 0; j < C::NACH; ++j) emit(s.opA[os], rq + 32 * j, a[j], sumA[j]);
                 }
                 if constexpr (AE) {
-                    // W with its sign: E4M3 of q 2^-9, the even codes of each word
-                    // first (the operand order of the activation bytes)
+                    // W as u = q + 8 (one XOR per word, no sums: the activation
+                    // row sums arrive with the activation scales), the even codes
+                    // of each word first (the operand order of the activation bytes)
 #pragma unroll
                     for (int j = 0; j < C::NWCH; ++j) {
                         const int row = rq + 32 * j;
                         uint8_t *rowp = s.opW[os] + row * 128;
                         const uint4 &v = w[j];
+                        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t lo[4], hi[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) widen(wv[i], lo[i], hi[i]);
                         const int g0 = (2 * ch) ^ (row & 7), g1 = (2 * ch + 1) ^ (row & 7);
-                        *reinterpret_cast<uint4 *>(rowp + 16 * g0) =
-                            make_uint4(tc_e4m3_lanes(v.x & 0x0f0f0f0fu), tc_e4m3_lanes((v.x >> 4) & 0x0f0f0f0fu),
-                                       tc_e4m3_lanes(v.y & 0x0f0f0f0fu), tc_e4m3_lanes((v.y >> 4) & 0x0f0f0f0fu));
-                        *reinterpret_cast<uint4 *>(rowp + 16 * g1) =
-                            make_uint4(tc_e4m3_lanes(v.z & 0x0f0f0f0fu), tc_e4m3_lanes((v.z >> 4) & 0x0f0f0f0fu),
-                                       tc_e4m3_lanes(v.w & 0x0f0f0f0fu), tc_e4m3_lanes((v.w >> 4) & 0x0f0f0f0fu));
+                        *reinterpret_cast<uint4 *>(rowp + 16 * g0) = make_uint4(lo[0], hi[0], lo[1], hi[1]);
+                        *reinterpret_cast<uint4 *>(rowp + 16 * g1) = make_uint4(lo[2], hi[2], lo[3], hi[3]);
                     }
                 } else {
 #pragma unroll
@@ -663,7 +658,7 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int buf = it & 1;
             if (!mbar_wait(s, &s.sum_empty[buf], (uint32_t)((it >> 1) & 1) ^ 1, prm.err)) { ok = false; break; }
             if constexpr (AE) {
-                // no offset sums: the products are of signed codes
+                // the row terms come from the activation row sums (epilogue)
             } else if constexpr (A8) {
                 if ((tt & 7) == 0) {
 #pragma unroll
@@ -725,9 +720,19 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int64_t m0 = (tile % n_tiles_m) * C::TILE_M + (int64_t)rank * BM, n0 = (tile / n_tiles_m) * BN;
             const int mr = 32 * q + lane;
             const int64_t m = A8 ? (m0 + mr) >> 1 : m0 + mr;
-            const int rowt = -8 * s.rowsum[buf][mr];
-            s.rowsum[buf][mr] = 0;
-            const float sa = (YMODE != 2 && m < prm.M) ? prm.sa[m] : 0.f;
+            int rowt;
+            float sa;
+            if constexpr (AE) {
+                // sum_k q_a (q_w + 8) = sum_k q_a q_w + 8 S_a: the pair (scale, S_a)
+                // of row m (S_a exact in fp32)
+                const float2 p = m < prm.M ? reinterpret_cast<const float2 *>(prm.sa)[m] : make_float2(0.f, 0.f);
+                rowt = -8 * (int)p.y;
+                sa = p.x;
+            } else {
+                rowt = -8 * s.rowsum[buf][mr];
+                s.rowsum[buf][mr] = 0;
+                sa = (YMODE != 2 && m < prm.M) ? prm.sa[m] : 0.f;
+            }
             // A8: the u_l lane (odd) takes no column term; its partner adds 16 x its own
             const bool odd = A8 && (lane & 1);
             const int cmask = odd ? 0 : -1;

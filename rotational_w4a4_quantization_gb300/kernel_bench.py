@@ -75,10 +75,10 @@ def main(argv=None):
         x = synth.activations(w.rows, n, w.x_dtype, w.data_seed, n_out, w.outlier_factor).to(dev)
         e4 = args.a_form == "e4m3"
         q = torch.empty(w.rows, n if e4 else n // 2, dtype=torch.uint8, device=dev)
-        s = torch.empty(w.rows, dtype=torch.float32, device=dev)
+        s = torch.empty((w.rows, 2) if e4 else (w.rows,), dtype=torch.float32, device=dev)   # e4m3: scale, code sum
         fl = flags | (rq.RQ_E4M3_CODES if e4 else 0)
         fn = lambda: rq.fwht_quant(x, seed, fl, q=q, scales=s)
-        work, unit = w.rows * (n * x.element_size() + (n if e4 else n // 2) + 4), "GB/s"
+        work, unit = w.rows * (n * x.element_size() + (n if e4 else n // 2) + (8 if e4 else 4)), "GB/s"
         what = f"fwht_quant {w.rows}x{n} {str(x.dtype).split('.')[-1]}{' e4m3 codes' if e4 else ''}"
     elif args.kernel == "kv":
         kw = synth.KV

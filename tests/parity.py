@@ -139,6 +139,14 @@ def operand_form(packed: np.ndarray) -> np.ndarray:
     return byte.astype(np.uint8).reshape(rows, 2 * half)
 
 
+def operand_scales(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """The (rows x 2) fp32 scales that go with operand_form(packed): each row's
+    scale and the sum of its codes (rq_fwht_quant with RQ_E4M3_CODES)."""
+    n = 2 * packed.shape[-1]
+    sums = unpack_codes(packed, n).astype(np.int64).sum(axis=1)
+    return np.stack([np.asarray(scales, np.float32).reshape(-1), sums.astype(np.float32)], axis=1)
+
+
 def from_operand_form(e4: np.ndarray, n: int) -> np.ndarray:
     """Inverse of operand_form: operand bytes -> int16 codes in natural order."""
     b = e4.reshape(-1, n // 8, 8).astype(np.int16)

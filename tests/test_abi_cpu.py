@@ -89,6 +89,8 @@ def gemm(lib, M=16, N=64, K=256, a=A16, w=A16, sa=A16, sw=A16, y=A16, ydt=2, fla
     (dict(flags=32), 1),
     (dict(flags=16), 2),              # operand-form activations feed the M > 64 kernel only
     (dict(flags=16, M=0, a=NULL), 0),  # empty: nothing to do
+    (dict(flags=16, M=128, ydt=3, sa=NULL, sw=NULL), 1),   # operand form: the row code sums are read for int32 too
+    (dict(flags=16, M=128, ydt=3, sa=A1, sw=NULL), 3),
     (dict(ydt=1), 2),                 # bf16 output not offered
     (dict(a=NULL), 1),
     (dict(sa=NULL), 1),
@@ -300,6 +302,16 @@ def test_binding_checks_gemm_buffers(lib, which, bad, match):
         args[which] = bad
     with pytest.raises(ValueError, match=match):
         rq.w4a4_gemm(args["a_q"], args["a_scales"], args["w_q"], args["w_scales"], out=out)
+
+
+@pytest.mark.parametrize("sa,match", [
+    (_t((128,), torch.float32), "a_scales: expected shape"),   # operand form: (scale, code sum) per row
+    (None, "a_scales is required"),                            # read for int32 output too
+])
+def test_binding_checks_operand_form_scales(lib, sa, match):
+    M, N, K = 128, 64, 256
+    with pytest.raises(ValueError, match=match):
+        rq.w4a4_gemm(_t((M, K), torch.uint8), sa, _t((N, K // 2), torch.uint8), None, out=_t((M, N), torch.int32))
 
 
 def test_binding_gemm_raw_mode_needs_no_scales(lib):

@@ -157,18 +157,43 @@ def test_output_guard_bands_untouched():
 @pytest.mark.parametrize("flags", [rq.RQ_SIGNS_FIRST, 0])
 def test_e4m3_operand_codes(n, dt, flags):
     """RQ_E4M3_CODES: the same codes and scales as the packed INT4 output, one
-    operand byte per code (decoded here by bit arithmetic), and the oracle's codes
-    within the tie window."""
+    operand byte per code (decoded here by bit arithmetic), each row's code sum
+    beside its scale (exact), and the oracle's codes within the tie window (the
+    oracle's row sums off by at most the row's tie-window differences)."""
     from parity import from_operand_form, unpack_codes
     rows = 77
     x = synth.activations(rows, n, dt, n + rows, 4, 100.0)
     xd = x.to(DEV)
     q_p, s_p = rq.fwht_quant(xd, 5, flags)
     q_e, s_e = rq.fwht_quant(xd, 5, flags | rq.RQ_E4M3_CODES)
-    assert q_e.shape == (rows, n) and q_e.dtype == torch.uint8
-    assert torch.equal(s_e, s_p)
+    assert q_e.shape == (rows, n) and q_e.dtype == torch.uint8 and s_e.shape == (rows, 2)
+    assert torch.equal(s_e[:, 0], s_p)
     codes_e = from_operand_form(to_np(q_e), n)
     assert np.array_equal(codes_e, unpack_codes(to_np(q_p), n))
     assert np.abs(codes_e).max() <= 8
+    assert np.array_equal(to_np(s_e)[:, 1], codes_e.astype(np.int64).sum(axis=1).astype(np.float32))
     ref = oracle.fwht_quant(x.double().numpy(), 5, flags, want_ratio=True)
     compare_codes(oracle.pack(codes_e.astype(np.int8)), ref["q"], ref["ratio"], n)
+    ref_codes = unpack_codes(ref["q"], n).astype(np.int64)
+    per_row = np.abs(codes_e - ref_codes).sum(axis=1)
+    assert (np.abs(to_np(s_e)[:, 1] - ref_codes.sum(axis=1)) <= per_row).all()
+
+
+@pytest.mark.parametrize("n", [128, 4096, 8192])
+def test_e4m3_row_sums_ragged_and_zero_rows(n):
+    """Code sums at a ragged row count with zero rows and single spikes mixed in
+    (sum 0 for a zero row; a spike's row holds +-7 everywhere)."""
+    from parity import from_operand_form
+    rows = 301
+    x = synth.activations(rows, n, torch.bfloat16, n + 11, 4, 100.0)
+    x[5] = 0
+    x[6] = 0
+    x[6, 17] = 3.0
+    q, s = rq.fwht_quant(x.to(DEV), 9, rq.RQ_SIGNS_FIRST | rq.RQ_E4M3_CODES)
+    codes = from_operand_form(to_np(q), n).astype(np.int64)
+    sn = to_np(s)
+    assert sn[5, 0] == 0.0 and sn[5, 1] == 0.0
+    assert set(np.unique(np.abs(codes[6])).tolist()) == {7}
+    assert np.array_equal(sn[:, 1], codes.sum(axis=1).astype(np.float32))
+    ref = oracle.fwht_quant(x[6:7].double().numpy(), 9, rq.RQ_SIGNS_FIRST)
+    assert sn[6, 1] == unpack_codes(ref["q"], n).sum()

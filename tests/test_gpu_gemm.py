@@ -15,7 +15,7 @@ import oracle
 import rotational_w4a4_quantization_gb300 as rq
 from rotational_w4a4_quantization_gb300 import synth
 
-from parity import compare_f16, host_threads, operand_form, oracle_gemm_row_blocks, record, to_dev, to_np
+from parity import compare_f16, host_threads, operand_form, operand_scales, oracle_gemm_row_blocks, record, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -230,11 +230,13 @@ def test_decode_tensor_core_large_model_width():
 
 
 # Activations in the operand form (RQ_A_E4M3, M > 64): the product reads the
-# codes as signed E4M3 bytes straight into its operand ring and widens only W.
+# codes as signed E4M3 bytes straight into its operand ring, widens only W (to
+# q + 8) and removes 8 x each row's code sum, which comes beside its scale.
 def _e4m3_all_modes(aq, sa, wq, sw):
     ae = torch.from_numpy(operand_form(aq.numpy())).to(DEV)
-    d = [t.to(DEV) for t in (sa, wq, sw)]
-    return {dt: to_np(rq.w4a4_gemm(ae, d[0], d[1], d[2], out_dtype=dt)) for dt in (torch.int32, torch.float32, torch.float16)}
+    sa2 = torch.from_numpy(operand_scales(aq.numpy(), sa.numpy())).to(DEV)
+    d = [t.to(DEV) for t in (wq, sw)]
+    return {dt: to_np(rq.w4a4_gemm(ae, sa2, d[0], d[1], out_dtype=dt)) for dt in (torch.int32, torch.float32, torch.float16)}
 
 
 @pytest.mark.parametrize("M,N,K", [
@@ -258,7 +260,8 @@ def test_e4m3_activations_extreme_codes_at_max_k(ba, bw):
     wq = synth.extreme_codes(N, K, bw)
     one_m, one_n = torch.ones(M), torch.ones(N)
     ae = torch.from_numpy(operand_form(aq.numpy())).to(DEV)
-    acc = to_np(rq.w4a4_gemm(ae, one_m.to(DEV), wq.to(DEV), one_n.to(DEV), out_dtype=torch.int32))
+    sa2 = torch.from_numpy(operand_scales(aq.numpy(), one_m.numpy())).to(DEV)
+    acc = to_np(rq.w4a4_gemm(ae, sa2, wq.to(DEV), one_n.to(DEV), out_dtype=torch.int32))
     ref, _ = oracle.w4a4_gemm(aq[:1].numpy(), one_m[:1].numpy(), wq[:1].numpy(), one_n[:1].numpy(), 1, 1, K)
     assert (acc.astype(np.int64) == ref[0, 0]).all()
 
