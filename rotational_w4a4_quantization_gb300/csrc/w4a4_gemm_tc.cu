@@ -805,14 +805,16 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 //    exact), so a partial needs no offset terms; INT8 activations split as in
 //    the A8 variant (a = 16 h + l: row 2i holds h with its sign, row 2i+1 l);
 //  * the MMA (CTA pairs, M256 N128 K32) writes each K block into a fresh
-//    partial in a 3-deep TMEM ring (columns 0..383);
-//  * the epilogue warps (two per TMEM lane quarter, 64 columns each) read a
-//    partial and the running sum kept in TMEM (columns 384..511) with one wait,
-//    add sw[c][g] x partial, store the sum back and release the partial.  The
-//    round trips to TMEM, not the MMAs, set the pace, so the epilogue gets eight
-//    warps and the widening two teams.  After the last block the two rows of an
-//    activation row (adjacent TMEM lanes) combine as 16 S_h + S_l, times 2^18
-//    and sa[m];
+//    partial in a 4-deep TMEM ring (all 512 columns);
+//  * the epilogue warps (four per TMEM lane quarter, 32 columns each) read a
+//    partial, release it, and add sw[c][g] x partial into running sums kept in
+//    registers (32 per thread), so each block costs one TMEM load per warp and
+//    no store.  The release is a CTA-scope arrive on the leader's barrier: the
+//    warp only read tensor memory (ordered by tcgen05.fence), and a cluster-scope
+//    release per warp and block stalled the epilogue on memory barriers.  Two
+//    converter teams take alternate K blocks.  After the last block the two
+//    rows of an activation row (adjacent TMEM lanes) combine as 16 S_h + S_l,
+//    times 2^18 and sa[m];
 //  * the tile's group scales (128 columns x K/128 groups, K <= 8192) are staged
 //    in shared memory by the epilogue threads with cp.async, one tile ahead,
 //    transposed to [group][column] so that a block's 32 columns are 8 vector
@@ -821,13 +823,12 @@ w4a4_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // ---------------------------------------------------------------------------
 constexpr int GBN = 128;                   // tile columns
 constexpr int GWROWS = GBN / 2;            // W rows (output channels) per CTA of the pair
-constexpr int GPK = 6, GOP = 3, GPR = 3;   // packed stages, operand stages, TMEM partial ring
-constexpr int GTEAMS = 2;                  // converter teams (the epilogue, not the widening, sets the pace)
-constexpr int GEPI = 8;                    // epilogue warps: two per TMEM lane quarter, 64 columns each
+constexpr int GPK = 4, GOP = 4, GPR = 4;   // packed stages, operand stages, TMEM partial ring
+constexpr int GTEAMS = 2;                  // converter teams, taking alternate K blocks
+constexpr int GEPI = 16;                   // epilogue warps: four per TMEM lane quarter, 32 columns each
 constexpr int GTHREADS = 32 * (2 + GTEAMS * kTeamWarps + GEPI);
 constexpr int GMAXG = 64;                  // groups staged per column: K <= 8192
-constexpr uint32_t GSCOL = GPR * GBN;      // first TMEM column of the running sum
-static_assert(GSCOL + GBN <= 512, "TMEM budget");
+static_assert(GPR * GBN <= 512, "TMEM budget");
 static_assert(GPK % GTEAMS == 0 && GOP >= GTEAMS, "parity waits stay one phase ahead at most");
 
 struct GSmem {
@@ -864,37 +865,15 @@ __device__ __forceinline__ void mma_f8_pair_n128(uint32_t d_tmem, uint64_t adesc
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+// 16 columns of the warp's 32 TMEM lanes, one register each, behind its wait.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-}
-
-// Two 32-column TMEM loads (a partial and the running sum) behind one wait.
-__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t (&a)[32], uint32_t tb, uint32_t (&b)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
-          "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
-          "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]),
-          "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
-          "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
-          "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]),
-          "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]),
-          "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
-        : "r"(ta), "r"(tb)
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
         : "memory");
 }
 
@@ -1074,9 +1053,9 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         }
     } else {
         // ---------------- epilogue: scale and add the partials, then combine and store ----------------
-        const int e = threadIdx.x - 64 - 32 * kConvWarps;   // 0..255; threads e < 128 stage column e's scales
+        const int e = threadIdx.x - 64 - 32 * kConvWarps;   // 0..511; threads e < 128 stage column e's scales
         const int q = warp & 3;                              // TMEM lane quarter
-        const int half = e >> 7;                             // columns 64 half .. 64 half + 63
+        const int part = e >> 7;                             // columns 32 part .. 32 part + 31
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const bool odd = (lane & 1) != 0;
         const int G = kblocks;
@@ -1111,63 +1090,51 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             const int64_t m = (m0 + 32 * q + lane) >> 1;                             // activation row
             const int64_t n0 = (tile / n_tiles_m) * GBN;
             const float sa = m < prm.M ? prm.sa[m] * 262144.0f : 0.f;               // x 2^18: partials are 2^-18 units
+            float acc[32];   // the running sums of this thread's row, columns 32 part .. 32 part + 31
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.f;
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
                 const int pr = (int)(g % GPR);
                 if (!mbar_wait<true, false>(s, &s.p_full[pr], (uint32_t)((g / GPR) & 1), prm.err)) { ok = false; break; }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                // the previous block's stores of the running sum are complete before it is read
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                const float4 *sc4 = reinterpret_cast<const float4 *>(s.gsc[b] + kb * GBN);
-                const bool last = kb + 1 == kblocks;
-#pragma unroll 1
-                for (int c = 2 * half; c < 2 * half + 2; ++c) {
-                    uint32_t pv[32], sv[32];
-                    const uint32_t tp = tmem + lane_base + (uint32_t)(pr * GBN + 32 * c);
-                    const uint32_t ts = tmem + lane_base + GSCOL + (uint32_t)(32 * c);
-                    if (kb > 0) {
-                        tmem_ld32x2(tp, pv, ts, sv);
-                    } else {
-                        tmem_ld32(tp, pv);
+                const float4 *sc4 = reinterpret_cast<const float4 *>(s.gsc[b] + kb * GBN + 32 * part);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) sv[j] = 0u;
+                for (int h = 0; h < 2; ++h) {   // two 16-column halves: fewer live registers
+                    uint32_t pv[16];
+                    tmem_ld16(tmem + lane_base + (uint32_t)(pr * GBN + 32 * part + 16 * h), pv);
+                    if (h == 1) {
+                        // the partial may be overwritten: it was only read (tensor memory, ordered
+                        // by the fence), so a CTA-scope release is enough, as for the operands
+                        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_remote_cta_scope(&s.p_empty[pr], 0);
                     }
-                    float acc[32];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float4 w4 = sc4[8 * c + j / 4];
+                    for (int j = 0; j < 16; j += 4) {
+                        const float4 w4 = sc4[(16 * h + j) / 4];
                         const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            acc[j + i] = fmaf(wv[i], __uint_as_float(pv[j + i]), __uint_as_float(sv[j + i]));
-                    }
-                    if (!last) {
-                        uint32_t st[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) st[j] = __float_as_uint(acc[j]);
-                        tmem_st32(ts, st);
-                    } else {
-                        // rows 2i (h) and 2i+1 (l) are lanes 2i, 2i+1: the even lane outputs the
-                        // chunk's first 16 columns, the odd lane the next 16
-                        float out[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float mine = odd ? acc[j + 16] : acc[j];
-                            const float recv = __shfl_xor_sync(0xffffffffu, odd ? acc[j] : acc[j + 16], 1);
-                            out[j] = (odd ? fmaf(16.f, recv, mine) : fmaf(16.f, mine, recv)) * sa;
-                        }
-                        if (m < prm.M) store16_f<YMODE>(prm.y, prm.N, m, n0 + 32 * c + (odd ? 16 : 0), out);
+                            acc[16 * h + j + i] = fmaf(wv[i], __uint_as_float(pv[j + i]), acc[16 * h + j + i]);
                     }
                 }
-                // the partial may be overwritten (it was only read)
-                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cta(&s.p_empty[pr], 0);
+            }
+            if (ok) {
+                // rows 2i (h) and 2i+1 (l) are lanes 2i, 2i+1: the even lane outputs the
+                // chunk's first 16 columns, the odd lane the next 16
+                float out[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float mine = odd ? acc[j + 16] : acc[j];
+                    const float recv = __shfl_xor_sync(0xffffffffu, odd ? acc[j] : acc[j + 16], 1);
+                    out[j] = (odd ? fmaf(16.f, recv, mine) : fmaf(16.f, mine, recv)) * sa;
+                }
+                if (m < prm.M) store16_f<YMODE>(prm.y, prm.N, m, n0 + 32 * part + (odd ? 16 : 0), out);
             }
             if (!ok) break;
             __syncwarp();
             if (lane == 0) mbar_arrive(&s.sc_empty[b]);
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         asm volatile("cp.async.wait_all;" ::: "memory");   // no copy into shared memory outlives the CTA
     }
 

@@ -279,11 +279,13 @@ def _check_per_group(y, yref):
 
 
 @pytest.mark.parametrize("M", [65, 130, 600])
-@pytest.mark.parametrize("N,K", [(128, 128), (384, 2048), (256, 8192)])
+@pytest.mark.parametrize("N,K", [(128, 128), (2560, 384), (384, 2048), (256, 8192)])
 def test_product_per_group_tensor_cores(M, N, K):
     """N a multiple of 128 and K <= 8192: CTA pairs with 128 x 128 tiles, one
     TMEM partial per group; one group (K = 128) up to the 64 groups staged per
-    column (K = 8192); ragged M."""
+    column (K = 8192); ragged M.  The MMA issuer waits once per pair of K
+    blocks: K = 128 and K = 384 leave a pair's last block without a partner,
+    and at 600 x 2560 (100 tiles) pairs of blocks straddle two tiles."""
     qa, sa, qw, sw = _random_operands(M, N, K, 128, 5000 + M + N + K)
     _, yref = oracle.w4a8_gemm(qa, sa, qw, sw, M, N, K, 128)
     _check_per_group(_gpu(qa, sa, qw, sw, torch.float32), yref)
