@@ -90,8 +90,8 @@ enum { RQ_SIGNS_FIRST = 1u };
 /* rq_attn_decode: leave the output in the rotated basis (o~ instead of o~ R^T). */
 enum { RQ_ATTN_ROTATED_OUT = 2u };
 /* rq_fwht_quant (n = m 2^k, or a power of two from 256 to 8192): INT8 codes per row (activations of the W4A8 layer),
- * or INT4 codes with one scale per group of 128 elements (weights of the W4A8
- * layer with per-group scales). */
+ * or INT4 codes with one scale per group of 128 elements (weights with per-group
+ * scales); rq_w4a4_gemm: w_scales are per group of 128 (with RQ_A_E4M3). */
 enum { RQ_INT8_CODES = 4u, RQ_GROUP_SCALES = 8u };
 /* rq_fwht_quant (powers of two from 256 to 8192): the INT4 codes written as the
  * W4A4 product's operand, one byte per code (see rq_fwht_quant); rq_w4a4_gemm:
@@ -186,7 +186,9 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
  *   a_scales  [M] per-token fp32 scales.
  *   w_q       [N][K/2] packed weight codes, one output channel per row, e.g.
  *             from rq_fwht_quant on the rows of W^T (the offline fold).
- *   w_scales  [N] per-channel fp32 scales.
+ *   w_scales  [N] per-channel fp32 scales, or with RQ_GROUP_SCALES [N][K/128]
+ *             per-group scales (rq_fwht_quant with RQ_GROUP_SCALES on the rows
+ *             of W^T).
  *   M, N, K   M >= 0, N >= 0 (0: nothing is enqueued), K a positive multiple
  *             of 128 and at most 65536.
  *   seed      accepted for a uniform signature and ignored: the rotation is
@@ -196,6 +198,13 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
  *             only; RQ_ERR_UNSUPPORTED otherwise), and a_scales is [M][2]
  *             (scale, sum of the row's codes) as it writes them; a_scales is
  *             then required for RQ_I32 too.
+ *             RQ_A_E4M3 | RQ_GROUP_SCALES: per-group (128) weight scales
+ *             ([SQ] §The architecture, per-group scales):
+ *               y[m][c] = a_scales[m][0] * sum_g w_scales[c][g] * acc_g[m][c],
+ *             acc_g the exact sum over the 128 codes of group g, scaled and
+ *             summed in fp32 in group order.  M > 64, N a multiple of 128,
+ *             K <= 8192, RQ_F16 or RQ_F32 output; RQ_ERR_UNSUPPORTED otherwise
+ *             (rq_w4a8_gemm on RQ_INT4_BYTES codes covers the other shapes).
  *   y         out: [M][N] row-major, of y_dtype:
  *             RQ_F16  the dequantized product rounded to fp16;
  *             RQ_F32  the dequantized product in fp32;
@@ -208,7 +217,9 @@ rq_status rq_fwht_quant(const void *x, rq_dtype x_dtype, int64_t rows, int64_t n
  *     M <= 64, N a multiple of 128, K <= 8192: weights in tensor memory as
  *       the MMA's 128-row side, tokens as its N side, K split over thread-block
  *       clusters of up to 8 CTAs reduced in distributed shared memory;
- *     other shapes: legacy FP8 mma.sync, CTAs of 16 channels x 64 tokens.
+ *     other shapes: legacy FP8 mma.sync, CTAs of 16 channels x 64 tokens;
+ *     per-group scales: CTA pairs, 256 x 128 tiles, one tensor-memory partial
+ *       per group, scaled and summed by the epilogue warps in registers.
  */
 rq_status rq_w4a4_gemm(const uint8_t *a_q, const float *a_scales, const uint8_t *w_q,
                        const float *w_scales, int64_t M, int64_t N, int64_t K, uint64_t seed,

@@ -176,7 +176,10 @@ def w4a4_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_d
     a_scales (M,), w_scales (N,).  out_dtype float16 / float32, or int32 for the
     raw accumulators.  a_q of shape (M x K) holds the activation codes in the
     operand form of fwht_quant(..., RQ_E4M3_CODES) (more than 64 rows); a_scales
-    is then the (M x 2) scales-and-code-sums it returns, needed for int32 too."""
+    is then the (M x 2) scales-and-code-sums it returns, needed for int32 too.
+    With operand-form activations, w_scales of shape (N x K/128) are per-group
+    weight scales (fwht_quant(..., RQ_GROUP_SCALES) on the rows of W^T): fp16
+    or fp32 output, N a multiple of 128, K <= 8192."""
     lib = load_library()
     M, ka = a_q.shape
     N, kb2 = w_q.shape
@@ -186,6 +189,10 @@ def w4a4_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_d
         raise ValueError("packed operands must be contiguous")
     K = 2 * kb2
     flags = RQ_A_E4M3 if ka == K else 0
+    if isinstance(w_scales, torch.Tensor) and w_scales.dim() == 2:
+        if not flags:
+            raise ValueError("per-group w_scales need the operand-form activations (a_q of shape M x K)")
+        flags |= RQ_GROUP_SCALES
     if out is None:
         out = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
     _expect(out, "out", (M, N), _OUT_DTYPES)
@@ -194,7 +201,12 @@ def w4a4_gemm(a_q: torch.Tensor, a_scales, w_q: torch.Tensor, w_scales, *, out_d
         _expect(a_scales, "a_scales", (M, 2), torch.float32)   # (scale, code sum) per row
     else:
         _expect(a_scales, "a_scales", (M,), torch.float32, optional=raw)
-    _expect(w_scales, "w_scales", (N,), torch.float32, optional=raw)
+    if flags & RQ_GROUP_SCALES:
+        if raw:
+            raise ValueError("per-group scales give fp16 or fp32 output, not raw int32 accumulators")
+        _expect(w_scales, "w_scales", (N, K // 128), torch.float32)
+    else:
+        _expect(w_scales, "w_scales", (N,), torch.float32, optional=raw)
     _dev(a_q, w_q, a_scales, w_scales, out)
     with torch.cuda.device(a_q.device):
         st = lib.rq_w4a4_gemm(_ptr(a_q), _ptr(a_scales), _ptr(w_q), _ptr(w_scales), M, N, K, seed, flags,

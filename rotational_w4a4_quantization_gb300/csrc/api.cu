@@ -101,11 +101,14 @@ rq_status rq_w4a4_gemm(const uint8_t *a_q, const float *a_scales, const uint8_t 
                        uint32_t flags, void *y, rq_dtype y_dtype, void *stream) {
     (void)seed;  // the rotation is already folded into w_q
     if (M < 0 || N < 0 || K <= 0) return RQ_ERR_INVALID_ARG;
-    if (flags & ~uint32_t(RQ_A_E4M3)) return RQ_ERR_INVALID_ARG;
+    if (flags & ~uint32_t(RQ_A_E4M3 | RQ_GROUP_SCALES)) return RQ_ERR_INVALID_ARG;
     const bool a_e4m3 = (flags & RQ_A_E4M3) != 0;
+    const bool group = (flags & RQ_GROUP_SCALES) != 0;
     if (a_e4m3 && M > 0 && M <= 64) return RQ_ERR_UNSUPPORTED;   // the operand form feeds the tensor-core kernel
     if (K % 128 != 0 || K > 65536) return RQ_ERR_UNSUPPORTED;
     if (y_dtype != RQ_F16 && y_dtype != RQ_F32 && y_dtype != RQ_I32) return RQ_ERR_UNSUPPORTED;
+    // per-group weight scales: the group kernel, on operand-form activations only
+    if (group && (!a_e4m3 || y_dtype == RQ_I32 || N % 128 != 0 || K > 8192)) return RQ_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return RQ_OK;
     const bool need_scales = y_dtype != RQ_I32;
     const bool need_a = need_scales || a_e4m3;   // the operand form's row code sums sit in a_scales
@@ -113,6 +116,11 @@ rq_status rq_w4a4_gemm(const uint8_t *a_q, const float *a_scales, const uint8_t 
     if (!rq::aligned16(a_q) || !rq::aligned16(w_q) || !rq::aligned16(y)) return RQ_ERR_MISALIGNED;
     if ((need_a && !rq::aligned16(a_scales)) || (need_scales && !rq::aligned16(w_scales))) return RQ_ERR_MISALIGNED;
     if ((N * rq::elem_size(y_dtype)) % 16 != 0) return RQ_ERR_MISALIGNED;
+    if (group) {
+        cudaError_t e = rq::launch_w4a4_group_tc(a_q, a_scales, w_q, w_scales, M, N, K, y, y_dtype == RQ_F16 ? 0 : 1,
+                                                 static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+    }
     rq::GemmArgs g{a_q, a_scales, w_q, w_scales, M, N, K, y,
                    y_dtype == RQ_F16 ? 0 : (y_dtype == RQ_F32 ? 1 : 2), a_e4m3};
     cudaError_t e = rq::launch_w4a4_gemm(g, static_cast<cudaStream_t>(stream));

@@ -86,6 +86,11 @@ cudaError_t launch_w4a8_gemm_tc(const int8_t *aq, const float *sa, const uint8_t
 bool w4a8_group_tc_supported(int64_t M, int64_t N, int64_t K, int y_mode);
 cudaError_t launch_w4a8_group_tc(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,
                                  int64_t N, int64_t K, void *y, int y_mode, cudaStream_t stream);
+// The same kernel for INT4 activations in the product's operand form
+// ([M][K] signed E4M3 bytes, sa2 the [M][2] (scale, code sum) pairs): the W4A4
+// product with per-group (128) weight scales, under the same shape limits.
+cudaError_t launch_w4a4_group_tc(const uint8_t *aq_e4m3, const float *sa2, const uint8_t *wq, const float *sw,
+                                 int64_t M, int64_t N, int64_t K, void *y, int y_mode, cudaStream_t stream);
 cudaError_t launch_w4a8_gemm(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,
                              int64_t N, int64_t K, int64_t group, void *y, int y_mode, cudaStream_t stream);
 

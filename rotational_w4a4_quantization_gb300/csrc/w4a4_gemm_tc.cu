@@ -842,6 +842,7 @@ struct GSmem {
     uint64_t op_full[GOP], op_empty[GOP];               // op_full at the leader: both CTAs' teams
     uint64_t p_full[GPR], p_empty[GPR];                 // p_empty at the leader: both CTAs' epilogues
     uint64_t sc_full[2], sc_empty[2];                   // own epilogue threads / warps
+    uint64_t a_full[GOP];                               // AE: this CTA's operand tile of A landed (TMA)
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -904,7 +905,14 @@ __device__ __forceinline__ void store16_f(void *y, int64_t N, int64_t m, int64_t
     }
 }
 
-template <int YMODE>
+// AE: INT4 activation codes in the product's operand form (rq_fwht_quant with
+// RQ_E4M3_CODES: signed E4M3 bytes, scales as (scale, code sum) pairs).  Lane 1
+// of warp 0 loads each K block's 128 x 128-byte A tile by TMA straight into the
+// operand ring (completing on a_full), the converters widen only W, and each
+// TMEM lane is one activation row (no INT8 halves): tiles of 256 activation
+// rows per pair, half the MMA rows and epilogue work per output of the INT8
+// path.  The sums are not needed: the weights widen with their sign.
+template <int YMODE, bool AE = false>
 __global__ void __launch_bounds__(GTHREADS, 1)
 w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ GParams prm) {
@@ -917,7 +925,8 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const uint32_t rank = cluster_rank();
     const int kblocks = (int)(prm.K / BK);                    // = groups
     const int64_t n_tiles_n = prm.N / GBN;
-    const int64_t n_tiles_m = (prm.M + BM - 1) / BM;                // 128 activation rows per tile
+    constexpr int kRowsPerTile = AE ? 2 * BM : BM;                  // activation rows per tile (pair)
+    const int64_t n_tiles_m = (prm.M + kRowsPerTile - 1) / kRowsPerTile;
     const int64_t n_tiles = n_tiles_n * n_tiles_m;                  // run M-fastest (L2 reuse of W)
     const int64_t first_tile = blockIdx.x / 2, tile_step = gridDim.x / 2;
 
@@ -938,6 +947,7 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             mbar_init(&s.sc_full[i], GBN);      // the 128 staging threads
             mbar_init(&s.sc_empty[i], GEPI);
         }
+        for (int i = 0; i < GOP; ++i) mbar_init(&s.a_full[i], 1);
         s.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -963,9 +973,23 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 for (int kb = 0; kb < kblocks; ++kb, ++g) {
                     const int st = (int)(g % GPK);
                     if (!mbar_wait<false, true>(s, &s.pk_empty[st], (uint32_t)((g / GPK) & 1) ^ 1, prm.err)) { ok = false; break; }
-                    mbar_expect_tx(&s.pk_full[st], PK_A + PK_W);
-                    tma_load_2d(s.pkA[st], &tmA, &s.pk_full[st], kb * BK, m0);
+                    mbar_expect_tx(&s.pk_full[st], (AE ? 0 : PK_A) + PK_W);
+                    if constexpr (!AE) tma_load_2d(s.pkA[st], &tmA, &s.pk_full[st], kb * BK, m0);
                     tma_load_2d(s.pkW[st], &tmW, &s.pk_full[st], kb * (BK / 2), n0);
+                }
+            }
+        } else if (AE && lane == 1) {
+            // operand-form A: each K block's tile into the operand ring once the
+            // MMAs that last read that stage are done
+            int64_t g = 0;
+            bool ok = true;
+            for (int64_t tile = first_tile; tile < n_tiles && ok; tile += tile_step) {
+                const int m0 = (int)(tile % n_tiles_m) * (2 * BM) + (int)rank * BM;
+                for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                    const int os = (int)(g % GOP);
+                    if (!mbar_wait<true, true>(s, &s.op_empty[os], (uint32_t)((g / GOP) & 1) ^ 1, prm.err)) { ok = false; break; }
+                    mbar_expect_tx(&s.a_full[os], BM * BK);
+                    tma_load_2d(s.opA[os], &tmA, &s.a_full[os], kb * BK, m0);
                 }
             }
         }
@@ -1005,14 +1029,16 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 if ((int)(g % GTEAMS) != team) continue;
                 const int ps = (int)(g % GPK), os = (int)(g % GOP);
                 if (!mbar_wait(s, &s.pk_full[ps], (uint32_t)((g / GPK) & 1), prm.err)) { ok = false; break; }
-                uint4 a[4], w[2];
+                uint4 a[AE ? 1 : 4], w[2];
+                if constexpr (!AE) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) a[j] = reinterpret_cast<const uint4 *>(s.pkA[ps])[tt + kTeamThreads * j];
+                    for (int j = 0; j < 4; ++j) a[j] = reinterpret_cast<const uint4 *>(s.pkA[ps])[tt + kTeamThreads * j];
+                }
 #pragma unroll
                 for (int j = 0; j < 2; ++j) w[j] = reinterpret_cast<const uint4 *>(s.pkW[ps])[tt + kTeamThreads * j];
                 if (!warp_wait_commit(s, &s.op_empty[os], (uint32_t)((g / GOP) & 1) ^ 1, lane, prm.err)) { ok = false; break; }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < (AE ? 0 : 4); ++j) {
                     const uint4 &v = a[j];
                     const uint32_t p[4] = {__byte_perm(v.x, v.y, 0x6420u), __byte_perm(v.x, v.y, 0x7531u),
                                            __byte_perm(v.z, v.w, 0x6420u), __byte_perm(v.z, v.w, 0x7531u)};
@@ -1041,6 +1067,10 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     const int g0 = (2 * ch) ^ (row & 7), g1 = (2 * ch + 1) ^ (row & 7);
                     *reinterpret_cast<uint4 *>(rowp + 16 * g0) = make_uint4(lo[0], hi[0], lo[1], hi[1]);
                     *reinterpret_cast<uint4 *>(rowp + 16 * g1) = make_uint4(lo[2], hi[2], lo[3], hi[3]);
+                }
+                // AE: this CTA's A tile must be in place before the stage is released to the MMA
+                if constexpr (AE) {
+                    if (!mbar_wait(s, &s.a_full[os], (uint32_t)((g / GOP) & 1), prm.err)) { ok = false; break; }
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
@@ -1087,9 +1117,11 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 stage(nt, b ^ 1);
             }
             const int64_t m0 = (tile % n_tiles_m) * (2 * BM) + (int64_t)rank * BM;   // operand rows
-            const int64_t m = (m0 + 32 * q + lane) >> 1;                             // activation row
+            // activation row: one per TMEM lane (AE), or one per two lanes (INT8 halves)
+            const int64_t m = AE ? m0 + 32 * q + lane : (m0 + 32 * q + lane) >> 1;
             const int64_t n0 = (tile / n_tiles_m) * GBN;
-            const float sa = m < prm.M ? prm.sa[m] * 262144.0f : 0.f;               // x 2^18: partials are 2^-18 units
+            // x 2^18: partials are 2^-18 units; AE scales are (scale, code sum) pairs
+            const float sa = m < prm.M ? prm.sa[AE ? 2 * m : m] * 262144.0f : 0.f;
             float acc[32];   // the running sums of this thread's row, columns 32 part .. 32 part + 31
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc[j] = 0.f;
@@ -1119,7 +1151,16 @@ w4a8_group_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     }
                 }
             }
-            if (ok) {
+            if (ok && AE) {
+                // one activation row per lane: all 32 columns
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float out[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) out[j] = acc[16 * h + j] * sa;
+                    if (m < prm.M) store16_f<YMODE>(prm.y, prm.N, m, n0 + 32 * part + 16 * h, out);
+                }
+            } else if (ok) {
                 // rows 2i (h) and 2i+1 (l) are lanes 2i, 2i+1: the even lane outputs the
                 // chunk's first 16 columns, the odd lane the next 16
                 float out[16];
@@ -1235,16 +1276,17 @@ cudaError_t launch_mode(const GemmArgs &g, const TcParams &p, cudaStream_t strea
 // size measured: 2048 x 4096 -> 14336 102.4 us (three teams ~106 us), 4096 x
 // 8192 -> 28672 676 us (three teams 739 us).
 
-template <int YMODE>
+template <int YMODE, bool AE = false>
 cudaError_t launch_group_mode(const CUtensorMap &ta, const CUtensorMap &tw, const GParams &p, cudaStream_t stream) {
-    auto kern = w4a8_group_tc_kernel<YMODE>;
+    auto kern = w4a8_group_tc_kernel<YMODE, AE>;
     const size_t smem = sizeof(GSmem) + 1024;
     // set on every launch: the attribute is per device, and a process may use several
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorUnknown;
-    const int64_t tiles = (p.N / GBN) * ((p.M + BM - 1) / BM);
+    const int64_t rows_per_tile = AE ? 2 * BM : BM;
+    const int64_t tiles = (p.N / GBN) * ((p.M + rows_per_tile - 1) / rows_per_tile);
     const int64_t units = tiles < sms / 2 ? tiles : sms / 2;   // persistent CTA pairs
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(units * 2));
@@ -1318,6 +1360,19 @@ cudaError_t launch_w4a8_group_tc(const int8_t *aq, const float *sa, const uint8_
         !make_map(&tw, wq, N, K / 2, BK / 2, GWROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     return y_mode == 1 ? launch_group_mode<1>(ta, tw, p, stream) : launch_group_mode<0>(ta, tw, p, stream);
+}
+
+cudaError_t launch_w4a4_group_tc(const uint8_t *aq_e4m3, const float *sa2, const uint8_t *wq, const float *sw,
+                                 int64_t M, int64_t N, int64_t K, void *y, int y_mode, cudaStream_t stream) {
+    const GParams p{sa2, sw, y, M, N, K, error_word_device_ptr()};
+    if (!p.err) return cudaErrorUnknown;
+    CUtensorMap ta, tw;
+    // 128 rows x 128 bytes of operand-form codes with the 128-byte swizzle of the
+    // MMA's K-major operand layout
+    if (!make_map(&ta, aq_e4m3, M, K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tw, wq, N, K / 2, BK / 2, GWROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    return y_mode == 1 ? launch_group_mode<1, true>(ta, tw, p, stream) : launch_group_mode<0, true>(ta, tw, p, stream);
 }
 
 cudaError_t launch_w4a8_gemm_tc(const int8_t *aq, const float *sa, const uint8_t *wq, const float *sw, int64_t M,

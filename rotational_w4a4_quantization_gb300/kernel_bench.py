@@ -43,7 +43,9 @@ from rotational_w4a4_quantization_gb300 import synth  # noqa: E402
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["fwht", "kv", "gemm", "fused", "unfused", "attn", "w4a8"], required=True)
+    ap.add_argument("--kernel", choices=["fwht", "kv", "gemm", "fused", "unfused", "attn", "w4a8", "w4a4g"],
+                    required=True, help="w4a4g: the W4A4 product with per-group (128) weight scales, operand-form "
+                                        "activations from the rotation kernel")
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="prefill")
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
@@ -105,6 +107,20 @@ def main(argv=None):
         fn = lambda: rq.w4a8_gemm(a8, s8, wq, sg, out=y)
         work, unit = 2 * M * N * K, "TOPS"
         what = f"w4a8_gemm {M}x{K}x{N} {'per-channel' if per_channel else 'per-group-128'} fp16"
+    elif args.kernel == "w4a4g":
+        if not w.gemm_n:
+            raise SystemExit(f"workload {w.name} has no GEMM")
+        M, K, N = w.rows, w.n, w.gemm_n
+        x = synth.activations(M, K, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor).to(dev)
+        ae, sa2 = rq.fwht_quant(x, seed, flags | rq.RQ_E4M3_CODES)
+        wq, _ = synth.random_codes(N, K, 1001 + w.data_seed)
+        g8 = torch.Generator().manual_seed(1002 + w.data_seed)
+        sg = (torch.rand(N, K // 128, generator=g8) + 0.05).to(dev)
+        wq = wq.to(dev)
+        y = torch.empty(M, N, dtype=torch.float16, device=dev)
+        fn = lambda: rq.w4a4_gemm(ae, sa2, wq, sg, out=y)
+        work, unit = 2 * M * N * K, "TOPS"
+        what = f"w4a4_gemm {M}x{K}x{N} per-group-128 fp16 (e4m3 activations)"
     elif args.kernel == "attn":
         kw = synth.KV
         k, v = synth.kv_pair(kw.kv_tokens, kw.kv_heads, kw.kv_head_dim, kw.data_seed,

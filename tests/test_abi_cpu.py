@@ -91,6 +91,12 @@ def gemm(lib, M=16, N=64, K=256, a=A16, w=A16, sa=A16, sw=A16, y=A16, ydt=2, fla
     (dict(flags=16, M=0, a=NULL), 0),  # empty: nothing to do
     (dict(flags=16, M=128, ydt=3, sa=NULL, sw=NULL), 1),   # operand form: the row code sums are read for int32 too
     (dict(flags=16, M=128, ydt=3, sa=A1, sw=NULL), 3),
+    (dict(flags=8, M=128, N=128), 2),                     # per-group scales need operand-form activations
+    (dict(flags=24, M=16, N=128), 2),                     # ... and more than 64 rows
+    (dict(flags=24, M=128, N=128, ydt=3), 2),             # ... and fp16 / fp32 output
+    (dict(flags=24, M=128, N=192), 2),                    # ... and N a multiple of 128
+    (dict(flags=24, M=128, N=128, K=8320), 2),            # ... and at most 64 groups
+    (dict(flags=24, M=0, N=128, a=NULL), 0),              # empty: nothing to do
     (dict(ydt=1), 2),                 # bf16 output not offered
     (dict(a=NULL), 1),
     (dict(sa=NULL), 1),
@@ -312,6 +318,18 @@ def test_binding_checks_operand_form_scales(lib, sa, match):
     M, N, K = 128, 64, 256
     with pytest.raises(ValueError, match=match):
         rq.w4a4_gemm(_t((M, K), torch.uint8), sa, _t((N, K // 2), torch.uint8), None, out=_t((M, N), torch.int32))
+
+
+@pytest.mark.parametrize("a_cols,sw_shape,out_dtype,match", [
+    (128, (64, 2), torch.float16, "per-group w_scales need the operand-form activations"),
+    (256, (64, 2), torch.int32, "per-group scales give fp16 or fp32 output"),
+    (256, (64, 3), torch.float16, "w_scales: expected shape"),
+])
+def test_binding_checks_per_group_product(lib, a_cols, sw_shape, out_dtype, match):
+    M, N, K = 128, 64, 256
+    with pytest.raises(ValueError, match=match):
+        rq.w4a4_gemm(_t((M, a_cols), torch.uint8), _t((M, 2), torch.float32), _t((N, K // 2), torch.uint8),
+                      _t(sw_shape, torch.float32), out=_t((M, N), out_dtype))
 
 
 def test_binding_gemm_raw_mode_needs_no_scales(lib):

@@ -362,3 +362,65 @@ def test_w4a4_per_group_product(M, N, K):
     qb, _ = rq.fwht_quant(x.to(DEV), 5, rq.RQ_SIGNS_FIRST | rq.RQ_INT4_BYTES)
     ra2 = oracle.fwht_quant(x.double().numpy(), 5, rq.RQ_SIGNS_FIRST, want_ratio=True)
     _compare_int8(to_np(qb).astype(np.int16), qa.astype(np.int16), ra2["ratio"].reshape(M, K))
+
+
+# ---------------------------------------------------------------------------
+# W4A4 with per-group weight scales on the tensor cores: operand-form INT4
+# activations (RQ_E4M3_CODES) into rq_w4a4_gemm with [N][K/128] weight scales.
+# ---------------------------------------------------------------------------
+
+def _w4a4_group(qa_packed, sa, qw, sw, out_dtype):
+    """The operand form of the packed activation codes (bit arithmetic on the
+    host) and its (scale, code sum) pairs, through rq_w4a4_gemm's per-group path."""
+    from parity import operand_form, operand_scales
+    ae = torch.from_numpy(operand_form(qa_packed)).to(DEV)
+    sa2 = torch.from_numpy(operand_scales(qa_packed, sa)).to(DEV)
+    y = rq.w4a4_gemm(ae, sa2, torch.from_numpy(qw).to(DEV), torch.from_numpy(sw).to(DEV), out_dtype=out_dtype)
+    assert rq.sync_status() == 0
+    return to_np(y)
+
+
+@pytest.mark.parametrize("M", [65, 300, 600])
+@pytest.mark.parametrize("N,K", [(128, 128), (2560, 384), (384, 2048), (256, 8192)])
+def test_w4a4_per_group_tensor_cores(M, N, K):
+    """256-row tiles on CTA pairs: one group (K = 128) up to 64 groups, ragged M
+    (65: one CTA of the pair without rows; 300, 600: partial tiles), odd group
+    counts and, at 600 x 2560, pairs running several tiles; fp32 within 1e-5 of
+    each row's largest output, fp16 within one ulp of that."""
+    g = np.random.default_rng(7000 + M + N + K)
+    qa = g.integers(0, 256, size=(M, K // 2)).astype(np.uint8)
+    sa = (g.random(M) + 0.05).astype(np.float32)
+    qw = g.integers(0, 256, size=(N, K // 2)).astype(np.uint8)
+    sw = (g.random((N, K // 128)) + 0.05).astype(np.float32)
+    codes = oracle.unpack(qa, K).astype(np.int8)
+    _, yref = oracle.w4a8_gemm(codes, sa, qw, sw, M, N, K, 128)
+    _check_per_group(_w4a4_group(qa, sa, qw, sw, torch.float32), yref)
+    compare_f16(_w4a4_group(qa, sa, qw, sw, torch.float16), yref, atol=1e-5 * np.abs(yref).max(axis=1, keepdims=True))
+
+
+@pytest.mark.parametrize("ba,bw", [(0x77, 0x77), (0x88, 0x88), (0x88, 0x77)])
+def test_w4a4_per_group_extreme_codes(ba, bw):
+    """All codes at +7 or -8 over 64 groups with unit scales: every output is
+    64 x 128 x qa x qw exactly (fp32 sums of exact integers below 2^24)."""
+    M, N, K = 256, 256, 8192
+    qa = np.full((M, K // 2), ba, dtype=np.uint8)
+    qw = np.full((N, K // 2), bw, dtype=np.uint8)
+    y = _w4a4_group(qa, np.ones(M, np.float32), qw, np.ones((N, K // 128), np.float32), torch.float32)
+    qa1, qw1 = (ba & 15) - 16 * ((ba >> 3) & 1), (bw & 15) - 16 * ((bw >> 3) & 1)
+    assert (y == float(K * qa1 * qw1)).all()
+
+
+def test_w4a4_per_group_end_to_end():
+    """Rotation in operand form, then the per-group product, against the W4A8
+    route on the GPU's own INT4 codes (RQ_INT4_BYTES): the same codes and scales,
+    the same group partials; the two sum the scaled partials in different
+    orders, so they agree within 1e-5 of each row's largest output."""
+    M, N, K = 384, 1024, 4096
+    x = synth.activations(M, K, torch.bfloat16, 11, 4, 100.0).to(DEV)
+    wt = synth.weights_t(N, K, 13).to(DEV)
+    qw, sw = rq.fwht_quant(wt, 7, rq.RQ_SIGNS_FIRST | rq.RQ_GROUP_SCALES)
+    qe, se = rq.fwht_quant(x, 7, rq.RQ_SIGNS_FIRST | rq.RQ_E4M3_CODES)
+    qb, sb = rq.fwht_quant(x, 7, rq.RQ_SIGNS_FIRST | rq.RQ_INT4_BYTES)
+    y4 = to_np(rq.w4a4_gemm(qe, se, qw, sw, out_dtype=torch.float32))
+    y8 = to_np(rq.w4a8_gemm(qb, sb, qw, sw, out_dtype=torch.float32))
+    _check_per_group(y4, y8.astype(np.float64))
