@@ -147,13 +147,30 @@ __global__ void __launch_bounds__(kKThreads, 2) fwht_kron_kernel(const __grid_co
     for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
         const char *xrow = static_cast<const char *>(p.x) + r * p.ld * ES;
         // ---- step 1: the Sylvester transform of every length-B segment ----
+        // A warp's segments are a = warp, warp + 8, ...: the raw 16-byte granules of
+        // the next one are loaded before the current one is transformed, so a
+        // segment's load latency overlaps the previous segment's work.
+        constexpr int NG = E * ES >= 16 ? E * ES / 16 : 1;   // granules per lane and segment
+        uint4 nxt[NG];
+        auto load_seg = [&](int a) {
+            if constexpr (E * ES >= 16) {
+#pragma unroll
+                for (int c = 0; c < NG; ++c)
+                    nxt[c] = *reinterpret_cast<const uint4 *>(xrow + (int64_t)(a * B + lane * E) * ES + 16 * c);
+            }
+        };
+        if (warp < M) load_seg(warp);
         for (int a = warp; a < M; a += kKWarps) {
             const int base = a * B + lane * E;
+            uint4 cur[NG];
+#pragma unroll
+            for (int c = 0; c < NG; ++c) cur[c] = nxt[c];
+            if (a + kKWarps < M) load_seg(a + kKWarps);
             float v[E];
             if constexpr (E * ES >= 16) {
 #pragma unroll
                 for (int c = 0; c < E * ES / 16; ++c) {
-                    const uint4 g = *reinterpret_cast<const uint4 *>(xrow + (int64_t)base * ES + 16 * c);
+                    const uint4 g = cur[c];
                     uint32_t w[4] = {g.x, g.y, g.z, g.w};
                     if constexpr (IN == IN_F32) {
                         // elements base + 4c .. + 3: sign words (base + 4c) / 2 and + 1
