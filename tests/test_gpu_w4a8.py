@@ -424,3 +424,29 @@ def test_w4a4_per_group_end_to_end():
     y4 = to_np(rq.w4a4_gemm(qe, se, qw, sw, out_dtype=torch.float32))
     y8 = to_np(rq.w4a8_gemm(qb, sb, qw, sw, out_dtype=torch.float32))
     _check_per_group(y4, y8.astype(np.float64))
+
+
+def test_w4a4_per_group_prefill_shape_sampled_rows():
+    """2048 x 4096 -> 14336 with per-group weight scales on the prefill workload's
+    activations: the oracle's INT4 codes in the operand form, random per-group
+    weights; rows sampled over every 256-row tile and both CTAs of a pair,
+    against the oracle's per-group product (fp32 and fp16)."""
+    from parity import operand_form, operand_scales
+    w = synth.WORKLOADS["prefill"]
+    M, K, N = w.rows, w.n, w.gemm_n
+    x = synth.activations(M, K, w.x_dtype, w.data_seed, w.n_outliers, w.outlier_factor)
+    ra = oracle.fwht_quant(x.double().numpy(), synth.SIGN_SEED, rq.RQ_SIGNS_FIRST)
+    g = np.random.default_rng(6101)
+    qw = g.integers(0, 256, size=(N, K // 2)).astype(np.uint8)
+    sw = (g.random((N, K // 128)) + 0.05).astype(np.float32)
+    ae = torch.from_numpy(operand_form(ra["q"])).to(DEV)
+    sa2 = torch.from_numpy(operand_scales(ra["q"], ra["scales"])).to(DEV)
+    wd, sd = torch.from_numpy(qw).to(DEV), torch.from_numpy(sw).to(DEV)
+    y32 = to_np(rq.w4a4_gemm(ae, sa2, wd, sd, out_dtype=torch.float32))
+    y16 = to_np(rq.w4a4_gemm(ae, sa2, wd, sd, out_dtype=torch.float16))
+    assert rq.sync_status() == 0
+    rows = np.unique(np.concatenate([np.arange(0, M, 97), [127, 128, 255, 256, M - 1]]))
+    codes = oracle.unpack(ra["q"][rows], K).astype(np.int8)
+    _, yref = oracle.w4a8_gemm(codes, ra["scales"][rows], qw, sw, len(rows), N, K, 128)
+    _check_per_group(y32[rows], yref)
+    compare_f16(y16[rows], yref, atol=1e-5 * np.abs(yref).max(axis=1, keepdims=True))
