@@ -10,7 +10,8 @@ Entry points (same names as the C ABI):
 * :func:`fwht_quant` -- randomized Hadamard rotation of each row + per-row INT4
   quantization and nibble packing (also the offline weight fold when given W^T);
 * :func:`w4a4_gemm` -- exact INT4 x INT4 product with per-token x per-channel
-  dequant;
+  dequant (or per-group weight scales on the operand-form activations that
+  :func:`fwht_quant` writes with ``RQ_E4M3_CODES``);
 * :func:`kv_rotate_quant` -- head-wise rotation + INT4 quantization of K and V;
 * :func:`fwht_quant_gemm` -- decode-sized fusion of the rotation, quantization
   and W4A4 product in one launch;
