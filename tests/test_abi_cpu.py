@@ -285,6 +285,10 @@ def test_binding_checks_fwht_quant_code_modes(lib):
         rq.fwht_quant(x, 1, rq.RQ_INT8_CODES, q=_t((4, 256), torch.int8))
     with pytest.raises(ValueError, match="scales: expected shape"):  # one scale per group of 128
         rq.fwht_quant(x, 1, rq.RQ_GROUP_SCALES, scales=_t((4,), torch.float32))
+    with pytest.raises(ValueError, match="scales: expected shape"):  # operand form: (scale, code sum) per row
+        rq.fwht_quant(x, 1, rq.RQ_E4M3_CODES, scales=_t((4,), torch.float32))
+    with pytest.raises(ValueError, match="q: expected shape"):       # operand form: n bytes per row
+        rq.fwht_quant(x, 1, rq.RQ_E4M3_CODES, q=_t((4, 256), torch.uint8))
     with pytest.raises(ValueError, match="q must be contiguous"):
         rq.fwht_quant(x, 1, 1, q=_t((4, 512), torch.uint8)[:, ::2])
 
